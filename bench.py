@@ -1,0 +1,433 @@
+"""Throughput of the CSA / HCA layer on one B300, in query-tokens/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one pass of the whole hot path over one batch of synthetic input.
+Default workload: the Flash-shaped interleaved CSA + HCA prefill (n = 65536,
+64 heads of dim 512, indexer 64 x 128, top-k 512, m = 4 / m' = 128): the
+one workload whose step runs every step of the path (compression of both
+layers, indexer, top-k, sparse attention, dense HCA attention).
+Other workloads: csa_prefill_f32, hca_prefill_bf16, csa_decode_flash,
+hybrid_decode_pro.
+
+Under torchrun each rank runs its own replica of the workload (the layer
+does not shard for one sequence); value = all ranks' query-tokens / the
+slowest rank's time.  `--impl reference` times the fp64 CPU oracle on a
+bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+from long_context_sparse_22_b300 import accounting  # noqa: E402
+
+METRIC = "CSA/HCA query-tokens/s (decode & prefill), % of HBM/tensor roofline, 1xB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------- workloads
+
+class Workload:
+    """Device buffers and the step of one workload through the public API."""
+
+    def __init__(self, name: str, csa, torch):
+        self.name, self.csa, self.torch = name, csa, torch
+        t0 = time.time()
+        self.s, self.x = synth.make_inputs(name)
+        self.gen_s = time.time() - t0
+        self.kind = self.s["kind"]
+        s = self.s
+        if self.kind == "hybrid_prefill":
+            self.work = accounting.hybrid_prefill(s)
+        elif self.kind in ("csa_decode", "hybrid_decode"):
+            self.work = accounting.decode(s, self.kind == "hybrid_decode")
+        elif self.kind == "csa_prefill":
+            w = accounting.hybrid_prefill(dict(s, m2=s["m"]))
+            w["flops"] -= w["hca_attn_flops"]
+            self.work = w
+        else:
+            w = accounting.hybrid_prefill(dict(s, hI=1, dI=0, top_k=0, m2=s["m"]))
+            self.work = {"flops": w["hca_attn_flops"], "query_tokens": w["query_tokens"],
+                         "hca_attn_flops": w["hca_attn_flops"], "hca_attn_bytes": w["hca_attn_bytes"],
+                         "compress_bytes": 0}
+        self.units = self.work["query_tokens"]
+        self.in_keys = [k for k in self.x]
+        self.d = {k: self._dev(v) for k, v in self.x.items()}
+        self.h2d_bytes = sum(v.nbytes for v in self.x.values())
+        p = csa.params
+        self.p = p(m=s["m"], overlap=s.get("overlap", 0), top_k=s.get("top_k", 1),
+                   n_win=s["n_win"], rope_dims=s["rope_dims"], rope_theta=s["theta"])
+        self.p2 = p(m=s.get("m2", s["m"]), n_win=s["n_win"], rope_dims=s["rope_dims"],
+                    rope_theta=s["theta"])
+        self._alloc()
+
+    def _dev(self, a):
+        t = self.torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
+        return t.view(self.torch.bfloat16) if a.dtype == np.uint16 else t
+
+    def _alloc(self):
+        csa, d, s = self.csa, self.d, self.s
+        T = self.torch
+        if self.kind in ("hybrid_prefill", "csa_prefill"):
+            B, n, H, c = s["B"], s["n"], s["H"], s["c"]
+            dt = 1 if s["dtype"] == "bf16" else 0
+            self.out = T.empty_like(d["q"])
+            self.ws = csa.Workspace(csa.csa_prefill_ws_size(dt, B, n, H, c, s["hI"], s["dI"], self.p))
+            if self.kind == "hybrid_prefill":
+                self.out2 = T.empty_like(d["q2"])
+                self.ws2 = csa.Workspace(csa.hca_prefill_ws_size(dt, B, n, H, c, self.p2))
+        elif self.kind == "hca_prefill":
+            B, n, H, c = s["B"], s["n"], s["H"], s["c"]
+            self.out = T.empty_like(d["q"])
+            self.ws = csa.Workspace(csa.hca_prefill_ws_size(1, B, n, H, c, self.p))
+        else:
+            B, H, c = s["B"], s["H"], s["c"]
+            self.out = T.empty_like(d["q"])
+            self.out2 = T.empty_like(d["q2"]) if self.kind == "hybrid_decode" else None
+            self.ws = csa.Workspace(csa.hybrid_decode_ws_size(1, B, H, c, s["hI"], s["dI"],
+                                                              s["E"], s.get("E2", 0), self.p,
+                                                              self.p2))
+
+    def outputs(self):
+        return [o for o in (self.out, getattr(self, "out2", None)) if o is not None]
+
+    def step(self, d=None):
+        csa, d = self.csa, d or self.d
+        if self.kind in ("hybrid_prefill", "csa_prefill"):
+            csa.csa_prefill(d["C"], d["Z"], d["bias"], d["Ck"], d["Zk"], d["biask"], d["q"], d["qI"],
+                            d["w"], d["sink"], self.p, Cb=d.get("Cb"), Zb=d.get("Zb"),
+                            biasb=d.get("biasb"), Ckb=d.get("Ckb"), Zkb=d.get("Zkb"),
+                            biaskb=d.get("biaskb"), out=self.out, ws=self.ws)
+            if self.kind == "hybrid_prefill":
+                csa.hca_prefill(d["C2"], d["Z2"], d["bias2"], d["q2"], d["sink2"], self.p2,
+                                out=self.out2, ws=self.ws2)
+        elif self.kind == "hca_prefill":
+            csa.hca_prefill(d["C"], d["Z"], d["bias"], d["q"], d["sink"], self.p, out=self.out,
+                            ws=self.ws)
+        else:
+            kw = {}
+            if self.kind == "hybrid_decode":
+                kw = dict(q2=d["q2"], kvc2=d["kvc2"], kv_raw2=d["kv_raw2"], sink2=d["sink2"],
+                          p2=self.p2, out2=self.out2)
+            csa.hybrid_decode(d["q"], d["qI"], d["w"], d["kvc"], d["kIc"], d["kv_raw"], d["sink"],
+                              d["q_pos"], d["raw_pos0"], self.p, out=self.out, ws=self.ws, **kw)
+
+    # end-to-end: per step, the step's inputs go host -> device from pinned
+    # memory and the outputs come back.  For decode the compressed caches are
+    # resident state (as a KV cache is in serving) and stay on the device; the
+    # per-step inputs are the query-side tensors and the window rows.
+    def e2e_setup(self):
+        T = self.torch
+        if self.kind in ("csa_decode", "hybrid_decode"):
+            keys = [k for k in self.x if k not in ("kvc", "kIc", "kvc2", "sink", "sink2")]
+        else:
+            keys = list(self.x)
+        self.e2e_keys = keys
+        self.h_in = {}
+        for k in keys:
+            t = self.torch.from_numpy(self.x[k].view(np.int16) if self.x[k].dtype == np.uint16 else self.x[k])
+            self.h_in[k] = t.pin_memory()
+        self.d_e2e = dict(self.d)
+        self.h_out = [T.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in self.outputs()]
+        self.e2e_h2d = sum(self.x[k].nbytes for k in keys)
+        self.e2e_d2h = sum(o.numel() * o.element_size() for o in self.outputs())
+
+    def e2e_step(self):
+        for k in self.e2e_keys:
+            dst = self.d_e2e[k]
+            src = self.h_in[k]
+            if dst.dtype == self.torch.bfloat16:
+                dst.view(self.torch.int16).copy_(src, non_blocking=True)
+            else:
+                dst.copy_(src, non_blocking=True)
+        self.step(self.d_e2e)
+        for h, o in zip(self.h_out, self.outputs()):
+            h.copy_(o, non_blocking=True)
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def oracle_sample(name: str, budget_s: float = 15.0, x=None, s=None):
+    """Time the fp64 oracle on a bounded sample of the workload; returns
+    (query-tokens/s, threads, description)."""
+    import oracle
+    oracle.lib()
+    if x is None:
+        s, x = synth.make_inputs(name)
+    kind = s["kind"]
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    if kind in ("csa_decode", "hybrid_decode"):
+        t0 = time.time()
+        done = 0
+        for b in range(s["B"]):
+            oracle.csa_decode_seq(s, x, b)
+            if kind == "hybrid_decode":
+                oracle.hca_decode_seq(s, x, b)
+            done += 1
+            if time.time() - t0 > budget_s:
+                break
+        dt = time.time() - t0
+        return done / dt, threads, f"{done} of {s['B']} sequences, full decode step each"
+    # prefill: full compression of the layer(s), then a sample of query rows
+    n = s["n"]
+    rng = np.random.default_rng(0)
+    csa_l = kind in ("csa_prefill", "hybrid_prefill")
+    hca_l = kind in ("hca_prefill", "hybrid_prefill")
+    suf = "2" if kind == "hybrid_prefill" else ""
+    t0 = time.time()
+    prep = oracle.csa_prefill_prepare(s, x, 0) if csa_l else None
+    prep2 = oracle.hca_prefill_prepare(s, x, 0, suf) if hca_l else None
+    t_comp = time.time() - t0
+    S, t_q, batch = 0, 0.0, 8
+    while t_q < budget_s and S < n:
+        sel = np.sort(rng.integers(0, n, batch))
+        t1 = time.time()
+        if csa_l:
+            oracle.csa_prefill_queries(s, x, prep, 0, sel)
+        if hca_l:
+            oracle.hca_prefill_queries(s, x, prep2, 0, sel, suf)
+        t_q += time.time() - t1
+        S += batch
+        batch = min(batch * 2, 256)
+    total_s = t_comp + (t_q / S) * n
+    return n / total_s, threads, (f"full compression of every layer ({t_comp:.1f} s, once per "
+                                  f"step) plus {S} uniformly drawn query rows ({t_q:.1f} s), the "
+                                  f"per-row time extrapolated to all n={n} rows")
+
+
+# -------------------------------------------------------------------- arms
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    s, x = synth.make_inputs(args.workload)
+    vals = []
+    for _ in range(args.warmup):
+        oracle_sample(args.workload, budget_s=2.0, x=x, s=s)
+    desc = threads = None
+    for _ in range(args.steps):
+        v, threads, desc = oracle_sample(args.workload, budget_s=args.ref_budget, x=x, s=s)
+        vals.append(v)
+    value = float(statistics.median(vals))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "query-tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * s.get("n", s["B"]) / value if "n" in s else 1e3 * s["B"] / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload},
+            "cpu_baseline": {"value": value, "unit": "query-tokens/s", "cores": threads,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "query-tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+
+    import long_context_sparse_22_b300 as csa
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    csa.lib()
+    wl = Workload(args.workload, csa, torch)
+    dev_stream = torch.cuda.current_stream()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        wl.step()
+    torch.cuda.synchronize()
+
+    # per-stage device times of the same steps (library timing hooks)
+    csa.timing_enable(True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(dev_stream)
+    for _ in range(args.steps):
+        wl.step()
+    ev1.record(dev_stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    csa.timing_enable(False)
+    stages = csa.timing_read()
+    ms_total = ev0.elapsed_time(ev1)
+    ms_step = ms_total / args.steps
+    if dist is not None:
+        t = torch.tensor([ms_step], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = world * wl.units / (ms_step / 1e3)
+
+    # end to end through the public API with host buffers
+    wl.e2e_setup()
+    wl.e2e_step()
+    torch.cuda.synchronize()
+    k_e2e = max(1, min(args.steps, 3))
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(k_e2e):
+        wl.e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / k_e2e
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * wl.units / (e2e_ms / 1e3)
+
+    # roofline of the dominant stage
+    pk, pk_kind = peaks()
+    stage_ms = {k: v[0] / max(1, args.steps) for k, v in stages.items()}
+    launches = {k: v[1] for k, v in stages.items()}
+    dom = max(stage_ms, key=lambda k: stage_ms[k])
+    per_launch_ms = stages[dom][0] / max(1, stages[dom][1])
+    launches_per_step = max(1, stages[dom][1] // max(1, args.steps))
+    w = wl.work
+    flop_key = {"indexer": "indexer_flops", "sparse_attn": "csa_attn_flops",
+                "hca_attn": "hca_attn_flops"}.get(dom)
+    byte_key = {"compress": "compress_bytes", "topk": "topk_bytes", "indexer": "indexer_bytes",
+                "sparse_attn": "csa_attn_bytes", "hca_attn": "hca_attn_bytes"}.get(dom)
+    decode = wl.kind in ("csa_decode", "hybrid_decode")
+    if flop_key and not (decode and dom in ("indexer",)):
+        bound, unit = "tensor", "TFLOP/s"
+        achieved = w.get(flop_key, 0) / launches_per_step / (per_launch_ms / 1e3) / 1e12
+        peak = pk["bf16_tflops"]
+    else:
+        bound, unit = "hbm", "GB/s"
+        achieved = w.get(byte_key, 0) / launches_per_step / (per_launch_ms / 1e3) / 1e9
+        peak = pk["hbm_gbs"]
+    roof = {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "peak_source": pk_kind, "traffic": None,
+            "stage_ms_per_step": {k: round(v, 4) for k, v in stage_ms.items()},
+            "stage_launches": launches}
+
+    line = {"metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": wl.s["dtype"], "data": "synthetic",
+            "config": {"workload": args.workload, "global_batch": world * wl.s["B"],
+                       "seq_len": wl.s.get("n", wl.s.get("t")),
+                       "parallelism": f"replicas{world}",
+                       "l2": "inputs larger than L2 (126 MB) each step, no flush needed"},
+            "gpu_launches": int(sum(launches.values())),
+            "e2e": {"value": e2e_value, "unit": "query-tokens/s", "h2d_bytes_per_step": wl.e2e_h2d,
+                    "d2h_bytes_per_step": wl.e2e_d2h, "ms_per_step": e2e_ms},
+            "roofline": roof, "clocks": clk}
+    if rank == 0 and world == 1 and not args.no_cpu:
+        v, thr, desc = oracle_sample(args.workload, budget_s=args.ref_budget, x=wl.x, s=wl.s)
+        line["cpu_baseline"] = {"value": v, "unit": "query-tokens/s", "cores": thr, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="hybrid_prefill_flash", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

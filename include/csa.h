@@ -1,0 +1,294 @@
+/*
+ * csa.h -- C ABI of libcsa: the CSA / HCA attention layer of DeepSeek-V4 on
+ * one NVIDIA B300 (sm_103a).
+ *
+ * The layer (sources are web pages about the DeepSeek-V4 report):
+ *   1. compression: every m tokens' KV rows become one entry by a per-channel
+ *      softmax over the block of (compression logit + per-slot bias)
+ *      ["DeepSeek-V4: Making Million-Token Context an Architectural Problem",
+ *      Key design 1 and Key design 2 equations; DeepSeek-V4 book ch.5 "How
+ *      CSA Compresses Memory"];
+ *   2. lightning indexer: score[t,j] = sum_h w[t,h] * ReLU(qI[t,h] . kI[j]),
+ *      then top-k per query (CSA only) [same page, Key design 1 index-score
+ *      equation; book ch.6 "How CSA Selects and Reads Memory"];
+ *   3. shared-KV multi-query attention over the selected (CSA) or all
+ *      visible (HCA) entries, plus the last n_win raw rows, plus a per-head
+ *      sink logit in the denominator, with partial RoPE and output
+ *      de-rotation [book ch.6 "Shared key-value MQA", ch.7 "HCA, Local
+ *      Attention, and Position"].
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor pointer is a DEVICE pointer to a dense row-major array
+ *    (innermost dimension contiguous, batch outermost), 16-byte aligned.
+ *    The caller owns all memory, including workspaces; the library never
+ *    allocates or frees device memory.
+ *  - `stream` is a cudaStream_t passed as void*.  Every call only enqueues
+ *    work on it and returns; no call synchronises the host, except
+ *    csa_stream_status.  Calls from several host threads are safe.
+ *  - Argument validation happens before anything is enqueued; on failure
+ *    the call returns a non-zero csa_status, enqueues nothing, and
+ *    csa_last_error() describes the problem.  A launch failure returns
+ *    CSA_ERR_CUDA.
+ *  - Conditions only the GPU can see (an index outside the cache, a window
+ *    position missing from kv_raw, a bounded wait that ran out) never trap:
+ *    the offending read is skipped and a bit is set in the status word at
+ *    the start of the workspace; csa_stream_status() reports and clears it.
+ *  - Storage dtype: CSA_F32 or CSA_BF16 for q, qI, C, Z, caches and outputs.
+ *    bias, w, sink and scores are always float32; positions are int64;
+ *    selected indices and counts are int32.
+ *  - Positions: q_pos[b,t] is the absolute position of query t of sequence
+ *    b.  Entry j of a cache compressed with rate m covers positions
+ *    j*m .. j*m+m-1 and is visible to a query at t iff (j+1)*m <= t+1.  The
+ *    window of a query at t is the raw rows at positions
+ *    max(0, t-n_win+1) .. t; raw row l of sequence b holds position
+ *    raw_pos0[b] + l.
+ *  - RoPE rotates adjacent pairs (c-r+2i, c-r+2i+1) of the last r dims by
+ *    p * theta^(-2i/r).  Stored caches carry their rotation: csa_compress
+ *    rotates entry j at its block's last position (j+1)*m-1 and its raw-row
+ *    output at each row's position; attention rotates q at t, and rotates
+ *    the output's rotary dims back by -t when derotate = 1.
+ */
+#ifndef CSA_H
+#define CSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
+
+typedef enum {
+    CSA_OK = 0,
+    CSA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer   */
+    CSA_ERR_UNSUPPORTED = 2, /* valid but outside the supported shapes       */
+    CSA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required   */
+    CSA_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed         */
+    CSA_ERR_TIMEOUT = 5,     /* (status word) a bounded device wait ran out  */
+    CSA_ERR_DEVICE = 6       /* (status word) a device-side range check hit  */
+} csa_status;
+
+typedef enum { CSA_F32 = 0, CSA_BF16 = 1 } csa_dtype;
+
+/* Layer hyper-parameters. */
+typedef struct csa_params {
+    int32_t m;          /* compression rate: 1, 2, 4, 8, ..., 128            */
+    int32_t overlap;    /* 0: one branch (block i only); 1: two branches,   *
+                         * entry i also pools branch b of block i-1         */
+    int32_t top_k;      /* CSA selection budget k, 1 .. 2048                */
+    int32_t n_win;      /* window length, 0 .. 1024                         */
+    int32_t rope_dims;  /* r, even, 0 .. c                                  */
+    int32_t derotate;   /* 1: rotate the output's rotary dims by -t         */
+    double rope_theta;  /* RoPE base (> 1)                                  */
+    float scale;        /* attention logit scale; 0 means 1/sqrt(c)         */
+    int32_t reserved;   /* set to 0                                         */
+} csa_params;
+
+/* Supported sizes: c (main head dim) in {64, 128, 256, 512}; dI (indexer
+ * dim) in {32, 64, 128}; H (query heads) 1 .. 128; hI (indexer heads)
+ * 1 .. 64.  Anything else returns CSA_ERR_UNSUPPORTED. */
+
+/* Workspace bytes for the entry points that take one. */
+#define CSA_STATUS_BYTES 256
+
+const char *csa_last_error(void);   /* thread-local message of the last failure */
+const char *csa_version(void);
+
+/*
+ * Synchronise `stream`, read the status word at the start of `ws`, clear it
+ * and return CSA_OK, CSA_ERR_DEVICE or CSA_ERR_TIMEOUT.
+ */
+csa_status csa_stream_status(void *ws, void *stream);
+
+/* Zero the status word of a fresh workspace (enqueued on stream). */
+csa_status csa_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Per-stage device timing, for profiling.  While enabled, every entry point
+ * records a CUDA event before and after each kernel stage it enqueues (on
+ * the call's stream).  csa_timing_read() waits for the recorded events, adds
+ * their elapsed milliseconds and launch counts per stage into ms[s] and
+ * launches[s] for s < nstages (either may be NULL), and forgets them.  Do
+ * not enable it while a stream is being captured into a CUDA graph.
+ */
+typedef enum {
+    CSA_STAGE_COMPRESS = 0,
+    CSA_STAGE_INDEXER = 1,
+    CSA_STAGE_TOPK = 2,
+    CSA_STAGE_SPARSE_ATTN = 3,
+    CSA_STAGE_HCA_ATTN = 4,
+    CSA_NUM_STAGES = 5
+} csa_stage;
+csa_status csa_timing_enable(int32_t on);
+csa_status csa_timing_read(double *ms, int64_t *launches, int32_t nstages);
+
+/* --------------------------------------------------------------------- */
+/* 1. Compression.                                                        */
+/* --------------------------------------------------------------------- */
+/*
+ * ["DeepSeek-V4: Making Million-Token Context an Architectural Problem",
+ * Key design 1 (two-branch CSA equation) and Key design 2 (HCA equation);
+ * DeepSeek-V4 book ch.5 "One weight distribution per coordinate", "Which
+ * positions enter a compressed block"; "DeepSeek-V4" explainer: "every m
+ * consecutive tokens".]
+ *
+ * For each sequence b, block i < n/m and channel ch:
+ *   a_s = Z[b, m*i+s, ch] + bias[s, ch]            (s < m)
+ *   overlap = 1 also: b_s = Zb[b, m*(i-1)+s, ch] + biasb[s, ch]
+ *                     (for i = 0: logit -inf, content 0)
+ *   entry = sum softmax(a, b)_s * content_s   (content C, and Cb for b_s)
+ * then RoPE at position (i+1)*m-1 on the last rope_dims dims, rounded to
+ * dtype.  Trailing tokens that do not fill a block produce no entry.
+ *
+ *   C, Z       [B, n, c]  dtype      Cb, Zb [B, n, c] (overlap = 1 only)
+ *   bias       [m, c]     float32    biasb  [m, c]    (overlap = 1 only)
+ *   out        [B, n/m, c] dtype     compressed entries (stored, rotated)
+ *   raw_out    [B, n, c]  dtype or NULL: the raw rows C rotated at their
+ *              own positions, i.e. the stored rows a window reads
+ * Uses params->m, overlap, rope_dims, rope_theta.
+ */
+csa_status csa_compress(csa_dtype dtype, int64_t B, int64_t n, int32_t c,
+                        const void *C, const void *Z, const float *bias,
+                        const void *Cb, const void *Zb, const float *biasb,
+                        void *out, void *raw_out,
+                        const csa_params *params, void *stream);
+
+/* --------------------------------------------------------------------- */
+/* 2. Indexer scores and top-k.                                           */
+/* --------------------------------------------------------------------- */
+/*
+ * [Key design 1 index-score equation; book ch.6 "The index score".]
+ *   scores[b,t,j] = sum_h w[b,t,h] * ReLU(qI[b,t,h,:] . kI[b,j,:])
+ * for visible j ((j+1)*m <= q_pos[b,t]+1), -inf otherwise.  No RoPE, no scale.
+ *   qI [B, T, hI, dI] dtype;  w [B, T, hI] float32;  kI [B, E, dI] dtype;
+ *   q_pos [B, T] int64;  scores [B, T, E] float32.
+ * ws: at least indexer_score_ws_size() bytes (status word).
+ */
+size_t indexer_score_ws_size(void);
+csa_status indexer_score(csa_dtype dtype, int64_t B, int64_t T, int32_t hI, int32_t dI,
+                         int64_t E, int32_t m,
+                         const void *qI, const float *w, const void *kI,
+                         const int64_t *q_pos, float *scores,
+                         void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * [Key design 1, C_t = TopK_k(I[t,:]); book ch.6 "Top-k is a budget over
+ * compressed entries".]  Per query: if at most k entries are visible, all
+ * are kept; otherwise the k best by (score descending, index ascending),
+ * -0.0 equal to +0.0.  idx [B, T, k] int32 holds the kept indices in
+ * ascending order, padded with -1; cnt [B, T] int32 the number kept.
+ * scores [B, T, E] float32 (entries beyond the visible prefix are ignored).
+ */
+size_t topk_select_ws_size(int64_t B, int64_t T, int64_t E, int32_t k);
+csa_status topk_select(int64_t B, int64_t T, int64_t E, int32_t k, int32_t m,
+                       const float *scores, const int64_t *q_pos,
+                       int32_t *idx, int32_t *cnt,
+                       void *ws, size_t ws_bytes, void *stream);
+
+/* --------------------------------------------------------------------- */
+/* 3. Core attention.                                                     */
+/* --------------------------------------------------------------------- */
+/*
+ * [book ch.6 "Shared key-value MQA"; ch.7 "The sliding window", "Partial
+ * rotary position embeddings", "Why the output is de-rotated", "Attention
+ * sinks".]  For query t of sequence b and head h, over the set S of
+ * compressed entries (sparse_attn: idx[b,t,:] >= 0; hca_attn: every visible
+ * entry) and the window rows W:
+ *   q~ = RoPE(q[b,t,h], t);  l_u = scale * (q~ . u)  for u in S and W
+ *   out[b,t,h] = sum e^l_u u / (e^sink[h] + sum e^l_u)
+ *   derotate:  out[rotary dims] = RoPE(out, -t)[rotary dims]
+ *   lse[b,t,h] = log(e^sink[h] + sum e^l_u)          (lse may be NULL)
+ * Entries serve as both key and value (K = V).
+ *   q [B, T, H, c];  kvc [B, E, c] stored entries;  idx [B, T, k] int32;
+ *   kv_raw [B, L, c] stored raw rows;  raw_pos0 [B] int64;  sink [H] f32;
+ *   out [B, T, H, c] dtype;  lse [B, T, H] float32 or NULL.
+ * Uses params->m, n_win, rope_dims, rope_theta, scale, derotate.
+ */
+size_t attn_ws_size(csa_dtype dtype, int64_t B, int64_t T, int32_t H, int32_t c,
+                    int64_t E, int32_t k, const csa_params *params);
+csa_status sparse_attn(csa_dtype dtype, int64_t B, int64_t T, int32_t H, int32_t c,
+                       int64_t E, int32_t k, int64_t L,
+                       const void *q, const int64_t *q_pos, const void *kvc,
+                       const int32_t *idx, const void *kv_raw, const int64_t *raw_pos0,
+                       const float *sink, void *out, float *lse,
+                       const csa_params *params, void *ws, size_t ws_bytes, void *stream);
+csa_status hca_attn(csa_dtype dtype, int64_t B, int64_t T, int32_t H, int32_t c,
+                    int64_t E, int64_t L,
+                    const void *q, const int64_t *q_pos, const void *kvc,
+                    const void *kv_raw, const int64_t *raw_pos0,
+                    const float *sink, void *out, float *lse,
+                    const csa_params *params, void *ws, size_t ws_bytes, void *stream);
+
+/* --------------------------------------------------------------------- */
+/* 4. Fused layer entry points (one stream, graph-capturable).            */
+/* --------------------------------------------------------------------- */
+/*
+ * CSA prefill of B sequences of n tokens, query t at position t:
+ *   csa_compress(C, Z, bias[, Cb, Zb, biasb]) -> kvc (+ rotated raw rows)
+ *   csa_compress(Ck, Zk, biask[, Ckb, Zkb, biaskb]) -> kIc   (no RoPE)
+ *   indexer_score -> topk_select -> sparse_attn -> out
+ *   C, Z [B,n,c]; Ck, Zk [B,n,dI]; bias [m,c]; biask [m,dI];
+ *   q [B,n,H,c]; qI [B,n,hI,dI]; w [B,n,hI] f32; sink [H] f32;
+ *   out [B,n,H,c]; idx_out [B,n,k] int32 or NULL (the selected indices).
+ */
+size_t csa_prefill_ws_size(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t c,
+                           int32_t hI, int32_t dI, const csa_params *params);
+csa_status csa_prefill(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t c,
+                       int32_t hI, int32_t dI,
+                       const void *C, const void *Z, const float *bias,
+                       const void *Cb, const void *Zb, const float *biasb,
+                       const void *Ck, const void *Zk, const float *biask,
+                       const void *Ckb, const void *Zkb, const float *biaskb,
+                       const void *q, const void *qI, const float *w, const float *sink,
+                       void *out, int32_t *idx_out,
+                       const csa_params *params, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * HCA prefill: csa_compress(C, Z, bias) with params->m (e.g. 128) ->
+ * hca_attn over every visible entry + window + sink.
+ */
+size_t hca_prefill_ws_size(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t c,
+                           const csa_params *params);
+csa_status hca_prefill(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t c,
+                       const void *C, const void *Z, const float *bias,
+                       const void *q, const float *sink, void *out,
+                       const csa_params *params, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * One decode step for B sequences, one query each at q_pos[b]:
+ *   CSA layer: indexer_score(qI, w, kIc) -> topk_select -> sparse_attn(q,
+ *   kvc, kv_raw, sink) -> out.
+ *   HCA layer (skipped when q2 == NULL): hca_attn(q2, kvc2, kv_raw2, sink2)
+ *   -> out2, with compression rate params2->m.
+ *   q [B,1,H,c]; qI [B,1,hI,dI]; w [B,1,hI]; kvc [B,E,c]; kIc [B,E,dI];
+ *   kv_raw [B,L,c]; raw_pos0 [B]; q2 [B,1,H,c]; kvc2 [B,E2,c];
+ *   kv_raw2 [B,L,c]; out, out2 [B,1,H,c]; idx_out [B,1,k] or NULL.
+ */
+size_t hybrid_decode_ws_size(csa_dtype dtype, int64_t B, int32_t H, int32_t c, int32_t hI,
+                             int32_t dI, int64_t E, int64_t E2,
+                             const csa_params *params, const csa_params *params2);
+csa_status hybrid_decode(csa_dtype dtype, int64_t B, int32_t H, int32_t c, int32_t hI,
+                         int32_t dI, int64_t E, int64_t E2, int64_t L,
+                         const void *q, const void *qI, const float *w,
+                         const void *kvc, const void *kIc, const void *kv_raw,
+                         const float *sink,
+                         const void *q2, const void *kvc2, const void *kv_raw2,
+                         const float *sink2,
+                         const int64_t *q_pos, const int64_t *raw_pos0,
+                         void *out, void *out2, int32_t *idx_out,
+                         const csa_params *params, const csa_params *params2,
+                         void *ws, size_t ws_bytes, void *stream);
+
+#if defined(__GNUC__)
+#pragma GCC visibility pop
+#endif
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA_H */

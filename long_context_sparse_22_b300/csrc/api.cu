@@ -1,0 +1,589 @@
+// C ABI of libcsa: argument validation, workspace layout and the launch
+// sequence of every entry point declared in include/csa.h.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace csa;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+csa_status fail(csa_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+csa_status cuda_fail(cudaError_t e, const char *where) {
+    return fail(CSA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+#define CSA_TRY_CUDA(call, where)                      \
+    do {                                               \
+        cudaError_t e_ = (call);                       \
+        if (e_ != cudaSuccess) return cuda_fail(e_, where); \
+    } while (0)
+
+#define CSA_TRY(call)                       \
+    do {                                    \
+        csa_status s_ = (call);             \
+        if (s_ != CSA_OK) return s_;        \
+    } while (0)
+
+bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+csa_status need_ptr(const void *p, const char *name) {
+    if (p == nullptr) return fail(CSA_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!al16(p)) return fail(CSA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+    return CSA_OK;
+}
+
+size_t esize(csa_dtype dt) { return dt == CSA_BF16 ? 2 : 4; }
+
+csa_status check_dtype(csa_dtype dt) {
+    if (dt != CSA_F32 && dt != CSA_BF16) return fail(CSA_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+    return CSA_OK;
+}
+
+csa_status check_c(int c) {
+    if (c != 64 && c != 128 && c != 256 && c != 512)
+        return fail(CSA_ERR_UNSUPPORTED, "head dim c=%d not in {64,128,256,512}", c);
+    return CSA_OK;
+}
+
+csa_status check_params(const csa_params *p, int c, bool attn) {
+    if (p == nullptr) return fail(CSA_ERR_INVALID_ARG, "params is NULL");
+    if (p->m < 1 || p->m > 1024) return fail(CSA_ERR_UNSUPPORTED, "compression rate m=%d not in 1..1024", p->m);
+    if (p->overlap != 0 && p->overlap != 1) return fail(CSA_ERR_INVALID_ARG, "overlap must be 0 or 1");
+    if (p->rope_dims < 0 || (p->rope_dims & 1) || p->rope_dims > c || p->rope_dims / 2 > MAX_ROPE_PAIRS)
+        return fail(CSA_ERR_UNSUPPORTED, "rope_dims=%d must be even and <= c", p->rope_dims);
+    if (p->rope_dims > 0 && !(p->rope_theta > 1.0)) return fail(CSA_ERR_INVALID_ARG, "rope_theta must be > 1");
+    if (attn) {
+        if (p->n_win < 0 || p->n_win > 1024) return fail(CSA_ERR_UNSUPPORTED, "n_win=%d not in 0..1024", p->n_win);
+        if (p->derotate != 0 && p->derotate != 1) return fail(CSA_ERR_INVALID_ARG, "derotate must be 0 or 1");
+        if (!(p->scale >= 0.f) || std::isinf(p->scale)) return fail(CSA_ERR_INVALID_ARG, "scale must be finite and >= 0");
+    }
+    return CSA_OK;
+}
+
+RopeFreqs make_rope(int c, int r, double theta) {
+    RopeFreqs rf;
+    memset(&rf, 0, sizeof rf);
+    rf.pairs = r / 2;
+    rf.first = c - r;
+    for (int i = 0; i < r / 2; i++) rf.w[i] = pow(theta, -2.0 * i / (double)r);
+    return rf;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Bump allocator over a caller-provided workspace.
+struct Carve {
+    char *base;
+    size_t off;
+    void *take(size_t bytes) {
+        void *p = base ? base + off : nullptr;
+        off = align256(off + bytes);
+        return p;
+    }
+};
+
+__global__ void iota_pos_kernel(int64_t *pos, int64_t B, int64_t n) {
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < B * n) pos[i] = i % n;
+}
+
+cudaError_t fill_positions(int64_t *pos, int64_t B, int64_t n, cudaStream_t st) {
+    if (B * n == 0) return cudaSuccess;
+    iota_pos_kernel<<<(unsigned)((B * n + 255) / 256), 256, 0, st>>>(pos, B, n);
+    return cudaGetLastError();
+}
+
+csa_status check_ws(void *ws, size_t ws_bytes, size_t need) {
+    if (ws == nullptr) return fail(CSA_ERR_WORKSPACE, "workspace is NULL (need %zu bytes)", need);
+    if (!al16(ws)) return fail(CSA_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+    if (ws_bytes < need) return fail(CSA_ERR_WORKSPACE, "workspace has %zu bytes, need %zu", ws_bytes, need);
+    return CSA_OK;
+}
+
+// ------------------------------------------------------------ stage timing
+
+struct StageTimer {
+    std::mutex mu;
+    int on = 0;
+    struct Pending { int stage; cudaEvent_t a, b; };
+    std::vector<cudaEvent_t> pool;
+    std::vector<Pending> pending;
+    double ms[CSA_NUM_STAGES] = {};
+    long long launches[CSA_NUM_STAGES] = {};
+};
+StageTimer g_timer;
+
+// Records an event pair around one stage when timing is enabled.
+struct StageScope {
+    int stage;
+    cudaStream_t st;
+    cudaEvent_t a = nullptr, b = nullptr;
+    StageScope(int s, cudaStream_t stream) : stage(s), st(stream) {
+        std::lock_guard<std::mutex> g(g_timer.mu);
+        if (!g_timer.on) return;
+        for (cudaEvent_t *e : {&a, &b}) {
+            if (!g_timer.pool.empty()) {
+                *e = g_timer.pool.back();
+                g_timer.pool.pop_back();
+            } else if (cudaEventCreate(e) != cudaSuccess) {
+                *e = nullptr;
+            }
+        }
+        if (a && b) cudaEventRecord(a, st);
+    }
+    ~StageScope() {
+        if (!a || !b) return;
+        cudaEventRecord(b, st);
+        std::lock_guard<std::mutex> g(g_timer.mu);
+        g_timer.pending.push_back({stage, a, b});
+    }
+};
+
+// --------------------------------------------------------------- launchers
+
+csa_status do_compress(csa_dtype dt, int64_t B, int64_t n, int c, const void *C, const void *Z,
+                       const float *bias, const void *Cb, const void *Zb, const float *biasb,
+                       void *out, void *raw_out, const csa_params *p, int rope_dims,
+                       cudaStream_t st) {
+    RopeFreqs rf = make_rope(c, rope_dims, p->rope_theta);
+    StageScope sc(CSA_STAGE_COMPRESS, st);
+    CSA_TRY_CUDA(launch_compress(dt, B, n, c, p->m, p->overlap, C, Z, bias, Cb, Zb, biasb, out,
+                                 raw_out, rf, st),
+                 "csa_compress launch");
+    return CSA_OK;
+}
+
+csa_status do_indexer(csa_dtype dt, int64_t B, int64_t T, int hI, int dI, int64_t E, int m,
+                      const void *qI, const float *w, const void *kI, const int64_t *q_pos,
+                      float *scores, int write_masked, unsigned *status, cudaStream_t st) {
+    (void)status;
+    StageScope sc(CSA_STAGE_INDEXER, st);
+    CSA_TRY_CUDA(launch_indexer_simt(dt, B, T, hI, dI, E, m, qI, w, kI, q_pos, scores,
+                                     write_masked, st),
+                 "indexer_score launch");
+    return CSA_OK;
+}
+
+csa_status do_topk(int64_t B, int64_t T, int64_t E, int k, int m, const float *scores,
+                   const int64_t *q_pos, int32_t *idx, int32_t *cnt, cudaStream_t st) {
+    StageScope sc(CSA_STAGE_TOPK, st);
+    CSA_TRY_CUDA(launch_topk(B, T, E, k, m, scores, q_pos, idx, cnt, st), "topk_select launch");
+    return CSA_OK;
+}
+
+csa_status do_attn(csa_dtype dt, int64_t B, int64_t T, int H, int c, int64_t E, int k, int64_t L,
+                   const void *q, const int64_t *q_pos, const void *kvc, const int32_t *idx,
+                   const void *kv_raw, const int64_t *raw_pos0, const float *sink, void *out,
+                   float *lse, const csa_params *p, unsigned *status, cudaStream_t st) {
+    AttnArgs a;
+    a.q = q; a.q_pos = q_pos; a.kvc = kvc; a.idx = idx; a.kv_raw = kv_raw; a.raw_pos0 = raw_pos0;
+    a.sink = sink; a.out = out; a.lse = lse; a.status = status;
+    a.Tq = T; a.H = H; a.c = c; a.E = E; a.k = k; a.L = L;
+    a.m = p->m; a.n_win = p->n_win; a.derotate = p->derotate;
+    a.scale = p->scale > 0.f ? p->scale : (float)(1.0 / sqrt((double)c));
+    a.rope = make_rope(c, p->rope_dims, p->rope_theta);
+    StageScope sc(idx ? CSA_STAGE_SPARSE_ATTN : CSA_STAGE_HCA_ATTN, st);
+    CSA_TRY_CUDA(launch_attn_simt(dt, B, a, st), "attention launch");
+    return CSA_OK;
+}
+
+csa_status check_attn_common(csa_dtype dt, int64_t B, int64_t T, int H, int c, int64_t E, int64_t L,
+                             const void *q, const int64_t *q_pos, const void *kvc, const void *kv_raw,
+                             const int64_t *raw_pos0, const float *sink, const void *out,
+                             const csa_params *p) {
+    CSA_TRY(check_dtype(dt));
+    CSA_TRY(check_c(c));
+    CSA_TRY(check_params(p, c, true));
+    if (B < 0 || T < 0 || E < 0 || L < 0) return fail(CSA_ERR_INVALID_ARG, "negative size");
+    if (H < 1 || H > 128) return fail(CSA_ERR_UNSUPPORTED, "H=%d not in 1..128", H);
+    if (B * T == 0) return CSA_OK;
+    CSA_TRY(need_ptr(q, "q"));
+    CSA_TRY(need_ptr(q_pos, "q_pos"));
+    CSA_TRY(need_ptr(sink, "sink"));
+    CSA_TRY(need_ptr(out, "out"));
+    if (E > 0) CSA_TRY(need_ptr(kvc, "kvc"));
+    if (p->n_win > 0) {
+        if (L <= 0) return fail(CSA_ERR_INVALID_ARG, "n_win > 0 needs raw rows (L > 0)");
+        CSA_TRY(need_ptr(kv_raw, "kv_raw"));
+        if (raw_pos0 == nullptr) return fail(CSA_ERR_INVALID_ARG, "raw_pos0 is NULL");
+    }
+    return CSA_OK;
+}
+
+}  // namespace
+
+// ====================================================================== ABI
+
+extern "C" {
+
+const char *csa_last_error(void) { return g_err; }
+
+const char *csa_version(void) { return "csa-b300 0.1 (sm_103a)"; }
+
+csa_status csa_timing_enable(int32_t on) {
+    std::lock_guard<std::mutex> g(g_timer.mu);
+    g_timer.on = on ? 1 : 0;
+    return CSA_OK;
+}
+
+csa_status csa_timing_read(double *ms, int64_t *launches, int32_t nstages) {
+    std::vector<StageTimer::Pending> pend;
+    {
+        std::lock_guard<std::mutex> g(g_timer.mu);
+        pend.swap(g_timer.pending);
+    }
+    double acc[CSA_NUM_STAGES] = {};
+    long long cnt[CSA_NUM_STAGES] = {};
+    cudaError_t err = cudaSuccess;
+    for (auto &p : pend) {
+        float t = 0.f;
+        cudaError_t e = cudaEventSynchronize(p.b);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&t, p.a, p.b);
+        if (e != cudaSuccess) err = e;
+        acc[p.stage] += t;
+        cnt[p.stage] += 1;
+    }
+    {
+        std::lock_guard<std::mutex> g(g_timer.mu);
+        for (auto &p : pend) {
+            g_timer.pool.push_back(p.a);
+            g_timer.pool.push_back(p.b);
+        }
+    }
+    for (int s = 0; s < nstages && s < CSA_NUM_STAGES; s++) {
+        if (ms) ms[s] = acc[s];
+        if (launches) launches[s] = cnt[s];
+    }
+    if (err != cudaSuccess) return cuda_fail(err, "timing read");
+    return CSA_OK;
+}
+
+csa_status csa_workspace_init(void *ws, size_t ws_bytes, void *stream) {
+    CSA_TRY(check_ws(ws, ws_bytes, CSA_STATUS_BYTES));
+    CSA_TRY_CUDA(cudaMemsetAsync(ws, 0, CSA_STATUS_BYTES, (cudaStream_t)stream), "workspace init");
+    return CSA_OK;
+}
+
+csa_status csa_stream_status(void *ws, void *stream) {
+    if (ws == nullptr) return fail(CSA_ERR_INVALID_ARG, "workspace is NULL");
+    CSA_TRY_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "stream synchronize");
+    unsigned word = 0;
+    CSA_TRY_CUDA(cudaMemcpy(&word, ws, sizeof word, cudaMemcpyDeviceToHost), "status read");
+    if (word == 0) return CSA_OK;
+    CSA_TRY_CUDA(cudaMemset(ws, 0, sizeof word), "status clear");
+    if (word & ST_TIMEOUT) return fail(CSA_ERR_TIMEOUT, "a bounded device wait ran out (status 0x%x)", word);
+    return fail(CSA_ERR_DEVICE, "device range check: %s%s(status 0x%x)",
+                (word & ST_BAD_INDEX) ? "selected index outside the cache; " : "",
+                (word & ST_NO_WINDOW_ROW) ? "window position missing from kv_raw; " : "", word);
+}
+
+csa_status csa_compress(csa_dtype dtype, int64_t B, int64_t n, int32_t c, const void *C,
+                        const void *Z, const float *bias, const void *Cb, const void *Zb,
+                        const float *biasb, void *out, void *raw_out, const csa_params *params,
+                        void *stream) {
+    CSA_TRY(check_dtype(dtype));
+    if (c < 8 || c % 8 != 0 || c > 4096) return fail(CSA_ERR_UNSUPPORTED, "c=%d must be a multiple of 8 in 8..4096", c);
+    CSA_TRY(check_params(params, c, false));
+    if (B < 0 || n < 0) return fail(CSA_ERR_INVALID_ARG, "negative size");
+    if (B * n == 0) return CSA_OK;
+    CSA_TRY(need_ptr(C, "C"));
+    CSA_TRY(need_ptr(Z, "Z"));
+    CSA_TRY(need_ptr(bias, "bias"));
+    if (params->overlap) {
+        CSA_TRY(need_ptr(Cb, "Cb"));
+        CSA_TRY(need_ptr(Zb, "Zb"));
+        CSA_TRY(need_ptr(biasb, "biasb"));
+    }
+    if (n / params->m > 0) CSA_TRY(need_ptr(out, "out"));
+    if (raw_out != nullptr && !al16(raw_out)) return fail(CSA_ERR_INVALID_ARG, "raw_out is not 16-byte aligned");
+    return do_compress(dtype, B, n, c, C, Z, bias, Cb, Zb, biasb, out, raw_out, params,
+                       params->rope_dims, (cudaStream_t)stream);
+}
+
+size_t indexer_score_ws_size(void) { return CSA_STATUS_BYTES; }
+
+csa_status indexer_score(csa_dtype dtype, int64_t B, int64_t T, int32_t hI, int32_t dI, int64_t E,
+                         int32_t m, const void *qI, const float *w, const void *kI,
+                         const int64_t *q_pos, float *scores, void *ws, size_t ws_bytes,
+                         void *stream) {
+    CSA_TRY(check_dtype(dtype));
+    if (B < 0 || T < 0 || E < 0) return fail(CSA_ERR_INVALID_ARG, "negative size");
+    if (hI < 1 || hI > 64) return fail(CSA_ERR_UNSUPPORTED, "hI=%d not in 1..64", hI);
+    if (dI != 32 && dI != 64 && dI != 128) return fail(CSA_ERR_UNSUPPORTED, "dI=%d not in {32,64,128}", dI);
+    if (m < 1) return fail(CSA_ERR_INVALID_ARG, "m must be >= 1");
+    if (E > 2147483647LL) return fail(CSA_ERR_UNSUPPORTED, "E too large");
+    CSA_TRY(check_ws(ws, ws_bytes, indexer_score_ws_size()));
+    if (B * T == 0 || E == 0) return CSA_OK;
+    CSA_TRY(need_ptr(qI, "qI"));
+    CSA_TRY(need_ptr(w, "w"));
+    CSA_TRY(need_ptr(kI, "kI"));
+    CSA_TRY(need_ptr(q_pos, "q_pos"));
+    CSA_TRY(need_ptr(scores, "scores"));
+    return do_indexer(dtype, B, T, hI, dI, E, m, qI, w, kI, q_pos, scores, 1, (unsigned *)ws,
+                      (cudaStream_t)stream);
+}
+
+size_t topk_select_ws_size(int64_t B, int64_t T, int64_t E, int32_t k) {
+    (void)B; (void)T; (void)E; (void)k;
+    return CSA_STATUS_BYTES;
+}
+
+csa_status topk_select(int64_t B, int64_t T, int64_t E, int32_t k, int32_t m, const float *scores,
+                       const int64_t *q_pos, int32_t *idx, int32_t *cnt, void *ws, size_t ws_bytes,
+                       void *stream) {
+    if (B < 0 || T < 0 || E < 0) return fail(CSA_ERR_INVALID_ARG, "negative size");
+    if (k < 1 || k > 2048) return fail(CSA_ERR_UNSUPPORTED, "k=%d not in 1..2048", k);
+    if (m < 1) return fail(CSA_ERR_INVALID_ARG, "m must be >= 1");
+    if (E > 2147483647LL) return fail(CSA_ERR_UNSUPPORTED, "E too large");
+    CSA_TRY(check_ws(ws, ws_bytes, topk_select_ws_size(B, T, E, k)));
+    if (B * T == 0) return CSA_OK;
+    if (E > 0) CSA_TRY(need_ptr(scores, "scores"));
+    CSA_TRY(need_ptr(q_pos, "q_pos"));
+    CSA_TRY(need_ptr(idx, "idx"));
+    CSA_TRY(need_ptr(cnt, "cnt"));
+    return do_topk(B, T, E, k, m, scores, q_pos, idx, cnt, (cudaStream_t)stream);
+}
+
+size_t attn_ws_size(csa_dtype dtype, int64_t B, int64_t T, int32_t H, int32_t c, int64_t E,
+                    int32_t k, const csa_params *params) {
+    (void)dtype; (void)B; (void)T; (void)H; (void)c; (void)E; (void)k; (void)params;
+    return CSA_STATUS_BYTES;
+}
+
+csa_status sparse_attn(csa_dtype dtype, int64_t B, int64_t T, int32_t H, int32_t c, int64_t E,
+                       int32_t k, int64_t L, const void *q, const int64_t *q_pos, const void *kvc,
+                       const int32_t *idx, const void *kv_raw, const int64_t *raw_pos0,
+                       const float *sink, void *out, float *lse, const csa_params *params,
+                       void *ws, size_t ws_bytes, void *stream) {
+    CSA_TRY(check_attn_common(dtype, B, T, H, c, E, L, q, q_pos, kvc, kv_raw, raw_pos0, sink, out,
+                              params));
+    if (k < 1 || k > 2048) return fail(CSA_ERR_UNSUPPORTED, "k=%d not in 1..2048", k);
+    CSA_TRY(check_ws(ws, ws_bytes, attn_ws_size(dtype, B, T, H, c, E, k, params)));
+    if (B * T == 0) return CSA_OK;
+    CSA_TRY(need_ptr(idx, "idx"));
+    if (lse != nullptr && !al16(lse)) return fail(CSA_ERR_INVALID_ARG, "lse is not 16-byte aligned");
+    return do_attn(dtype, B, T, H, c, E, k, L, q, q_pos, kvc, idx, kv_raw, raw_pos0, sink, out, lse,
+                   params, (unsigned *)ws, (cudaStream_t)stream);
+}
+
+csa_status hca_attn(csa_dtype dtype, int64_t B, int64_t T, int32_t H, int32_t c, int64_t E,
+                    int64_t L, const void *q, const int64_t *q_pos, const void *kvc,
+                    const void *kv_raw, const int64_t *raw_pos0, const float *sink, void *out,
+                    float *lse, const csa_params *params, void *ws, size_t ws_bytes, void *stream) {
+    CSA_TRY(check_attn_common(dtype, B, T, H, c, E, L, q, q_pos, kvc, kv_raw, raw_pos0, sink, out,
+                              params));
+    CSA_TRY(check_ws(ws, ws_bytes, attn_ws_size(dtype, B, T, H, c, E, 0, params)));
+    if (B * T == 0) return CSA_OK;
+    if (lse != nullptr && !al16(lse)) return fail(CSA_ERR_INVALID_ARG, "lse is not 16-byte aligned");
+    return do_attn(dtype, B, T, H, c, E, 0, L, q, q_pos, kvc, nullptr, kv_raw, raw_pos0, sink, out,
+                   lse, params, (unsigned *)ws, (cudaStream_t)stream);
+}
+
+// ------------------------------------------------------------ fused: CSA prefill
+
+static size_t csa_prefill_layout(Carve &cv, csa_dtype dt, int64_t B, int64_t n, int c, int dI,
+                                 const csa_params *p, void **pos, void **rp0, void **kvc,
+                                 void **kic, void **raw, void **sc, void **idx, void **cnt) {
+    const int64_t E = n / p->m;
+    cv.take(CSA_STATUS_BYTES);
+    *pos = cv.take((size_t)B * n * 8);
+    *rp0 = cv.take((size_t)B * 8);
+    *kvc = cv.take((size_t)B * E * c * esize(dt));
+    *kic = cv.take((size_t)B * E * dI * esize(dt));
+    *raw = cv.take((size_t)B * n * c * esize(dt));
+    *sc = cv.take((size_t)B * n * E * 4);
+    *idx = cv.take((size_t)B * n * p->top_k * 4);
+    *cnt = cv.take((size_t)B * n * 4);
+    return cv.off;
+}
+
+size_t csa_prefill_ws_size(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t c, int32_t hI,
+                           int32_t dI, const csa_params *params) {
+    (void)H; (void)hI;
+    if (params == nullptr || params->m < 1 || B < 0 || n < 0) return 0;
+    Carve cv{nullptr, 0};
+    void *a, *b, *d, *e, *f, *g, *h, *i;
+    return csa_prefill_layout(cv, dtype, B, n, c, dI, params, &a, &b, &d, &e, &f, &g, &h, &i);
+}
+
+csa_status csa_prefill(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t c, int32_t hI,
+                       int32_t dI, const void *C, const void *Z, const float *bias, const void *Cb,
+                       const void *Zb, const float *biasb, const void *Ck, const void *Zk,
+                       const float *biask, const void *Ckb, const void *Zkb, const float *biaskb,
+                       const void *q, const void *qI, const float *w, const float *sink, void *out,
+                       int32_t *idx_out, const csa_params *params, void *ws, size_t ws_bytes,
+                       void *stream) {
+    CSA_TRY(check_dtype(dtype));
+    CSA_TRY(check_c(c));
+    CSA_TRY(check_params(params, c, true));
+    if (B < 0 || n < 0) return fail(CSA_ERR_INVALID_ARG, "negative size");
+    if (H < 1 || H > 128) return fail(CSA_ERR_UNSUPPORTED, "H=%d not in 1..128", H);
+    if (hI < 1 || hI > 64) return fail(CSA_ERR_UNSUPPORTED, "hI=%d not in 1..64", hI);
+    if (dI != 32 && dI != 64 && dI != 128) return fail(CSA_ERR_UNSUPPORTED, "dI=%d not in {32,64,128}", dI);
+    if (params->top_k < 1 || params->top_k > 2048) return fail(CSA_ERR_UNSUPPORTED, "top_k=%d not in 1..2048", params->top_k);
+    CSA_TRY(check_ws(ws, ws_bytes, csa_prefill_ws_size(dtype, B, n, H, c, hI, dI, params)));
+    if (B * n == 0) return CSA_OK;
+    const char *names[] = {"C", "Z", "bias", "Ck", "Zk", "biask", "q", "qI", "w", "sink", "out"};
+    const void *ptrs[] = {C, Z, bias, Ck, Zk, biask, q, qI, w, sink, out};
+    for (int i = 0; i < 11; i++) CSA_TRY(need_ptr(ptrs[i], names[i]));
+    if (params->overlap) {
+        const char *nb[] = {"Cb", "Zb", "biasb", "Ckb", "Zkb", "biaskb"};
+        const void *pb[] = {Cb, Zb, biasb, Ckb, Zkb, biaskb};
+        for (int i = 0; i < 6; i++) CSA_TRY(need_ptr(pb[i], nb[i]));
+    }
+    if (idx_out != nullptr && !al16(idx_out)) return fail(CSA_ERR_INVALID_ARG, "idx_out is not 16-byte aligned");
+    cudaStream_t st = (cudaStream_t)stream;
+    Carve cv{(char *)ws, 0};
+    void *pos, *rp0, *kvc, *kic, *raw, *sc, *idx, *cnt;
+    csa_prefill_layout(cv, dtype, B, n, c, dI, params, &pos, &rp0, &kvc, &kic, &raw, &sc, &idx, &cnt);
+    if (idx_out) idx = idx_out;
+    const int64_t E = n / params->m;
+    unsigned *status = (unsigned *)ws;
+    CSA_TRY_CUDA(fill_positions((int64_t *)pos, B, n, st), "positions");
+    CSA_TRY_CUDA(cudaMemsetAsync(rp0, 0, (size_t)B * 8, st), "raw_pos0");
+    CSA_TRY(do_compress(dtype, B, n, c, C, Z, bias, Cb, Zb, biasb, kvc, raw, params,
+                        params->rope_dims, st));
+    CSA_TRY(do_compress(dtype, B, n, dI, Ck, Zk, biask, Ckb, Zkb, biaskb, kic, nullptr, params, 0, st));
+    CSA_TRY(do_indexer(dtype, B, n, hI, dI, E, params->m, qI, w, kic, (const int64_t *)pos,
+                       (float *)sc, 0, status, st));
+    CSA_TRY(do_topk(B, n, E, params->top_k, params->m, (const float *)sc, (const int64_t *)pos,
+                    (int32_t *)idx, (int32_t *)cnt, st));
+    return do_attn(dtype, B, n, H, c, E, params->top_k, n, q, (const int64_t *)pos, kvc,
+                   (const int32_t *)idx, raw, (const int64_t *)rp0, sink, out, nullptr, params,
+                   status, st);
+}
+
+// ------------------------------------------------------------ fused: HCA prefill
+
+static size_t hca_prefill_layout(Carve &cv, csa_dtype dt, int64_t B, int64_t n, int c,
+                                 const csa_params *p, void **pos, void **rp0, void **kvc,
+                                 void **raw) {
+    const int64_t E = n / p->m;
+    cv.take(CSA_STATUS_BYTES);
+    *pos = cv.take((size_t)B * n * 8);
+    *rp0 = cv.take((size_t)B * 8);
+    *kvc = cv.take((size_t)B * E * c * esize(dt));
+    *raw = cv.take((size_t)B * n * c * esize(dt));
+    return cv.off;
+}
+
+size_t hca_prefill_ws_size(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t c,
+                           const csa_params *params) {
+    (void)H;
+    if (params == nullptr || params->m < 1 || B < 0 || n < 0) return 0;
+    Carve cv{nullptr, 0};
+    void *a, *b, *d, *e;
+    return hca_prefill_layout(cv, dtype, B, n, c, params, &a, &b, &d, &e);
+}
+
+csa_status hca_prefill(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t c, const void *C,
+                       const void *Z, const float *bias, const void *q, const float *sink,
+                       void *out, const csa_params *params, void *ws, size_t ws_bytes,
+                       void *stream) {
+    CSA_TRY(check_dtype(dtype));
+    CSA_TRY(check_c(c));
+    CSA_TRY(check_params(params, c, true));
+    if (params->overlap) return fail(CSA_ERR_UNSUPPORTED, "HCA compression has one branch (overlap = 0)");
+    if (B < 0 || n < 0) return fail(CSA_ERR_INVALID_ARG, "negative size");
+    if (H < 1 || H > 128) return fail(CSA_ERR_UNSUPPORTED, "H=%d not in 1..128", H);
+    CSA_TRY(check_ws(ws, ws_bytes, hca_prefill_ws_size(dtype, B, n, H, c, params)));
+    if (B * n == 0) return CSA_OK;
+    const char *names[] = {"C", "Z", "bias", "q", "sink", "out"};
+    const void *ptrs[] = {C, Z, bias, q, sink, out};
+    for (int i = 0; i < 6; i++) CSA_TRY(need_ptr(ptrs[i], names[i]));
+    cudaStream_t st = (cudaStream_t)stream;
+    Carve cv{(char *)ws, 0};
+    void *pos, *rp0, *kvc, *raw;
+    hca_prefill_layout(cv, dtype, B, n, c, params, &pos, &rp0, &kvc, &raw);
+    const int64_t E = n / params->m;
+    CSA_TRY_CUDA(fill_positions((int64_t *)pos, B, n, st), "positions");
+    CSA_TRY_CUDA(cudaMemsetAsync(rp0, 0, (size_t)B * 8, st), "raw_pos0");
+    CSA_TRY(do_compress(dtype, B, n, c, C, Z, bias, nullptr, nullptr, nullptr, kvc, raw, params,
+                        params->rope_dims, st));
+    return do_attn(dtype, B, n, H, c, E, 0, n, q, (const int64_t *)pos, kvc, nullptr, raw,
+                   (const int64_t *)rp0, sink, out, nullptr, params, (unsigned *)ws, st);
+}
+
+// ------------------------------------------------------------ fused: decode
+
+static size_t decode_layout(Carve &cv, int64_t B, int64_t E, int k, void **sc, void **idx,
+                            void **cnt) {
+    cv.take(CSA_STATUS_BYTES);
+    *sc = cv.take((size_t)B * E * 4);
+    *idx = cv.take((size_t)B * k * 4);
+    *cnt = cv.take((size_t)B * 4);
+    return cv.off;
+}
+
+size_t hybrid_decode_ws_size(csa_dtype dtype, int64_t B, int32_t H, int32_t c, int32_t hI,
+                             int32_t dI, int64_t E, int64_t E2, const csa_params *params,
+                             const csa_params *params2) {
+    (void)dtype; (void)H; (void)c; (void)hI; (void)dI; (void)E2; (void)params2;
+    if (params == nullptr || B < 0 || E < 0) return 0;
+    Carve cv{nullptr, 0};
+    void *a, *b, *d;
+    return decode_layout(cv, B, E, params->top_k, &a, &b, &d);
+}
+
+csa_status hybrid_decode(csa_dtype dtype, int64_t B, int32_t H, int32_t c, int32_t hI, int32_t dI,
+                         int64_t E, int64_t E2, int64_t L, const void *q, const void *qI,
+                         const float *w, const void *kvc, const void *kIc, const void *kv_raw,
+                         const float *sink, const void *q2, const void *kvc2, const void *kv_raw2,
+                         const float *sink2, const int64_t *q_pos, const int64_t *raw_pos0,
+                         void *out, void *out2, int32_t *idx_out, const csa_params *params,
+                         const csa_params *params2, void *ws, size_t ws_bytes, void *stream) {
+    CSA_TRY(check_attn_common(dtype, B, 1, H, c, E, L, q, q_pos, kvc, kv_raw, raw_pos0, sink, out,
+                              params));
+    if (hI < 1 || hI > 64) return fail(CSA_ERR_UNSUPPORTED, "hI=%d not in 1..64", hI);
+    if (dI != 32 && dI != 64 && dI != 128) return fail(CSA_ERR_UNSUPPORTED, "dI=%d not in {32,64,128}", dI);
+    if (params->top_k < 1 || params->top_k > 2048) return fail(CSA_ERR_UNSUPPORTED, "top_k=%d not in 1..2048", params->top_k);
+    if (E > 2147483647LL) return fail(CSA_ERR_UNSUPPORTED, "E too large");
+    const bool hca = q2 != nullptr;
+    if (hca) {
+        CSA_TRY(check_attn_common(dtype, B, 1, H, c, E2, L, q2, q_pos, kvc2, kv_raw2, raw_pos0,
+                                  sink2, out2, params2));
+    }
+    CSA_TRY(check_ws(ws, ws_bytes, hybrid_decode_ws_size(dtype, B, H, c, hI, dI, E, E2, params,
+                                                         params2)));
+    if (B == 0) return CSA_OK;
+    if (E > 0) {
+        CSA_TRY(need_ptr(qI, "qI"));
+        CSA_TRY(need_ptr(w, "w"));
+        CSA_TRY(need_ptr(kIc, "kIc"));
+    }
+    if (idx_out != nullptr && !al16(idx_out)) return fail(CSA_ERR_INVALID_ARG, "idx_out is not 16-byte aligned");
+    cudaStream_t st = (cudaStream_t)stream;
+    Carve cv{(char *)ws, 0};
+    void *sc, *idx, *cnt;
+    decode_layout(cv, B, E, params->top_k, &sc, &idx, &cnt);
+    if (idx_out) idx = idx_out;
+    unsigned *status = (unsigned *)ws;
+    CSA_TRY(do_indexer(dtype, B, 1, hI, dI, E, params->m, qI, w, kIc, q_pos, (float *)sc, 0,
+                       status, st));
+    CSA_TRY(do_topk(B, 1, E, params->top_k, params->m, (const float *)sc, q_pos, (int32_t *)idx,
+                    (int32_t *)cnt, st));
+    CSA_TRY(do_attn(dtype, B, 1, H, c, E, params->top_k, L, q, q_pos, kvc, (const int32_t *)idx,
+                    kv_raw, raw_pos0, sink, out, nullptr, params, status, st));
+    if (hca)
+        CSA_TRY(do_attn(dtype, B, 1, H, c, E2, 0, L, q2, q_pos, kvc2, nullptr, kv_raw2, raw_pos0,
+                        sink2, out2, nullptr, params2, status, st));
+    return CSA_OK;
+}
+
+}  // extern "C"

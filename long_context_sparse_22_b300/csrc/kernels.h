@@ -1,0 +1,47 @@
+// Internal launcher declarations of libcsa (not part of the C ABI).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/csa.h"
+#include "common.cuh"
+
+namespace csa {
+
+struct AttnArgs {
+    const void *q;
+    const int64_t *q_pos;
+    const void *kvc;
+    const int32_t *idx;   // nullptr: every visible entry (HCA)
+    const void *kv_raw;
+    const int64_t *raw_pos0;
+    const float *sink;
+    void *out;
+    float *lse;
+    unsigned *status;
+    int64_t Tq;
+    int H, c;
+    int64_t E;
+    int k;
+    int64_t L;
+    int m, n_win, derotate;
+    float scale;
+    RopeFreqs rope;
+};
+
+cudaError_t launch_compress(csa_dtype dt, int64_t B, int64_t n, int c, int m, int overlap,
+                            const void *C, const void *Z, const float *bias, const void *Cb,
+                            const void *Zb, const float *biasb, void *out, void *raw_out,
+                            const RopeFreqs &rope, cudaStream_t st);
+
+cudaError_t launch_indexer_simt(csa_dtype dt, int64_t B, int64_t Tq, int hI, int dI, int64_t E,
+                                int m, const void *qI, const float *w, const void *kI,
+                                const int64_t *q_pos, float *scores, int write_masked,
+                                cudaStream_t st);
+
+cudaError_t launch_topk(int64_t B, int64_t Tq, int64_t E, int k, int m, const float *scores,
+                        const int64_t *q_pos, int32_t *idx, int32_t *cnt, cudaStream_t st);
+
+cudaError_t launch_attn_simt(csa_dtype dt, int64_t B, const AttnArgs &a, cudaStream_t st);
+
+}  // namespace csa

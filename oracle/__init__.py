@@ -189,50 +189,70 @@ def _bf16_bits_exact(a: np.ndarray) -> np.ndarray:
     return (f.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
 
 
+def csa_prefill_prepare(s: dict, x: dict, b: int = 0) -> dict:
+    """CSA layer, the per-sequence part: compressed KV (rotated at each block's
+    last position), compressed indexer keys (no RoPE) and the stored raw rows
+    (rotated at their positions), each rounded to the storage dtype."""
+    dt, m, r, th = s["dtype"], s["m"], s["rope_dims"], s["theta"]
+    ov = s.get("overlap", 0)
+    kvc = compress(x["C"][b], x["Z"][b], x["bias"], m, overlap=ov,
+                   Cb=x["Cb"][b] if ov else None, Zb=x["Zb"][b] if ov else None,
+                   biasb=x.get("biasb"), rope_dims=r, theta=th, out_dtype=dt)
+    kIc = compress(x["Ck"][b], x["Zk"][b], x["biask"], m, overlap=ov,
+                   Cb=x["Ckb"][b] if ov else None, Zb=x["Zkb"][b] if ov else None,
+                   biasb=x.get("biaskb"), rope_dims=0, out_dtype=dt)
+    raw = rope_rows(x["C"][b], 0, r, th, dt)
+    return dict(kvc=kvc, kIc=kIc, raw=raw, kvc_s=_storage(kvc, dt), kIc_s=_storage(kIc, dt),
+                raw_s=_storage(raw, dt))
+
+
+def csa_prefill_queries(s: dict, x: dict, prep: dict, b: int = 0, q_sel=None) -> dict:
+    """CSA layer, per query: index scores -> top-k -> attention."""
+    m, r, th = s["m"], s["rope_dims"], s["theta"]
+    qp = x["q_pos"][b] if q_sel is None else np.asarray(q_sel, np.int64)
+    sel = qp if q_sel is not None else slice(None)
+    sc = index_scores(x["qI"][b][sel], x["w"][b][sel], qp, prep["kIc_s"], m)
+    idx, cnt = topk(sc, qp, m, s["top_k"])
+    out = attend(x["q"][b][sel], qp, prep["kvc_s"], m, prep["raw_s"], 0, x["sink"], idx=idx,
+                 n_win=s["n_win"], rope_dims=r, theta=th, derotate=s.get("derotate", 1))
+    return dict(scores=sc, idx=idx, cnt=cnt, out=out)
+
+
 def csa_prefill_seq(s: dict, x: dict, b: int = 0, q_sel=None, return_steps=False):
     """CSA layer prefill for batch row b of a workload (spec s, inputs x).
     q_sel: optional array of query positions to evaluate (default all)."""
-    dt, m, r, th = s["dtype"], s["m"], s["rope_dims"], s["theta"]
-    ov = s.get("overlap", 0)
-    def g(key):
-        return x[key][b]
-
-    kvc = compress(g("C"), g("Z"), x["bias"], m, overlap=ov,
-                   Cb=x["Cb"][b] if ov else None, Zb=x["Zb"][b] if ov else None,
-                   biasb=x.get("biasb"), rope_dims=r, theta=th, out_dtype=dt)
-    kIc = compress(g("Ck"), g("Zk"), x["biask"], m, overlap=ov,
-                   Cb=x["Ckb"][b] if ov else None, Zb=x["Zkb"][b] if ov else None,
-                   biasb=x.get("biaskb"), rope_dims=0, out_dtype=dt)
-    raw = rope_rows(g("C"), 0, r, th, dt)
-    qp = x["q_pos"][b] if q_sel is None else np.asarray(q_sel, np.int64)
-    sel = qp if q_sel is not None else slice(None)
-    qI = g("qI")[sel]
-    w = g("w")[sel]
-    q = g("q")[sel]
-    kvc_s, kIc_s, raw_s = _storage(kvc, dt), _storage(kIc, dt), _storage(raw, dt)
-    sc = index_scores(qI, w, qp, kIc_s, m)
-    idx, cnt = topk(sc, qp, m, s["top_k"])
-    out = attend(q, qp, kvc_s, m, raw_s, 0, x["sink"], idx=idx, n_win=s["n_win"],
-                 rope_dims=r, theta=th, derotate=s.get("derotate", 1))
+    prep = csa_prefill_prepare(s, x, b)
+    res = csa_prefill_queries(s, x, prep, b, q_sel)
     if return_steps:
-        return dict(kvc=kvc, kIc=kIc, raw=raw, scores=sc, idx=idx, cnt=cnt, out=out)
-    return out
+        return dict(kvc=prep["kvc"], kIc=prep["kIc"], raw=prep["raw"], **res)
+    return res["out"]
 
 
-def hca_prefill_seq(s: dict, x: dict, b: int = 0, q_sel=None, suffix="", return_steps=False):
-    """HCA layer prefill for batch row b (suffix "2" = the HCA layer of a hybrid)."""
+def hca_prefill_prepare(s: dict, x: dict, b: int = 0, suffix="") -> dict:
     dt, r, th = s["dtype"], s["rope_dims"], s["theta"]
     m = s["m2"] if suffix else s["m"]
     kvc = compress(x["C" + suffix][b], x["Z" + suffix][b], x["bias" + suffix], m,
                    rope_dims=r, theta=th, out_dtype=dt)
     raw = rope_rows(x["C" + suffix][b], 0, r, th, dt)
+    return dict(kvc=kvc, raw=raw, kvc_s=_storage(kvc, dt), raw_s=_storage(raw, dt))
+
+
+def hca_prefill_queries(s: dict, x: dict, prep: dict, b: int = 0, q_sel=None, suffix=""):
+    r, th = s["rope_dims"], s["theta"]
+    m = s["m2"] if suffix else s["m"]
     qp = x["q_pos"][b] if q_sel is None else np.asarray(q_sel, np.int64)
     sel = qp if q_sel is not None else slice(None)
-    out = attend(x["q" + suffix][b][sel], qp, _storage(kvc, dt), m, _storage(raw, dt), 0,
-                 x["sink" + suffix], idx=None, n_win=s["n_win"], rope_dims=r, theta=th,
-                 derotate=s.get("derotate", 1))
+    return attend(x["q" + suffix][b][sel], qp, prep["kvc_s"], m, prep["raw_s"], 0,
+                  x["sink" + suffix], idx=None, n_win=s["n_win"], rope_dims=r, theta=th,
+                  derotate=s.get("derotate", 1))
+
+
+def hca_prefill_seq(s: dict, x: dict, b: int = 0, q_sel=None, suffix="", return_steps=False):
+    """HCA layer prefill for batch row b (suffix "2" = the HCA layer of a hybrid)."""
+    prep = hca_prefill_prepare(s, x, b, suffix)
+    out = hca_prefill_queries(s, x, prep, b, q_sel, suffix)
     if return_steps:
-        return dict(kvc=kvc, raw=raw, out=out)
+        return dict(kvc=prep["kvc"], raw=prep["raw"], out=out)
     return out
 
 

@@ -1,0 +1,106 @@
+"""CPU-only checks of the C ABI: the library builds and loads, exports every
+function include/csa.h declares, and rejects bad arguments before touching
+the GPU (these calls return from validation, so no device is needed)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "csa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def csa():
+    from long_context_sparse_22_b300 import build
+    build.build()
+    import long_context_sparse_22_b300 as m
+    m.lib()
+    return m
+
+
+def test_exports_every_declared_symbol(csa):
+    declared = _header_functions()
+    assert len(declared) >= 17, declared
+    L = csa.lib()
+    for name in declared:
+        assert hasattr(L, name), f"{name} declared in csa.h but not exported"
+    assert sorted(csa.exported_symbols()) == declared
+
+
+def test_version(csa):
+    assert b"sm_103a" in csa.lib().csa_version()
+
+
+def _err(csa, status):
+    assert status != 0
+    return csa.lib().csa_last_error().decode()
+
+
+def test_validation_rejects_before_launch(csa):
+    L = csa.lib()
+    p = csa.params(m=4, rope_dims=64)
+    fake = C.c_void_p(1 << 20)           # never dereferenced: validation fails first
+    # bad dtype
+    s = L.csa_compress(7, 1, 8, 64, fake, fake, fake, None, None, None, fake, None, C.byref(p), None)
+    assert s == 1 and "dtype" in _err(csa, s)
+    # unsupported head dim for attention
+    s = L.hca_attn(1, 1, 1, 16, 96, 4, 4, fake, fake, fake, fake, fake, fake, fake, None,
+                   C.byref(p), fake, 256, None)
+    assert s == 2 and "c=96" in _err(csa, s)
+    # misaligned pointer
+    s = L.csa_compress(1, 1, 8, 64, C.c_void_p((1 << 20) + 2), fake, fake, None, None, None, fake,
+                       None, C.byref(p), None)
+    assert s == 1 and "aligned" in _err(csa, s)
+    # odd rope dims
+    p_bad = csa.params(m=4, rope_dims=3)
+    s = L.csa_compress(1, 1, 8, 64, fake, fake, fake, None, None, None, fake, None, C.byref(p_bad), None)
+    assert s == 2 and "rope_dims" in _err(csa, s)
+    # k out of range
+    s = L.topk_select(1, 1, 10, 4096, 4, fake, fake, fake, fake, fake, 256, None)
+    assert s == 2 and "k=4096" in _err(csa, s)
+    # workspace missing / too small
+    s = L.topk_select(1, 1, 10, 4, 4, fake, fake, fake, fake, None, 0, None)
+    assert s == 3
+    s = L.indexer_score(1, 1, 1, 64, 128, 10, 4, fake, fake, fake, fake, fake, fake, 8, None)
+    assert s == 3 and "workspace" in _err(csa, s)
+    # unsupported indexer dim
+    s = L.indexer_score(1, 1, 1, 64, 96, 10, 4, fake, fake, fake, fake, fake, fake, 256, None)
+    assert s == 2
+    # null tensor
+    s = L.indexer_score(1, 1, 1, 64, 128, 10, 4, None, fake, fake, fake, fake, fake, 256, None)
+    assert s == 1 and "qI" in _err(csa, s)
+    # hca prefill refuses the two-branch compressor
+    p_ov = csa.params(m=128, overlap=1)
+    s = L.hca_prefill(1, 1, 256, 16, 128, fake, fake, fake, fake, fake, fake, C.byref(p_ov), fake,
+                      1 << 30, None)
+    assert s == 2
+
+
+def test_workspace_sizes(csa):
+    L = csa.lib()
+    p = csa.params(m=4, top_k=512)
+    n, c, dI = 65536, 512, 128
+    got = csa.csa_prefill_ws_size(1, 1, n, 64, c, 64, dI, p)
+    E = n // 4
+    floor = E * c * 2 + E * dI * 2 + n * c * 2 + n * E * 4 + n * 512 * 4
+    assert got >= floor and got < floor + (1 << 20)
+    assert L.indexer_score_ws_size() == 256
+    p2 = csa.params(m=128)
+    assert csa.hca_prefill_ws_size(1, 1, 8192, 16, 128, p2) >= 8192 * 128 * 2
+
+
+def test_no_cpu_fallback(csa):
+    """Without a CUDA device the binding raises rather than computing on the CPU."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(RuntimeError):
+        csa._stream()

@@ -1,0 +1,351 @@
+"""GPU parity: every C-ABI entry point against the fp64 oracle on the same
+seeded inputs, at sizes that span several tiles and a ragged tail, plus the
+five workloads (full size where the oracle can follow, sampled outputs where
+it cannot), edge cases, the device status word, determinism and batch
+invariance.  Tolerances are in tests/parity.py."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from parity import (check_close, compare_topk, dev, gap_rows, host)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def csa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import long_context_sparse_22_b300 as m
+    m.lib()
+    return m
+
+
+def _np_rng(seed):
+    return np.random.default_rng(seed)
+
+
+# ------------------------------------------------------------- compression
+
+@pytest.mark.parametrize("dtype,n,c,m,r,overlap,sc", [
+    ("f32", 2048, 64, 4, 32, 0, 1.0),
+    ("f32", 2046, 64, 4, 32, 1, 1.0),         # ragged tail, two branches
+    ("bf16", 1030, 512, 4, 64, 0, 1.0),
+    ("bf16", 1024, 128, 4, 0, 1, 1.0),        # indexer-key form, two branches
+    ("bf16", 8192 + 37, 128, 128, 64, 0, 128 ** -0.5),
+    ("f32", 300, 64, 1, 32, 0, 1.0),          # m = 1
+])
+def test_compress(csa, orc, dtype, n, c, m, r, overlap, sc):
+    B = 2
+    seed = 100 + n + m
+    C_ = synth.normal(seed, 1, (B, n, c), sc, dtype)
+    Z = synth.normal(seed, 2, (B, n, c), sc, dtype)
+    bias = synth.normal(seed, 3, (m, c), 0.1, "f32")
+    kw = {}
+    if overlap:
+        kw = dict(Cb=synth.normal(seed, 4, (B, n, c), sc, dtype),
+                  Zb=synth.normal(seed, 5, (B, n, c), sc, dtype),
+                  biasb=synth.normal(seed, 6, (m, c), 0.1, "f32"))
+    dkw = {k: dev(v) for k, v in kw.items()}
+    out, raw = csa.csa_compress(dev(C_), dev(Z), dev(bias), m=m, overlap=overlap, rope_dims=r,
+                                want_raw=True, **dkw)
+    torch.cuda.synchronize()
+    for b in range(B):
+        ref = orc.compress(C_[b], Z[b], bias, m, overlap=overlap,
+                           Cb=kw["Cb"][b] if overlap else None, Zb=kw["Zb"][b] if overlap else None,
+                           biasb=kw.get("biasb"), rope_dims=r, out_dtype=dtype)
+        g = host(out[b])
+        if dtype == "f32":
+            check_close(g, ref, "f32", "entries")
+        else:   # stored bf16 entries: at most one bf16 step apart
+            assert np.all(np.abs(g - ref) <= 2.0 ** -7 * np.abs(ref) + 1e-5), "entries"
+        rref = orc.rope_rows(C_[b], 0, r, 10000.0, dtype)
+        gr = host(raw[b])
+        if dtype == "f32":
+            check_close(gr, rref, "f32", "raw rows")
+        else:
+            assert np.all(np.abs(gr - rref) <= 2.0 ** -7 * np.abs(rref) + 1e-5), "raw rows"
+
+
+# ----------------------------------------------------------------- indexer
+
+@pytest.mark.parametrize("dtype,B,T,hI,dI,E,m,pos0", [
+    ("f32", 1, 2048, 4, 32, 512, 4, 0),
+    ("bf16", 2, 40, 64, 128, 2100, 4, 8000),
+    ("bf16", 3, 1, 64, 128, 5000, 4, 19999),      # decode shape
+    ("bf16", 1, 33, 16, 64, 300, 2, 500),
+])
+def test_indexer_score(csa, orc, dtype, B, T, hI, dI, E, m, pos0):
+    seed = 200 + T + E
+    qI = synth.normal(seed, 1, (B, T, hI, dI), 1.0, dtype)
+    kI = synth.normal(seed, 2, (B, E, dI), 1.0, dtype)
+    w = synth.softmax_normal(seed, 3, (B, T, hI))
+    w[..., ::3] *= -1.0                                # signs are unconstrained
+    pos = np.tile(pos0 + np.arange(T, dtype=np.int64) * (1 if T > 1 else 0), (B, 1))
+    if pos0 == 0:
+        pos = np.tile(np.arange(T, dtype=np.int64), (B, 1))
+    s = csa.indexer_score(dev(qI), dev(w), dev(kI), dev(pos), m)
+    g = host(s)
+    for b in range(B):
+        ref = orc.index_scores(qI[b], w[b], pos[b], kI[b], m)
+        fin = np.isfinite(ref)
+        assert np.array_equal(np.isfinite(g[b]), fin)
+        assert np.all(np.isneginf(g[b][~fin]))
+        scale = np.abs(ref[fin]).max() if fin.any() else 1.0
+        assert np.abs(g[b][fin] - ref[fin]).max() <= 2e-6 * scale
+
+
+# ------------------------------------------------------------------- top-k
+
+@pytest.mark.parametrize("B,T,E,k,m", [
+    (1, 300, 512, 64, 4),
+    (2, 5, 50000, 512, 1),        # beyond the shared-memory key cache
+    (3, 4, 40000, 1024, 1),
+    (1, 1, 262144, 1024, 4),
+])
+def test_topk_exact(csa, orc, B, T, E, k, m):
+    r = _np_rng(300 + E)
+    sc = (np.round(r.standard_normal((B, T, E)) * 8) / 8).astype(np.float32)   # many ties
+    sc[..., ::7] = 0.0
+    sc[..., 3::7] = -0.0
+    sc[..., 5::11] = np.float32(r.standard_normal()) * 1e-30
+    if T > 3:
+        pos = np.tile(np.linspace(0, (E - 1) * m + m - 1, T).astype(np.int64), (B, 1))
+        pos[:, 0] = max(0, k * m - 1 - m)      # k-1 visible
+        pos[:, 1] = k * m - 1                  # exactly k
+        pos[:, 2] = k * m + m - 1              # k+1
+        pos[:, 3] = 1 if m > 2 else 0          # nothing (m > 2) or 1 entry
+    else:
+        pos = np.full((B, T), E * m - 1, np.int64)
+    idx, cnt = csa.topk_select(dev(sc), dev(pos), m, k)
+    gi, gc = host(idx), host(cnt)
+    for b in range(B):
+        oi, oc = orc.topk(sc[b].astype(np.float64), pos[b], m, k)
+        np.testing.assert_array_equal(gc[b], oc)
+        np.testing.assert_array_equal(gi[b], oi)
+
+
+# --------------------------------------------------------------- attention
+
+@pytest.mark.parametrize("dtype,B,T,H,c,E,k,m,n_win,r,derot", [
+    ("f32", 1, 200, 4, 64, 60, 16, 4, 128, 32, 1),
+    ("bf16", 2, 3, 64, 512, 3000, 512, 4, 128, 64, 1),
+    ("bf16", 1, 17, 16, 128, 100, 8, 4, 5, 64, 0),
+])
+def test_sparse_attn(csa, orc, dtype, B, T, H, c, E, k, m, n_win, r, derot):
+    seed = 400 + E
+    q = synth.normal(seed, 1, (B, T, H, c), 1.0, dtype)
+    kvc = synth.normal(seed, 2, (B, E, c), 1.0, dtype)
+    t_last = E * m + 7
+    L = t_last + 1                                  # raw rows 0 .. t_last
+    kv_raw = synth.normal(seed, 3, (B, L, c), 1.0, dtype)
+    sink = synth.normal(seed, 4, (H,), 1.0, "f32")
+    pos = np.tile(t_last - T + 1 + np.arange(T, dtype=np.int64), (B, 1))
+    pos[:, 0] = 2                                   # an early query: few entries, short window
+    raw_pos0 = np.zeros(B, np.int64)
+    r_ = _np_rng(seed)
+    idx = np.full((B, T, k), -1, np.int32)
+    for b in range(B):
+        for t in range(T):
+            nv = min(E, (pos[b, t] + 1) // m)
+            kk = min(k, nv)
+            sel = np.sort(r_.choice(nv, kk, replace=False)) if kk else np.zeros(0, int)
+            idx[b, t, :kk] = sel
+    p = csa.params(m=m, top_k=k, n_win=n_win, rope_dims=r, derotate=derot)
+    lse = torch.empty((B, T, H), dtype=torch.float32, device="cuda")
+    out = csa.sparse_attn(dev(q), dev(pos), dev(kvc), dev(idx), dev(kv_raw), dev(raw_pos0),
+                          dev(sink), p, lse=lse)
+    g, gl = host(out), host(lse)
+    for b in range(B):
+        ro, rl = orc.attend(q[b], pos[b], kvc[b], m, kv_raw[b], int(raw_pos0[b]), sink, idx=idx[b],
+                            n_win=n_win, rope_dims=r, derotate=derot, want_lse=True)
+        check_close(g[b], ro, dtype, "sparse_attn out")
+        assert np.abs(gl[b] - rl).max() <= 1e-3
+
+
+@pytest.mark.parametrize("dtype,B,T,H,c,E,m,n_win,r", [
+    ("bf16", 1, 70, 16, 128, 64, 128, 128, 64),
+    ("bf16", 2, 1, 128, 512, 700, 128, 128, 64),
+    ("f32", 1, 40, 4, 64, 30, 4, 16, 32),
+])
+def test_hca_attn(csa, orc, dtype, B, T, H, c, E, m, n_win, r):
+    seed = 500 + E
+    q = synth.normal(seed, 1, (B, T, H, c), 1.0, dtype)
+    kvc = synth.normal(seed, 2, (B, E, c), 1.0, dtype)
+    t_last = E * m + m // 2
+    L = n_win + T
+    kv_raw = synth.normal(seed, 3, (B, L, c), 1.0, dtype)
+    sink = synth.normal(seed, 4, (H,), 1.0, "f32")
+    pos = np.tile(t_last - T + 1 + np.arange(T, dtype=np.int64), (B, 1))
+    raw_pos0 = np.full(B, t_last - L + 1, np.int64)
+    p = csa.params(m=m, n_win=n_win, rope_dims=r)
+    out = csa.hca_attn(dev(q), dev(pos), dev(kvc), dev(kv_raw), dev(raw_pos0), dev(sink), p)
+    g = host(out)
+    for b in range(B):
+        ro = orc.attend(q[b], pos[b], kvc[b], m, kv_raw[b], int(raw_pos0[b]), sink, idx=None,
+                        n_win=n_win, rope_dims=r)
+        check_close(g[b], ro, dtype, "hca_attn out")
+
+
+# ---------------------------------------------------------------- fused
+
+def _prefill_csa_gpu(csa, s, x, idx_out=True):
+    d = {k: dev(v) for k, v in x.items()}
+    p = csa.params(m=s["m"], overlap=s.get("overlap", 0), top_k=s["top_k"], n_win=s["n_win"],
+                   rope_dims=s["rope_dims"], rope_theta=s["theta"])
+    io = torch.empty((s["B"], s["n"], s["top_k"]), dtype=torch.int32, device="cuda") if idx_out else None
+    out = csa.csa_prefill(d["C"], d["Z"], d["bias"], d["Ck"], d["Zk"], d["biask"], d["q"], d["qI"],
+                          d["w"], d["sink"], p, Cb=d.get("Cb"), Zb=d.get("Zb"), biasb=d.get("biasb"),
+                          Ckb=d.get("Ckb"), Zkb=d.get("Zkb"), biaskb=d.get("biaskb"), idx_out=io)
+    return out, io
+
+
+def _check_csa_prefill(orc, s, x, out, io, q_sel=None):
+    dt = s["dtype"]
+    st = orc.csa_prefill_seq(s, x, 0, q_sel=q_sel, return_steps=True)
+    qp = np.arange(s["n"]) if q_sel is None else np.asarray(q_sel)
+    g_out = host(out[0])[qp]
+    g_idx = host(io[0])[qp]
+    differ = compare_topk(g_idx, st["idx"], st["scores"], qp, s["m"], s["top_k"])
+    ref = st["out"].copy()
+    if differ.size:       # below-gap rows: compare against the oracle on the GPU's set
+        kvc_s = orc._storage(st["kvc"], dt)
+        raw_s = orc._storage(st["raw"], dt)
+        ref[differ] = orc.attend(x["q"][0][qp[differ]], qp[differ], kvc_s, s["m"], raw_s, 0,
+                                 x["sink"], idx=g_idx[differ], n_win=s["n_win"],
+                                 rope_dims=s["rope_dims"], theta=s["theta"])
+    check_close(g_out, ref, dt, "csa_prefill out")
+    return differ.size
+
+
+def test_csa_prefill_cfg1_full(csa, orc):
+    """CSA single-layer prefill in fp32, n = 2048 (the whole workload)."""
+    s, x = synth.make_inputs("csa_prefill_f32")
+    out, io = _prefill_csa_gpu(csa, s, x)
+    _check_csa_prefill(orc, s, x, out, io)
+
+
+def test_csa_prefill_cfg1_overlap(csa, orc):
+    s, x = synth.make_inputs("csa_prefill_f32", n=1030, overlap=1)
+    out, io = _prefill_csa_gpu(csa, s, x)
+    _check_csa_prefill(orc, s, x, out, io)
+
+
+def test_csa_prefill_bf16_sampled(csa, orc):
+    """Flash-shaped CSA layer (H=64, c=512, hI=64, dI=128, k=512) at n=4100,
+    where the top-k binds for t >= 2048; oracle on sampled rows."""
+    s, x = synth.make_inputs("hybrid_prefill_flash", n=4100)
+    out, io = _prefill_csa_gpu(csa, s, x)
+    q_sel = np.unique(np.r_[0, 1, 2, 3, 4, 127, 128, 2043, 2047, 2048, 2051, 2052, 3000,
+                            _np_rng(5).integers(0, 4100, 24), 4095, 4099])
+    _check_csa_prefill(orc, s, x, out, io, q_sel)
+
+
+def test_hca_prefill_cfg2_full(csa, orc):
+    """HCA single-layer prefill in bf16, n = 8192 (the whole workload)."""
+    s, x = synth.make_inputs("hca_prefill_bf16")
+    d = {k: dev(v) for k, v in x.items()}
+    p = csa.params(m=s["m"], n_win=s["n_win"], rope_dims=s["rope_dims"], rope_theta=s["theta"])
+    out = csa.hca_prefill(d["C"], d["Z"], d["bias"], d["q"], d["sink"], p)
+    ref = orc.hca_prefill_seq(s, x, 0)
+    check_close(host(out[0]), ref, "bf16", "hca_prefill out")
+
+
+def _decode_gpu(csa, s, x, hca):
+    d = {k: dev(v) for k, v in x.items()}
+    p = csa.params(m=s["m"], top_k=s["top_k"], n_win=s["n_win"], rope_dims=s["rope_dims"],
+                   rope_theta=s["theta"])
+    p2 = csa.params(m=s.get("m2", 128), n_win=s["n_win"], rope_dims=s["rope_dims"],
+                    rope_theta=s["theta"])
+    io = torch.empty((s["B"], 1, s["top_k"]), dtype=torch.int32, device="cuda")
+    kw = dict(q2=d["q2"], kvc2=d["kvc2"], kv_raw2=d["kv_raw2"], sink2=d["sink2"], p2=p2) if hca else {}
+    res = csa.hybrid_decode(d["q"], d["qI"], d["w"], d["kvc"], d["kIc"], d["kv_raw"], d["sink"],
+                            d["q_pos"], d["raw_pos0"], p, idx_out=io, **kw)
+    return res, io
+
+
+def _check_decode(orc, s, x, res, io, seqs, hca):
+    out, out2 = (res if hca else (res, None))
+    for b in seqs:
+        st = orc.csa_decode_seq(s, x, b, return_steps=True)
+        gi = host(io[b])
+        differ = compare_topk(gi, st["idx"], st["scores"], x["q_pos"][b], s["m"], s["top_k"])
+        ref = st["out"]
+        if differ.size:
+            ref = orc.attend(x["q"][b], x["q_pos"][b], x["kvc"][b], s["m"], x["kv_raw"][b],
+                             int(x["raw_pos0"][b]), x["sink"], idx=gi, n_win=s["n_win"],
+                             rope_dims=s["rope_dims"], theta=s["theta"])
+        check_close(host(out[b]), ref, s["dtype"], f"decode out seq {b}")
+        if hca:
+            check_close(host(out2[b]), orc.hca_decode_seq(s, x, b), s["dtype"], f"hca out seq {b}")
+
+
+def test_decode_cfg3_flash(csa, orc):
+    """Flash-shaped CSA decode: B=32, 32768 entries each; oracle on 4 sequences."""
+    s, x = synth.make_inputs("csa_decode_flash")
+    res, io = _decode_gpu(csa, s, x, False)
+    _check_decode(orc, s, x, res, io, [0, 7, 19, 31], False)
+
+
+def test_decode_cfg5_pro(csa, orc):
+    """Pro-shaped hybrid decode at 1,048,576 positions: B=8; oracle on 2 sequences."""
+    s, x = synth.make_inputs("hybrid_decode_pro")
+    res, io = _decode_gpu(csa, s, x, True)
+    _check_decode(orc, s, x, res, io, [0, 5], True)
+
+
+def test_prefill_cfg4_flash_sampled(csa, orc):
+    """Flash-shaped interleaved CSA + HCA prefill at the full n = 65536, in the
+    launch configuration the bench times; oracle on sampled query rows."""
+    s, x = synth.make_inputs("hybrid_prefill_flash")
+    out, io = _prefill_csa_gpu(csa, s, x)
+    q_sel = np.array([0, 3, 4, 2047, 2048, 2051, 30000, 65535])
+    _check_csa_prefill(orc, s, x, out, io, q_sel)
+    d = {k: dev(v) for k, v in x.items() if k.endswith("2")}
+    p2 = csa.params(m=s["m2"], n_win=s["n_win"], rope_dims=s["rope_dims"], rope_theta=s["theta"])
+    out2 = csa.hca_prefill(d["C2"], d["Z2"], d["bias2"], d["q2"], d["sink2"], p2)
+    ref2 = orc.hca_prefill_seq(s, x, 0, q_sel=q_sel, suffix="2")
+    check_close(host(out2[0])[q_sel], ref2, "bf16", "hca layer out")
+
+
+# ------------------------------------------------- status word, determinism
+
+def test_status_word_reports_missing_window(csa):
+    B, T, H, c, E, m = 1, 1, 4, 64, 8, 4
+    q = torch.randn(B, T, H, c, device="cuda")
+    kvc = torch.randn(B, E, c, device="cuda")
+    kv_raw = torch.randn(B, 4, c, device="cuda")
+    pos = torch.tensor([[100]], device="cuda")
+    rp0 = torch.tensor([90], device="cuda")          # rows hold 90..93: window 0..100 not covered
+    sink = torch.zeros(H, device="cuda")
+    ws = csa.Workspace(4096)
+    p = csa.params(m=m, n_win=8, rope_dims=0)
+    csa.hca_attn(q, pos, kvc, kv_raw, rp0, sink, p, ws=ws)
+    with pytest.raises(csa.CsaError) as e:
+        ws.status()
+    assert e.value.status == 6
+    ws.status()                                     # cleared
+    idx = torch.tensor([[[0, 99, -1, -1]]], dtype=torch.int32, device="cuda")
+    rp0 = torch.tensor([97], device="cuda")
+    csa.sparse_attn(q, pos, kvc, idx, kv_raw, rp0, sink, csa.params(m=m, top_k=4, n_win=4, rope_dims=0), ws=ws)
+    with pytest.raises(csa.CsaError):
+        ws.status()
+
+
+def test_prefill_deterministic(csa):
+    s, x = synth.make_inputs("csa_prefill_f32", n=1024)
+    a, ia = _prefill_csa_gpu(csa, s, x)
+    b, ib = _prefill_csa_gpu(csa, s, x)
+    assert torch.equal(a, b) and torch.equal(ia, ib)
+
+
+def test_decode_batch_invariant(csa):
+    """A sequence decoded alone gives bitwise the same output as inside a batch."""
+    s, x = synth.make_inputs("csa_decode_flash", B=6, t=8191)
+    res, io = _decode_gpu(csa, s, x, False)
+    for b in (0, 4):
+        xb = {k: (v[b:b + 1] if k not in ("sink",) else v) for k, v in x.items()}
+        sb = dict(s, B=1)
+        rb, ib = _decode_gpu(csa, sb, xb, False)
+        assert torch.equal(rb[0], res[b]) and torch.equal(ib[0], io[b])
