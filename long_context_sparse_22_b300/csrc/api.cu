@@ -172,8 +172,12 @@ csa_status do_compress(csa_dtype dt, int64_t B, int64_t n, int c, const void *C,
 csa_status do_indexer(csa_dtype dt, int64_t B, int64_t T, int hI, int dI, int64_t E, int m,
                       const void *qI, const float *w, const void *kI, const int64_t *q_pos,
                       float *scores, int write_masked, unsigned *status, cudaStream_t st) {
-    (void)status;
     StageScope sc(CSA_STAGE_INDEXER, st);
+    if (dt == CSA_BF16 && indexer_tc_supported(hI, dI, B, T, E)) {
+        CSA_TRY_CUDA(launch_indexer_tc(B, T, E, m, qI, w, kI, q_pos, scores, write_masked, status, st),
+                     "indexer_score launch (tensor cores)");
+        return CSA_OK;
+    }
     CSA_TRY_CUDA(launch_indexer_simt(dt, B, T, hI, dI, E, m, qI, w, kI, q_pos, scores,
                                      write_masked, st),
                  "indexer_score launch");

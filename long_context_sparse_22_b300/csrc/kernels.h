@@ -39,6 +39,12 @@ cudaError_t launch_indexer_simt(csa_dtype dt, int64_t B, int64_t Tq, int hI, int
                                 const int64_t *q_pos, float *scores, int write_masked,
                                 cudaStream_t st);
 
+bool indexer_tc_supported(int hI, int dI, int64_t B, int64_t T, int64_t E);
+
+cudaError_t launch_indexer_tc(int64_t B, int64_t T, int64_t E, int m, const void *qI,
+                              const float *w, const void *kI, const int64_t *q_pos, float *scores,
+                              int write_masked, unsigned *status, cudaStream_t st);
+
 cudaError_t launch_topk(int64_t B, int64_t Tq, int64_t E, int k, int m, const float *scores,
                         const int64_t *q_pos, int32_t *idx, int32_t *cnt, cudaStream_t st);
 

@@ -1,0 +1,137 @@
+"""Small, self-contained launches of one stage each, sized for an ncu capture
+(inputs larger than L2 so DRAM counters mean something, a few GB at most).
+
+    python -m long_context_sparse_22_b300.profile_cases CASE [--reps R]
+
+Cases:
+  indexer_prefill   indexer_score, 16384 queries x 4096 entries, 64 x 128 (bf16)
+  indexer_decode    indexer_score, 8 sequences x 262144 entries, 1 query each (bf16)
+  topk_prefill      topk_select over [16384, 4096] fp32 scores, k = 512
+  topk_decode       topk_select over [8, 262144] fp32 scores, k = 1024
+  compress          csa_compress, n = 65536, c = 512, m = 4 (bf16, with raw rows)
+  sparse_attn       sparse_attn, 4096 queries, 64 heads x 512, k = 512 + window
+  hca_decode        hca_attn, 8 sequences x 8192 entries, 128 heads x 512
+  csa_prefill       csa_prefill, n = 16384, Flash shapes
+"""
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+import long_context_sparse_22_b300 as csa
+
+
+def _bf16(*shape, scale=1.0):
+    return (torch.randn(*shape, device="cuda") * scale).to(torch.bfloat16)
+
+
+def case_indexer(T, E, B, m=4):
+    qI = _bf16(B, T, 64, 128)
+    w = torch.softmax(torch.randn(B, T, 64, device="cuda"), -1)
+    kI = _bf16(B, E, 128)
+    if T == 1:
+        pos = torch.full((B, 1), E * m - 1, dtype=torch.int64, device="cuda")
+    else:
+        pos = (torch.arange(T, device="cuda") + (E * m - T)).repeat(B, 1)
+    scores = torch.empty(B, T, E, device="cuda")
+    return lambda: csa.indexer_score(qI, w, kI, pos, m, scores=scores)
+
+
+def case_topk(T, E, B, k, m=4):
+    sc = torch.randn(B, T, E, device="cuda")
+    if T == 1:
+        pos = torch.full((B, 1), E * m - 1, dtype=torch.int64, device="cuda")
+    else:
+        pos = (torch.arange(T, device="cuda") + (E * m - T)).repeat(B, 1)
+    idx = torch.empty(B, T, k, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(B, T, dtype=torch.int32, device="cuda")
+    return lambda: csa.topk_select(sc, pos, m, k, idx=idx, cnt=cnt)
+
+
+def case_compress():
+    n, c = 65536, 512
+    C, Z = _bf16(1, n, c), _bf16(1, n, c)
+    bias = torch.randn(4, c, device="cuda") * 0.1
+    out = torch.empty(1, n // 4, c, device="cuda", dtype=torch.bfloat16)
+    raw = torch.empty_like(C)
+    return lambda: csa.csa_compress(C, Z, bias, m=4, rope_dims=64, want_raw=True, out=out, raw_out=raw)
+
+
+def case_sparse_attn():
+    T, H, c, E, k, m = 4096, 64, 512, 16384, 512, 4
+    q = _bf16(1, T, H, c)
+    kvc = _bf16(1, E, c)
+    L = E * m
+    raw = _bf16(1, L, c)
+    pos = (torch.arange(T, device="cuda") + (L - T)).view(1, T)
+    idx = torch.sort(torch.stack([torch.randperm(E, device="cuda")[:k] for _ in range(T)]), -1)[0]
+    idx = idx.to(torch.int32).view(1, T, k).contiguous()
+    rp0 = torch.zeros(1, dtype=torch.int64, device="cuda")
+    sink = torch.randn(H, device="cuda")
+    out = torch.empty_like(q)
+    p = csa.params(m=m, top_k=k, n_win=128, rope_dims=64)
+    return lambda: csa.sparse_attn(q, pos, kvc, idx, raw, rp0, sink, p, out=out)
+
+
+def case_hca_decode():
+    B, H, c, E, m = 8, 128, 512, 8192, 128
+    t = E * m
+    q = _bf16(B, 1, H, c)
+    kvc = _bf16(B, E, c)
+    raw = _bf16(B, 128, c)
+    pos = torch.full((B, 1), t, dtype=torch.int64, device="cuda")
+    rp0 = torch.full((B,), t - 127, dtype=torch.int64, device="cuda")
+    sink = torch.randn(H, device="cuda")
+    out = torch.empty_like(q)
+    p = csa.params(m=m, n_win=128, rope_dims=64)
+    return lambda: csa.hca_attn(q, pos, kvc, raw, rp0, sink, p, out=out)
+
+
+def case_csa_prefill():
+    n, H, c = 16384, 64, 512
+    C, Z = _bf16(1, n, c), _bf16(1, n, c)
+    Ck, Zk = _bf16(1, n, 128), _bf16(1, n, 128)
+    bias = torch.randn(4, c, device="cuda") * 0.1
+    biask = torch.randn(4, 128, device="cuda") * 0.1
+    q, qI = _bf16(1, n, H, c), _bf16(1, n, 64, 128)
+    w = torch.softmax(torch.randn(1, n, 64, device="cuda"), -1)
+    sink = torch.randn(H, device="cuda")
+    out = torch.empty_like(q)
+    p = csa.params(m=4, top_k=512, n_win=128, rope_dims=64)
+    return lambda: csa.csa_prefill(C, Z, bias, Ck, Zk, biask, q, qI, w, sink, p, out=out)
+
+
+CASES = {
+    "indexer_prefill": lambda: case_indexer(16384, 4096, 1),
+    "indexer_decode": lambda: case_indexer(1, 262144, 8),
+    "topk_prefill": lambda: case_topk(16384, 4096, 1, 512),
+    "topk_decode": lambda: case_topk(1, 262144, 8, 1024),
+    "compress": case_compress,
+    "sparse_attn": case_sparse_attn,
+    "hca_decode": case_hca_decode,
+    "csa_prefill": case_csa_prefill,
+}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=sorted(CASES))
+    ap.add_argument("--reps", type=int, default=3)
+    args = ap.parse_args()
+    torch.manual_seed(0)
+    fn = CASES[args.case]()
+    for _ in range(args.reps):
+        fn()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev[0].record()
+    for _ in range(args.reps):
+        fn()
+    ev[1].record()
+    torch.cuda.synchronize()
+    print(f"{args.case}: {ev[0].elapsed_time(ev[1]) / args.reps:.3f} ms per call")
+
+
+if __name__ == "__main__":
+    main()
