@@ -185,9 +185,10 @@ csa_status do_indexer(csa_dtype dt, int64_t B, int64_t T, int hI, int dI, int64_
 }
 
 csa_status do_topk(int64_t B, int64_t T, int64_t E, int k, int m, const float *scores,
-                   const int64_t *q_pos, int32_t *idx, int32_t *cnt, cudaStream_t st) {
+                   const int64_t *q_pos, int32_t *idx, int32_t *cnt, void *scratch, cudaStream_t st) {
     StageScope sc(CSA_STAGE_TOPK, st);
-    CSA_TRY_CUDA(launch_topk(B, T, E, k, m, scores, q_pos, idx, cnt, st), "topk_select launch");
+    CSA_TRY_CUDA(launch_topk(B, T, E, k, m, scores, q_pos, idx, cnt, scratch, st),
+                 "topk_select launch");
     return CSA_OK;
 }
 
@@ -344,8 +345,9 @@ csa_status indexer_score(csa_dtype dtype, int64_t B, int64_t T, int32_t hI, int3
 }
 
 size_t topk_select_ws_size(int64_t B, int64_t T, int64_t E, int32_t k) {
-    (void)B; (void)T; (void)E; (void)k;
-    return CSA_STATUS_BYTES;
+    (void)k;
+    if (B < 0 || T < 0 || E < 0) return 0;
+    return CSA_STATUS_BYTES + topk_scratch_bytes(B * T, E);
 }
 
 csa_status topk_select(int64_t B, int64_t T, int64_t E, int32_t k, int32_t m, const float *scores,
@@ -361,7 +363,8 @@ csa_status topk_select(int64_t B, int64_t T, int64_t E, int32_t k, int32_t m, co
     CSA_TRY(need_ptr(q_pos, "q_pos"));
     CSA_TRY(need_ptr(idx, "idx"));
     CSA_TRY(need_ptr(cnt, "cnt"));
-    return do_topk(B, T, E, k, m, scores, q_pos, idx, cnt, (cudaStream_t)stream);
+    return do_topk(B, T, E, k, m, scores, q_pos, idx, cnt, (char *)ws + CSA_STATUS_BYTES,
+                   (cudaStream_t)stream);
 }
 
 size_t attn_ws_size(csa_dtype dtype, int64_t B, int64_t T, int32_t H, int32_t c, int64_t E,
@@ -403,7 +406,8 @@ csa_status hca_attn(csa_dtype dtype, int64_t B, int64_t T, int32_t H, int32_t c,
 
 static size_t csa_prefill_layout(Carve &cv, csa_dtype dt, int64_t B, int64_t n, int c, int dI,
                                  const csa_params *p, void **pos, void **rp0, void **kvc,
-                                 void **kic, void **raw, void **sc, void **idx, void **cnt) {
+                                 void **kic, void **raw, void **sc, void **idx, void **cnt,
+                                 void **tks) {
     const int64_t E = n / p->m;
     cv.take(CSA_STATUS_BYTES);
     *pos = cv.take((size_t)B * n * 8);
@@ -414,6 +418,7 @@ static size_t csa_prefill_layout(Carve &cv, csa_dtype dt, int64_t B, int64_t n, 
     *sc = cv.take((size_t)B * n * E * 4);
     *idx = cv.take((size_t)B * n * p->top_k * 4);
     *cnt = cv.take((size_t)B * n * 4);
+    *tks = cv.take(topk_scratch_bytes(B * n, E));
     return cv.off;
 }
 
@@ -422,8 +427,8 @@ size_t csa_prefill_ws_size(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int
     (void)H; (void)hI;
     if (params == nullptr || params->m < 1 || B < 0 || n < 0) return 0;
     Carve cv{nullptr, 0};
-    void *a, *b, *d, *e, *f, *g, *h, *i;
-    return csa_prefill_layout(cv, dtype, B, n, c, dI, params, &a, &b, &d, &e, &f, &g, &h, &i);
+    void *a, *b, *d, *e, *f, *g, *h, *i, *j;
+    return csa_prefill_layout(cv, dtype, B, n, c, dI, params, &a, &b, &d, &e, &f, &g, &h, &i, &j);
 }
 
 csa_status csa_prefill(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t c, int32_t hI,
@@ -454,8 +459,9 @@ csa_status csa_prefill(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t
     if (idx_out != nullptr && !al16(idx_out)) return fail(CSA_ERR_INVALID_ARG, "idx_out is not 16-byte aligned");
     cudaStream_t st = (cudaStream_t)stream;
     Carve cv{(char *)ws, 0};
-    void *pos, *rp0, *kvc, *kic, *raw, *sc, *idx, *cnt;
-    csa_prefill_layout(cv, dtype, B, n, c, dI, params, &pos, &rp0, &kvc, &kic, &raw, &sc, &idx, &cnt);
+    void *pos, *rp0, *kvc, *kic, *raw, *sc, *idx, *cnt, *tks;
+    csa_prefill_layout(cv, dtype, B, n, c, dI, params, &pos, &rp0, &kvc, &kic, &raw, &sc, &idx, &cnt,
+                       &tks);
     if (idx_out) idx = idx_out;
     const int64_t E = n / params->m;
     unsigned *status = (unsigned *)ws;
@@ -467,7 +473,7 @@ csa_status csa_prefill(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t
     CSA_TRY(do_indexer(dtype, B, n, hI, dI, E, params->m, qI, w, kic, (const int64_t *)pos,
                        (float *)sc, 0, status, st));
     CSA_TRY(do_topk(B, n, E, params->top_k, params->m, (const float *)sc, (const int64_t *)pos,
-                    (int32_t *)idx, (int32_t *)cnt, st));
+                    (int32_t *)idx, (int32_t *)cnt, tks, st));
     return do_attn(dtype, B, n, H, c, E, params->top_k, n, q, (const int64_t *)pos, kvc,
                    (const int32_t *)idx, raw, (const int64_t *)rp0, sink, out, nullptr, params,
                    status, st);
@@ -527,11 +533,12 @@ csa_status hca_prefill(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t
 // ------------------------------------------------------------ fused: decode
 
 static size_t decode_layout(Carve &cv, int64_t B, int64_t E, int k, void **sc, void **idx,
-                            void **cnt) {
+                            void **cnt, void **tks) {
     cv.take(CSA_STATUS_BYTES);
     *sc = cv.take((size_t)B * E * 4);
     *idx = cv.take((size_t)B * k * 4);
     *cnt = cv.take((size_t)B * 4);
+    *tks = cv.take(topk_scratch_bytes(B, E));
     return cv.off;
 }
 
@@ -541,8 +548,8 @@ size_t hybrid_decode_ws_size(csa_dtype dtype, int64_t B, int32_t H, int32_t c, i
     (void)dtype; (void)H; (void)c; (void)hI; (void)dI; (void)E2; (void)params2;
     if (params == nullptr || B < 0 || E < 0) return 0;
     Carve cv{nullptr, 0};
-    void *a, *b, *d;
-    return decode_layout(cv, B, E, params->top_k, &a, &b, &d);
+    void *a, *b, *d, *e;
+    return decode_layout(cv, B, E, params->top_k, &a, &b, &d, &e);
 }
 
 csa_status hybrid_decode(csa_dtype dtype, int64_t B, int32_t H, int32_t c, int32_t hI, int32_t dI,
@@ -574,14 +581,14 @@ csa_status hybrid_decode(csa_dtype dtype, int64_t B, int32_t H, int32_t c, int32
     if (idx_out != nullptr && !al16(idx_out)) return fail(CSA_ERR_INVALID_ARG, "idx_out is not 16-byte aligned");
     cudaStream_t st = (cudaStream_t)stream;
     Carve cv{(char *)ws, 0};
-    void *sc, *idx, *cnt;
-    decode_layout(cv, B, E, params->top_k, &sc, &idx, &cnt);
+    void *sc, *idx, *cnt, *tks;
+    decode_layout(cv, B, E, params->top_k, &sc, &idx, &cnt, &tks);
     if (idx_out) idx = idx_out;
     unsigned *status = (unsigned *)ws;
     CSA_TRY(do_indexer(dtype, B, 1, hI, dI, E, params->m, qI, w, kIc, q_pos, (float *)sc, 0,
                        status, st));
     CSA_TRY(do_topk(B, 1, E, params->top_k, params->m, (const float *)sc, q_pos, (int32_t *)idx,
-                    (int32_t *)cnt, st));
+                    (int32_t *)cnt, tks, st));
     CSA_TRY(do_attn(dtype, B, 1, H, c, E, params->top_k, L, q, q_pos, kvc, (const int32_t *)idx,
                     kv_raw, raw_pos0, sink, out, nullptr, params, status, st));
     if (hca)

@@ -308,6 +308,17 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
 }
 
+// Standalone scores are fully defined: every entry a query cannot see gets
+// -inf (the fused paths skip this; their selection reads the visible prefix).
+__global__ void mask_tail_kernel(float *scores, const int64_t *q_pos, int64_t rows, int64_t E, int m) {
+    const int64_t row = blockIdx.y + (int64_t)blockIdx.z * 65535;
+    if (row >= rows) return;
+    const int64_t nv = visible_count(q_pos[row], m, E);
+    for (int64_t j = nv + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < E;
+         j += (int64_t)gridDim.x * blockDim.x)
+        scores[row * E + j] = -INFINITY;
+}
+
 // ------------------------------------------------------------------- host
 
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -386,14 +397,21 @@ cudaError_t launch_indexer_tc(int64_t B, int64_t T, int64_t E, int m, const void
         !make_tmap_bf16_2d(&tk, kI, (uint64_t)(B * E), 128, 128))
         return cudaErrorInvalidValue;
     const int sms = num_sms();
+    cudaError_t e;
     if (decode) {
         long long tiles = (long long)B * T * a.tps;
         int grid = (int)(tiles < sms ? tiles : sms);
-        return launch_tc<1>(tq, tk, a, grid, st);
+        e = launch_tc<1>(tq, tk, a, grid, st);
+    } else {
+        long long items = (long long)B * a.nqb;
+        int grid = (int)(items < sms ? items : sms);
+        e = launch_tc<4>(tq, tk, a, grid, st);
     }
-    long long items = (long long)B * a.nqb;
-    int grid = (int)(items < sms ? items : sms);
-    return launch_tc<4>(tq, tk, a, grid, st);
+    if (e != cudaSuccess || !write_masked) return e;
+    const int64_t rows = B * T;
+    dim3 g(8, (unsigned)(rows < 65535 ? rows : 65535), (unsigned)((rows + 65534) / 65535));
+    mask_tail_kernel<<<g, 256, 0, st>>>(scores, q_pos, rows, E, m);
+    return cudaGetLastError();
 }
 
 }  // namespace csa

@@ -45,8 +45,12 @@ cudaError_t launch_indexer_tc(int64_t B, int64_t T, int64_t E, int m, const void
                               const float *w, const void *kI, const int64_t *q_pos, float *scores,
                               int write_masked, unsigned *status, cudaStream_t st);
 
+// scratch: topk_scratch_bytes(B*Tq, E) bytes of device memory (0 for the
+// one-CTA-per-row path, used for rows of at most 16384 entries or many rows)
+size_t topk_scratch_bytes(int64_t rows, int64_t E);
 cudaError_t launch_topk(int64_t B, int64_t Tq, int64_t E, int k, int m, const float *scores,
-                        const int64_t *q_pos, int32_t *idx, int32_t *cnt, cudaStream_t st);
+                        const int64_t *q_pos, int32_t *idx, int32_t *cnt, void *scratch,
+                        cudaStream_t st);
 
 cudaError_t launch_attn_simt(csa_dtype dt, int64_t B, const AttnArgs &a, cudaStream_t st);
 

@@ -1,16 +1,23 @@
-// Per-query top-k selection: block-level radix select in shared memory.
+// Per-query top-k selection: radix select on order-preserving score keys.
 //
 // ["DeepSeek-V4: Making Million-Token Context an Architectural Problem",
 // Key design 1, C_t = TopK_k(I[t,:]); DeepSeek-V4 book ch.6 "Top-k is a
 // budget over compressed entries": with at most k eligible entries, all are
 // kept.]  Ties go to the lower index.
 //
-// Scores are mapped to order-preserving uint32 keys (-0.0 folded onto +0.0).
-// Three histogram passes (11 + 11 + 10 bits) find the exact k-th largest key
-// tau and how many keys equal to tau must be taken; one ordered pass then
-// emits every index with key > tau plus the first (in index order) keys
-// equal to tau, in ascending index order, using block-wide prefix sums.
-// Keys are cached in shared memory when the visible prefix fits.
+// Scores map to uint32 keys that order like the floats (-0.0 folded onto
+// +0.0).  Three histogram passes (11 + 11 + 10 bits) find the exact k-th
+// largest key tau and how many keys equal to tau must be taken; one ordered
+// pass then emits every index with key > tau plus the first keys equal to
+// tau in index order, in ascending index order, using block-wide prefix sums.
+//
+// Many rows of at most a few ten-thousand entries (prefill): one CTA per row
+// with the row's keys cached in shared memory.
+// Few long rows (decode, up to 262144 entries): three launches spread each
+// row over many CTAs: (1) an 11-bit histogram of the keys, (2) each chunk
+// keeps, in index order, only the entries whose top bits reach the bin that
+// holds the k-th largest key, (3) one CTA per row runs the exact selection on
+// those candidates (a few thousand) in index order.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -46,14 +53,93 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *wsum, 
     return before + x - v;
 }
 
+struct TkShared {
+    uint32_t hist[2048];
+    uint32_t wsum[32];
+    uint32_t mirror[TK_THREADS];
+    uint32_t bin, above;
+};
+
+// Given a histogram of nb bins (nb a multiple of TK_THREADS), find the bin
+// holding the remaining-th largest key counting down from the top bin; sets
+// sh.bin and sh.above (the count in the bins above it).  All threads call.
+__device__ __forceinline__ void find_bin(TkShared &sh, int nb, uint32_t remaining) {
+    const int tid = threadIdx.x;
+    const int per = nb / TK_THREADS;
+    uint32_t mine = 0;
+    for (int i = 0; i < per; i++) mine += sh.hist[tid * per + i];
+    // above(t) = sum over threads t' > t: an exclusive prefix sum taken in
+    // mirrored thread order, then read back mirrored
+    sh.mirror[TK_THREADS - 1 - tid] = mine;
+    __syncthreads();
+    uint32_t tot;
+    const uint32_t ex = block_excl_scan(sh.mirror[tid], sh.wsum, &tot);
+    sh.mirror[tid] = ex;
+    __syncthreads();
+    uint32_t above = sh.mirror[TK_THREADS - 1 - tid];
+    __syncthreads();
+    for (int i = per - 1; i >= 0; i--) {
+        const int bin = tid * per + i;
+        const uint32_t h = sh.hist[bin];
+        if (above < remaining && above + h >= remaining) {
+            sh.bin = (uint32_t)bin;
+            sh.above = above;
+        }
+        above += h;
+    }
+    __syncthreads();
+}
+
+// Exact top-k over n > k items given in index order: key(i) is the item's
+// uint32 key, id(i) its output index.  Writes the k kept indices to orow in
+// the items' order.
+template <typename KeyF, typename IdF>
+__device__ void select_core(TkShared &sh, int64_t n, int k, KeyF key, IdF id, int32_t *orow) {
+    const int tid = threadIdx.x;
+    uint32_t prefix = 0, pmask = 0;
+    uint32_t remaining = (uint32_t)k;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; pass++) {
+        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+        const int nb = pass < 2 ? 2048 : 1024;
+        for (int i = tid; i < nb; i += TK_THREADS) sh.hist[i] = 0;
+        __syncthreads();
+        for (int64_t j = tid; j < n; j += TK_THREADS) {
+            const uint32_t kv = key(j);
+            if ((kv & pmask) == prefix) atomicAdd(&sh.hist[(kv >> shift) & (nb - 1)], 1u);
+        }
+        __syncthreads();
+        find_bin(sh, nb, remaining);
+        remaining -= sh.above;
+        prefix |= sh.bin << shift;
+        pmask |= (uint32_t)(nb - 1) << shift;
+        __syncthreads();
+    }
+    const uint32_t tau = prefix, need_eq = remaining;
+    uint32_t run_sel = 0, run_eq = 0;
+    for (int64_t base = 0; base < n && run_sel < (uint32_t)k; base += TK_THREADS) {
+        const int64_t j = base + tid;
+        const uint32_t kv = j < n ? key(j) : 0u;
+        const uint32_t gt = (j < n && kv > tau) ? 1u : 0u;
+        const uint32_t eq = (j < n && kv == tau) ? 1u : 0u;
+        uint32_t eq_tot, sel_tot;
+        const uint32_t eq_rank = run_eq + block_excl_scan(eq, sh.wsum, &eq_tot);
+        const uint32_t sel = (gt || (eq && eq_rank < need_eq)) ? 1u : 0u;
+        const uint32_t pos = run_sel + block_excl_scan(sel, sh.wsum, &sel_tot);
+        if (sel && pos < (uint32_t)k) orow[pos] = id(j);
+        run_eq += eq_tot;
+        run_sel += sel_tot;
+    }
+}
+
+// ----------------------------------------------------------- one CTA per row
+
 __global__ void __launch_bounds__(TK_THREADS)
 topk_kernel(const float *__restrict__ scores, const int64_t *__restrict__ q_pos,
             int32_t *__restrict__ idx, int32_t *__restrict__ cnt, int64_t E, int k, int m,
             int kcap) {
     extern __shared__ uint32_t smk[];   // cached keys [kcap]
-    __shared__ uint32_t hist[2048];
-    __shared__ uint32_t wsum[32];
-    __shared__ uint32_t s_bin, s_above;
+    __shared__ TkShared sh;
     const int tid = threadIdx.x;
     const int64_t row = blockIdx.x;
     const int64_t nv = visible_count(q_pos[row], m, E);
@@ -65,89 +151,197 @@ topk_kernel(const float *__restrict__ scores, const int64_t *__restrict__ q_pos,
         if (tid == 0) cnt[row] = (int32_t)nv;
         return;
     }
-    const bool cached = nv <= kcap;
-    if (cached) {
+    auto id = [](int64_t j) { return (int32_t)j; };
+    if (nv <= kcap) {
         for (int64_t j = tid; j < nv; j += TK_THREADS) smk[j] = score_key(__ldcs(srow + j));
         __syncthreads();
-    }
-    uint32_t prefix = 0, pmask = 0;
-    uint32_t remaining = (uint32_t)k;
-#pragma unroll 1
-    for (int pass = 0; pass < 3; pass++) {
-        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-        const int nb = pass < 2 ? 2048 : 1024;
-        for (int i = tid; i < nb; i += TK_THREADS) hist[i] = 0;
-        __syncthreads();
-        for (int64_t j = tid; j < nv; j += TK_THREADS) {
-            uint32_t key = cached ? smk[j] : score_key(srow[j]);
-            if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
-        }
-        __syncthreads();
-        // thread t owns bins [t*per, (t+1)*per); count of keys above its bins
-        const int per = nb / TK_THREADS;
-        uint32_t mine = 0;
-        for (int i = 0; i < per; i++) mine += hist[tid * per + i];
-        // above(t) = sum over threads t' > t of mine(t'): an exclusive prefix
-        // sum taken in mirrored thread order, then read back mirrored
-        uint32_t tot;
-        __shared__ uint32_t mirror[TK_THREADS];
-        mirror[TK_THREADS - 1 - tid] = mine;
-        __syncthreads();
-        uint32_t mv = mirror[tid];
-        uint32_t ex = block_excl_scan(mv, wsum, &tot);
-        mirror[tid] = ex;           // = above-count of thread TK_THREADS-1-tid
-        __syncthreads();
-        uint32_t above = mirror[TK_THREADS - 1 - tid];
-        __syncthreads();
-        for (int i = per - 1; i >= 0; i--) {
-            const int bin = tid * per + i;
-            const uint32_t h = hist[bin];
-            if (above < remaining && above + h >= remaining) {
-                s_bin = (uint32_t)bin;
-                s_above = above;
-            }
-            above += h;
-        }
-        __syncthreads();
-        remaining -= s_above;
-        prefix |= s_bin << shift;
-        pmask |= (uint32_t)(nb - 1) << shift;
-        __syncthreads();
-    }
-    const uint32_t tau = prefix;
-    const uint32_t need_eq = remaining;
-    uint32_t run_sel = 0, run_eq = 0;
-    for (int64_t base = 0; base < nv && run_sel < (uint32_t)k; base += TK_THREADS) {
-        const int64_t j = base + tid;
-        const uint32_t key = j < nv ? (cached ? smk[j] : score_key(srow[j])) : 0u;
-        const uint32_t gt = (j < nv && key > tau) ? 1u : 0u;
-        const uint32_t eq = (j < nv && key == tau) ? 1u : 0u;
-        uint32_t eq_tot, sel_tot;
-        const uint32_t eq_rank = run_eq + block_excl_scan(eq, wsum, &eq_tot);
-        const uint32_t sel = (gt || (eq && eq_rank < need_eq)) ? 1u : 0u;
-        const uint32_t pos = run_sel + block_excl_scan(sel, wsum, &sel_tot);
-        if (sel && pos < (uint32_t)k) orow[pos] = (int32_t)j;
-        run_eq += eq_tot;
-        run_sel += sel_tot;
+        select_core(sh, nv, k, [&](int64_t j) { return smk[j]; }, id, orow);
+    } else {
+        select_core(sh, nv, k, [&](int64_t j) { return score_key(srow[j]); }, id, orow);
     }
     if (tid == 0) cnt[row] = k;
 }
 
+// ------------------------------------------------------- few long rows (decode)
+
+struct TkLong {
+    const float *scores;
+    const int64_t *q_pos;
+    uint32_t *hist;        // [rows][2048], zeroed before the histogram pass
+    uint32_t *chunk_cnt;   // [rows][CH]
+    uint32_t *cand_key;    // [rows][E]: chunk c's candidates at [c*CS, ...)
+    int32_t *cand_idx;     // [rows][E]
+    int32_t *idx;          // [rows][k]
+    int32_t *cnt;          // [rows]
+    int64_t E, CS;         // CS: chunk size
+    int CH, k, m;
+};
+
+__global__ void __launch_bounds__(TK_THREADS) topk_hist_kernel(TkLong a) {
+    __shared__ uint32_t h[2048];
+    const int64_t row = blockIdx.y;
+    const int64_t nv = visible_count(a.q_pos[row], a.m, a.E);
+    if (nv <= a.k) return;
+    for (int i = threadIdx.x; i < 2048; i += TK_THREADS) h[i] = 0;
+    __syncthreads();
+    const int64_t c0 = (int64_t)blockIdx.x * a.CS;
+    const int64_t c1 = c0 + a.CS < nv ? c0 + a.CS : nv;
+    const float *s = a.scores + row * a.E;
+    for (int64_t j = c0 + threadIdx.x; j < c1; j += TK_THREADS) atomicAdd(&h[score_key(s[j]) >> 21], 1u);
+    __syncthreads();
+    uint32_t *g = a.hist + row * 2048;
+    for (int i = threadIdx.x; i < 2048; i += TK_THREADS)
+        if (h[i]) atomicAdd(&g[i], h[i]);
+}
+
+__global__ void __launch_bounds__(TK_THREADS) topk_gather_kernel(TkLong a) {
+    __shared__ TkShared sh;
+    const int64_t row = blockIdx.y;
+    const int64_t nv = visible_count(a.q_pos[row], a.m, a.E);
+    if (nv <= a.k) return;
+    for (int i = threadIdx.x; i < 2048; i += TK_THREADS) sh.hist[i] = a.hist[row * 2048 + i];
+    __syncthreads();
+    find_bin(sh, 2048, (uint32_t)a.k);
+    const uint32_t bstar = sh.bin;
+    const int64_t c0 = (int64_t)blockIdx.x * a.CS;
+    const int64_t c1 = c0 + a.CS < nv ? c0 + a.CS : nv;
+    const float *s = a.scores + row * a.E;
+    uint32_t *ok = a.cand_key + row * a.E + c0;
+    int32_t *oi = a.cand_idx + row * a.E + c0;
+    uint32_t run = 0;
+    for (int64_t base = c0; base < c1; base += TK_THREADS) {
+        const int64_t j = base + threadIdx.x;
+        const uint32_t kv = j < c1 ? score_key(s[j]) : 0u;
+        const uint32_t keep = (j < c1 && (kv >> 21) >= bstar) ? 1u : 0u;
+        uint32_t tot;
+        const uint32_t pos = run + block_excl_scan(keep, sh.wsum, &tot);
+        if (keep) {
+            ok[pos] = kv;
+            oi[pos] = (int32_t)j;
+        }
+        run += tot;
+    }
+    if (threadIdx.x == 0) a.chunk_cnt[row * a.CH + blockIdx.x] = run;
+}
+
+__global__ void __launch_bounds__(TK_THREADS) topk_final_kernel(TkLong a, int cap) {
+    extern __shared__ uint32_t smc[];   // [cap] keys, then [cap] indices
+    __shared__ TkShared sh;
+    __shared__ uint32_t offs[257];
+    const int tid = threadIdx.x;
+    const int64_t row = blockIdx.x;
+    const int64_t nv = visible_count(a.q_pos[row], a.m, a.E);
+    int32_t *orow = a.idx + row * (int64_t)a.k;
+    if (nv <= a.k) {
+        for (int i = tid; i < a.k; i += TK_THREADS) orow[i] = i < nv ? i : -1;
+        if (tid == 0) a.cnt[row] = (int32_t)nv;
+        return;
+    }
+    if (tid == 0) {
+        uint32_t o = 0;
+        for (int c = 0; c < a.CH; c++) {
+            offs[c] = o;
+            o += a.chunk_cnt[row * a.CH + c];
+        }
+        offs[a.CH] = o;
+    }
+    __syncthreads();
+    const int64_t n = offs[a.CH];
+    const uint32_t *gk = a.cand_key + row * a.E;
+    const int32_t *gi = a.cand_idx + row * a.E;
+    if (n <= cap) {
+        // the chunks' candidates, in index order, packed into shared memory
+        int32_t *si = (int32_t *)(smc + cap);
+        for (int c = 0; c < a.CH; c++) {
+            const uint32_t o = offs[c], nc = offs[c + 1] - offs[c];
+            for (uint32_t i = tid; i < nc; i += TK_THREADS) {
+                smc[o + i] = gk[c * a.CS + i];
+                si[o + i] = gi[c * a.CS + i];
+            }
+        }
+        __syncthreads();
+        select_core(sh, n, a.k, [&](int64_t j) { return smc[j]; }, [&](int64_t j) { return si[j]; },
+                    orow);
+    } else {
+        // many candidates (heavy ties): read them in place, chunk by chunk
+        auto where = [&](int64_t j) {
+            int c = 0;
+            while (c + 1 < a.CH && (int64_t)offs[c + 1] <= j) c++;
+            return c * a.CS + (j - offs[c]);
+        };
+        select_core(sh, n, a.k, [&](int64_t j) { return gk[where(j)]; },
+                    [&](int64_t j) { return gi[where(j)]; }, orow);
+    }
+    if (tid == 0) a.cnt[row] = a.k;
+}
+
+// -------------------------------------------------------------------- host
+
 static int g_topk_smem_set = 0;
+static int g_final_smem_set = 0;
+constexpr int KCAP_MAX = 40960;      // keys cached per row (160 KB)
+constexpr int CAND_CAP = 24576;      // candidates cached per row (192 KB)
+
+bool topk_use_long(int64_t rows, int64_t E) { return rows < 256 && E > 16384; }
+
+int topk_chunks(int64_t rows, int64_t E) {
+    int64_t ch = (296 + rows - 1) / rows;
+    const int64_t maxch = (E + 4095) / 4096;
+    if (ch > maxch) ch = maxch;
+    if (ch > 256) ch = 256;
+    return ch < 1 ? 1 : (int)ch;
+}
+
+static size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t topk_scratch_bytes(int64_t rows, int64_t E) {
+    if (!topk_use_long(rows, E)) return 0;
+    const int ch = topk_chunks(rows, E);
+    return a256((size_t)rows * 2048 * 4) + a256((size_t)rows * ch * 4) + 2 * a256((size_t)rows * E * 4);
+}
 
 cudaError_t launch_topk(int64_t B, int64_t Tq, int64_t E, int k, int m, const float *scores,
-                        const int64_t *q_pos, int32_t *idx, int32_t *cnt, cudaStream_t st) {
-    if (B * Tq == 0) return cudaSuccess;
-    const int kcap_max = 40960;   // 160 KB of cached keys
-    int kcap = (int)(E < kcap_max ? E : kcap_max);
-    size_t smem = (size_t)kcap * 4;
+                        const int64_t *q_pos, int32_t *idx, int32_t *cnt, void *scratch,
+                        cudaStream_t st) {
+    const int64_t rows = B * Tq;
+    if (rows == 0) return cudaSuccess;
+    if (topk_use_long(rows, E)) {
+        if (scratch == nullptr) return cudaErrorInvalidValue;
+        TkLong a;
+        const int ch = topk_chunks(rows, E);
+        char *p = (char *)scratch;
+        a.hist = (uint32_t *)p;
+        p += a256((size_t)rows * 2048 * 4);
+        a.chunk_cnt = (uint32_t *)p;
+        p += a256((size_t)rows * ch * 4);
+        a.cand_key = (uint32_t *)p;
+        p += a256((size_t)rows * E * 4);
+        a.cand_idx = (int32_t *)p;
+        a.scores = scores; a.q_pos = q_pos; a.idx = idx; a.cnt = cnt;
+        a.E = E; a.CH = ch; a.CS = (E + ch - 1) / ch; a.k = k; a.m = m;
+        cudaError_t e = cudaMemsetAsync(a.hist, 0, (size_t)rows * 2048 * 4, st);
+        if (e != cudaSuccess) return e;
+        dim3 g((unsigned)ch, (unsigned)rows);
+        topk_hist_kernel<<<g, TK_THREADS, 0, st>>>(a);
+        topk_gather_kernel<<<g, TK_THREADS, 0, st>>>(a);
+        if (!g_final_smem_set) {
+            e = cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     CAND_CAP * 8);
+            if (e != cudaSuccess) return e;
+            g_final_smem_set = 1;
+        }
+        topk_final_kernel<<<(unsigned)rows, TK_THREADS, CAND_CAP * 8, st>>>(a, CAND_CAP);
+        return cudaGetLastError();
+    }
+    const int kcap = (int)(E < KCAP_MAX ? E : KCAP_MAX);
+    const size_t smem = (size_t)kcap * 4;
     if (!g_topk_smem_set) {
         cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kcap_max * 4);
+                                             KCAP_MAX * 4);
         if (e != cudaSuccess) return e;
         g_topk_smem_set = 1;
     }
-    topk_kernel<<<(unsigned)(B * Tq), TK_THREADS, smem, st>>>(scores, q_pos, idx, cnt, E, k, m, kcap);
+    topk_kernel<<<(unsigned)rows, TK_THREADS, smem, st>>>(scores, q_pos, idx, cnt, E, k, m, kcap);
     return cudaGetLastError();
 }
 
