@@ -192,10 +192,19 @@ csa_status do_topk(int64_t B, int64_t T, int64_t E, int k, int m, const float *s
     return CSA_OK;
 }
 
+// scratch bytes an attention call needs beyond the status word
+size_t attn_scratch_bytes(csa_dtype dt, int64_t rows, int H, int c, int64_t E, int k, int n_win) {
+    if (!attn_tc_supported(dt, c)) return 0;
+    const int64_t max_list = (k > 0 ? (int64_t)k : E) + n_win;
+    const int ch = attn_tc_chunks(rows, H, max_list);
+    return ch > 1 ? attn_tc_split_bytes(rows, H, c, ch) : 0;
+}
+
 csa_status do_attn(csa_dtype dt, int64_t B, int64_t T, int H, int c, int64_t E, int k, int64_t L,
                    const void *q, const int64_t *q_pos, const void *kvc, const int32_t *idx,
-                   const void *kv_raw, const int64_t *raw_pos0, const float *sink, void *out,
-                   float *lse, const csa_params *p, unsigned *status, cudaStream_t st) {
+                   const int32_t *cnt, const void *kv_raw, const int64_t *raw_pos0,
+                   const float *sink, void *out, float *lse, const csa_params *p, unsigned *status,
+                   void *scratch, cudaStream_t st) {
     AttnArgs a;
     a.q = q; a.q_pos = q_pos; a.kvc = kvc; a.idx = idx; a.kv_raw = kv_raw; a.raw_pos0 = raw_pos0;
     a.sink = sink; a.out = out; a.lse = lse; a.status = status;
@@ -204,6 +213,13 @@ csa_status do_attn(csa_dtype dt, int64_t B, int64_t T, int H, int c, int64_t E, 
     a.scale = p->scale > 0.f ? p->scale : (float)(1.0 / sqrt((double)c));
     a.rope = make_rope(c, p->rope_dims, p->rope_theta);
     StageScope sc(idx ? CSA_STAGE_SPARSE_ATTN : CSA_STAGE_HCA_ATTN, st);
+    if (attn_tc_supported(dt, c)) {
+        const int64_t max_list = (idx ? (int64_t)k : E) + p->n_win;
+        int ch = attn_tc_chunks(B * T, H, max_list);
+        if (ch > 1 && scratch == nullptr) ch = 1;
+        CSA_TRY_CUDA(launch_attn_tc(B, a, cnt, ch, scratch, st), "attention launch (tensor cores)");
+        return CSA_OK;
+    }
     CSA_TRY_CUDA(launch_attn_simt(dt, B, a, st), "attention launch");
     return CSA_OK;
 }
@@ -369,8 +385,8 @@ csa_status topk_select(int64_t B, int64_t T, int64_t E, int32_t k, int32_t m, co
 
 size_t attn_ws_size(csa_dtype dtype, int64_t B, int64_t T, int32_t H, int32_t c, int64_t E,
                     int32_t k, const csa_params *params) {
-    (void)dtype; (void)B; (void)T; (void)H; (void)c; (void)E; (void)k; (void)params;
-    return CSA_STATUS_BYTES;
+    if (params == nullptr || B < 0 || T < 0 || E < 0) return CSA_STATUS_BYTES;
+    return CSA_STATUS_BYTES + attn_scratch_bytes(dtype, B * T, H, c, E, k, params->n_win);
 }
 
 csa_status sparse_attn(csa_dtype dtype, int64_t B, int64_t T, int32_t H, int32_t c, int64_t E,
@@ -385,8 +401,9 @@ csa_status sparse_attn(csa_dtype dtype, int64_t B, int64_t T, int32_t H, int32_t
     if (B * T == 0) return CSA_OK;
     CSA_TRY(need_ptr(idx, "idx"));
     if (lse != nullptr && !al16(lse)) return fail(CSA_ERR_INVALID_ARG, "lse is not 16-byte aligned");
-    return do_attn(dtype, B, T, H, c, E, k, L, q, q_pos, kvc, idx, kv_raw, raw_pos0, sink, out, lse,
-                   params, (unsigned *)ws, (cudaStream_t)stream);
+    return do_attn(dtype, B, T, H, c, E, k, L, q, q_pos, kvc, idx, nullptr, kv_raw, raw_pos0, sink,
+                   out, lse, params, (unsigned *)ws, (char *)ws + CSA_STATUS_BYTES,
+                   (cudaStream_t)stream);
 }
 
 csa_status hca_attn(csa_dtype dtype, int64_t B, int64_t T, int32_t H, int32_t c, int64_t E,
@@ -398,16 +415,17 @@ csa_status hca_attn(csa_dtype dtype, int64_t B, int64_t T, int32_t H, int32_t c,
     CSA_TRY(check_ws(ws, ws_bytes, attn_ws_size(dtype, B, T, H, c, E, 0, params)));
     if (B * T == 0) return CSA_OK;
     if (lse != nullptr && !al16(lse)) return fail(CSA_ERR_INVALID_ARG, "lse is not 16-byte aligned");
-    return do_attn(dtype, B, T, H, c, E, 0, L, q, q_pos, kvc, nullptr, kv_raw, raw_pos0, sink, out,
-                   lse, params, (unsigned *)ws, (cudaStream_t)stream);
+    return do_attn(dtype, B, T, H, c, E, 0, L, q, q_pos, kvc, nullptr, nullptr, kv_raw, raw_pos0,
+                   sink, out, lse, params, (unsigned *)ws, (char *)ws + CSA_STATUS_BYTES,
+                   (cudaStream_t)stream);
 }
 
 // ------------------------------------------------------------ fused: CSA prefill
 
-static size_t csa_prefill_layout(Carve &cv, csa_dtype dt, int64_t B, int64_t n, int c, int dI,
-                                 const csa_params *p, void **pos, void **rp0, void **kvc,
+static size_t csa_prefill_layout(Carve &cv, csa_dtype dt, int64_t B, int64_t n, int H, int c,
+                                 int dI, const csa_params *p, void **pos, void **rp0, void **kvc,
                                  void **kic, void **raw, void **sc, void **idx, void **cnt,
-                                 void **tks) {
+                                 void **tks, void **asc) {
     const int64_t E = n / p->m;
     cv.take(CSA_STATUS_BYTES);
     *pos = cv.take((size_t)B * n * 8);
@@ -419,16 +437,18 @@ static size_t csa_prefill_layout(Carve &cv, csa_dtype dt, int64_t B, int64_t n, 
     *idx = cv.take((size_t)B * n * p->top_k * 4);
     *cnt = cv.take((size_t)B * n * 4);
     *tks = cv.take(topk_scratch_bytes(B * n, E));
+    *asc = cv.take(attn_scratch_bytes(dt, B * n, H, c, E, p->top_k, p->n_win));
     return cv.off;
 }
 
 size_t csa_prefill_ws_size(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t c, int32_t hI,
                            int32_t dI, const csa_params *params) {
-    (void)H; (void)hI;
+    (void)hI;
     if (params == nullptr || params->m < 1 || B < 0 || n < 0) return 0;
     Carve cv{nullptr, 0};
-    void *a, *b, *d, *e, *f, *g, *h, *i, *j;
-    return csa_prefill_layout(cv, dtype, B, n, c, dI, params, &a, &b, &d, &e, &f, &g, &h, &i, &j);
+    void *a, *b, *d, *e, *f, *g, *h, *i, *j, *k;
+    return csa_prefill_layout(cv, dtype, B, n, H, c, dI, params, &a, &b, &d, &e, &f, &g, &h, &i, &j,
+                              &k);
 }
 
 csa_status csa_prefill(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t c, int32_t hI,
@@ -459,9 +479,9 @@ csa_status csa_prefill(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t
     if (idx_out != nullptr && !al16(idx_out)) return fail(CSA_ERR_INVALID_ARG, "idx_out is not 16-byte aligned");
     cudaStream_t st = (cudaStream_t)stream;
     Carve cv{(char *)ws, 0};
-    void *pos, *rp0, *kvc, *kic, *raw, *sc, *idx, *cnt, *tks;
-    csa_prefill_layout(cv, dtype, B, n, c, dI, params, &pos, &rp0, &kvc, &kic, &raw, &sc, &idx, &cnt,
-                       &tks);
+    void *pos, *rp0, *kvc, *kic, *raw, *sc, *idx, *cnt, *tks, *asc;
+    csa_prefill_layout(cv, dtype, B, n, H, c, dI, params, &pos, &rp0, &kvc, &kic, &raw, &sc, &idx, &cnt,
+                       &tks, &asc);
     if (idx_out) idx = idx_out;
     const int64_t E = n / params->m;
     unsigned *status = (unsigned *)ws;
@@ -475,31 +495,31 @@ csa_status csa_prefill(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t
     CSA_TRY(do_topk(B, n, E, params->top_k, params->m, (const float *)sc, (const int64_t *)pos,
                     (int32_t *)idx, (int32_t *)cnt, tks, st));
     return do_attn(dtype, B, n, H, c, E, params->top_k, n, q, (const int64_t *)pos, kvc,
-                   (const int32_t *)idx, raw, (const int64_t *)rp0, sink, out, nullptr, params,
-                   status, st);
+                   (const int32_t *)idx, (const int32_t *)cnt, raw, (const int64_t *)rp0, sink, out,
+                   nullptr, params, status, asc, st);
 }
 
 // ------------------------------------------------------------ fused: HCA prefill
 
-static size_t hca_prefill_layout(Carve &cv, csa_dtype dt, int64_t B, int64_t n, int c,
+static size_t hca_prefill_layout(Carve &cv, csa_dtype dt, int64_t B, int64_t n, int H, int c,
                                  const csa_params *p, void **pos, void **rp0, void **kvc,
-                                 void **raw) {
+                                 void **raw, void **asc) {
     const int64_t E = n / p->m;
     cv.take(CSA_STATUS_BYTES);
     *pos = cv.take((size_t)B * n * 8);
     *rp0 = cv.take((size_t)B * 8);
     *kvc = cv.take((size_t)B * E * c * esize(dt));
     *raw = cv.take((size_t)B * n * c * esize(dt));
+    *asc = cv.take(attn_scratch_bytes(dt, B * n, H, c, E, 0, p->n_win));
     return cv.off;
 }
 
 size_t hca_prefill_ws_size(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t c,
                            const csa_params *params) {
-    (void)H;
     if (params == nullptr || params->m < 1 || B < 0 || n < 0) return 0;
     Carve cv{nullptr, 0};
-    void *a, *b, *d, *e;
-    return hca_prefill_layout(cv, dtype, B, n, c, params, &a, &b, &d, &e);
+    void *a, *b, *d, *e, *f;
+    return hca_prefill_layout(cv, dtype, B, n, H, c, params, &a, &b, &d, &e, &f);
 }
 
 csa_status hca_prefill(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t c, const void *C,
@@ -519,37 +539,41 @@ csa_status hca_prefill(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t
     for (int i = 0; i < 6; i++) CSA_TRY(need_ptr(ptrs[i], names[i]));
     cudaStream_t st = (cudaStream_t)stream;
     Carve cv{(char *)ws, 0};
-    void *pos, *rp0, *kvc, *raw;
-    hca_prefill_layout(cv, dtype, B, n, c, params, &pos, &rp0, &kvc, &raw);
+    void *pos, *rp0, *kvc, *raw, *asc;
+    hca_prefill_layout(cv, dtype, B, n, H, c, params, &pos, &rp0, &kvc, &raw, &asc);
     const int64_t E = n / params->m;
     CSA_TRY_CUDA(fill_positions((int64_t *)pos, B, n, st), "positions");
     CSA_TRY_CUDA(cudaMemsetAsync(rp0, 0, (size_t)B * 8, st), "raw_pos0");
     CSA_TRY(do_compress(dtype, B, n, c, C, Z, bias, nullptr, nullptr, nullptr, kvc, raw, params,
                         params->rope_dims, st));
-    return do_attn(dtype, B, n, H, c, E, 0, n, q, (const int64_t *)pos, kvc, nullptr, raw,
-                   (const int64_t *)rp0, sink, out, nullptr, params, (unsigned *)ws, st);
+    return do_attn(dtype, B, n, H, c, E, 0, n, q, (const int64_t *)pos, kvc, nullptr, nullptr, raw,
+                   (const int64_t *)rp0, sink, out, nullptr, params, (unsigned *)ws, asc, st);
 }
 
 // ------------------------------------------------------------ fused: decode
 
-static size_t decode_layout(Carve &cv, int64_t B, int64_t E, int k, void **sc, void **idx,
-                            void **cnt, void **tks) {
+static size_t decode_layout(Carve &cv, csa_dtype dt, int64_t B, int H, int c, int64_t E,
+                            int64_t E2, const csa_params *p, const csa_params *p2, void **sc,
+                            void **idx, void **cnt, void **tks, void **asc) {
     cv.take(CSA_STATUS_BYTES);
     *sc = cv.take((size_t)B * E * 4);
-    *idx = cv.take((size_t)B * k * 4);
+    *idx = cv.take((size_t)B * p->top_k * 4);
     *cnt = cv.take((size_t)B * 4);
     *tks = cv.take(topk_scratch_bytes(B, E));
+    size_t a1 = attn_scratch_bytes(dt, B, H, c, E, p->top_k, p->n_win);
+    size_t a2 = p2 ? attn_scratch_bytes(dt, B, H, c, E2, 0, p2->n_win) : 0;
+    *asc = cv.take(a1 > a2 ? a1 : a2);
     return cv.off;
 }
 
 size_t hybrid_decode_ws_size(csa_dtype dtype, int64_t B, int32_t H, int32_t c, int32_t hI,
                              int32_t dI, int64_t E, int64_t E2, const csa_params *params,
                              const csa_params *params2) {
-    (void)dtype; (void)H; (void)c; (void)hI; (void)dI; (void)E2; (void)params2;
+    (void)hI; (void)dI;
     if (params == nullptr || B < 0 || E < 0) return 0;
     Carve cv{nullptr, 0};
-    void *a, *b, *d, *e;
-    return decode_layout(cv, B, E, params->top_k, &a, &b, &d, &e);
+    void *a, *b, *d, *e, *f;
+    return decode_layout(cv, dtype, B, H, c, E, E2, params, params2, &a, &b, &d, &e, &f);
 }
 
 csa_status hybrid_decode(csa_dtype dtype, int64_t B, int32_t H, int32_t c, int32_t hI, int32_t dI,
@@ -581,8 +605,9 @@ csa_status hybrid_decode(csa_dtype dtype, int64_t B, int32_t H, int32_t c, int32
     if (idx_out != nullptr && !al16(idx_out)) return fail(CSA_ERR_INVALID_ARG, "idx_out is not 16-byte aligned");
     cudaStream_t st = (cudaStream_t)stream;
     Carve cv{(char *)ws, 0};
-    void *sc, *idx, *cnt, *tks;
-    decode_layout(cv, B, E, params->top_k, &sc, &idx, &cnt, &tks);
+    void *sc, *idx, *cnt, *tks, *asc;
+    decode_layout(cv, dtype, B, H, c, E, E2, params, hca ? params2 : nullptr, &sc, &idx, &cnt, &tks,
+                  &asc);
     if (idx_out) idx = idx_out;
     unsigned *status = (unsigned *)ws;
     CSA_TRY(do_indexer(dtype, B, 1, hI, dI, E, params->m, qI, w, kIc, q_pos, (float *)sc, 0,
@@ -590,10 +615,11 @@ csa_status hybrid_decode(csa_dtype dtype, int64_t B, int32_t H, int32_t c, int32
     CSA_TRY(do_topk(B, 1, E, params->top_k, params->m, (const float *)sc, q_pos, (int32_t *)idx,
                     (int32_t *)cnt, tks, st));
     CSA_TRY(do_attn(dtype, B, 1, H, c, E, params->top_k, L, q, q_pos, kvc, (const int32_t *)idx,
-                    kv_raw, raw_pos0, sink, out, nullptr, params, status, st));
+                    (const int32_t *)cnt, kv_raw, raw_pos0, sink, out, nullptr, params, status, asc,
+                    st));
     if (hca)
-        CSA_TRY(do_attn(dtype, B, 1, H, c, E2, 0, L, q2, q_pos, kvc2, nullptr, kv_raw2, raw_pos0,
-                        sink2, out2, nullptr, params2, status, st));
+        CSA_TRY(do_attn(dtype, B, 1, H, c, E2, 0, L, q2, q_pos, kvc2, nullptr, nullptr, kv_raw2,
+                        raw_pos0, sink2, out2, nullptr, params2, status, asc, st));
     return CSA_OK;
 }
 

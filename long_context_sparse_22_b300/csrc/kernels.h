@@ -54,4 +54,13 @@ cudaError_t launch_topk(int64_t B, int64_t Tq, int64_t E, int k, int m, const fl
 
 cudaError_t launch_attn_simt(csa_dtype dt, int64_t B, const AttnArgs &a, cudaStream_t st);
 
+// Tensor-core attention (bf16, c = 512).  n_chunks > 1 splits each query's
+// entry list over several CTAs (decode) and needs attn_tc_split_bytes of
+// scratch; cnt (nullable) gives the number of valid leading slots of idx.
+bool attn_tc_supported(csa_dtype dt, int c);
+int attn_tc_chunks(int64_t rows, int H, int64_t max_list);
+size_t attn_tc_split_bytes(int64_t rows, int H, int c, int n_chunks);
+cudaError_t launch_attn_tc(int64_t B, const AttnArgs &a, const int32_t *cnt, int n_chunks,
+                           void *split_ws, cudaStream_t st);
+
 }  // namespace csa

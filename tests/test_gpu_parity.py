@@ -132,6 +132,7 @@ def test_topk_exact(csa, orc, B, T, E, k, m):
     ("f32", 1, 200, 4, 64, 60, 16, 4, 128, 32, 1),
     ("bf16", 2, 3, 64, 512, 3000, 512, 4, 128, 64, 1),
     ("bf16", 1, 17, 16, 128, 100, 8, 4, 5, 64, 0),
+    ("bf16", 1, 300, 96, 512, 200, 64, 4, 128, 64, 1),    # two head groups, one partial
 ])
 def test_sparse_attn(csa, orc, dtype, B, T, H, c, E, k, m, n_win, r, derot):
     seed = 400 + E
