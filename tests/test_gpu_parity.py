@@ -162,7 +162,9 @@ def test_sparse_attn(csa, orc, dtype, B, T, H, c, E, k, m, n_win, r, derot):
         ro, rl = orc.attend(q[b], pos[b], kvc[b], m, kv_raw[b], int(raw_pos0[b]), sink, idx=idx[b],
                             n_win=n_win, rope_dims=r, derotate=derot, want_lse=True)
         check_close(g[b], ro, dtype, "sparse_attn out")
-        assert np.abs(gl[b] - rl).max() <= 1e-3
+        # log-denominator: fp32 path to 1e-4; the bf16 path rounds the rotated
+        # query to bf16 before the product, so its logits carry ~2^-9 relative error
+        assert np.abs(gl[b] - rl).max() <= (1e-4 if dtype == "f32" else 1e-2)
 
 
 @pytest.mark.parametrize("dtype,B,T,H,c,E,m,n_win,r", [
