@@ -98,6 +98,8 @@ typedef struct csa_params {
 
 const char *csa_last_error(void);   /* thread-local message of the last failure */
 const char *csa_version(void);
+/* Number of kernels this library has launched in this process (all devices). */
+int64_t csa_launch_count(void);
 
 /*
  * Synchronise `stream`, read the status word at the start of `ws`, clear it

@@ -44,6 +44,7 @@ def params(m=4, overlap=0, top_k=512, n_win=128, rope_dims=64, derotate=1, rope_
 _SIGS = {
     "csa_last_error": ([], C.c_char_p),
     "csa_version": ([], C.c_char_p),
+    "csa_launch_count": ([], C.c_int64),
     "csa_stream_status": ([C.c_void_p, C.c_void_p], C.c_int),
     "csa_workspace_init": ([C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
     "csa_timing_enable": ([C.c_int32], C.c_int),
@@ -305,6 +306,11 @@ def hybrid_decode(q, qI, w, kvc, kIc, kv_raw, sink, q_pos, raw_pos0, p: CsaParam
 
 
 STAGES = ["compress", "indexer", "topk", "sparse_attn", "hca_attn"]
+
+
+def launch_count() -> int:
+    """Kernels launched by libcsa in this process so far."""
+    return int(lib().csa_launch_count())
 
 
 def timing_enable(on: bool = True):

@@ -4,6 +4,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -11,6 +12,9 @@
 #include "kernels.h"
 
 using namespace csa;
+
+static std::atomic<long long> g_launches{0};
+void csa::count_launches(int n) { g_launches += n; }
 
 namespace {
 
@@ -106,6 +110,7 @@ __global__ void iota_pos_kernel(int64_t *pos, int64_t B, int64_t n) {
 cudaError_t fill_positions(int64_t *pos, int64_t B, int64_t n, cudaStream_t st) {
     if (B * n == 0) return cudaSuccess;
     iota_pos_kernel<<<(unsigned)((B * n + 255) / 256), 256, 0, st>>>(pos, B, n);
+    count_launches(1);
     return cudaGetLastError();
 }
 
@@ -256,6 +261,8 @@ extern "C" {
 const char *csa_last_error(void) { return g_err; }
 
 const char *csa_version(void) { return "csa-b300 0.1 (sm_103a)"; }
+
+int64_t csa_launch_count(void) { return g_launches.load(); }
 
 csa_status csa_timing_enable(int32_t on) {
     std::lock_guard<std::mutex> g(g_timer.mu);

@@ -218,6 +218,7 @@ cudaError_t launch_attn_simt(csa_dtype dt, int64_t B, const AttnArgs &a, cudaStr
     }
     if (dt == CSA_BF16) attn_simt_kernel<__nv_bfloat16><<<grid, AT_THREADS, smem, st>>>(a);
     else attn_simt_kernel<float><<<grid, AT_THREADS, smem, st>>>(a);
+    count_launches(1);
     return cudaGetLastError();
 }
 

@@ -21,10 +21,11 @@
 // logit seeds the running max and enters only the denominator.
 //
 // Warp roles (persistent CTAs, items dealt round-robin):
-//   warps 0-1  q~ preparation (RoPE at t, bf16, swizzled) and the cp.async
-//              gather of each 64-entry tile into a 128-byte-swizzled K-major
-//              layout (two tile buffers);
-//   warp 2     TMEM allocator and MMA issuer: QK(j+1) is issued before
+//   warps 0-2  q~ preparation (cp.async of the q rows into the swizzled
+//              layout, then RoPE at t in place) and the cp.async gather of
+//              each 64-entry tile into a 128-byte-swizzled K-major layout
+//              (two tile buffers);
+//   warp 3     TMEM allocator and MMA issuer: QK(j+1) is issued before
 //              PV(j), so the tensor core works while tile j's softmax runs;
 //   warps 4-7  softmax, O rescale, and the epilogue (normalise, de-rotate,
 //              store), or fp32 partial outputs for a split-KV combine.
@@ -49,7 +50,7 @@ struct AtCfg {
     static constexpr int OFF_P = OFF_Q + Q_BYTES;
     static constexpr int OFF_STAGE = OFF_P + 2 * P_BYTES;
     static constexpr int OFF_MISC = OFF_STAGE + TE * STAGE_LD * 4;
-    static constexpr int MISC_BYTES = 2048;
+    static constexpr int MISC_BYTES = 2176;
     static constexpr int SMEM = OFF_MISC + MISC_BYTES;
     static constexpr int TMEM_COLS = 512;
     static constexpr int S_COL = 0;               // two S^T buffers: cols 0, 64
@@ -196,6 +197,7 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const __grid_constant__
     float *den_s = (float *)(misc + 512);              // [64]
     float *cs_s = (float *)(misc + 768);               // [64] cos, then sin
     const __nv_bfloat16 **rowp = (const __nv_bfloat16 **)(misc + 1024);   // [2][64]
+    uint8_t *valid = misc + 2048;                      // [2][64] entry present
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x;
@@ -205,14 +207,14 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const __grid_constant__
     }
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; i++) {
-            tc::mbar_init(&kfull[i], 64);
+            tc::mbar_init(&kfull[i], 96);
             tc::mbar_init(&kempty[i], 1);
             tc::mbar_init(&sfull[i], 1);
             tc::mbar_init(&sempty[i], 4);
             tc::mbar_init(&pfull[i], 1);
             tc::mbar_init(&pempty[i], 1);
         }
-        tc::mbar_init(qfull, 64);
+        tc::mbar_init(qfull, 96);
         tc::mbar_init(qempty, 1);
         tc::mbar_init(ofull, 1);
         tc::mbar_init(oempty, 4);
@@ -220,57 +222,51 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const __grid_constant__
         *rescale_flag = 0;
         tc::fence_barrier_init();
     }
-    if (warp == 2) tc::tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    if (warp == 3) tc::tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp < 2) {
+    if (warp < 3) {
         // ------------------------------------------------------ loader / q~ prep
-        const int tid = threadIdx.x;     // 0..63
-        uint32_t g = 0, ii = 0;      // ii counts processed (non-empty) items
+        constexpr int NL = 96;           // loader threads
+        const int tid = threadIdx.x;     // 0..95
+        const uint32_t qb = tc::smem_u32(sQ);
+        uint32_t g = 0, ii = 0;          // ii counts processed (non-empty) items
         for (int64_t it = blockIdx.x; it < a.n_items; it += G) {
             ItemInfo f;
             item_info(a, it, f);
             if (f.j0 >= f.j1) continue;
-            // q~ = RoPE(q, t) -> bf16, K-major swizzled [NA][64 heads][128 B]
+            // q rows -> the K-major swizzled layout [NA][64 heads][128 B] by cp.async
             tc::mbar_wait(qempty, (ii & 1) ^ 1, a.status, abort_flag);
+            const int h0 = f.hg * Cfg::HG;
+            for (int i = tid; i < Cfg::HG * Cfg::NA * 8; i += NL) {
+                const int h = i / (Cfg::NA * 8);
+                const int gr = i % (Cfg::NA * 8);           // 16-byte granule of the row
+                const uint32_t dst = qb + (gr >> 3) * (Cfg::HG * 128) + (h >> 3) * 1024 + swz128(h, (gr & 7) * 16);
+                const bool ok = h0 + h < a.H;
+                cp_async16(dst, ok ? (const void *)(a.q + (f.bt * a.H + h0 + h) * (int64_t)C + gr * 8)
+                                   : (const void *)a.q, ok ? 16u : 0u);
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
             if (tid < a.rope.pairs && tid < 32) {
                 float cs, sn;
                 rope_cos_sin((double)f.t, a.rope.w[tid], cs, sn);
                 cs_s[tid] = cs;
                 cs_s[32 + tid] = sn;
             }
-            named_bar(2, 64);
-            const int h0 = f.hg * Cfg::HG;
-            for (int i = tid; i < Cfg::HG * Cfg::NA * 8; i += 64) {
-                const int h = i / (Cfg::NA * 8);
-                const int gr = i % (Cfg::NA * 8);           // 16-byte granule of the row
-                const int d0 = gr * 8;
-                float v[8];
-                if (h0 + h < a.H) {
-                    Vec<__nv_bfloat16>::load(a.q + (f.bt * a.H + h0 + h) * (int64_t)C + d0, v);
-                    if (d0 + 8 > a.rope.first) {
-#pragma unroll
-                        for (int u = 0; u < 4; u++) {
-                            const int d = d0 + 2 * u;
-                            if (d >= a.rope.first) {
-                                const int pi = (d - a.rope.first) >> 1;
-                                const float c_ = cs_s[pi], s_ = cs_s[32 + pi];
-                                const float x0 = v[2 * u], x1 = v[2 * u + 1];
-                                v[2 * u] = x0 * c_ - x1 * s_;
-                                v[2 * u + 1] = x0 * s_ + x1 * c_;
-                            }
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int u = 0; u < 8; u++) v[u] = 0.f;
-                }
-                const int atom = d0 / 64;
-                uint8_t *dst = sQ + atom * (Cfg::HG * 128) + (h >> 3) * 1024 + swz128(h, (d0 % 64) * 2);
-                Vec<__nv_bfloat16>::store((__nv_bfloat16 *)dst, v);
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+            named_bar(2, NL);
+            // q~ = RoPE(q, t): rotate the rotary pairs in place
+            for (int i = tid; i < Cfg::HG * a.rope.pairs; i += NL) {
+                const int h = i / a.rope.pairs, pi = i % a.rope.pairs;
+                const int d = a.rope.first + 2 * pi;
+                __nv_bfloat162 *pv = (__nv_bfloat162 *)(sQ + (d >> 6) * (Cfg::HG * 128) + (h >> 3) * 1024 +
+                                                        swz128(h, (d & 63) * 2));
+                const float2 x = __bfloat1622float2(*pv);
+                const float c_ = cs_s[pi], s_ = cs_s[32 + pi];
+                *pv = __floats2bfloat162_rn(x.x * c_ - x.y * s_, x.x * s_ + x.y * c_);
             }
             fence_proxy_async();
             tc::mbar_arrive(qfull);
@@ -278,13 +274,16 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const __grid_constant__
             for (int j = f.j0; j < f.j1; j++, g++) {
                 const int buf = g & 1;
                 tc::mbar_wait(&kempty[buf], ((g >> 1) & 1) ^ 1, a.status, abort_flag);
-                rowp[buf * 64 + tid] = entry_row(a, f, (int64_t)j * 64 + tid, C, true);
-                named_bar(2, 64);
+                if (tid < 64) {
+                    const __nv_bfloat16 *rp = entry_row(a, f, (int64_t)j * 64 + tid, C, true);
+                    rowp[buf * 64 + tid] = rp;
+                    valid[buf * 64 + tid] = rp != nullptr;
+                }
+                named_bar(2, NL);
                 const uint32_t kb = tc::smem_u32(sK + buf * Cfg::K_BYTES);
-                // row r: 64 threads x 16 bytes = one C=512 row; smaller C loops rows faster
                 constexpr int GR = C / 8;            // granules per row
 #pragma unroll 4
-                for (int i = tid; i < Cfg::TE * GR; i += 64) {
+                for (int i = tid; i < Cfg::TE * GR; i += NL) {
                     const int r = i / GR, gr = i % GR;
                     const __nv_bfloat16 *src = rowp[buf * 64 + r];
                     const int atom = gr >> 3;
@@ -298,7 +297,7 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const __grid_constant__
             }
             ii++;
         }
-    } else if (warp == 2) {
+    } else if (warp == 3) {
         // ------------------------------------------------------------- MMA
         if (lane == 0) {
             constexpr uint32_t idQK = tc::idesc_bf16_f32(64, 64);
@@ -379,9 +378,12 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const __grid_constant__
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&sempty[buf]);
+                // the loader's presence flags for this tile (its kfull phase has
+                // completed, and cannot advance again before this tile's PV)
+                tc::mbar_wait(&kfull[buf], (g >> 1) & 1, a.status, abort_flag);
                 if (lane < 16) {
                     const int e = quarter * 16 + lane;
-                    const bool ok = entry_row(a, f, (int64_t)j * 64 + e, C, false) != nullptr;
+                    const bool ok = valid[buf * 64 + e] != 0;
 #pragma unroll
                     for (int h = 0; h < 64; h++) stage[e * Cfg::STAGE_LD + h] = ok ? v[h] * a.scale_log2 : -INFINITY;
                 }
@@ -501,7 +503,7 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const __grid_constant__
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 2) {
+    if (warp == 3) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, Cfg::TMEM_COLS);
     }
@@ -627,9 +629,11 @@ cudaError_t launch_attn_tc(int64_t B, const AttnArgs &g, const int32_t *cnt, int
     const int sms = attn_sms();
     const int grid = (int)(a.n_items < sms ? a.n_items : sms);
     attn_tc_kernel<512><<<grid, Cfg::THREADS, Cfg::SMEM, st>>>(a);
+    count_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.chunk_tiles == 0) return e;
     attn_combine_kernel<512><<<dim3((unsigned)rows, (unsigned)g.H), 128, 0, st>>>(a);
+    count_launches(1);
     return cudaGetLastError();
 }
 

@@ -124,6 +124,7 @@ cudaError_t launch_compress(csa_dtype dt, int64_t B, int64_t n, int c, int m, in
             (const float *)C, (const float *)Z, bias, (const float *)Cb, (const float *)Zb, biasb,
             (float *)out, (float *)raw_out, B, n, c, m, overlap, E, Eg, rope);
     }
+    count_launches(1);
     return cudaGetLastError();
 }
 

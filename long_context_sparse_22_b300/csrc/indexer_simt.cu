@@ -83,6 +83,7 @@ static cudaError_t launch_simt_t(int64_t B, int64_t Tq, int hI, int dI, int64_t 
         indexer_simt_kernel<T, 128><<<grid, 128, smem, st>>>(q, w, k, q_pos, scores, Tq, hI, E, m, write_masked);
         break;
     }
+    count_launches(1);
     return cudaGetLastError();
 }
 

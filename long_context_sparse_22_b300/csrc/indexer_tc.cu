@@ -378,6 +378,7 @@ static cudaError_t launch_tc(const CUtensorMap &tq, const CUtensorMap &tk, const
         attr = true;
     }
     indexer_tc_kernel<QT><<<grid, Cfg::THREADS, Cfg::SMEM, st>>>(tq, tk, a);
+    count_launches(1);
     return cudaGetLastError();
 }
 
@@ -411,6 +412,7 @@ cudaError_t launch_indexer_tc(int64_t B, int64_t T, int64_t E, int m, const void
     const int64_t rows = B * T;
     dim3 g(8, (unsigned)(rows < 65535 ? rows : 65535), (unsigned)((rows + 65534) / 65535));
     mask_tail_kernel<<<g, 256, 0, st>>>(scores, q_pos, rows, E, m);
+    count_launches(1);
     return cudaGetLastError();
 }
 

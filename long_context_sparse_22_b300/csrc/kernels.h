@@ -8,6 +8,9 @@
 
 namespace csa {
 
+// Every kernel launch of the library is counted (csa_launch_count).
+void count_launches(int n);
+
 struct AttnArgs {
     const void *q;
     const int64_t *q_pos;

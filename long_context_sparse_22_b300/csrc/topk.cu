@@ -57,8 +57,39 @@ struct TkShared {
     uint32_t hist[2048];
     uint32_t wsum[32];
     uint32_t mirror[TK_THREADS];
-    uint32_t bin, above;
+    uint32_t wcnt[2][TK_THREADS / 32];
+    uint32_t bin, above, binsz;
 };
+
+// Add one to hist[bin] for every lane with `in` set; lanes of a warp that
+// hit the same bin are merged into one shared-memory atomic (scores crowd
+// into a few bins, so plain per-lane atomics serialise).  Warp-uniform call.
+__device__ __forceinline__ void hist_add(uint32_t *hist, bool in, uint32_t bin) {
+    const unsigned m_in = __ballot_sync(0xffffffffu, in);
+    if (in) {
+        const unsigned peers = __match_any_sync(m_in, bin);
+        if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+    }
+}
+
+// Exclusive prefix over the block of per-warp counts c (lane 0 of each warp
+// supplies its warp's count); returns the sum over earlier warps and sets
+// *total.  Two barriers.
+__device__ __forceinline__ uint32_t warp_offsets(uint32_t *wc, uint32_t c, uint32_t *total) {
+    const int wid = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) wc[wid] = c;
+    __syncthreads();
+    uint32_t before = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < TK_THREADS / 32; w++) {
+        const uint32_t v = wc[w];
+        before += w < wid ? v : 0u;
+        tot += v;
+    }
+    *total = tot;
+    __syncthreads();
+    return before;
+}
 
 // Given a histogram of nb bins (nb a multiple of TK_THREADS), find the bin
 // holding the remaining-th largest key counting down from the top bin; sets
@@ -84,6 +115,7 @@ __device__ __forceinline__ void find_bin(TkShared &sh, int nb, uint32_t remainin
         if (above < remaining && above + h >= remaining) {
             sh.bin = (uint32_t)bin;
             sh.above = above;
+            sh.binsz = h;
         }
         above += h;
     }
@@ -95,39 +127,54 @@ __device__ __forceinline__ void find_bin(TkShared &sh, int nb, uint32_t remainin
 // the items' order.
 template <typename KeyF, typename IdF>
 __device__ void select_core(TkShared &sh, int64_t n, int k, KeyF key, IdF id, int32_t *orow) {
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31;
     uint32_t prefix = 0, pmask = 0;
     uint32_t remaining = (uint32_t)k;
+    uint32_t n_eq = 0;
 #pragma unroll 1
     for (int pass = 0; pass < 3; pass++) {
         const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
         const int nb = pass < 2 ? 2048 : 1024;
         for (int i = tid; i < nb; i += TK_THREADS) sh.hist[i] = 0;
         __syncthreads();
-        for (int64_t j = tid; j < n; j += TK_THREADS) {
-            const uint32_t kv = key(j);
-            if ((kv & pmask) == prefix) atomicAdd(&sh.hist[(kv >> shift) & (nb - 1)], 1u);
+        for (int64_t base = 0; base < n; base += TK_THREADS) {
+            const int64_t j = base + tid;
+            const uint32_t kv = j < n ? key(j) : 0u;
+            hist_add(sh.hist, j < n && (kv & pmask) == prefix, (kv >> shift) & (nb - 1));
         }
         __syncthreads();
         find_bin(sh, nb, remaining);
         remaining -= sh.above;
         prefix |= sh.bin << shift;
         pmask |= (uint32_t)(nb - 1) << shift;
+        n_eq = sh.binsz;                 // after the last pass: keys equal to tau
         __syncthreads();
     }
     const uint32_t tau = prefix, need_eq = remaining;
+    const bool all_eq = need_eq == n_eq;  // every tie is kept: selection is key >= tau
+    const unsigned lt = (1u << lane) - 1u;
     uint32_t run_sel = 0, run_eq = 0;
     for (int64_t base = 0; base < n && run_sel < (uint32_t)k; base += TK_THREADS) {
         const int64_t j = base + tid;
         const uint32_t kv = j < n ? key(j) : 0u;
-        const uint32_t gt = (j < n && kv > tau) ? 1u : 0u;
-        const uint32_t eq = (j < n && kv == tau) ? 1u : 0u;
-        uint32_t eq_tot, sel_tot;
-        const uint32_t eq_rank = run_eq + block_excl_scan(eq, sh.wsum, &eq_tot);
-        const uint32_t sel = (gt || (eq && eq_rank < need_eq)) ? 1u : 0u;
-        const uint32_t pos = run_sel + block_excl_scan(sel, sh.wsum, &sel_tot);
+        const bool gt = j < n && kv > tau;
+        const bool eq = j < n && kv == tau;
+        bool sel;
+        if (all_eq) {
+            sel = gt || eq;
+        } else {
+            const unsigned be = __ballot_sync(0xffffffffu, eq);
+            uint32_t eq_tot;
+            const uint32_t eq_before = warp_offsets(sh.wcnt[0], (uint32_t)__popc(be), &eq_tot);
+            const uint32_t eq_rank = run_eq + eq_before + (uint32_t)__popc(be & lt);
+            sel = gt || (eq && eq_rank < need_eq);
+            run_eq += eq_tot;
+        }
+        const unsigned bs = __ballot_sync(0xffffffffu, sel);
+        uint32_t sel_tot;
+        const uint32_t pos = run_sel + warp_offsets(sh.wcnt[1], (uint32_t)__popc(bs), &sel_tot) +
+                             (uint32_t)__popc(bs & lt);
         if (sel && pos < (uint32_t)k) orow[pos] = id(j);
-        run_eq += eq_tot;
         run_sel += sel_tot;
     }
 }
@@ -187,7 +234,11 @@ __global__ void __launch_bounds__(TK_THREADS) topk_hist_kernel(TkLong a) {
     const int64_t c0 = (int64_t)blockIdx.x * a.CS;
     const int64_t c1 = c0 + a.CS < nv ? c0 + a.CS : nv;
     const float *s = a.scores + row * a.E;
-    for (int64_t j = c0 + threadIdx.x; j < c1; j += TK_THREADS) atomicAdd(&h[score_key(s[j]) >> 21], 1u);
+    for (int64_t base = c0; base < c1; base += TK_THREADS) {
+        const int64_t j = base + threadIdx.x;
+        const uint32_t kv = j < c1 ? score_key(s[j]) : 0u;
+        hist_add(h, j < c1, kv >> 21);
+    }
     __syncthreads();
     uint32_t *g = a.hist + row * 2048;
     for (int i = threadIdx.x; i < 2048; i += TK_THREADS)
@@ -331,6 +382,7 @@ cudaError_t launch_topk(int64_t B, int64_t Tq, int64_t E, int k, int m, const fl
             g_final_smem_set = 1;
         }
         topk_final_kernel<<<(unsigned)rows, TK_THREADS, CAND_CAP * 8, st>>>(a, CAND_CAP);
+        count_launches(3);
         return cudaGetLastError();
     }
     const int kcap = (int)(E < KCAP_MAX ? E : KCAP_MAX);
@@ -342,6 +394,7 @@ cudaError_t launch_topk(int64_t B, int64_t Tq, int64_t E, int k, int m, const fl
         g_topk_smem_set = 1;
     }
     topk_kernel<<<(unsigned)rows, TK_THREADS, smem, st>>>(scores, q_pos, idx, cnt, E, k, m, kcap);
+    count_launches(1);
     return cudaGetLastError();
 }
 
