@@ -176,10 +176,12 @@ csa_status do_compress(csa_dtype dt, int64_t B, int64_t n, int c, const void *C,
 
 csa_status do_indexer(csa_dtype dt, int64_t B, int64_t T, int hI, int dI, int64_t E, int m,
                       const void *qI, const float *w, const void *kI, const int64_t *q_pos,
-                      float *scores, int write_masked, unsigned *status, cudaStream_t st) {
+                      float *scores, int write_masked, unsigned *status, cudaStream_t st,
+                      int max_ctas = 0) {
     StageScope sc(CSA_STAGE_INDEXER, st);
     if (dt == CSA_BF16 && indexer_tc_supported(hI, dI, B, T, E)) {
-        CSA_TRY_CUDA(launch_indexer_tc(B, T, E, m, qI, w, kI, q_pos, scores, write_masked, status, st),
+        CSA_TRY_CUDA(launch_indexer_tc(B, T, E, m, qI, w, kI, q_pos, scores, write_masked, status,
+                                       max_ctas, st),
                      "indexer_score launch (tensor cores)");
         return CSA_OK;
     }
@@ -209,7 +211,7 @@ csa_status do_attn(csa_dtype dt, int64_t B, int64_t T, int H, int c, int64_t E, 
                    const void *q, const int64_t *q_pos, const void *kvc, const int32_t *idx,
                    const int32_t *cnt, const void *kv_raw, const int64_t *raw_pos0,
                    const float *sink, void *out, float *lse, const csa_params *p, unsigned *status,
-                   void *scratch, cudaStream_t st) {
+                   void *scratch, cudaStream_t st, int max_ctas = 0) {
     AttnArgs a;
     a.q = q; a.q_pos = q_pos; a.kvc = kvc; a.idx = idx; a.kv_raw = kv_raw; a.raw_pos0 = raw_pos0;
     a.sink = sink; a.out = out; a.lse = lse; a.status = status;
@@ -222,7 +224,8 @@ csa_status do_attn(csa_dtype dt, int64_t B, int64_t T, int H, int c, int64_t E, 
         const int64_t max_list = (idx ? (int64_t)k : E) + p->n_win;
         int ch = attn_tc_chunks(B * T, H, max_list);
         if (ch > 1 && scratch == nullptr) ch = 1;
-        CSA_TRY_CUDA(launch_attn_tc(B, a, cnt, ch, scratch, st), "attention launch (tensor cores)");
+        CSA_TRY_CUDA(launch_attn_tc(B, a, cnt, ch, scratch, max_ctas, st),
+                     "attention launch (tensor cores)");
         return CSA_OK;
     }
     CSA_TRY_CUDA(launch_attn_simt(dt, B, a, st), "attention launch");
@@ -561,16 +564,40 @@ csa_status hca_prefill(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t
 
 static size_t decode_layout(Carve &cv, csa_dtype dt, int64_t B, int H, int c, int64_t E,
                             int64_t E2, const csa_params *p, const csa_params *p2, void **sc,
-                            void **idx, void **cnt, void **tks, void **asc) {
+                            void **idx, void **cnt, void **tks, void **asc, void **asc2) {
     cv.take(CSA_STATUS_BYTES);
     *sc = cv.take((size_t)B * E * 4);
     *idx = cv.take((size_t)B * p->top_k * 4);
     *cnt = cv.take((size_t)B * 4);
     *tks = cv.take(topk_scratch_bytes(B, E));
-    size_t a1 = attn_scratch_bytes(dt, B, H, c, E, p->top_k, p->n_win);
-    size_t a2 = p2 ? attn_scratch_bytes(dt, B, H, c, E2, 0, p2->n_win) : 0;
-    *asc = cv.take(a1 > a2 ? a1 : a2);
+    *asc = cv.take(attn_scratch_bytes(dt, B, H, c, E, p->top_k, p->n_win));
+    *asc2 = cv.take(p2 ? attn_scratch_bytes(dt, B, H, c, E2, 0, p2->n_win) : 0);
     return cv.off;
+}
+
+// One auxiliary stream and two events per device, created on the first
+// hybrid_decode call that has an HCA layer, kept until the process exits.
+// They let the HCA layer's attention run beside the CSA indexer.
+struct AuxStreams {
+    cudaStream_t aux = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+static AuxStreams g_aux[64];
+static std::mutex g_aux_mu;
+
+static csa_status get_aux(AuxStreams **out) {
+    int dev = 0;
+    CSA_TRY_CUDA(cudaGetDevice(&dev), "get device");
+    if (dev < 0 || dev >= 64) return fail(CSA_ERR_UNSUPPORTED, "device index %d", dev);
+    std::lock_guard<std::mutex> g(g_aux_mu);
+    AuxStreams &a = g_aux[dev];
+    if (!a.aux) {
+        CSA_TRY_CUDA(cudaStreamCreateWithFlags(&a.aux, cudaStreamNonBlocking), "aux stream");
+        CSA_TRY_CUDA(cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming), "fork event");
+        CSA_TRY_CUDA(cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming), "join event");
+    }
+    *out = &a;
+    return CSA_OK;
 }
 
 size_t hybrid_decode_ws_size(csa_dtype dtype, int64_t B, int32_t H, int32_t c, int32_t hI,
@@ -579,8 +606,8 @@ size_t hybrid_decode_ws_size(csa_dtype dtype, int64_t B, int32_t H, int32_t c, i
     (void)hI; (void)dI;
     if (params == nullptr || B < 0 || E < 0) return 0;
     Carve cv{nullptr, 0};
-    void *a, *b, *d, *e, *f;
-    return decode_layout(cv, dtype, B, H, c, E, E2, params, params2, &a, &b, &d, &e, &f);
+    void *a, *b, *d, *e, *f, *g;
+    return decode_layout(cv, dtype, B, H, c, E, E2, params, params2, &a, &b, &d, &e, &f, &g);
 }
 
 csa_status hybrid_decode(csa_dtype dtype, int64_t B, int32_t H, int32_t c, int32_t hI, int32_t dI,
@@ -612,21 +639,47 @@ csa_status hybrid_decode(csa_dtype dtype, int64_t B, int32_t H, int32_t c, int32
     if (idx_out != nullptr && !al16(idx_out)) return fail(CSA_ERR_INVALID_ARG, "idx_out is not 16-byte aligned");
     cudaStream_t st = (cudaStream_t)stream;
     Carve cv{(char *)ws, 0};
-    void *sc, *idx, *cnt, *tks, *asc;
+    void *sc, *idx, *cnt, *tks, *asc, *asc2;
     decode_layout(cv, dtype, B, H, c, E, E2, params, hca ? params2 : nullptr, &sc, &idx, &cnt, &tks,
-                  &asc);
+                  &asc, &asc2);
     if (idx_out) idx = idx_out;
     unsigned *status = (unsigned *)ws;
-    CSA_TRY(do_indexer(dtype, B, 1, hI, dI, E, params->m, qI, w, kIc, q_pos, (float *)sc, 0,
-                       status, st));
+    // The HCA layer's attention does not depend on the CSA layer: when both
+    // run on the tensor-core paths it goes to an auxiliary stream on a slice
+    // of the SMs while the CSA indexer streams kI on the rest.
+    const bool concurrent = hca && dtype == CSA_BF16 && attn_tc_supported(dtype, c) &&
+                            indexer_tc_supported(hI, dI, B, 1, E);
+    int idx_ctas = 0, hca_ctas = 0;
+    if (concurrent) {
+        AuxStreams *ax = nullptr;
+        CSA_TRY(get_aux(&ax));
+        const int sms = device_sms();
+        hca_ctas = sms / 4;
+        idx_ctas = sms - hca_ctas;
+        CSA_TRY_CUDA(cudaEventRecord(ax->fork, st), "fork");
+        CSA_TRY_CUDA(cudaStreamWaitEvent(ax->aux, ax->fork, 0), "fork wait");
+        CSA_TRY(do_attn(dtype, B, 1, H, c, E2, 0, L, q2, q_pos, kvc2, nullptr, nullptr, kv_raw2,
+                        raw_pos0, sink2, out2, nullptr, params2, status, asc2, ax->aux, hca_ctas));
+        CSA_TRY_CUDA(cudaEventRecord(ax->join, ax->aux), "join");
+        CSA_TRY(do_indexer(dtype, B, 1, hI, dI, E, params->m, qI, w, kIc, q_pos, (float *)sc, 0,
+                           status, st, idx_ctas));
+    } else {
+        CSA_TRY(do_indexer(dtype, B, 1, hI, dI, E, params->m, qI, w, kIc, q_pos, (float *)sc, 0,
+                           status, st));
+    }
     CSA_TRY(do_topk(B, 1, E, params->top_k, params->m, (const float *)sc, q_pos, (int32_t *)idx,
                     (int32_t *)cnt, tks, st));
     CSA_TRY(do_attn(dtype, B, 1, H, c, E, params->top_k, L, q, q_pos, kvc, (const int32_t *)idx,
                     (const int32_t *)cnt, kv_raw, raw_pos0, sink, out, nullptr, params, status, asc,
                     st));
-    if (hca)
+    if (concurrent) {
+        AuxStreams *ax = nullptr;
+        CSA_TRY(get_aux(&ax));
+        CSA_TRY_CUDA(cudaStreamWaitEvent(st, ax->join, 0), "join wait");
+    } else if (hca) {
         CSA_TRY(do_attn(dtype, B, 1, H, c, E2, 0, L, q2, q_pos, kvc2, nullptr, nullptr, kv_raw2,
-                        raw_pos0, sink2, out2, nullptr, params2, status, asc, st));
+                        raw_pos0, sink2, out2, nullptr, params2, status, asc2, st));
+    }
     return CSA_OK;
 }
 

@@ -510,31 +510,54 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const __grid_constant__
 }
 
 // Split-KV combine: out[bt, h] = sum_c O_c e^(m_c - M) / (e^(z - M) + sum_c l_c e^(m_c - M)),
-// chunks in a fixed order, then de-rotation.
+// chunks in a fixed order, then de-rotation.  One CTA per (query, head).
 template <int C>
-__global__ void attn_combine_kernel(const AttnTcArgs a) {
+__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnTcArgs a) {
+    __shared__ float s_sc[64], s_red[4];
+    __shared__ float s_M, s_den;
     const int64_t bt = blockIdx.x;
     const int h = blockIdx.y;
     const int hg = h / 64, hl = h % 64;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t t = a.q_pos[bt];
     const int64_t base = (bt * a.n_hg + hg) * a.n_chunks;
     const float zl2 = a.sink[h] * 1.4426950408889634f;
-    float M = zl2;
-    for (int c = 0; c < a.n_chunks; c++) M = fmaxf(M, a.part_ml[((base + c) * 64 + hl) * 2]);
-    float den = (zl2 == -INFINITY) ? 0.f : exp2f(zl2 - M);
-    for (int c = 0; c < a.n_chunks; c++) {
-        const float mc = a.part_ml[((base + c) * 64 + hl) * 2];
-        if (mc != -INFINITY) den += a.part_ml[((base + c) * 64 + hl) * 2 + 1] * exp2f(mc - M);
+    // every chunk's (max, sum) loaded at once, one per thread
+    float mc = -INFINITY, lc = 0.f;
+    if (tid < a.n_chunks) {
+        mc = a.part_ml[((base + tid) * 64 + hl) * 2];
+        lc = a.part_ml[((base + tid) * 64 + hl) * 2 + 1];
     }
-    for (int d = threadIdx.x * 2; d < C; d += blockDim.x * 2) {
+    float mx = mc;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) s_red[warp] = mx;
+    __syncthreads();
+    if (tid == 0) s_M = fmaxf(fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3])), zl2);
+    __syncthreads();
+    const float M = s_M;
+    const float sc = (tid < a.n_chunks && mc != -INFINITY) ? exp2f(mc - M) : 0.f;
+    if (tid < 64) s_sc[tid] = sc;
+    float dl = lc * sc;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, o);
+    __syncthreads();
+    if (lane == 0) s_red[warp] = dl;
+    __syncthreads();
+    if (tid == 0) {
+        float den = s_red[0] + s_red[1] + s_red[2] + s_red[3];
+        if (zl2 != -INFINITY) den += exp2f(zl2 - M);
+        s_den = den;
+    }
+    __syncthreads();
+    const float den = s_den;
+    for (int d = tid * 2; d < C; d += blockDim.x * 2) {
         float y0 = 0.f, y1 = 0.f;
+#pragma unroll 4
         for (int c = 0; c < a.n_chunks; c++) {
-            const float mc = a.part_ml[((base + c) * 64 + hl) * 2];
-            if (mc == -INFINITY) continue;
-            const float sc = exp2f(mc - M);
-            const float *po = a.part_o + ((base + c) * 64 + hl) * (int64_t)C + d;
-            y0 += po[0] * sc;
-            y1 += po[1] * sc;
+            const float2 v = *reinterpret_cast<const float2 *>(a.part_o + ((base + c) * 64 + hl) * (int64_t)C + d);
+            y0 = fmaf(v.x, s_sc[c], y0);
+            y1 = fmaf(v.y, s_sc[c], y1);
         }
         y0 = den > 0.f ? y0 / den : 0.f;
         y1 = den > 0.f ? y1 / den : 0.f;
@@ -545,17 +568,16 @@ __global__ void attn_combine_kernel(const AttnTcArgs a) {
             y0 = r0;
             y1 = r1;
         }
-        __nv_bfloat16 *op = a.out + (bt * a.H + h) * (int64_t)C + d;
-        op[0] = __float2bfloat16_rn(y0);
-        op[1] = __float2bfloat16_rn(y1);
+        *reinterpret_cast<__nv_bfloat162 *>(a.out + (bt * a.H + h) * (int64_t)C + d) =
+            __floats2bfloat162_rn(y0, y1);
     }
-    if (a.lse && threadIdx.x == 0)
+    if (a.lse && tid == 0)
         a.lse[bt * a.H + h] = den > 0.f ? (M + log2f(den)) * 0.6931471805599453f : -INFINITY;
 }
 
 // ------------------------------------------------------------------- host
 
-static int attn_sms() {
+int device_sms() {
     static int n = 0;
     if (!n) {
         int dev = 0;
@@ -585,7 +607,7 @@ int attn_tc_chunks(int64_t rows, int H, int64_t max_list) {
 }
 
 cudaError_t launch_attn_tc(int64_t B, const AttnArgs &g, const int32_t *cnt, int n_chunks,
-                           void *split_ws, cudaStream_t st) {
+                           void *split_ws, int max_ctas, cudaStream_t st) {
     if (B * g.Tq == 0) return cudaSuccess;
     AttnTcArgs a;
     a.q = (const __nv_bfloat16 *)g.q;
@@ -626,7 +648,7 @@ cudaError_t launch_attn_tc(int64_t B, const AttnArgs &g, const int32_t *cnt, int
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    const int sms = attn_sms();
+    const int sms = max_ctas > 0 && max_ctas < device_sms() ? max_ctas : device_sms();
     const int grid = (int)(a.n_items < sms ? a.n_items : sms);
     attn_tc_kernel<512><<<grid, Cfg::THREADS, Cfg::SMEM, st>>>(a);
     count_launches(1);

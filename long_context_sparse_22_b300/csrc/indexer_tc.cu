@@ -384,7 +384,7 @@ static cudaError_t launch_tc(const CUtensorMap &tq, const CUtensorMap &tk, const
 
 cudaError_t launch_indexer_tc(int64_t B, int64_t T, int64_t E, int m, const void *qI,
                               const float *w, const void *kI, const int64_t *q_pos, float *scores,
-                              int write_masked, unsigned *status, cudaStream_t st) {
+                              int write_masked, unsigned *status, int max_ctas, cudaStream_t st) {
     if (B * T == 0 || E == 0) return cudaSuccess;
     IdxArgs a;
     a.w = w; a.q_pos = q_pos; a.scores = scores; a.status = status;
@@ -397,7 +397,7 @@ cudaError_t launch_indexer_tc(int64_t B, int64_t T, int64_t E, int m, const void
     if (!make_tmap_bf16_2d(&tq, qI, (uint64_t)(B * T * 64), 128, decode ? 64 : 256) ||
         !make_tmap_bf16_2d(&tk, kI, (uint64_t)(B * E), 128, 128))
         return cudaErrorInvalidValue;
-    const int sms = num_sms();
+    const int sms = max_ctas > 0 && max_ctas < num_sms() ? max_ctas : num_sms();
     cudaError_t e;
     if (decode) {
         long long tiles = (long long)B * T * a.tps;

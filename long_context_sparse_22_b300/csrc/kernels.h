@@ -44,9 +44,10 @@ cudaError_t launch_indexer_simt(csa_dtype dt, int64_t B, int64_t Tq, int hI, int
 
 bool indexer_tc_supported(int hI, int dI, int64_t B, int64_t T, int64_t E);
 
+// max_ctas > 0 caps the persistent grid (to leave SMs to a concurrent kernel)
 cudaError_t launch_indexer_tc(int64_t B, int64_t T, int64_t E, int m, const void *qI,
                               const float *w, const void *kI, const int64_t *q_pos, float *scores,
-                              int write_masked, unsigned *status, cudaStream_t st);
+                              int write_masked, unsigned *status, int max_ctas, cudaStream_t st);
 
 // scratch: topk_scratch_bytes(B*Tq, E) bytes of device memory (0 for the
 // one-CTA-per-row path, used for rows of at most 16384 entries or many rows)
@@ -64,6 +65,7 @@ bool attn_tc_supported(csa_dtype dt, int c);
 int attn_tc_chunks(int64_t rows, int H, int64_t max_list);
 size_t attn_tc_split_bytes(int64_t rows, int H, int c, int n_chunks);
 cudaError_t launch_attn_tc(int64_t B, const AttnArgs &a, const int32_t *cnt, int n_chunks,
-                           void *split_ws, cudaStream_t st);
+                           void *split_ws, int max_ctas, cudaStream_t st);
+int device_sms();
 
 }  // namespace csa

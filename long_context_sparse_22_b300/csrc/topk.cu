@@ -301,14 +301,19 @@ __global__ void __launch_bounds__(TK_THREADS) topk_final_kernel(TkLong a, int ca
     const uint32_t *gk = a.cand_key + row * a.E;
     const int32_t *gi = a.cand_idx + row * a.E;
     if (n <= cap) {
-        // the chunks' candidates, in index order, packed into shared memory
+        // the chunks' candidates, in index order, packed into shared memory;
+        // every thread locates its items' chunks by binary search so all the
+        // loads are in flight together
         int32_t *si = (int32_t *)(smc + cap);
-        for (int c = 0; c < a.CH; c++) {
-            const uint32_t o = offs[c], nc = offs[c + 1] - offs[c];
-            for (uint32_t i = tid; i < nc; i += TK_THREADS) {
-                smc[o + i] = gk[c * a.CS + i];
-                si[o + i] = gi[c * a.CS + i];
+        for (int64_t j = tid; j < n; j += TK_THREADS) {
+            int lo = 0, hi = a.CH - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if ((int64_t)offs[mid] <= j) lo = mid; else hi = mid - 1;
             }
+            const int64_t src = lo * a.CS + (j - offs[lo]);
+            smc[j] = gk[src];
+            si[j] = gi[src];
         }
         __syncthreads();
         select_core(sh, n, a.k, [&](int64_t j) { return smc[j]; }, [&](int64_t j) { return si[j]; },
