@@ -118,10 +118,12 @@ __device__ __forceinline__ void item_info(const AttnTcArgs &a, int64_t it, ItemI
 }
 
 // Row pointer of list position pos (nullptr: skipped).  Reports bad input.
+// pre: the selected index already loaded for this position, or -2.
 __device__ __forceinline__ const __nv_bfloat16 *entry_row(const AttnTcArgs &a, const ItemInfo &f,
-                                                          int64_t pos, int C, bool report) {
+                                                          int64_t pos, int C, bool report,
+                                                          int32_t pre = -2) {
     if (pos < f.ncomp) {
-        int64_t j = a.idx ? (int64_t)a.idx[f.bt * a.k + pos] : pos;
+        int64_t j = a.idx ? (pre != -2 ? (int64_t)pre : (int64_t)a.idx[f.bt * a.k + pos]) : pos;
         if (j >= 0 && j < a.E) return a.kvc + (f.b * a.E + j) * C;
         if (report && (j != -1 || !a.idx)) atomicOr(a.status, ST_BAD_INDEX);
         return nullptr;
@@ -270,12 +272,23 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const __grid_constant__
             }
             fence_proxy_async();
             tc::mbar_arrive(qfull);
+            // the first 16 tiles' selected indices, loaded together up front
+            int32_t pre[16];
+#pragma unroll
+            for (int u = 0; u < 16; u++) {
+                const int64_t pos = (int64_t)(f.j0 + u) * 64 + tid;
+                pre[u] = (a.idx && tid < 64 && f.j0 + u < f.j1 && pos < f.ncomp) ? a.idx[f.bt * a.k + pos] : -1;
+            }
             // entry tiles
             for (int j = f.j0; j < f.j1; j++, g++) {
                 const int buf = g & 1;
                 tc::mbar_wait(&kempty[buf], ((g >> 1) & 1) ^ 1, a.status, abort_flag);
                 if (tid < 64) {
-                    const __nv_bfloat16 *rp = entry_row(a, f, (int64_t)j * 64 + tid, C, true);
+                    int32_t jv = -2;                 // -2: not prefetched
+#pragma unroll
+                    for (int u = 0; u < 16; u++)
+                        if (j - f.j0 == u) jv = pre[u];
+                    const __nv_bfloat16 *rp = entry_row(a, f, (int64_t)j * 64 + tid, C, true, jv);
                     rowp[buf * 64 + tid] = rp;
                     valid[buf * 64 + tid] = rp != nullptr;
                 }
@@ -306,8 +319,6 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const __grid_constant__
             uint32_t g = 0, ii = 0;
             auto issue_pv = [&](uint32_t gp, bool first) {
                 const int bp = gp & 1;
-                tc::mbar_wait(&pfull[bp], (gp >> 1) & 1, a.status, abort_flag);
-                if (first) tc::mbar_wait(oempty, (ii & 1) ^ 1, a.status, abort_flag);
                 tc::fence_after_sync();
                 const uint32_t kb = kBase + bp * Cfg::K_BYTES, pb = pBase + bp * Cfg::P_BYTES;
 #pragma unroll
@@ -328,25 +339,54 @@ __global__ void __launch_bounds__(256, 1) attn_tc_kernel(const __grid_constant__
                 if (f.j0 >= f.j1) continue;
                 tc::mbar_wait(qfull, ii & 1, a.status, abort_flag);
                 const uint32_t gfirst = g;
-                for (int j = f.j0; j < f.j1; j++, g++) {
-                    const int buf = g & 1;
-                    tc::mbar_wait(&kfull[buf], (g >> 1) & 1, a.status, abort_flag);
-                    tc::mbar_wait(&sempty[buf], ((g >> 1) & 1) ^ 1, a.status, abort_flag);
-                    tc::fence_after_sync();
-                    const uint32_t kb = kBase + buf * Cfg::K_BYTES;
-#pragma unroll
-                    for (int at = 0; at < Cfg::NA; at++)
-#pragma unroll
-                        for (int kk = 0; kk < 4; kk++) {
-                            const uint64_t ad = desc_sw128(kb + at * (Cfg::TE * 128) + kk * 32, 16, 1024);
-                            const uint64_t bd = desc_sw128(qBase + at * (Cfg::HG * 128) + kk * 32, 16, 1024);
-                            tc::mma_bf16(tmem + Cfg::S_COL + buf * 64, ad, bd, idQK, (at | kk) != 0);
+                const int nt = f.j1 - f.j0;
+                // Issue whichever product is ready: PV(j) as soon as P(j) is
+                // written (it frees tile j's buffer for the loader), QK(j+1) as
+                // soon as tile j+1 has landed.  A fixed order would make each
+                // tile's load wait for the previous tile's load.
+                int nq = 0, np = 0;
+                long long idle = 0;
+                while (np < nt) {
+                    bool did = false;
+                    if (np < nq) {
+                        const uint32_t gp = gfirst + np;
+                        if (tc::mbar_test(&pfull[gp & 1], (gp >> 1) & 1) &&
+                            (np > 0 || tc::mbar_test(oempty, (ii & 1) ^ 1))) {
+                            issue_pv(gp, np == 0);
+                            np++;
+                            did = true;
                         }
-                    tc::mma_commit(&sfull[buf]);
-                    if (j == f.j1 - 1) tc::mma_commit(qempty);
-                    if (j > f.j0) issue_pv(g - 1, g - 1 == gfirst);
+                    }
+                    if (nq < nt && nq <= np + 1) {
+                        const uint32_t gq = gfirst + nq;
+                        const int buf = gq & 1;
+                        if (tc::mbar_test(&kfull[buf], (gq >> 1) & 1) &&
+                            tc::mbar_test(&sempty[buf], ((gq >> 1) & 1) ^ 1)) {
+                            tc::fence_after_sync();
+                            const uint32_t kb = kBase + buf * Cfg::K_BYTES;
+#pragma unroll
+                            for (int at = 0; at < Cfg::NA; at++)
+#pragma unroll
+                                for (int kk = 0; kk < 4; kk++) {
+                                    const uint64_t ad = desc_sw128(kb + at * (Cfg::TE * 128) + kk * 32, 16, 1024);
+                                    const uint64_t bd = desc_sw128(qBase + at * (Cfg::HG * 128) + kk * 32, 16, 1024);
+                                    tc::mma_bf16(tmem + Cfg::S_COL + buf * 64, ad, bd, idQK, (at | kk) != 0);
+                                }
+                            tc::mma_commit(&sfull[buf]);
+                            if (nq == nt - 1) tc::mma_commit(qempty);
+                            nq++;
+                            did = true;
+                        }
+                    }
+                    if (did) {
+                        idle = 0;
+                    } else if (++idle > tc::SPIN_LIMIT || ((idle & 1023) == 0 && *abort_flag)) {
+                        if (!*abort_flag) atomicOr(a.status, ST_TIMEOUT);
+                        *abort_flag = 1;
+                        break;
+                    }
                 }
-                issue_pv(g - 1, g - 1 == gfirst);
+                g = gfirst + nt;
                 tc::mma_commit(ofull);
                 ii++;
             }
