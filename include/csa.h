@@ -192,6 +192,28 @@ csa_status topk_select(int64_t B, int64_t T, int64_t E, int32_t k, int32_t m,
                        int32_t *idx, int32_t *cnt,
                        void *ws, size_t ws_bytes, void *stream);
 
+/*
+ * topk_select without a workspace: the same selection and outputs as
+ * topk_select, for callers that cannot allocate device memory (for example
+ * code that runs where cudaMalloc is unavailable or forbidden and only gets
+ * its input and output buffers from someone else).  The pages have no
+ * counterpart; this is a property of the library, not of the method.
+ *  - Scratch lives in a 17 MiB device array inside the library, held by every
+ *    GPU that loads it until the process exits.  Rows of more than 16384
+ *    entries (the multi-CTA path) need it; they are limited to at most 64
+ *    rows and 2^21 row x entry products, and larger requests return
+ *    CSA_ERR_UNSUPPORTED with nothing enqueued.
+ *  - The first call on a device looks up that array's device address (with
+ *    the device current); make that first call before any stream capture.
+ *  - All calls share the one array: calls that overlap on the GPU (two
+ *    streams, or two threads) race and corrupt each other.  Serialise them.
+ *  - It allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ *    call.
+ */
+csa_status topk_select_noalloc(int64_t B, int64_t T, int64_t E, int32_t k, int32_t m,
+                               const float *scores, const int64_t *q_pos,
+                               int32_t *idx, int32_t *cnt, void *stream);
+
 /* --------------------------------------------------------------------- */
 /* 3. Core attention.                                                     */
 /* --------------------------------------------------------------------- */

@@ -57,6 +57,8 @@ _SIGS = {
     "topk_select_ws_size": ([C.c_int64, C.c_int64, C.c_int64, C.c_int32], C.c_size_t),
     "topk_select": ([C.c_int64, C.c_int64, C.c_int64, C.c_int32, C.c_int32] + [C.c_void_p] * 4
                     + [C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
+    "topk_select_noalloc": ([C.c_int64, C.c_int64, C.c_int64, C.c_int32, C.c_int32] + [C.c_void_p] * 4
+                            + [C.c_void_p], C.c_int),
     "attn_ws_size": ([C.c_int, C.c_int64, C.c_int64, C.c_int32, C.c_int32, C.c_int64, C.c_int32,
                       C.POINTER(CsaParams)], C.c_size_t),
     "sparse_attn": ([C.c_int, C.c_int64, C.c_int64, C.c_int32, C.c_int32, C.c_int64, C.c_int32,
@@ -208,6 +210,19 @@ def topk_select(scores, q_pos, m, k, idx=None, cnt=None, ws=None):
     ws = _ws(lib().topk_select_ws_size(B, T, E, k), ws)
     _check(lib().topk_select(B, T, E, k, m, _p(scores), _p(q_pos), _p(idx), _p(cnt), ws.ptr,
                              ws.nbytes, _stream()), "topk_select")
+    return idx, cnt
+
+
+def topk_select_noalloc(scores, q_pos, m, k, idx=None, cnt=None):
+    """topk_select that takes no workspace (its scratch is a fixed array inside
+    the library); for callers that cannot allocate device memory."""
+    B, T, E = scores.shape
+    if idx is None:
+        idx = torch.empty((B, T, k), dtype=torch.int32, device=scores.device)
+    if cnt is None:
+        cnt = torch.empty((B, T), dtype=torch.int32, device=scores.device)
+    _check(lib().topk_select_noalloc(B, T, E, k, m, _p(scores), _p(q_pos), _p(idx), _p(cnt),
+                                     _stream()), "topk_select_noalloc")
     return idx, cnt
 
 

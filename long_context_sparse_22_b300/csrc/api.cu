@@ -28,6 +28,12 @@ csa_status fail(csa_status s, const char *fmt, ...) {
     return s;
 }
 
+}  // namespace
+
+csa_status csa::report_error(csa_status s, const char *msg) { return fail(s, "%s", msg); }
+
+namespace {
+
 csa_status cuda_fail(cudaError_t e, const char *where) {
     return fail(CSA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
 }

@@ -11,6 +11,9 @@ namespace csa {
 // Every kernel launch of the library is counted (csa_launch_count).
 void count_launches(int n);
 
+// Record a failure message for csa_last_error() and return s.
+csa_status report_error(csa_status s, const char *msg);
+
 struct AttnArgs {
     const void *q;
     const int64_t *q_pos;

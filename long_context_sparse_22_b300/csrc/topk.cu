@@ -18,6 +18,8 @@
 // keeps, in index order, only the entries whose top bits reach the bin that
 // holds the k-th largest key, (3) one CTA per row runs the exact selection on
 // those candidates (a few thousand) in index order.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -403,4 +405,67 @@ cudaError_t launch_topk(int64_t B, int64_t Tq, int64_t E, int k, int m, const fl
     return cudaGetLastError();
 }
 
+// -------------------------------------------------- allocation-free selection
+//
+// Callers that cannot allocate device memory (code running where cudaMalloc
+// is not available or not allowed, e.g. inside an allocator-free serving loop
+// or a host that only hands over pre-registered buffers) can still select
+// over long rows: topk_select_noalloc keeps its scratch (histograms, chunk
+// counts, candidates) in the file-scope device array below instead of a
+// caller workspace.  Limits: at most NOALLOC_MAX_ROWS rows and
+// NOALLOC_MAX_ENTRIES = rows x E entries when the long-row path is taken.
+constexpr int64_t NOALLOC_MAX_ROWS = 64;
+constexpr int64_t NOALLOC_MAX_ENTRIES = int64_t(1) << 21;
+constexpr size_t NOALLOC_BYTES = size_t(17) << 20;   // 17 MiB on every device that loads the library
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_BYTES];
+
+static std::mutex g_noalloc_mu;
+static void *g_noalloc_ptr[64];
+
+// The array's device address, looked up once per device with that device
+// current (host code only holds a stand-in for the symbol).
+static cudaError_t noalloc_scratch(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> g(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+
 }  // namespace csa
+
+extern "C" csa_status topk_select_noalloc(int64_t B, int64_t T, int64_t E, int32_t k, int32_t m,
+                                         const float *scores, const int64_t *q_pos, int32_t *idx,
+                                         int32_t *cnt, void *stream) {
+    using namespace csa;
+    auto bad = [](const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+    if (B < 0 || T < 0 || E < 0) return report_error(CSA_ERR_INVALID_ARG, "negative size");
+    if (k < 1 || k > 2048) return report_error(CSA_ERR_UNSUPPORTED, "k not in 1..2048");
+    if (m < 1) return report_error(CSA_ERR_INVALID_ARG, "m must be >= 1");
+    if (E > 2147483647LL) return report_error(CSA_ERR_UNSUPPORTED, "E too large");
+    const int64_t rows = B * T;
+    if (rows == 0) return CSA_OK;
+    if ((E > 0 && bad(scores)) || bad(q_pos) || bad(idx) || bad(cnt))
+        return report_error(CSA_ERR_INVALID_ARG, "a tensor pointer is NULL or not 16-byte aligned");
+    void *scratch = nullptr;
+    if (topk_use_long(rows, E)) {
+        if (rows > NOALLOC_MAX_ROWS || rows * E > NOALLOC_MAX_ENTRIES ||
+            topk_scratch_bytes(rows, E) > NOALLOC_BYTES)
+            return report_error(CSA_ERR_UNSUPPORTED,
+                                "topk_select_noalloc: rows x entries beyond its static scratch "
+                                "(at most 64 rows and 2^21 entries in all); use topk_select");
+        cudaError_t e = noalloc_scratch(&scratch);
+        if (e != cudaSuccess) return report_error(CSA_ERR_CUDA, cudaGetErrorString(e));
+    }
+    cudaError_t e = launch_topk(B, T, E, k, m, scores, q_pos, idx, cnt, scratch, (cudaStream_t)stream);
+    if (e != cudaSuccess) return report_error(CSA_ERR_CUDA, cudaGetErrorString(e));
+    return CSA_OK;
+}
