@@ -70,6 +70,30 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
+    def samples(self) -> int:
+        """Rows nvidia-smi has written so far."""
+        if self.proc is None:
+            return 0
+        try:
+            with open(self.file.name) as f:
+                return sum(1 for line in f if line.count(",") >= 8)
+        except OSError:
+            return 0
+
+    def keep_busy(self, step, rows: int, limit_s: float = 5.0):
+        """Run untimed steps until `rows` more samples have arrived, so that
+        the samples taken right before and after a short timed region are
+        taken under the same load."""
+        if self.proc is None:
+            return
+        import torch
+        want = self.samples() + rows
+        t0 = time.time()
+        while self.samples() < want and time.time() - t0 < limit_s:
+            for _ in range(4):
+                step()
+            torch.cuda.synchronize()
+
     def stop(self):
         if self.proc is None:
             return None
@@ -319,6 +343,8 @@ def run_ours(args, rank, world, dist):
     csa.timing_enable(True)
     clocks = ClockSampler(local)
     clocks.start()
+    clocks.keep_busy(wl.step, 2)
+    csa.timing_read()            # drop the stage times of the untimed steps
     barrier()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -330,9 +356,10 @@ def run_ours(args, rank, world, dist):
     n_launches = csa.launch_count() - n_launch0
     torch.cuda.synchronize()
     barrier()
-    clk = clocks.stop()
     csa.timing_enable(False)
     stages = csa.timing_read()
+    clocks.keep_busy(wl.step, 2)
+    clk = clocks.stop()
     ms_total = ev0.elapsed_time(ev1)
     ms_step = ms_total / args.steps
     if dist is not None:
