@@ -226,7 +226,10 @@ csa_status do_attn(csa_dtype dt, int64_t B, int64_t T, int H, int c, int64_t E, 
     a.scale = p->scale > 0.f ? p->scale : (float)(1.0 / sqrt((double)c));
     a.rope = make_rope(c, p->rope_dims, p->rope_theta);
     StageScope sc(idx ? CSA_STAGE_SPARSE_ATTN : CSA_STAGE_HCA_ATTN, st);
-    if (attn_tc_supported(dt, c)) {
+    // the tensor-core path addresses rows of q, kvc and kv_raw with 32-bit TMA coordinates
+    const int64_t lim = 2147483647LL - 65536;
+    const bool fits = B * T * H < lim && B * E < lim && B * L < lim;
+    if (attn_tc_supported(dt, c) && fits) {
         const int64_t max_list = (idx ? (int64_t)k : E) + p->n_win;
         int ch = attn_tc_chunks(B * T, H, max_list);
         if (ch > 1 && scratch == nullptr) ch = 1;

@@ -1,34 +1,43 @@
-// Core attention on the 5th-generation tensor cores (bf16 in, fp32 out of
-// tensor memory): shared-KV MQA over a per-query list of entries (selected
-// or visible compressed entries, then the window rows) plus a sink logit.
+// Core attention on the 5th-generation tensor cores (bf16 in, fp32 in tensor
+// memory): shared-KV MQA over a per-query list of entries (selected or
+// visible compressed entries, then the window rows) plus a sink logit.
 //
 // [DeepSeek-V4 book ch.6 "Shared key-value MQA"; ch.7 "The sliding window",
 // "Partial rotary position embeddings", "Why the output is de-rotated",
 // "Attention sinks"; "DeepSeek-V4: Making Million-Token Context an
 // Architectural Problem", Key design 1 and 2.]
 //
-// Orientation: the entries of one tile (64) sit on the MMA's M side and the
-// 64 heads of a head group on N, so one entry row read from HBM/L2 feeds all
-// heads:
-//   S^T[e, h]  = K[e, :] . q~[h, :]           M = 64 entries,  N = 64 heads
-//   O^T[d, h] += V[:, d]^T . P^T[:, h]         M = 128 dims (x C/128), N = 64
-// K = V is the same gathered tile; for the second product it is read as an
-// MN-major operand, so no transposed copy exists.  The softmax runs across
-// TMEM lanes: S^T is staged through shared memory, each head's max and
-// exponentials are taken by two threads, and O^T in tensor memory is
-// rescaled only when a head's running max grows by more than 2^8 (results
-// are exact either way because the denominator uses the same max).  The sink
-// logit seeds the running max and enters only the denominator.
+// One work item is (query, group of 64 heads[, split-KV chunk]).  Its list is
+// cut into 64-entry tiles: first the compressed slots (padded up to a whole
+// tile), then the window rows p0..t (at most two tiles).  Per tile:
+//   S[h, e]    = q~[h, :] . K[e, :]             M = 64 heads,  N = 64 entries
+//   O^T[d, h] += V[:, d]^T . P^T[:, h]           M = 128 dims (x C/128), N = 64
+// K = V is the same tile in shared memory; the second product reads it as an
+// MN-major operand.  With heads on the rows of S, every head's logits of a
+// tile sit in one thread, so the running max, the exponentials and the sum
+// need no cross-thread exchange.  O^T is rescaled in tensor memory only when
+// some head's running max grows by more than 2^8 (exact either way, because
+// the denominator uses the same max); a barrier reduction tells the four
+// softmax warps whether any head needs it.  The sink logit seeds the running
+// max and enters only the denominator.
+//
+// Selected compressed entries are gathered by cp.async, 16 bytes per thread
+// and instruction, into the 128-byte-swizzled layout (the tensor-memory
+// copy engine's four-row gather sustains only about a fifth of that rate);
+// contiguous rows (the window, or every visible entry of the dense variant)
+// arrive as 64-row TMA boxes.  Rows that are not part of the list (padding,
+// -1 slots, rows past t) are zero-filled or hold finite data, and are masked
+// out of the softmax by a per-tile presence mask.
 //
 // Warp roles (persistent CTAs, items dealt round-robin):
-//   warps 0-2  q~ preparation (cp.async of the q rows into the swizzled
-//              layout, then RoPE at t in place) and the cp.async gather of
-//              each 64-entry tile into a 128-byte-swizzled K-major layout
-//              (two tile buffers);
-//   warp 3     TMEM allocator and MMA issuer: QK(j+1) is issued before
-//              PV(j), so the tensor core works while tile j's softmax runs;
-//   warps 4-7  softmax, O rescale, and the epilogue (normalise, de-rotate,
-//              store), or fp32 partial outputs for a split-KV combine.
+//   warps 0-3  loaders: q tile (box TMA, then RoPE at t in place), the entry
+//              tiles (two buffers), the presence masks;
+//   warp 4     TMEM allocator and MMA issuer (one thread): QK and PV in
+//              whichever order their inputs become ready;
+//   warps 5-8  softmax (one head per thread), the O rescale, and the
+//              epilogue: normalise, de-rotate, stage a 128-dim chunk in
+//              shared memory and write it with one TMA store (or fp32
+//              partial outputs for a split-KV combine).
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -37,34 +46,37 @@ namespace csa {
 
 template <int C>
 struct AtCfg {
-    static constexpr int NA = C / 64;             // 64-dim atoms
-    static constexpr int NC = C / 128;            // 128-dim output chunks
+    static constexpr int NA = C / 64;             // 64-dim atoms (128-byte rows)
+    static constexpr int NC = C / 128;            // 128-dim O^T chunks
     static constexpr int TE = 64;                 // entries per tile
-    static constexpr int HG = 64;                 // heads per CTA item
-    static constexpr int K_BYTES = NA * TE * 128; // one tile
+    static constexpr int HG = 64;                 // heads per item
+    static constexpr int ATOM = TE * 128;         // one atom of a tile: 64 rows x 128 B
+    static constexpr int K_BYTES = NA * ATOM;
     static constexpr int Q_BYTES = NA * HG * 128;
     static constexpr int P_BYTES = HG * 128;      // 64 heads x 64 entries bf16
-    static constexpr int STAGE_LD = 65;
     static constexpr int OFF_K = 0;
     static constexpr int OFF_Q = OFF_K + 2 * K_BYTES;
     static constexpr int OFF_P = OFF_Q + Q_BYTES;
-    static constexpr int OFF_STAGE = OFF_P + 2 * P_BYTES;
-    static constexpr int OFF_MISC = OFF_STAGE + TE * STAGE_LD * 4;
-    static constexpr int MISC_BYTES = 2176;
-    static constexpr int SMEM = OFF_MISC + MISC_BYTES;
+    static constexpr int OFF_MISC = OFF_P + 2 * P_BYTES;
+    static constexpr int MISC_BYTES = 6144;
+    static constexpr int SMEM = OFF_MISC + MISC_BYTES + 1024;   // + alignment slack
     static constexpr int TMEM_COLS = 512;
-    static constexpr int S_COL = 0;               // two S^T buffers: cols 0, 64
+    static constexpr int S_COL = 0;               // two S buffers: cols 0, 64
     static constexpr int O_COL = 128;             // O^T chunks: 128 + 64 c
-    static constexpr int THREADS = 256;
+    static constexpr int LOAD_WARPS = 4;          // warps 0-3: loaders
+    static constexpr int NLOAD = LOAD_WARPS * 32;
+    static constexpr int MMA_WARP = 4;            // warp 4: TMEM allocation, QK issue
+    static constexpr int SM_WARP0 = 5;            // warps 5-8: softmax and epilogue
+    static constexpr int PV_WARP = 9;             // warp 9: PV issue
+    static constexpr int THREADS = (PV_WARP + 1) * 32;
 };
 
 struct AttnTcArgs {
-    const __nv_bfloat16 *q;
-    const int64_t *q_pos;
     const __nv_bfloat16 *kvc;
+    const void *zsrc;        // any valid 16-byte-aligned address (source of zero-filled copies)
+    const int64_t *q_pos;
     const int32_t *idx;      // [B,T,k] or nullptr: every visible entry
     const int32_t *cnt;      // [B,T] kept count of idx rows, or nullptr (use k)
-    const __nv_bfloat16 *kv_raw;
     const int64_t *raw_pos0;
     const float *sink;
     __nv_bfloat16 *out;
@@ -84,8 +96,10 @@ struct AttnTcArgs {
 struct ItemInfo {
     int64_t bt, b, t;
     int hg, chunk;
-    int64_t ncomp, p0, total;   // list: ncomp compressed slots, then window rows p0..t
-    int j0, j1;                 // tile range of this item
+    int64_t ncomp;           // compressed slots (tiles 0 .. ntc-1)
+    int64_t p0, nwin;        // window rows p0 .. p0+nwin-1 (tiles ntc ..)
+    int ntc, nt;             // compressed tiles, all tiles
+    int j0, j1;              // tile range of this item
 };
 
 __device__ __forceinline__ void item_info(const AttnTcArgs &a, int64_t it, ItemInfo &f) {
@@ -101,48 +115,25 @@ __device__ __forceinline__ void item_info(const AttnTcArgs &a, int64_t it, ItemI
     f.t = a.q_pos[f.bt];
     if (a.idx) f.ncomp = a.cnt ? a.cnt[f.bt] : a.k;
     else f.ncomp = visible_count(f.t, a.m, a.E);
+    if (f.ncomp < 0) f.ncomp = 0;
     int64_t p0 = f.t - a.n_win + 1;
     if (p0 < 0) p0 = 0;
     f.p0 = p0;
-    const int64_t nwin = a.n_win > 0 ? f.t - p0 + 1 : 0;
-    f.total = f.ncomp + (nwin > 0 ? nwin : 0);
-    const int nt = (int)((f.total + 63) / 64);
+    f.nwin = a.n_win > 0 && f.t >= 0 ? f.t - p0 + 1 : 0;
+    f.ntc = (int)((f.ncomp + 63) / 64);
+    f.nt = f.ntc + (int)((f.nwin + 63) / 64);
     if (a.chunk_tiles > 0) {
         f.j0 = f.chunk * a.chunk_tiles;
-        f.j1 = f.j0 + a.chunk_tiles < nt ? f.j0 + a.chunk_tiles : nt;
+        f.j1 = f.j0 + a.chunk_tiles < f.nt ? f.j0 + a.chunk_tiles : f.nt;
         if (f.j0 > f.j1) f.j0 = f.j1;
     } else {
         f.j0 = 0;
-        f.j1 = nt;
+        f.j1 = f.nt;
     }
-}
-
-// Row pointer of list position pos (nullptr: skipped).  Reports bad input.
-// pre: the selected index already loaded for this position, or -2.
-__device__ __forceinline__ const __nv_bfloat16 *entry_row(const AttnTcArgs &a, const ItemInfo &f,
-                                                          int64_t pos, int C, bool report,
-                                                          int32_t pre = -2) {
-    if (pos < f.ncomp) {
-        int64_t j = a.idx ? (pre != -2 ? (int64_t)pre : (int64_t)a.idx[f.bt * a.k + pos]) : pos;
-        if (j >= 0 && j < a.E) return a.kvc + (f.b * a.E + j) * C;
-        if (report && (j != -1 || !a.idx)) atomicOr(a.status, ST_BAD_INDEX);
-        return nullptr;
-    }
-    if (pos < f.total) {
-        const int64_t row = f.p0 + (pos - f.ncomp) - a.raw_pos0[f.b];
-        if (row >= 0 && row < a.L) return a.kv_raw + (f.b * a.L + row) * C;
-        if (report) atomicOr(a.status, ST_NO_WINDOW_ROW);
-    }
-    return nullptr;
 }
 
 __device__ __forceinline__ int swz128(int row, int byte) {   // within a 1024-byte atom group
     return (row & 7) * 128 + ((((byte >> 4) ^ row) & 7) << 4) + (byte & 15);
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
-                 : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async() {
@@ -153,15 +144,43 @@ __device__ __forceinline__ void named_bar(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
+// Barrier over n threads that also returns whether any of them passed true.
+__device__ __forceinline__ bool named_bar_or(int id, int n, bool v) {
+    uint32_t r;
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
-        "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]),
-        "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]),
-        "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %3, 0;\n\t"
+        "barrier.cta.red.or.pred q, %1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(id), "r"(n), "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// 32 lanes x 16 consecutive 32-bit columns, load and store.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
 
@@ -179,371 +198,512 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr, uint32_t lbo, uint
     return d;
 }
 
+// Wait by lane 0 of a warp, result broadcast to the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, unsigned *status,
+                                          volatile int *abort_flag, int lane) {
+    bool ok = true;
+    if (lane == 0) ok = tc::mbar_wait(bar, parity, status, abort_flag);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
+                 : "memory");
+}
+
 template <int C>
-__global__ void __launch_bounds__(256, 1) attn_tc_kernel(const __grid_constant__ AttnTcArgs a) {
+__global__ void __launch_bounds__(AtCfg<C>::THREADS, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
+               const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_o,
+               const __grid_constant__ AttnTcArgs a) {
     using Cfg = AtCfg<C>;
-    extern __shared__ __align__(1024) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sK = smem + Cfg::OFF_K;
     uint8_t *sQ = smem + Cfg::OFF_Q;
     uint8_t *sP = smem + Cfg::OFF_P;
-    float *stage = (float *)(smem + Cfg::OFF_STAGE);
     uint8_t *misc = smem + Cfg::OFF_MISC;
-    uint64_t *bar = (uint64_t *)misc;                  // 16 barriers
+    uint64_t *bar = (uint64_t *)misc;                  // 32 barrier slots
     uint64_t *kfull = bar + 0, *kempty = bar + 2, *sfull = bar + 4, *sempty = bar + 6;
     uint64_t *pfull = bar + 8, *pempty = bar + 10;
-    uint64_t *qfull = bar + 12, *qempty = bar + 13, *ofull = bar + 14, *oempty = bar + 15;
-    uint32_t *tmem_slot = (uint32_t *)(misc + 128);
-    volatile int *abort_flag = (volatile int *)(misc + 132);
-    volatile int *rescale_flag = (volatile int *)(misc + 136);
-    float *alpha_s = (float *)(misc + 256);            // [64]
-    float *den_s = (float *)(misc + 512);              // [64]
-    float *cs_s = (float *)(misc + 768);               // [64] cos, then sin
-    const __nv_bfloat16 **rowp = (const __nv_bfloat16 **)(misc + 1024);   // [2][64]
-    uint8_t *valid = misc + 2048;                      // [2][64] entry present
+    uint64_t *qland = bar + 12, *qfull = bar + 13, *qempty = bar + 14;
+    uint64_t *ofull = bar + 15, *oempty = bar + 16, *mdone = bar + 17;
+    uint32_t *tmem_slot = (uint32_t *)(misc + 256);
+    volatile int *abort_flag = (volatile int *)(misc + 260);
+    uint32_t *vmask32 = (uint32_t *)(misc + 272);      // [2 buffers][2 halves] presence bits
+    float *alpha_s = (float *)(misc + 512);            // [2][64]
+    float *inv_den_s = (float *)(misc + 1024);         // [64]
+    float *cs_s = (float *)(misc + 2048);              // [2][256]: cos, sin of the query angle
+    const __nv_bfloat16 **rowp = (const __nv_bfloat16 **)(misc + 4096);   // [2][64] gathered rows
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x;
-    if ((tc::smem_u32(smem) & 1023u) != 0) {            // the layout needs 1024-byte alignment
-        if (threadIdx.x == 0) atomicOr(a.status, ST_TIMEOUT);
-        return;
-    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; i++) {
-            tc::mbar_init(&kfull[i], 96);
+            tc::mbar_init(&kfull[i], Cfg::NLOAD);
             tc::mbar_init(&kempty[i], 1);
             tc::mbar_init(&sfull[i], 1);
             tc::mbar_init(&sempty[i], 4);
-            tc::mbar_init(&pfull[i], 1);
+            tc::mbar_init(&pfull[i], 4);
             tc::mbar_init(&pempty[i], 1);
         }
-        tc::mbar_init(qfull, 96);
+        tc::mbar_init(qland, 1);
+        tc::mbar_init(qfull, 1);
         tc::mbar_init(qempty, 1);
         tc::mbar_init(ofull, 1);
         tc::mbar_init(oempty, 4);
+        tc::mbar_init(mdone, 2);
         *abort_flag = 0;
-        *rescale_flag = 0;
         tc::fence_barrier_init();
+        tc::prefetch_tmap(&tm_q);
+        tc::prefetch_tmap(&tm_c);
+        tc::prefetch_tmap(&tm_w);
+        tc::prefetch_tmap(&tm_o);
     }
-    if (warp == 3) tc::tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    if (warp == Cfg::MMA_WARP) tc::tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp < 3) {
-        // ------------------------------------------------------ loader / q~ prep
-        constexpr int NL = 96;           // loader threads
-        const int tid = threadIdx.x;     // 0..95
-        const uint32_t qb = tc::smem_u32(sQ);
-        uint32_t g = 0, ii = 0;          // ii counts processed (non-empty) items
-        for (int64_t it = blockIdx.x; it < a.n_items; it += G) {
+    if (warp < Cfg::LOAD_WARPS) {
+        // ------------------------------------------------------------ loaders
+        const int tid = threadIdx.x;                     // 0 .. NLOAD-1
+        const uint32_t kb0 = tc::smem_u32(sK);
+        uint32_t g = 0, ii = 0;
+        uint32_t tma_issued = 0, last_g[2] = {0, 0}, q_pending = 0;
+        bool ok = true;
+        for (int64_t it = blockIdx.x; ok && it < a.n_items; it += G) {
             ItemInfo f;
             item_info(a, it, f);
             if (f.j0 >= f.j1) continue;
-            // q rows -> the K-major swizzled layout [NA][64 heads][128 B] by cp.async
-            tc::mbar_wait(qempty, (ii & 1) ^ 1, a.status, abort_flag);
-            const int h0 = f.hg * Cfg::HG;
-            for (int i = tid; i < Cfg::HG * Cfg::NA * 8; i += NL) {
-                const int h = i / (Cfg::NA * 8);
-                const int gr = i % (Cfg::NA * 8);           // 16-byte granule of the row
-                const uint32_t dst = qb + (gr >> 3) * (Cfg::HG * 128) + (h >> 3) * 1024 + swz128(h, (gr & 7) * 16);
-                const bool ok = h0 + h < a.H;
-                cp_async16(dst, ok ? (const void *)(a.q + (f.bt * a.H + h0 + h) * (int64_t)C + gr * 8)
-                                   : (const void *)a.q, ok ? 16u : 0u);
+            // q rows of the next item on their way to L2 while this one runs
+            if (it + G < a.n_items && tid < Cfg::NA) {
+                ItemInfo fn;
+                item_info(a, it + G, fn);
+                const int y = (int)(fn.bt * a.H + fn.hg * Cfg::HG);
+                asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                                 reinterpret_cast<uint64_t>(&tm_q)),
+                             "r"(tid * 64), "r"(y)
+                             : "memory");
             }
-            asm volatile("cp.async.commit_group;" ::: "memory");
-            if (tid < a.rope.pairs && tid < 32) {
-                float cs, sn;
-                rope_cos_sin((double)f.t, a.rope.w[tid], cs, sn);
-                cs_s[tid] = cs;
-                cs_s[32 + tid] = sn;
+            // this item's q rows (box TMA) and the cos / sin of its angle.  Waits
+            // are warp-uniform and the four loader warps agree on a failure
+            // through a barrier reduction, so none is left at a named barrier.
+            if (named_bar_or(2, Cfg::NLOAD, !warp_wait(qempty, (ii & 1) ^ 1, a.status, abort_flag, lane))) {
+                ok = false;
+                break;
             }
-            asm volatile("cp.async.wait_group 0;" ::: "memory");
-            named_bar(2, NL);
-            // q~ = RoPE(q, t): rotate the rotary pairs in place
-            for (int i = tid; i < Cfg::HG * a.rope.pairs; i += NL) {
-                const int h = i / a.rope.pairs, pi = i % a.rope.pairs;
-                const int d = a.rope.first + 2 * pi;
-                __nv_bfloat162 *pv = (__nv_bfloat162 *)(sQ + (d >> 6) * (Cfg::HG * 128) + (h >> 3) * 1024 +
-                                                        swz128(h, (d & 63) * 2));
-                const float2 x = __bfloat1622float2(*pv);
-                const float c_ = cs_s[pi], s_ = cs_s[32 + pi];
-                *pv = __floats2bfloat162_rn(x.x * c_ - x.y * s_, x.x * s_ + x.y * c_);
+            if (tid == 0) {
+                tc::mbar_expect_tx(qland, Cfg::Q_BYTES);
+                for (int at = 0; at < Cfg::NA; at++)
+                    tc::tma_load_2d(sQ + at * (Cfg::HG * 128), &tm_q, at * 64,
+                                    (int)(f.bt * a.H + f.hg * Cfg::HG), qland);
+                q_pending = 1;
             }
-            fence_proxy_async();
-            tc::mbar_arrive(qfull);
-            // the first 16 tiles' selected indices, loaded together up front
-            int32_t pre[16];
-#pragma unroll
-            for (int u = 0; u < 16; u++) {
-                const int64_t pos = (int64_t)(f.j0 + u) * 64 + tid;
-                pre[u] = (a.idx && tid < 64 && f.j0 + u < f.j1 && pos < f.ncomp) ? a.idx[f.bt * a.k + pos] : -1;
+            for (int pi = tid; pi < a.rope.pairs; pi += Cfg::NLOAD) {
+                float c_, s_;
+                rope_cos_sin((double)f.t, a.rope.w[pi], c_, s_);
+                cs_s[pi] = c_;
+                cs_s[256 + pi] = s_;
             }
-            // entry tiles
+            named_bar(2, Cfg::NLOAD);
+            const int q_after = (f.j1 - f.j0 > 1 ? f.j0 + 1 : f.j0);
+            int32_t iv = -1;                     // selected index of this thread's slot, next tile
+            if (a.idx && tid < 64 && f.j0 < f.ntc) {
+                const int64_t pos = (int64_t)f.j0 * 64 + tid;
+                iv = pos < f.ncomp ? a.idx[f.bt * a.k + pos] : -1;
+            }
             for (int j = f.j0; j < f.j1; j++, g++) {
                 const int buf = g & 1;
-                tc::mbar_wait(&kempty[buf], ((g >> 1) & 1) ^ 1, a.status, abort_flag);
-                if (tid < 64) {
-                    int32_t jv = -2;                 // -2: not prefetched
-#pragma unroll
-                    for (int u = 0; u < 16; u++)
-                        if (j - f.j0 == u) jv = pre[u];
-                    const __nv_bfloat16 *rp = entry_row(a, f, (int64_t)j * 64 + tid, C, true, jv);
-                    rowp[buf * 64 + tid] = rp;
-                    valid[buf * 64 + tid] = rp != nullptr;
+                if (named_bar_or(2, Cfg::NLOAD,
+                                 !warp_wait(&kempty[buf], ((g >> 1) & 1) ^ 1, a.status, abort_flag, lane))) {
+                    ok = false;
+                    break;
                 }
-                named_bar(2, NL);
-                const uint32_t kb = tc::smem_u32(sK + buf * Cfg::K_BYTES);
-                constexpr int GR = C / 8;            // granules per row
-#pragma unroll 4
-                for (int i = tid; i < Cfg::TE * GR; i += NL) {
-                    const int r = i / GR, gr = i % GR;
-                    const __nv_bfloat16 *src = rowp[buf * 64 + r];
-                    const int atom = gr >> 3;
-                    const uint32_t dst = kb + atom * (Cfg::TE * 128) + (r >> 3) * 1024 + swz128(r, (gr & 7) * 16);
-                    cp_async16(dst, src ? (const void *)(src + gr * 8) : (const void *)a.kvc, src ? 16u : 0u);
+                const uint32_t kb = kb0 + buf * Cfg::K_BYTES;
+                if (j < f.ntc && a.idx) {
+                    // gather of selected entries: cp.async, 16 bytes per thread and instruction
+                    if (tid < 64) {
+                        const int64_t pos = (int64_t)j * 64 + tid;
+                        const bool in = pos < f.ncomp;
+                        const bool v = in && iv >= 0 && iv < a.E;
+                        if (in && !v && iv != -1) atomicOr(a.status, ST_BAD_INDEX);
+                        rowp[buf * 64 + tid] = v ? a.kvc + (f.b * a.E + iv) * (int64_t)C : nullptr;
+                        const uint32_t bal = __ballot_sync(0xffffffffu, v);
+                        if (lane == 0) vmask32[buf * 2 + warp] = bal;
+                    }
+                    named_bar(2, Cfg::NLOAD);
+                    // the next tile's selected indices, fetched while this one loads
+                    if (tid < 64 && j + 1 < f.j1 && j + 1 < f.ntc) {
+                        const int64_t pos = (int64_t)(j + 1) * 64 + tid;
+                        iv = pos < f.ncomp ? a.idx[f.bt * a.k + pos] : -1;
+                    }
+                    constexpr int GR = C / 8;            // 16-byte granules per row
+                    const int gr = tid % GR;
+                    const uint32_t dcol = (gr >> 3) * Cfg::ATOM;
+#pragma unroll 8
+                    for (int r = tid / GR; r < Cfg::TE; r += Cfg::NLOAD / GR) {
+                        const __nv_bfloat16 *src = rowp[buf * 64 + r];
+                        const uint32_t dst = kb + dcol + (r >> 3) * 1024 + swz128(r, (gr & 7) * 16);
+                        cp_async16(dst, src ? (const void *)(src + gr * 8) : a.zsrc, src ? 16u : 0u);
+                    }
+                    asm volatile("cp.async.commit_group;" ::: "memory");
+                    asm volatile("cp.async.wait_group 0;" ::: "memory");
+                    fence_proxy_async();
+                    tc::mbar_arrive(&kfull[buf]);
+                } else {
+                    // contiguous rows (every visible entry, or the window) as 64-row boxes
+                    int64_t y;
+                    if (j < f.ntc) {
+                        if (tid < 64) {
+                            const bool v = (int64_t)j * 64 + tid < f.ncomp;
+                            const uint32_t bal = __ballot_sync(0xffffffffu, v);
+                            if (lane == 0) vmask32[buf * 2 + warp] = bal;
+                        }
+                        y = f.b * a.E + (int64_t)j * 64;
+                    } else {
+                        const int64_t jw = j - f.ntc;
+                        const int64_t rp0 = a.raw_pos0[f.b];
+                        if (tid < 64) {
+                            const int64_t raw = f.p0 - rp0 + jw * 64 + tid;
+                            const bool in = jw * 64 + tid < f.nwin;
+                            const bool v = in && raw >= 0 && raw < a.L;
+                            if (in && !v) atomicOr(a.status, ST_NO_WINDOW_ROW);
+                            const uint32_t bal = __ballot_sync(0xffffffffu, v);
+                            if (lane == 0) vmask32[buf * 2 + warp] = bal;
+                        }
+                        // rows outside the array are zero-filled by the copy
+                        y = f.b * a.L + f.p0 - rp0 + jw * 64;
+                        if (y < -64) y = -64;
+                        if (y > 0x7fff0000LL) y = 0x7fff0000LL;
+                    }
+                    if (tid == 0) {
+                        tc::mbar_expect_tx(&kfull[buf], Cfg::K_BYTES);
+                        for (int at = 0; at < Cfg::NA; at++)
+                            tc::tma_load_2d(sK + buf * Cfg::K_BYTES + at * Cfg::ATOM, j < f.ntc ? &tm_c : &tm_w,
+                                            at * 64, (int)y, &kfull[buf]);
+                        tma_issued |= 1u << buf;
+                        last_g[buf] = g;
+                    } else {
+                        tc::mbar_arrive(&kfull[buf]);
+                    }
                 }
-                asm volatile("cp.async.commit_group;" ::: "memory");
-                asm volatile("cp.async.wait_group 0;" ::: "memory");
-                fence_proxy_async();
-                tc::mbar_arrive(&kfull[buf]);
+                if (j == q_after) {
+                    // q~ = RoPE(q, t): rotate the rotary pairs in place, then hand q to the MMA
+                    if (named_bar_or(2, Cfg::NLOAD, !warp_wait(qland, ii & 1, a.status, abort_flag, lane))) {
+                        ok = false;
+                        break;
+                    }
+                    if (tid == 0) q_pending = 0;
+                    const int np = a.rope.pairs;
+                    for (int i = tid; i < Cfg::HG * np; i += Cfg::NLOAD) {
+                        const int h = i / np, pi = i - h * np;
+                        const int d = a.rope.first + 2 * pi;
+                        __nv_bfloat162 *pv = (__nv_bfloat162 *)(sQ + (d >> 6) * (Cfg::HG * 128) +
+                                                                (h >> 3) * 1024 + swz128(h, (d & 63) * 2));
+                        const float2 x = __bfloat1622float2(*pv);
+                        const float c_ = cs_s[pi], s_ = cs_s[256 + pi];
+                        *pv = __floats2bfloat162_rn(x.x * c_ - x.y * s_, x.x * s_ + x.y * c_);
+                    }
+                    fence_proxy_async();
+                    named_bar(2, Cfg::NLOAD);
+                    if (tid == 0) tc::mbar_arrive(qfull);
+                }
             }
             ii++;
         }
-    } else if (warp == 3) {
-        // ------------------------------------------------------------- MMA
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        if (*abort_flag && tid == 0) {
+            // let every copy issued by TMA land before the CTA exits
+            for (int s = 0; s < 2; s++)
+                if (tma_issued & (1u << s))
+                    for (long long i = 0; i < tc::SPIN_LIMIT; i++)
+                        if (tc::mbar_test(&kfull[s], (last_g[s] >> 1) & 1)) break;
+            if (q_pending)
+                for (long long i = 0; i < tc::SPIN_LIMIT; i++)
+                    if (tc::mbar_test(qland, (ii & 1))) break;
+        }
+    } else if (warp == Cfg::MMA_WARP || warp == Cfg::PV_WARP) {
+        // --------------------------------------------------------------- MMA
+        // Two issuing threads: QK on warp 4, PV on warp 9.  A tcgen05.mma of
+        // these small shapes costs more to issue than to execute, so the two
+        // streams are issued side by side; the barriers order them.
         if (lane == 0) {
+            const bool is_qk = warp == Cfg::MMA_WARP;
             constexpr uint32_t idQK = tc::idesc_bf16_f32(64, 64);
             constexpr uint32_t idPV = tc::idesc_bf16_f32(128, 64) | (1u << 15);   // A MN-major
-            const uint32_t kBase = tc::smem_u32(sK), qBase = tc::smem_u32(sQ), pBase = tc::smem_u32(sP);
+            // descriptors at the buffer bases; a byte offset o adds o >> 4
+            const uint64_t dq = desc_sw128(tc::smem_u32(sQ), 16, 1024);
+            const uint64_t dk[2] = {desc_sw128(tc::smem_u32(sK), 16, 1024),
+                                    desc_sw128(tc::smem_u32(sK + Cfg::K_BYTES), 16, 1024)};
+            const uint64_t dv[2] = {desc_sw128(tc::smem_u32(sK), Cfg::ATOM, 1024),
+                                    desc_sw128(tc::smem_u32(sK + Cfg::K_BYTES), Cfg::ATOM, 1024)};
+            const uint64_t dp[2] = {desc_sw128(tc::smem_u32(sP), 16, 1024),
+                                    desc_sw128(tc::smem_u32(sP + Cfg::P_BYTES), 16, 1024)};
             uint32_t g = 0, ii = 0;
-            auto issue_pv = [&](uint32_t gp, bool first) {
-                const int bp = gp & 1;
-                tc::fence_after_sync();
-                const uint32_t kb = kBase + bp * Cfg::K_BYTES, pb = pBase + bp * Cfg::P_BYTES;
-#pragma unroll
-                for (int c = 0; c < Cfg::NC; c++)
-#pragma unroll
-                    for (int ks = 0; ks < 4; ks++) {
-                        const uint64_t ad = desc_sw128(kb + (2 * c) * (Cfg::TE * 128) + ks * 2048,
-                                                       Cfg::TE * 128, 1024);
-                        const uint64_t bd = desc_sw128(pb + ks * 32, 16, 1024);
-                        tc::mma_bf16(tmem + Cfg::O_COL + c * 64, ad, bd, idPV, (first && ks == 0) ? 0u : 1u);
-                    }
-                tc::mma_commit(&pempty[bp]);
-                tc::mma_commit(&kempty[bp]);
-            };
-            for (int64_t it = blockIdx.x; it < a.n_items; it += G) {
+            bool ok = true;
+            for (int64_t it = blockIdx.x; ok && it < a.n_items; it += G) {
                 ItemInfo f;
                 item_info(a, it, f);
                 if (f.j0 >= f.j1) continue;
-                tc::mbar_wait(qfull, ii & 1, a.status, abort_flag);
-                const uint32_t gfirst = g;
                 const int nt = f.j1 - f.j0;
-                // Issue whichever product is ready: PV(j) as soon as P(j) is
-                // written (it frees tile j's buffer for the loader), QK(j+1) as
-                // soon as tile j+1 has landed.  A fixed order would make each
-                // tile's load wait for the previous tile's load.
-                int nq = 0, np = 0;
-                long long idle = 0;
-                while (np < nt) {
-                    bool did = false;
-                    if (np < nq) {
-                        const uint32_t gp = gfirst + np;
-                        if (tc::mbar_test(&pfull[gp & 1], (gp >> 1) & 1) &&
-                            (np > 0 || tc::mbar_test(oempty, (ii & 1) ^ 1))) {
-                            issue_pv(gp, np == 0);
-                            np++;
-                            did = true;
-                        }
-                    }
-                    if (nq < nt && nq <= np + 1) {
-                        const uint32_t gq = gfirst + nq;
+                if (is_qk) {
+                    if (!tc::mbar_wait(qfull, ii & 1, a.status, abort_flag)) break;
+                    for (int n = 0; n < nt; n++) {
+                        const uint32_t gq = g + n;
                         const int buf = gq & 1;
-                        if (tc::mbar_test(&kfull[buf], (gq >> 1) & 1) &&
-                            tc::mbar_test(&sempty[buf], ((gq >> 1) & 1) ^ 1)) {
-                            tc::fence_after_sync();
-                            const uint32_t kb = kBase + buf * Cfg::K_BYTES;
-#pragma unroll
-                            for (int at = 0; at < Cfg::NA; at++)
-#pragma unroll
-                                for (int kk = 0; kk < 4; kk++) {
-                                    const uint64_t ad = desc_sw128(kb + at * (Cfg::TE * 128) + kk * 32, 16, 1024);
-                                    const uint64_t bd = desc_sw128(qBase + at * (Cfg::HG * 128) + kk * 32, 16, 1024);
-                                    tc::mma_bf16(tmem + Cfg::S_COL + buf * 64, ad, bd, idQK, (at | kk) != 0);
-                                }
-                            tc::mma_commit(&sfull[buf]);
-                            if (nq == nt - 1) tc::mma_commit(qempty);
-                            nq++;
-                            did = true;
+                        if (!tc::mbar_wait(&kfull[buf], (gq >> 1) & 1, a.status, abort_flag) ||
+                            !tc::mbar_wait(&sempty[buf], ((gq >> 1) & 1) ^ 1, a.status, abort_flag)) {
+                            ok = false;
+                            break;
                         }
+                        tc::fence_after_sync();
+#pragma unroll
+                        for (int at = 0; at < Cfg::NA; at++)
+#pragma unroll
+                            for (int kk = 0; kk < 4; kk++)
+                                tc::mma_bf16(tmem + Cfg::S_COL + buf * 64,
+                                             dq + (uint64_t)((at * (Cfg::HG * 128) + kk * 32) >> 4),
+                                             dk[buf] + (uint64_t)((at * Cfg::ATOM + kk * 32) >> 4), idQK,
+                                             (at | kk) != 0);
+                        tc::mma_commit(&sfull[buf]);
+                        if (n == nt - 1) tc::mma_commit(qempty);
                     }
-                    if (did) {
-                        idle = 0;
-                    } else if (++idle > tc::SPIN_LIMIT || ((idle & 1023) == 0 && *abort_flag)) {
-                        if (!*abort_flag) atomicOr(a.status, ST_TIMEOUT);
-                        *abort_flag = 1;
-                        break;
+                } else {
+                    for (int n = 0; n < nt; n++) {
+                        const uint32_t gp = g + n;
+                        const int bp = gp & 1;
+                        if (!tc::mbar_wait(&pfull[bp], (gp >> 1) & 1, a.status, abort_flag) ||
+                            (n == 0 && !tc::mbar_wait(oempty, (ii & 1) ^ 1, a.status, abort_flag))) {
+                            ok = false;
+                            break;
+                        }
+                        tc::fence_after_sync();
+#pragma unroll
+                        for (int c = 0; c < Cfg::NC; c++)
+#pragma unroll
+                            for (int ks = 0; ks < 4; ks++)
+                                tc::mma_bf16(tmem + Cfg::O_COL + c * 64,
+                                             dv[bp] + (uint64_t)(((2 * c) * Cfg::ATOM + ks * 2048) >> 4),
+                                             dp[bp] + (uint64_t)((ks * 32) >> 4), idPV,
+                                             (n == 0 && ks == 0) ? 0u : 1u);
+                        tc::mma_commit(&pempty[bp]);
+                        tc::mma_commit(&kempty[bp]);
                     }
+                    if (ok) tc::mma_commit(ofull);
                 }
-                g = gfirst + nt;
-                tc::mma_commit(ofull);
+                g += nt;
                 ii++;
             }
+            // every MMA issued above has completed before TMEM is released
+            tc::mma_commit(mdone);
+            if (is_qk)
+                for (long long i = 0; i < tc::SPIN_LIMIT; i++)
+                    if (tc::mbar_test(mdone, 0)) break;
         }
-    } else if (warp >= 4) {
+    } else {
         // ------------------------------------------- softmax, rescale, epilogue
-        const int st = threadIdx.x - 128;        // 0..127
-        const int quarter = warp & 3;
-        const int hh = st >> 1, half = st & 1;   // head-major role
+        // Waits are warp-uniform, and a failed wait never skips a named
+        // barrier: the four warps agree on failure through a barrier
+        // reduction and leave together.
+        const int st = threadIdx.x - Cfg::SM_WARP0 * 32;   // 0 .. 127
+        const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
+        const bool owner = lane < 16;            // owns head hh (rows of S)
+        const int hh = quarter * 16 + (lane & 15);
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const bool tma_out = a.chunk_tiles == 0 && (a.H % Cfg::HG) == 0;
         uint32_t g = 0, ii = 0;
         for (int64_t it = blockIdx.x; it < a.n_items; it += G) {
             ItemInfo f;
             item_info(a, it, f);
             if (f.j0 >= f.j1) continue;
             const int h0 = f.hg * Cfg::HG;
-            const float zl2 = (h0 + hh < a.H) ? a.sink[h0 + hh] * 1.4426950408889634f : -INFINITY;
+            const bool real = owner && h0 + hh < a.H;
+            const float zl2 = real ? a.sink[h0 + hh] * 1.4426950408889634f : -INFINITY;
             float m_run = a.chunk_tiles > 0 ? -INFINITY : zl2;
-            float l_part = 0.f;
+            float l_run = 0.f;
             const uint32_t gfirst = g;
+            bool fail = false;
             for (int j = f.j0; j < f.j1; j++, g++) {
                 const int buf = g & 1;
-                tc::mbar_wait(&sfull[buf], (g >> 1) & 1, a.status, abort_flag);
-                tc::fence_after_sync();
+                const uint32_t par = (g >> 1) & 1;
+                bool ok = warp_wait(&sfull[buf], par, a.status, abort_flag, lane);
                 float v[64];
-                const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + Cfg::S_COL + buf * 64;
-                tc::tmem_ld32(ta, v);
-                tc::tmem_ld32(ta + 32, v + 32);
-                tc::tmem_ld_wait();
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&sempty[buf]);
-                // the loader's presence flags for this tile (its kfull phase has
-                // completed, and cannot advance again before this tile's PV)
-                tc::mbar_wait(&kfull[buf], (g >> 1) & 1, a.status, abort_flag);
-                if (lane < 16) {
-                    const int e = quarter * 16 + lane;
-                    const bool ok = valid[buf * 64 + e] != 0;
-#pragma unroll
-                    for (int h = 0; h < 64; h++) stage[e * Cfg::STAGE_LD + h] = ok ? v[h] * a.scale_log2 : -INFINITY;
-                }
-                named_bar(1, 128);
-                float x[32];
-                float mt = -INFINITY;
-#pragma unroll
-                for (int i = 0; i < 32; i++) {
-                    x[i] = stage[(half * 32 + i) * Cfg::STAGE_LD + hh];
-                    mt = fmaxf(mt, x[i]);
-                }
-                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
-                const float m_new = fmaxf(m_run, mt);
-                const bool need = m_new > m_run + 8.0f;
-                const float alpha = need ? exp2f(m_run - m_new) : 1.0f;
-                if (need) m_run = m_new;
-                tc::mbar_wait(&pempty[buf], ((g >> 1) & 1) ^ 1, a.status, abort_flag);
-                float ps = 0.f;
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; i++) {
-                    const float p0 = m_run == -INFINITY ? 0.f : exp2f(x[2 * i] - m_run);
-                    const float p1 = m_run == -INFINITY ? 0.f : exp2f(x[2 * i + 1] - m_run);
-                    ps += p0 + p1;
-                    __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-                    pk[i] = *reinterpret_cast<uint32_t *>(&h2);
-                }
-                l_part = l_part * alpha + ps;
-                uint8_t *prow = sP + buf * Cfg::P_BYTES + (hh >> 3) * 1024;
-#pragma unroll
-                for (int c4 = 0; c4 < 4; c4++) {
-                    uint4 w4 = make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
-                    *reinterpret_cast<uint4 *>(prow + swz128(hh, (half * 4 + c4) * 16)) = w4;
-                }
-                if (half == 0) alpha_s[hh] = alpha;
-                if (need) *rescale_flag = 1;
-                fence_proxy_async();
-                named_bar(1, 128);
-                if (*rescale_flag && g != gfirst) {
-                    // O^T was accumulated with the old maxima: scale column h by alpha[h]
-                    const uint32_t gp = g - 1;
-                    tc::mbar_wait(&pempty[gp & 1], (gp >> 1) & 1, a.status, abort_flag);
+                if (ok) {
                     tc::fence_after_sync();
-#pragma unroll 1
-                    for (int c = 0; c < Cfg::NC; c++) {
-                        const uint32_t to = tmem + ((uint32_t)(quarter * 32) << 16) + Cfg::O_COL + c * 64;
-                        float o[32];
-#pragma unroll
-                        for (int hb = 0; hb < 64; hb += 32) {
-                            tc::tmem_ld32(to + hb, o);
-                            tc::tmem_ld_wait();
-#pragma unroll
-                            for (int u = 0; u < 32; u++) o[u] *= alpha_s[hb + u];
-                            tmem_st32(to + hb, o);
-                        }
-                    }
-                    tmem_st_wait();
+                    tc::tmem_ld32(tmem + lane_base + Cfg::S_COL + buf * 64, v);
+                    tc::tmem_ld32(tmem + lane_base + Cfg::S_COL + buf * 64 + 32, v + 32);
+                    tc::tmem_ld_wait();
                     tc::fence_before_sync();
                 }
-                named_bar(1, 128);
-                if (st == 0) {
-                    *rescale_flag = 0;
-                    tc::mbar_arrive(&pfull[buf]);
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&sempty[buf]);
+                // the loaders' presence mask for this tile (its kfull phase has
+                // completed and cannot advance again before this tile's PV)
+                ok = ok && warp_wait(&kfull[buf], par, a.status, abort_flag, lane);
+                const uint32_t mlo = ok ? vmask32[buf * 2] : 0u, mhi = ok ? vmask32[buf * 2 + 1] : 0u;
+#pragma unroll
+                for (int e = 0; e < 64; e++) {
+                    const uint32_t bit = e < 32 ? (mlo >> e) & 1u : (mhi >> (e - 32)) & 1u;
+                    v[e] = bit ? v[e] * a.scale_log2 : -INFINITY;
                 }
+                float mx[8];
+#pragma unroll
+                for (int u = 0; u < 8; u++) mx[u] = fmaxf(fmaxf(v[u], v[u + 8]), fmaxf(v[u + 16], v[u + 24]));
+#pragma unroll
+                for (int u = 0; u < 8; u++)
+                    mx[u] = fmaxf(mx[u], fmaxf(fmaxf(v[u + 32], v[u + 40]), fmaxf(v[u + 48], v[u + 56])));
+                const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                const float m_new = fmaxf(m_run, mt);
+                const bool need = real && m_new > m_run + 8.0f;
+                const float alpha = need ? ex2(m_run - m_new) : 1.0f;
+                if (need) m_run = m_new;
+                ok = ok && warp_wait(&pempty[buf], par ^ 1, a.status, abort_flag, lane);
+                // P row of head hh (64 entries, bf16), written 16 bytes at a time
+                float ps = 0.f;
+                const float msub = m_run == -INFINITY ? 0.f : m_run;
+                uint8_t *prow = sP + buf * Cfg::P_BYTES + (hh >> 3) * 1024;
+                const bool wr = ok && owner;
+#pragma unroll
+                for (int c4 = 0; c4 < 8; c4++) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const float p0 = ex2(v[8 * c4 + 2 * i] - msub);
+                        const float p1 = ex2(v[8 * c4 + 2 * i + 1] - msub);
+                        ps += p0 + p1;
+                        __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+                        pk[i] = *reinterpret_cast<uint32_t *>(&h2);
+                    }
+                    if (wr) *reinterpret_cast<uint4 *>(prow + swz128(hh, c4 * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+                l_run = l_run * alpha + ps;
+                if (wr) alpha_s[buf * 64 + hh] = alpha;
+                fence_proxy_async();
+                // one barrier in the common case: nothing failed, no head needs a rescale
+                if (named_bar_or(1, 128, !ok || (need && g != gfirst))) {
+                    if (named_bar_or(1, 128, !ok)) { fail = true; break; }
+                    // some head's max grew: O^T was accumulated with older maxima,
+                    // scale column h by alpha[h]
+                    const uint32_t gp = g - 1;
+                    if (warp_wait(&pempty[gp & 1], (gp >> 1) & 1, a.status, abort_flag, lane)) {
+                        tc::fence_after_sync();
+                        const float *al = alpha_s + buf * 64;
+#pragma unroll 1
+                        for (int cb = 0; cb < Cfg::NC * 64; cb += 16) {
+                            const uint32_t to = tmem + lane_base + Cfg::O_COL + cb;
+                            uint32_t o[16];
+                            tmem_ld16(to, o);
+                            tc::tmem_ld_wait();
+                            const float *alc = al + (cb & 63);
+#pragma unroll
+                            for (int u = 0; u < 16; u++) o[u] = __float_as_uint(__uint_as_float(o[u]) * alc[u]);
+                            tmem_st16(to, o);
+                        }
+                        tmem_st_wait();
+                    }
+                }
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&pfull[buf]);
             }
+            if (fail) break;
             // item end: denominators
-            const float l_tot = l_part + __shfl_xor_sync(0xffffffffu, l_part, 1);
-            float den = l_tot;
-            if (a.chunk_tiles == 0 && zl2 != -INFINITY) den += exp2f(zl2 - m_run);
-            if (half == 0) {
-                den_s[hh] = den;
-                alpha_s[hh] = m_run;       // reused: final running max
-                if (a.chunk_tiles > 0 && h0 + hh < a.H) {
+            float den = l_run;
+            if (a.chunk_tiles == 0 && zl2 != -INFINITY) den += ex2(zl2 - m_run);
+            if (real) {
+                inv_den_s[hh] = den > 0.f ? 1.0f / den : 0.f;
+                if (a.chunk_tiles > 0) {
                     a.part_ml[(it * 64 + hh) * 2] = m_run;
-                    a.part_ml[(it * 64 + hh) * 2 + 1] = l_tot;
-                } else if (a.lse && h0 + hh < a.H) {
+                    a.part_ml[(it * 64 + hh) * 2 + 1] = l_run;
+                } else if (a.lse) {
                     a.lse[f.bt * a.H + h0 + hh] =
                         den > 0.f ? (m_run + log2f(den)) * 0.6931471805599453f : -INFINITY;
                 }
             }
-            named_bar(1, 128);
-            tc::mbar_wait(ofull, ii & 1, a.status, abort_flag);
+            const bool ok = warp_wait(ofull, ii & 1, a.status, abort_flag, lane);
+            if (named_bar_or(1, 128, !ok)) break;
             tc::fence_after_sync();
             const int nh = a.H - h0 < 64 ? a.H - h0 : 64;
+            __nv_bfloat16 *stage = (__nv_bfloat16 *)sP;        // [64 heads][128 dims], P is free now
             for (int c = 0; c < Cfg::NC; c++) {
-                const int d = c * 128 + quarter * 32 + lane;
-                const uint32_t to = tmem + ((uint32_t)(quarter * 32) << 16) + Cfg::O_COL + c * 64;
-                float o[64];
-                tc::tmem_ld32(to, o);
-                tc::tmem_ld32(to + 32, o + 32);
-                tc::tmem_ld_wait();
-                if (a.chunk_tiles > 0) {
-                    float *po = a.part_o + (it * 64) * (int64_t)C + d;
-#pragma unroll
-                    for (int h = 0; h < 64; h++)
-                        if (h < nh) po[(int64_t)h * C] = o[h];
-                    continue;
-                }
+                const int dl = quarter * 32 + lane;             // dim within the chunk
+                const int d = c * 128 + dl;
+                const uint32_t to = tmem + lane_base + Cfg::O_COL + c * 64;
                 float cr = 1.f, sr = 0.f;
-                const bool rot = a.derotate && d >= a.rope.first;
+                const bool rot = a.chunk_tiles == 0 && a.derotate && d >= a.rope.first;
                 if (rot) rope_cos_sin(-(double)f.t, a.rope.w[(d - a.rope.first) >> 1], cr, sr);
-                __nv_bfloat16 *op = a.out + (f.bt * a.H + h0) * (int64_t)C + d;
+                const bool rot_w = a.chunk_tiles == 0 && a.derotate &&
+                                   c * 128 + quarter * 32 + 31 >= a.rope.first;   // warp-uniform
+#pragma unroll 1
+                for (int hb = 0; hb < 64; hb += 32) {           // 32 heads at a time
+                    float o[32];
+                    tc::tmem_ld32(to + hb, o);
+                    tc::tmem_ld_wait();
+                    if (a.chunk_tiles > 0) {
+                        float *po = a.part_o + (it * 64 + hb) * (int64_t)C + d;
 #pragma unroll
-                for (int h = 0; h < 64; h++) {
-                    const float dn = den_s[h];
-                    float y = dn > 0.f ? o[h] / dn : 0.f;
-                    const float yp = __shfl_xor_sync(0xffffffffu, y, 1);
-                    if (rot) y = (lane & 1) ? (yp * sr + y * cr) : (y * cr - yp * sr);
-                    if (h < nh) op[(int64_t)h * C] = __float2bfloat16_rn(y);
+                        for (int h = 0; h < 32; h++)
+                            if (hb + h < nh) po[(int64_t)h * C] = o[h];
+                        continue;
+                    }
+                    const float4 *id4 = reinterpret_cast<const float4 *>(inv_den_s + hb);
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; q4++) {
+                        const float4 iv4 = id4[q4];
+                        o[4 * q4] *= iv4.x;
+                        o[4 * q4 + 1] *= iv4.y;
+                        o[4 * q4 + 2] *= iv4.z;
+                        o[4 * q4 + 3] *= iv4.w;
+                    }
+                    if (rot_w) {
+                        float op[32];
+#pragma unroll
+                        for (int h = 0; h < 32; h++) op[h] = __shfl_xor_sync(0xffffffffu, o[h], 1);
+                        if (rot) {
+#pragma unroll
+                            for (int h = 0; h < 32; h++)
+                                o[h] = (lane & 1) ? (op[h] * sr + o[h] * cr) : (o[h] * cr - op[h] * sr);
+                        }
+                    }
+                    if (tma_out) {
+#pragma unroll
+                        for (int h = 0; h < 32; h++) stage[(hb + h) * 128 + dl] = __float2bfloat16_rn(o[h]);
+                    } else {
+                        __nv_bfloat16 *op = a.out + (f.bt * a.H + h0 + hb) * (int64_t)C + d;
+#pragma unroll
+                        for (int h = 0; h < 32; h++)
+                            if (hb + h < nh) op[(int64_t)h * C] = __float2bfloat16_rn(o[h]);
+                    }
+                }
+                if (tma_out) {
+                    // the normalised chunk leaves shared memory by one TMA store
+                    fence_proxy_async();
+                    named_bar(1, 128);
+                    if (st == 0) {
+                        asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                                     ::"l"(reinterpret_cast<uint64_t>(&tm_o)), "r"(c * 128),
+                                     "r"((int)(f.bt * a.H + h0)), "r"(tc::smem_u32(stage))
+                                     : "memory");
+                        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                    }
+                    named_bar(1, 128);
                 }
             }
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(oempty);
+            named_bar(1, 128);                 // inv_den_s is rewritten by the next item
             ii++;
         }
+        if (st == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 3) {
+    if (warp == Cfg::MMA_WARP) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, Cfg::TMEM_COLS);
     }
@@ -639,7 +799,7 @@ size_t attn_tc_split_bytes(int64_t rows, int H, int c, int n_chunks) {
 // to cover the GPU, each at least 4 tiles; independent of the batch size when
 // rows are few, so a sequence's result does not depend on the batch around it.
 int attn_tc_chunks(int64_t rows, int H, int64_t max_list) {
-    const int64_t tiles = (max_list + 63) / 64;
+    const int64_t tiles = (max_list + 63) / 64 + 1;       // + 1: padding of the compressed part
     if (rows * ((H + 63) / 64) >= 2 * 148 || tiles <= 4) return 1;
     int64_t ch = (tiles + 7) / 8;          // 8 tiles per chunk
     if (ch > 64) ch = 64;
@@ -650,12 +810,11 @@ cudaError_t launch_attn_tc(int64_t B, const AttnArgs &g, const int32_t *cnt, int
                            void *split_ws, int max_ctas, cudaStream_t st) {
     if (B * g.Tq == 0) return cudaSuccess;
     AttnTcArgs a;
-    a.q = (const __nv_bfloat16 *)g.q;
-    a.q_pos = g.q_pos;
     a.kvc = (const __nv_bfloat16 *)g.kvc;
+    a.zsrc = g.q;
+    a.q_pos = g.q_pos;
     a.idx = g.idx;
     a.cnt = cnt;
-    a.kv_raw = (const __nv_bfloat16 *)g.kv_raw;
     a.raw_pos0 = g.raw_pos0;
     a.sink = g.sink;
     a.out = (__nv_bfloat16 *)g.out;
@@ -668,9 +827,10 @@ cudaError_t launch_attn_tc(int64_t B, const AttnArgs &g, const int32_t *cnt, int
     a.rope = g.rope;
     const int64_t max_list = (g.idx ? (int64_t)g.k : g.E) + g.n_win;
     const int64_t rows = B * g.Tq;
+    const int64_t max_tiles = (max_list + 63) / 64 + 1;
     if (n_chunks > 1 && split_ws) {
         a.n_chunks = n_chunks;
-        a.chunk_tiles = (int)(((max_list + 63) / 64 + n_chunks - 1) / n_chunks);
+        a.chunk_tiles = (int)((max_tiles + n_chunks - 1) / n_chunks);
         a.part_o = (float *)split_ws;
         a.part_ml = (float *)((char *)split_ws + (size_t)rows * a.n_hg * n_chunks * 64 * 512 * 4);
     } else {
@@ -681,6 +841,19 @@ cudaError_t launch_attn_tc(int64_t B, const AttnArgs &g, const int32_t *cnt, int
     }
     a.n_items = rows * a.n_hg * a.n_chunks;
     using Cfg = AtCfg<512>;
+    // tensor maps: q rows [B*T*H, C]; compressed entries [B*E, C] and raw
+    // window rows [B*L, C] as 64-row boxes (a map that is never read points
+    // at q); out [B*T*H, C] for the epilogue's 64 x 128 stores.
+    CUtensorMap tq, tcmp, tw, to;
+    const bool have_c = g.E > 0 && g.kvc != nullptr;
+    const bool have_w = g.L > 0 && g.kv_raw != nullptr;
+    if (!make_tmap_bf16_2d(&tq, g.q, (uint64_t)(rows * g.H), 512, 64) ||
+        !make_tmap_bf16_2d(&tcmp, have_c ? g.kvc : g.q, have_c ? (uint64_t)(B * g.E) : (uint64_t)(rows * g.H),
+                           512, 64) ||
+        !make_tmap_bf16_2d(&tw, have_w ? g.kv_raw : g.q, have_w ? (uint64_t)(B * g.L) : (uint64_t)(rows * g.H),
+                           512, 64) ||
+        !make_tmap_bf16_2d_plain(&to, g.out, (uint64_t)(rows * g.H), 512, 128, 64))
+        return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -690,7 +863,7 @@ cudaError_t launch_attn_tc(int64_t B, const AttnArgs &g, const int32_t *cnt, int
     }
     const int sms = max_ctas > 0 && max_ctas < device_sms() ? max_ctas : device_sms();
     const int grid = (int)(a.n_items < sms ? a.n_items : sms);
-    attn_tc_kernel<512><<<grid, Cfg::THREADS, Cfg::SMEM, st>>>(a);
+    attn_tc_kernel<512><<<grid, Cfg::THREADS, Cfg::SMEM, st>>>(tq, tcmp, tw, to, a);
     count_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.chunk_tiles == 0) return e;

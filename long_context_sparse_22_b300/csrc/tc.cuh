@@ -184,4 +184,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 }
 
 }  // namespace tc
+
+// 2D bf16 tensor map over a row-major [rows, cols] array, box [box_rows, 64],
+// 128-byte swizzle (defined with the indexer kernels).
+bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                       uint32_t box_rows);
+// The same without swizzle, box [box_rows, box_cols] (box_cols <= 256).
+bool make_tmap_bf16_2d_plain(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                             uint32_t box_cols, uint32_t box_rows);
+
 }  // namespace csa
