@@ -509,8 +509,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // reduction and leave together.
         const int st = threadIdx.x - Cfg::SM_WARP0 * 32;   // 0 .. 127
         const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
-        const bool owner = lane < 16;            // owns head hh (rows of S)
-        const int hh = quarter * 16 + (lane & 15);
+        // S rows (heads) of an M = 64 product sit in TMEM lanes 0-15 of each
+        // quarter.  A 16x256b load spreads them over the whole warp: thread
+        // t holds heads r = 16*quarter + t/4 and r + 8, entries 8i + 2(t%4)
+        // and 8i + 2(t%4) + 1 for i = 0..7.  The four threads of a head
+        // agree on its running max by two shuffles; the running sums stay
+        // per-thread until the item ends.
+        const int t4 = lane & 3;
+        const int hr[2] = {quarter * 16 + (lane >> 2), quarter * 16 + (lane >> 2) + 8};
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         const bool tma_out = a.chunk_tiles == 0 && (a.H % Cfg::HG) == 0;
         uint32_t g = 0, ii = 0;
@@ -519,21 +525,35 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             item_info(a, it, f);
             if (f.j0 >= f.j1) continue;
             const int h0 = f.hg * Cfg::HG;
-            const bool real = owner && h0 + hh < a.H;
-            const float zl2 = real ? a.sink[h0 + hh] * 1.4426950408889634f : -INFINITY;
-            float m_run = a.chunk_tiles > 0 ? -INFINITY : zl2;
-            float l_run = 0.f;
+            bool real[2];
+            float zl2[2], m_run[2], l_run[2];
+#pragma unroll
+            for (int u = 0; u < 2; u++) {
+                real[u] = h0 + hr[u] < a.H;
+                zl2[u] = real[u] ? a.sink[h0 + hr[u]] * 1.4426950408889634f : -INFINITY;
+                m_run[u] = a.chunk_tiles > 0 ? -INFINITY : zl2[u];
+                l_run[u] = 0.f;
+            }
             const uint32_t gfirst = g;
             bool fail = false;
             for (int j = f.j0; j < f.j1; j++, g++) {
                 const int buf = g & 1;
                 const uint32_t par = (g >> 1) & 1;
                 bool ok = warp_wait(&sfull[buf], par, a.status, abort_flag, lane);
-                float v[64];
+                uint32_t raw[32];
                 if (ok) {
                     tc::fence_after_sync();
-                    tc::tmem_ld32(tmem + lane_base + Cfg::S_COL + buf * 64, v);
-                    tc::tmem_ld32(tmem + lane_base + Cfg::S_COL + buf * 64 + 32, v + 32);
+                    asm volatile(
+                        "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+                        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+                        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+                        : "=r"(raw[0]), "=r"(raw[1]), "=r"(raw[2]), "=r"(raw[3]), "=r"(raw[4]), "=r"(raw[5]),
+                          "=r"(raw[6]), "=r"(raw[7]), "=r"(raw[8]), "=r"(raw[9]), "=r"(raw[10]), "=r"(raw[11]),
+                          "=r"(raw[12]), "=r"(raw[13]), "=r"(raw[14]), "=r"(raw[15]), "=r"(raw[16]), "=r"(raw[17]),
+                          "=r"(raw[18]), "=r"(raw[19]), "=r"(raw[20]), "=r"(raw[21]), "=r"(raw[22]), "=r"(raw[23]),
+                          "=r"(raw[24]), "=r"(raw[25]), "=r"(raw[26]), "=r"(raw[27]), "=r"(raw[28]), "=r"(raw[29]),
+                          "=r"(raw[30]), "=r"(raw[31])
+                        : "r"(tmem + lane_base + Cfg::S_COL + buf * 64));
                     tc::tmem_ld_wait();
                     tc::fence_before_sync();
                 }
@@ -543,47 +563,57 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 // completed and cannot advance again before this tile's PV)
                 ok = ok && warp_wait(&kfull[buf], par, a.status, abort_flag, lane);
                 const uint32_t mlo = ok ? vmask32[buf * 2] : 0u, mhi = ok ? vmask32[buf * 2 + 1] : 0u;
+                // v[u][2i + e]: head hr[u], entry 8i + 2 t4 + e  (raw[4i + 2u + e])
+                float v[2][16];
 #pragma unroll
-                for (int e = 0; e < 64; e++) {
-                    const uint32_t bit = e < 32 ? (mlo >> e) & 1u : (mhi >> (e - 32)) & 1u;
-                    v[e] = bit ? v[e] * a.scale_log2 : -INFINITY;
+                for (int i = 0; i < 8; i++)
+#pragma unroll
+                    for (int e = 0; e < 2; e++) {
+                        const int ent = 8 * i + 2 * t4 + e;
+                        const uint32_t bit = ent < 32 ? (mlo >> ent) & 1u : (mhi >> (ent - 32)) & 1u;
+#pragma unroll
+                        for (int u = 0; u < 2; u++)
+                            v[u][2 * i + e] = bit ? __uint_as_float(raw[4 * i + 2 * u + e]) * a.scale_log2 : -INFINITY;
+                    }
+                bool need[2];
+                float alpha[2];
+#pragma unroll
+                for (int u = 0; u < 2; u++) {
+                    float mx = fmaxf(fmaxf(fmaxf(v[u][0], v[u][1]), fmaxf(v[u][2], v[u][3])),
+                                     fmaxf(fmaxf(v[u][4], v[u][5]), fmaxf(v[u][6], v[u][7])));
+                    mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(v[u][8], v[u][9]), fmaxf(v[u][10], v[u][11])),
+                                         fmaxf(fmaxf(v[u][12], v[u][13]), fmaxf(v[u][14], v[u][15]))));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                    const float m_new = fmaxf(m_run[u], mx);
+                    need[u] = real[u] && m_new > m_run[u] + 8.0f;
+                    alpha[u] = need[u] ? ex2(m_run[u] - m_new) : 1.0f;
+                    if (need[u]) m_run[u] = m_new;
                 }
-                float mx[8];
-#pragma unroll
-                for (int u = 0; u < 8; u++) mx[u] = fmaxf(fmaxf(v[u], v[u + 8]), fmaxf(v[u + 16], v[u + 24]));
-#pragma unroll
-                for (int u = 0; u < 8; u++)
-                    mx[u] = fmaxf(mx[u], fmaxf(fmaxf(v[u + 32], v[u + 40]), fmaxf(v[u + 48], v[u + 56])));
-                const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-                const float m_new = fmaxf(m_run, mt);
-                const bool need = real && m_new > m_run + 8.0f;
-                const float alpha = need ? ex2(m_run - m_new) : 1.0f;
-                if (need) m_run = m_new;
                 ok = ok && warp_wait(&pempty[buf], par ^ 1, a.status, abort_flag, lane);
-                // P row of head hh (64 entries, bf16), written 16 bytes at a time
-                float ps = 0.f;
-                const float msub = m_run == -INFINITY ? 0.f : m_run;
-                uint8_t *prow = sP + buf * Cfg::P_BYTES + (hh >> 3) * 1024;
-                const bool wr = ok && owner;
+                // P rows (bf16): this thread's two entries of chunk i are 4 bytes
+                // at byte 4 t4 of the row's (swizzled) 16-byte chunk i
 #pragma unroll
-                for (int c4 = 0; c4 < 8; c4++) {
-                    uint32_t pk[4];
+                for (int u = 0; u < 2; u++) {
+                    const int h = hr[u];
+                    const float msub = m_run[u] == -INFINITY ? 0.f : m_run[u];
+                    uint8_t *prow = sP + buf * Cfg::P_BYTES + (h >> 3) * 1024 + (h & 7) * 128 + 4 * t4;
+                    float ps = 0.f;
 #pragma unroll
-                    for (int i = 0; i < 4; i++) {
-                        const float p0 = ex2(v[8 * c4 + 2 * i] - msub);
-                        const float p1 = ex2(v[8 * c4 + 2 * i + 1] - msub);
+                    for (int i = 0; i < 8; i++) {
+                        const float p0 = ex2(v[u][2 * i] - msub), p1 = ex2(v[u][2 * i + 1] - msub);
                         ps += p0 + p1;
                         __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-                        pk[i] = *reinterpret_cast<uint32_t *>(&h2);
+                        if (ok) *reinterpret_cast<uint32_t *>(prow + ((i ^ (h & 7)) << 4)) =
+                            *reinterpret_cast<uint32_t *>(&h2);
                     }
-                    if (wr) *reinterpret_cast<uint4 *>(prow + swz128(hh, c4 * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    l_run[u] = l_run[u] * alpha[u] + ps;
+                    if (ok && t4 == 0) alpha_s[buf * 64 + h] = alpha[u];
                 }
-                l_run = l_run * alpha + ps;
-                if (wr) alpha_s[buf * 64 + hh] = alpha;
                 fence_proxy_async();
                 // one barrier in the common case: nothing failed, no head needs a rescale
-                if (named_bar_or(1, 128, !ok || (need && g != gfirst))) {
+                const bool resc = (need[0] || need[1]) && g != gfirst;
+                if (named_bar_or(1, 128, !ok || resc)) {
                     if (named_bar_or(1, 128, !ok)) { fail = true; break; }
                     // some head's max grew: O^T was accumulated with older maxima,
                     // scale column h by alpha[h]
@@ -599,7 +629,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             tc::tmem_ld_wait();
                             const float *alc = al + (cb & 63);
 #pragma unroll
-                            for (int u = 0; u < 16; u++) o[u] = __float_as_uint(__uint_as_float(o[u]) * alc[u]);
+                            for (int q = 0; q < 16; q++) o[q] = __float_as_uint(__uint_as_float(o[q]) * alc[q]);
                             tmem_st16(to, o);
                         }
                         tmem_st_wait();
@@ -610,17 +640,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (lane == 0) tc::mbar_arrive(&pfull[buf]);
             }
             if (fail) break;
-            // item end: denominators
-            float den = l_run;
-            if (a.chunk_tiles == 0 && zl2 != -INFINITY) den += ex2(zl2 - m_run);
-            if (real) {
-                inv_den_s[hh] = den > 0.f ? 1.0f / den : 0.f;
-                if (a.chunk_tiles > 0) {
-                    a.part_ml[(it * 64 + hh) * 2] = m_run;
-                    a.part_ml[(it * 64 + hh) * 2 + 1] = l_run;
-                } else if (a.lse) {
-                    a.lse[f.bt * a.H + h0 + hh] =
-                        den > 0.f ? (m_run + log2f(den)) * 0.6931471805599453f : -INFINITY;
+            // item end: the four threads of a head add their partial sums
+#pragma unroll
+            for (int u = 0; u < 2; u++) {
+                float l = l_run[u];
+                l += __shfl_xor_sync(0xffffffffu, l, 1);
+                l += __shfl_xor_sync(0xffffffffu, l, 2);
+                float den = l;
+                if (a.chunk_tiles == 0 && zl2[u] != -INFINITY) den += ex2(zl2[u] - m_run[u]);
+                const int h = hr[u];
+                if (t4 == 0) {
+                    inv_den_s[h] = (real[u] && den > 0.f) ? 1.0f / den : 0.f;
+                    if (real[u]) {
+                        if (a.chunk_tiles > 0) {
+                            a.part_ml[(it * 64 + h) * 2] = m_run[u];
+                            a.part_ml[(it * 64 + h) * 2 + 1] = l;
+                        } else if (a.lse) {
+                            a.lse[f.bt * a.H + h0 + h] =
+                                den > 0.f ? (m_run[u] + log2f(den)) * 0.6931471805599453f : -INFINITY;
+                        }
+                    }
                 }
             }
             const bool ok = warp_wait(ofull, ii & 1, a.status, abort_flag, lane);

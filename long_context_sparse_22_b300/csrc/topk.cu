@@ -6,18 +6,24 @@
 // kept.]  Ties go to the lower index.
 //
 // Scores map to uint32 keys that order like the floats (-0.0 folded onto
-// +0.0).  Three histogram passes (11 + 11 + 10 bits) find the exact k-th
-// largest key tau and how many keys equal to tau must be taken; one ordered
-// pass then emits every index with key > tau plus the first keys equal to
-// tau in index order, in ascending index order, using block-wide prefix sums.
+// +0.0).  The exact selection: three histogram passes (11 + 11 + 10 bits)
+// find the k-th largest key tau and how many keys equal to tau must be taken;
+// one ordered pass then emits every index with key > tau plus the first keys
+// equal to tau, in ascending index order, using block-wide prefix sums.
 //
-// Many rows of at most a few ten-thousand entries (prefill): one CTA per row
-// with the row's keys cached in shared memory.
-// Few long rows (decode, up to 262144 entries): three launches spread each
-// row over many CTAs: (1) an 11-bit histogram of the keys, (2) each chunk
-// keeps, in index order, only the entries whose top bits reach the bin that
-// holds the k-th largest key, (3) one CTA per row runs the exact selection on
-// those candidates (a few thousand) in index order.
+// Most of a row cannot reach the top k, so the exact selection runs on a
+// short candidate list: an evenly spaced sample of the row gives a key lo that
+// lies below the k-th largest with a margin of five standard deviations; the
+// keys >= lo are compacted in index order and the exact selection runs on
+// them.  If fewer than k keys reach lo (or too many to hold), the exact
+// selection runs on the whole row instead, so the result never depends on the
+// sample.
+//
+// Many rows (prefill): one warp per row.
+// Few long rows (decode, up to 262144 entries): three launches: (1) one CTA
+// per row takes the sample, (2) the row's chunks are spread over many CTAs,
+// each keeping its keys >= lo in index order, (3) one CTA per row runs the
+// exact selection on the candidates.
 #include <mutex>
 
 #include "common.cuh"
@@ -124,12 +130,16 @@ __device__ __forceinline__ void find_bin(TkShared &sh, int nb, uint32_t remainin
     __syncthreads();
 }
 
-// Exact top-k over n > k items given in index order: key(i) is the item's
-// uint32 key, id(i) its output index.  Writes the k kept indices to orow in
-// the items' order.
-template <typename KeyF, typename IdF>
-__device__ void select_core(TkShared &sh, int64_t n, int k, KeyF key, IdF id, int32_t *orow) {
-    const int tid = threadIdx.x, lane = tid & 31;
+// The k-th largest key tau of n > k items, how many items equal to tau the
+// selection takes (need_eq), and whether that is all of them.
+struct Thr {
+    uint32_t tau, need_eq;
+    bool all_eq;
+};
+
+template <typename KeyF>
+__device__ Thr find_threshold(TkShared &sh, int64_t n, int k, KeyF key) {
+    const int tid = threadIdx.x;
     uint32_t prefix = 0, pmask = 0;
     uint32_t remaining = (uint32_t)k;
     uint32_t n_eq = 0;
@@ -152,24 +162,35 @@ __device__ void select_core(TkShared &sh, int64_t n, int k, KeyF key, IdF id, in
         n_eq = sh.binsz;                 // after the last pass: keys equal to tau
         __syncthreads();
     }
-    const uint32_t tau = prefix, need_eq = remaining;
-    const bool all_eq = need_eq == n_eq;  // every tie is kept: selection is key >= tau
+    Thr t;
+    t.tau = prefix;
+    t.need_eq = remaining;
+    t.all_eq = remaining == n_eq;        // every tie is kept: selection is key >= tau
+    return t;
+}
+
+// Writes, in the items' order, the id of every item with key > tau and of the
+// first need_eq items with key == tau (k in all) to orow.
+template <typename KeyF, typename IdF>
+__device__ void emit_ordered(TkShared &sh, int64_t n, int k, const Thr &th, KeyF key, IdF id,
+                             int32_t *orow) {
+    const int tid = threadIdx.x, lane = tid & 31;
     const unsigned lt = (1u << lane) - 1u;
     uint32_t run_sel = 0, run_eq = 0;
     for (int64_t base = 0; base < n && run_sel < (uint32_t)k; base += TK_THREADS) {
         const int64_t j = base + tid;
         const uint32_t kv = j < n ? key(j) : 0u;
-        const bool gt = j < n && kv > tau;
-        const bool eq = j < n && kv == tau;
+        const bool gt = j < n && kv > th.tau;
+        const bool eq = j < n && kv == th.tau;
         bool sel;
-        if (all_eq) {
+        if (th.all_eq) {
             sel = gt || eq;
         } else {
             const unsigned be = __ballot_sync(0xffffffffu, eq);
             uint32_t eq_tot;
             const uint32_t eq_before = warp_offsets(sh.wcnt[0], (uint32_t)__popc(be), &eq_tot);
             const uint32_t eq_rank = run_eq + eq_before + (uint32_t)__popc(be & lt);
-            sel = gt || (eq && eq_rank < need_eq);
+            sel = gt || (eq && eq_rank < th.need_eq);
             run_eq += eq_tot;
         }
         const unsigned bs = __ballot_sync(0xffffffffu, sel);
@@ -181,34 +202,259 @@ __device__ void select_core(TkShared &sh, int64_t n, int k, KeyF key, IdF id, in
     }
 }
 
+// Exact top-k over n > k items given in index order: key(i) is the item's
+// uint32 key, id(i) its output index.  Writes the k kept indices to orow in
+// the items' order.
+template <typename KeyF, typename IdF>
+__device__ void select_core(TkShared &sh, int64_t n, int k, KeyF key, IdF id, int32_t *orow) {
+    const Thr th = find_threshold(sh, n, k, key);
+    emit_ordered(sh, n, k, th, key, id, orow);
+}
+
+// Rank in a sample of S keys (drawn from n) whose key lower-bounds the k-th
+// largest of all n with a margin of five standard deviations of the number of
+// sample keys above it; >= S means "no useful bound".
+__device__ __forceinline__ int sample_rank(int64_t n, int k, int S) {
+    const double p = (double)k / (double)n;
+    const double mu = S * p;
+    const double sd = sqrt(S * p * (1.0 - p));
+    return (int)ceil(mu + 5.0 * sd + 2.0);
+}
+
 // ----------------------------------------------------------- one CTA per row
 
-__global__ void __launch_bounds__(TK_THREADS)
-topk_kernel(const float *__restrict__ scores, const int64_t *__restrict__ q_pos,
-            int32_t *__restrict__ idx, int32_t *__restrict__ cnt, int64_t E, int k, int m,
-            int kcap) {
-    extern __shared__ uint32_t smk[];   // cached keys [kcap]
-    __shared__ TkShared sh;
-    const int tid = threadIdx.x;
-    const int64_t row = blockIdx.x;
-    const int64_t nv = visible_count(q_pos[row], m, E);
-    const float *srow = scores + row * E;
-    int32_t *orow = idx + row * (int64_t)k;
+// ----------------------------------------------- one warp per row (prefill)
+//
+// Each warp selects for its own rows with warp-level synchronisation only:
+// the exact threshold is a radix select with 8-bit digits (four passes) on
+// a per-warp 256-bin histogram; the bin holding the remaining-th largest key
+// is found by a suffix sum across the lanes, each lane owning eight bins.
 
-    if (nv <= k) {
-        for (int i = tid; i < k; i += TK_THREADS) orow[i] = i < nv ? i : -1;
-        if (tid == 0) cnt[row] = (int32_t)nv;
-        return;
+constexpr int TW_WARPS = 16;                  // warps per CTA
+constexpr int TW_SAMPLE = 512;                // sampled keys per row
+constexpr int TW_LCAP = 2048;                 // candidates kept per warp
+
+struct TwShared {
+    uint32_t hist[256];                       // histogram of the exact whole-row fallback
+    uint32_t lkey[TW_LCAP];                   // candidates, in index order
+    uint16_t lidx[TW_LCAP];                   // their positions (rows of at most 65536 entries)
+};
+
+// hist[bin] += 1 for every lane with `in`, lanes of the same bin merged.
+__device__ __forceinline__ void warp_hist_add(uint32_t *hist, bool in, uint32_t bin) {
+    const unsigned m_in = __ballot_sync(0xffffffffu, in);
+    if (in) {
+        const unsigned peers = __match_any_sync(m_in, bin);
+        if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
     }
-    auto id = [](int64_t j) { return (int32_t)j; };
-    if (nv <= kcap) {
-        for (int64_t j = tid; j < nv; j += TK_THREADS) smk[j] = score_key(__ldcs(srow + j));
-        __syncthreads();
-        select_core(sh, nv, k, [&](int64_t j) { return smk[j]; }, id, orow);
-    } else {
-        select_core(sh, nv, k, [&](int64_t j) { return score_key(srow[j]); }, id, orow);
+    __syncwarp();
+}
+
+// The k-th largest of n keys, exact: radix select with digits of at most 8
+// bits, run only over the bits in which the keys differ (bits they all share
+// are found first by a warp-wide AND / OR and taken as given).
+template <typename KeyF>
+__device__ Thr warp_threshold(uint32_t *hist, int64_t n, int k, KeyF key) {
+    const int lane = threadIdx.x & 31;
+    uint32_t all1 = 0xffffffffu, any1 = 0u;
+    for (int64_t j = lane; j < n; j += 32) {
+        const uint32_t kv = key(j);
+        all1 &= kv;
+        any1 |= kv;
     }
-    if (tid == 0) cnt[row] = k;
+    all1 = __reduce_and_sync(0xffffffffu, all1);
+    any1 = __reduce_or_sync(0xffffffffu, any1);
+    const uint32_t vary = all1 ^ any1;
+    uint32_t prefix = all1 & ~vary, pmask = ~vary, remaining = (uint32_t)k;
+    uint32_t n_eq = (uint32_t)n;
+    int hi = vary ? 31 - __clz(vary) : -1;
+#pragma unroll 1
+    while (hi >= 0) {
+        const int lo_bit = hi >= 7 ? hi - 7 : 0;
+        const uint32_t dmask = (2u << (hi - lo_bit)) - 1u;     // digit of hi - lo_bit + 1 bits
+#pragma unroll
+        for (int i = 0; i < 8; i++) hist[lane * 8 + i] = 0u;
+        __syncwarp();
+        for (int64_t base = 0; base < n; base += 32) {
+            const int64_t j = base + lane;
+            const uint32_t kv = j < n ? key(j) : 0u;
+            warp_hist_add(hist, j < n && (kv & pmask) == prefix, (kv >> lo_bit) & dmask);
+        }
+        uint32_t h[8], c = 0;
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            h[i] = hist[lane * 8 + i];
+            c += h[i];
+        }
+        // suffix sum over lanes: keys in bins above this lane's eight
+        uint32_t sfx = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_down_sync(0xffffffffu, sfx, o);
+            if (lane + o < 32) sfx += t;
+        }
+        uint32_t above = sfx - c;
+        int found = -1;
+        uint32_t f_above = 0, f_size = 0;
+#pragma unroll
+        for (int i = 7; i >= 0; i--) {
+            if (found < 0 && above < remaining && above + h[i] >= remaining) {
+                found = lane * 8 + i;
+                f_above = above;
+                f_size = h[i];
+            }
+            above += h[i];
+        }
+        const unsigned who = __ballot_sync(0xffffffffu, found >= 0);
+        const int src = __ffs(who) - 1;
+        const uint32_t bin = (uint32_t)__shfl_sync(0xffffffffu, found, src);
+        remaining -= __shfl_sync(0xffffffffu, f_above, src);
+        n_eq = __shfl_sync(0xffffffffu, f_size, src);
+        prefix |= bin << lo_bit;
+        pmask |= dmask << lo_bit;
+        __syncwarp();
+        hi = lo_bit - 1;
+    }
+    Thr t;
+    t.tau = prefix;
+    t.need_eq = remaining;
+    t.all_eq = remaining == n_eq;
+    return t;
+}
+
+template <typename KeyF, typename IdF>
+__device__ void warp_emit(int64_t n, int k, const Thr &th, KeyF key, IdF id, int32_t *orow) {
+    const int lane = threadIdx.x & 31;
+    const unsigned lt = (1u << lane) - 1u;
+    uint32_t run_sel = 0, run_eq = 0;
+    for (int64_t base = 0; base < n && run_sel < (uint32_t)k; base += 32) {
+        const int64_t j = base + lane;
+        const uint32_t kv = j < n ? key(j) : 0u;
+        const bool gt = j < n && kv > th.tau;
+        const bool eq = j < n && kv == th.tau;
+        const unsigned be = __ballot_sync(0xffffffffu, eq);
+        const bool sel = gt || (eq && (th.all_eq || run_eq + (uint32_t)__popc(be & lt) < th.need_eq));
+        run_eq += (uint32_t)__popc(be);
+        const unsigned bs = __ballot_sync(0xffffffffu, sel);
+        const uint32_t pos = run_sel + (uint32_t)__popc(bs & lt);
+        if (sel && pos < (uint32_t)k) orow[pos] = id(j);
+        run_sel += (uint32_t)__popc(bs);
+    }
+}
+
+// Keys of the lane's NK registers that are >= t, summed over the warp
+// (padding holds key 0, which no t >= 1 counts).
+template <int NK>
+__device__ __forceinline__ uint32_t warp_count_ge(const uint32_t (&kr)[NK], uint32_t t) {
+    uint32_t c = 0;
+#pragma unroll
+    for (int i = 0; i < NK; i++) c += kr[i] >= t ? 1u : 0u;
+    return __reduce_add_sync(0xffffffffu, c);
+}
+
+// The largest t whose low (32 - bits) bits are zero and that at least k keys
+// reach: with bits = 32, the k-th largest key; with fewer bits, a lower bound
+// on it.  One bit per step, decided by a count.
+template <int NK>
+__device__ __forceinline__ uint32_t warp_kth(const uint32_t (&kr)[NK], int k, int bits) {
+    uint32_t t = 0;
+#pragma unroll 1
+    for (int b = 31; b >= 32 - bits; b--) {
+        const uint32_t c = t | (1u << b);
+        if (warp_count_ge(kr, c) >= (uint32_t)k) t = c;
+    }
+    return t;
+}
+
+__global__ void __launch_bounds__(TW_WARPS * 32, 1)
+topk_kernel(const float *__restrict__ scores, const int64_t *__restrict__ q_pos,
+            int32_t *__restrict__ idx, int32_t *__restrict__ cnt, int64_t rows, int64_t E, int k,
+            int m) {
+    extern __shared__ __align__(16) uint8_t tw_raw[];
+    TwShared &sh = reinterpret_cast<TwShared *>(tw_raw)[threadIdx.x >> 5];
+    const int lane = threadIdx.x & 31;
+    const unsigned lt = (1u << lane) - 1u;
+    const int64_t nwarps = (int64_t)gridDim.x * TW_WARPS;
+    for (int64_t row = (int64_t)blockIdx.x * TW_WARPS + (threadIdx.x >> 5); row < rows; row += nwarps) {
+        const int64_t nv = visible_count(q_pos[row], m, E);
+        const float *srow = scores + row * E;
+        int32_t *orow = idx + row * (int64_t)k;
+        if (nv <= k) {
+            for (int i = lane; i < k; i += 32) orow[i] = i < nv ? i : -1;
+            if (lane == 0) cnt[row] = (int32_t)nv;
+            continue;
+        }
+        auto gkey = [&](int64_t j) { return score_key(__ldg(srow + j)); };
+        auto gid = [](int64_t j) { return (int32_t)j; };
+        bool done = false;
+        const bool whole = nv <= TW_SAMPLE;                 // the row itself is the sample
+        const int r = whole ? k : sample_rank(nv, k, TW_SAMPLE);
+        if ((whole || r < TW_SAMPLE) && 2 * k <= TW_LCAP && nv <= 65536) {
+            // sample keys (or the whole row) in registers: sk[u] is sample 32u + lane, taken at
+            // position (i * nv) / TW_SAMPLE (exact in 32 bits for rows of at most 65536)
+            uint32_t sk[TW_SAMPLE / 32];
+#pragma unroll
+            for (int u = 0; u < TW_SAMPLE / 32; u++) {
+                const uint32_t i = 32 * u + lane;
+                if (whole) sk[u] = i < nv ? score_key(__ldcs(srow + i)) : 0u;
+                else sk[u] = gkey((int64_t)((i * (uint32_t)nv) / TW_SAMPLE));
+            }
+            // lo: the top 24 bits of the r-th largest sample key, a lower bound on the k-th largest key
+            const uint32_t lo = warp_kth(sk, r, 24);
+            // the keys >= lo, in index order, 64 loads in flight per lane
+            uint32_t n = 0;
+            if (whole) {
+#pragma unroll
+                for (int u = 0; u < TW_SAMPLE / 32; u++) {
+                    const int j = 32 * u + lane;
+                    const bool in = j < nv && sk[u] >= lo;
+                    const unsigned bm = __ballot_sync(0xffffffffu, in);
+                    const uint32_t p = n + (uint32_t)__popc(bm & lt);
+                    if (in) {
+                        sh.lkey[p] = sk[u];
+                        sh.lidx[p] = (uint16_t)j;
+                    }
+                    n += (uint32_t)__popc(bm);
+                }
+            } else {
+                constexpr int NB = 64;
+                for (int64_t base = 0; base < nv && n <= (uint32_t)TW_LCAP; base += 32 * NB) {
+                    uint32_t kv[NB];
+#pragma unroll
+                    for (int u = 0; u < NB; u++) {
+                        const int64_t j = base + 32 * u + lane;
+                        kv[u] = j < nv ? score_key(__ldcs(srow + j)) : 0u;
+                    }
+#pragma unroll
+                    for (int u = 0; u < NB; u++) {
+                        const int64_t j = base + 32 * u + lane;
+                        const bool in = j < nv && kv[u] >= lo;
+                        const unsigned bm = __ballot_sync(0xffffffffu, in);
+                        const uint32_t p = n + (uint32_t)__popc(bm & lt);
+                        if (in && p < (uint32_t)TW_LCAP) {
+                            sh.lkey[p] = kv[u];
+                            sh.lidx[p] = (uint16_t)j;
+                        }
+                        n += (uint32_t)__popc(bm);
+                    }
+                }
+            }
+            __syncwarp();
+            if (n <= (uint32_t)TW_LCAP && n >= (uint32_t)k) {
+                auto ckey = [&](int64_t j) { return sh.lkey[j]; };
+                const Thr th = warp_threshold(sh.hist, n, k, ckey);
+                warp_emit(n, k, th, ckey, [&](int64_t j) { return (int32_t)sh.lidx[j]; }, orow);
+                done = true;
+            }
+        }
+        if (!done) {
+            // exact over the whole row, from global memory
+            const Thr th = warp_threshold(sh.hist, nv, k, gkey);
+            warp_emit(nv, k, th, gkey, gid, orow);
+        }
+        if (lane == 0) cnt[row] = k;
+        __syncwarp();
+    }
 }
 
 // ------------------------------------------------------- few long rows (decode)
@@ -216,7 +462,7 @@ topk_kernel(const float *__restrict__ scores, const int64_t *__restrict__ q_pos,
 struct TkLong {
     const float *scores;
     const int64_t *q_pos;
-    uint32_t *hist;        // [rows][2048], zeroed before the histogram pass
+    uint32_t *lo;          // [rows] lower bound on the k-th largest key
     uint32_t *chunk_cnt;   // [rows][CH]
     uint32_t *cand_key;    // [rows][E]: chunk c's candidates at [c*CS, ...)
     int32_t *cand_idx;     // [rows][E]
@@ -226,36 +472,33 @@ struct TkLong {
     int CH, k, m;
 };
 
-__global__ void __launch_bounds__(TK_THREADS) topk_hist_kernel(TkLong a) {
-    __shared__ uint32_t h[2048];
-    const int64_t row = blockIdx.y;
+constexpr int TK_LSAMPLE = 4096;
+
+// (1) per row: a bound lo below the k-th largest key, from an evenly spaced
+// sample of the row (0 = no bound: every key is a candidate)
+__global__ void __launch_bounds__(TK_THREADS) topk_sample_kernel(TkLong a) {
+    __shared__ TkShared sh;
+    __shared__ uint32_t samp[TK_LSAMPLE];
+    const int64_t row = blockIdx.x;
     const int64_t nv = visible_count(a.q_pos[row], a.m, a.E);
     if (nv <= a.k) return;
-    for (int i = threadIdx.x; i < 2048; i += TK_THREADS) h[i] = 0;
-    __syncthreads();
-    const int64_t c0 = (int64_t)blockIdx.x * a.CS;
-    const int64_t c1 = c0 + a.CS < nv ? c0 + a.CS : nv;
+    const int S = (int)(nv < TK_LSAMPLE ? nv : TK_LSAMPLE);
     const float *s = a.scores + row * a.E;
-    for (int64_t base = c0; base < c1; base += TK_THREADS) {
-        const int64_t j = base + threadIdx.x;
-        const uint32_t kv = j < c1 ? score_key(s[j]) : 0u;
-        hist_add(h, j < c1, kv >> 21);
-    }
+    for (int i = threadIdx.x; i < S; i += TK_THREADS) samp[i] = score_key(s[(int64_t)i * nv / S]);
     __syncthreads();
-    uint32_t *g = a.hist + row * 2048;
-    for (int i = threadIdx.x; i < 2048; i += TK_THREADS)
-        if (h[i]) atomicAdd(&g[i], h[i]);
+    const int r = sample_rank(nv, a.k, S);
+    uint32_t lo = 0u;
+    if (r < S) lo = find_threshold(sh, S, r, [&](int64_t j) { return samp[j]; }).tau;
+    if (threadIdx.x == 0) a.lo[row] = lo;
 }
 
-__global__ void __launch_bounds__(TK_THREADS) topk_gather_kernel(TkLong a) {
-    __shared__ TkShared sh;
+// (2) per chunk: the keys >= lo, in index order
+__global__ void __launch_bounds__(TK_THREADS) topk_collect_kernel(TkLong a) {
+    __shared__ uint32_t wsum[32];
     const int64_t row = blockIdx.y;
     const int64_t nv = visible_count(a.q_pos[row], a.m, a.E);
     if (nv <= a.k) return;
-    for (int i = threadIdx.x; i < 2048; i += TK_THREADS) sh.hist[i] = a.hist[row * 2048 + i];
-    __syncthreads();
-    find_bin(sh, 2048, (uint32_t)a.k);
-    const uint32_t bstar = sh.bin;
+    const uint32_t lo = a.lo[row];
     const int64_t c0 = (int64_t)blockIdx.x * a.CS;
     const int64_t c1 = c0 + a.CS < nv ? c0 + a.CS : nv;
     const float *s = a.scores + row * a.E;
@@ -264,10 +507,10 @@ __global__ void __launch_bounds__(TK_THREADS) topk_gather_kernel(TkLong a) {
     uint32_t run = 0;
     for (int64_t base = c0; base < c1; base += TK_THREADS) {
         const int64_t j = base + threadIdx.x;
-        const uint32_t kv = j < c1 ? score_key(s[j]) : 0u;
-        const uint32_t keep = (j < c1 && (kv >> 21) >= bstar) ? 1u : 0u;
+        const uint32_t kv = j < c1 ? score_key(__ldcs(s + j)) : 0u;
+        const uint32_t keep = (j < c1 && kv >= lo) ? 1u : 0u;
         uint32_t tot;
-        const uint32_t pos = run + block_excl_scan(keep, sh.wsum, &tot);
+        const uint32_t pos = run + block_excl_scan(keep, wsum, &tot);
         if (keep) {
             ok[pos] = kv;
             oi[pos] = (int32_t)j;
@@ -302,7 +545,12 @@ __global__ void __launch_bounds__(TK_THREADS) topk_final_kernel(TkLong a, int ca
     const int64_t n = offs[a.CH];
     const uint32_t *gk = a.cand_key + row * a.E;
     const int32_t *gi = a.cand_idx + row * a.E;
-    if (n <= cap) {
+    if (n < a.k) {
+        // the sampled bound missed (fewer than k keys reach it): exact over the row
+        const float *s = a.scores + row * a.E;
+        select_core(sh, nv, a.k, [&](int64_t j) { return score_key(s[j]); },
+                    [](int64_t j) { return (int32_t)j; }, orow);
+    } else if (n <= cap) {
         // the chunks' candidates, in index order, packed into shared memory;
         // every thread locates its items' chunks by binary search so all the
         // loads are in flight together
@@ -335,9 +583,7 @@ __global__ void __launch_bounds__(TK_THREADS) topk_final_kernel(TkLong a, int ca
 
 // -------------------------------------------------------------------- host
 
-static int g_topk_smem_set = 0;
 static int g_final_smem_set = 0;
-constexpr int KCAP_MAX = 40960;      // keys cached per row (160 KB)
 constexpr int CAND_CAP = 24576;      // candidates cached per row (192 KB)
 
 bool topk_use_long(int64_t rows, int64_t E) { return rows < 256 && E > 16384; }
@@ -355,7 +601,7 @@ static size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t topk_scratch_bytes(int64_t rows, int64_t E) {
     if (!topk_use_long(rows, E)) return 0;
     const int ch = topk_chunks(rows, E);
-    return a256((size_t)rows * 2048 * 4) + a256((size_t)rows * ch * 4) + 2 * a256((size_t)rows * E * 4);
+    return a256((size_t)rows * 4) + a256((size_t)rows * ch * 4) + 2 * a256((size_t)rows * E * 4);
 }
 
 cudaError_t launch_topk(int64_t B, int64_t Tq, int64_t E, int k, int m, const float *scores,
@@ -368,8 +614,8 @@ cudaError_t launch_topk(int64_t B, int64_t Tq, int64_t E, int k, int m, const fl
         TkLong a;
         const int ch = topk_chunks(rows, E);
         char *p = (char *)scratch;
-        a.hist = (uint32_t *)p;
-        p += a256((size_t)rows * 2048 * 4);
+        a.lo = (uint32_t *)p;
+        p += a256((size_t)rows * 4);
         a.chunk_cnt = (uint32_t *)p;
         p += a256((size_t)rows * ch * 4);
         a.cand_key = (uint32_t *)p;
@@ -377,14 +623,12 @@ cudaError_t launch_topk(int64_t B, int64_t Tq, int64_t E, int k, int m, const fl
         a.cand_idx = (int32_t *)p;
         a.scores = scores; a.q_pos = q_pos; a.idx = idx; a.cnt = cnt;
         a.E = E; a.CH = ch; a.CS = (E + ch - 1) / ch; a.k = k; a.m = m;
-        cudaError_t e = cudaMemsetAsync(a.hist, 0, (size_t)rows * 2048 * 4, st);
-        if (e != cudaSuccess) return e;
         dim3 g((unsigned)ch, (unsigned)rows);
-        topk_hist_kernel<<<g, TK_THREADS, 0, st>>>(a);
-        topk_gather_kernel<<<g, TK_THREADS, 0, st>>>(a);
+        topk_sample_kernel<<<(unsigned)rows, TK_THREADS, 0, st>>>(a);
+        topk_collect_kernel<<<g, TK_THREADS, 0, st>>>(a);
         if (!g_final_smem_set) {
-            e = cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     CAND_CAP * 8);
+            cudaError_t e = cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 CAND_CAP * 8);
             if (e != cudaSuccess) return e;
             g_final_smem_set = 1;
         }
@@ -392,15 +636,17 @@ cudaError_t launch_topk(int64_t B, int64_t Tq, int64_t E, int k, int m, const fl
         count_launches(3);
         return cudaGetLastError();
     }
-    const int kcap = (int)(E < KCAP_MAX ? E : KCAP_MAX);
-    const size_t smem = (size_t)kcap * 4;
-    if (!g_topk_smem_set) {
-        cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             KCAP_MAX * 4);
+    static int tw_attr = 0;
+    const size_t smem = TW_WARPS * sizeof(TwShared);
+    if (!tw_attr) {
+        cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        g_topk_smem_set = 1;
+        tw_attr = 1;
     }
-    topk_kernel<<<(unsigned)rows, TK_THREADS, smem, st>>>(scores, q_pos, idx, cnt, E, k, m, kcap);
+    int64_t blocks = (rows + TW_WARPS - 1) / TW_WARPS;
+    const int64_t cap = (int64_t)device_sms();           // one resident CTA per SM
+    if (blocks > cap) blocks = cap;
+    topk_kernel<<<(unsigned)blocks, TW_WARPS * 32, smem, st>>>(scores, q_pos, idx, cnt, rows, E, k, m);
     count_launches(1);
     return cudaGetLastError();
 }

@@ -126,6 +126,52 @@ def test_topk_exact(csa, orc, B, T, E, k, m):
         np.testing.assert_array_equal(gi[b], oi)
 
 
+def _topk_check(csa, orc, sc, pos, m, k):
+    idx, cnt = csa.topk_select(dev(sc), dev(pos), m, k)
+    gi, gc = host(idx), host(cnt)
+    for b in range(sc.shape[0]):
+        oi, oc = orc.topk(sc[b].astype(np.float64), pos[b], m, k)
+        np.testing.assert_array_equal(gc[b], oc)
+        np.testing.assert_array_equal(gi[b], oi)
+
+
+@pytest.mark.parametrize("ties", [False, True])
+def test_topk_prefill_rows(csa, orc, ties):
+    """Many rows of up to 16384 visible entries (one CTA per row, keys in
+    registers, sampled candidate bound); with heavy ties the candidates
+    overflow and the exact whole-row selection runs."""
+    r = _np_rng(311 + ties)
+    T, E, k, m = 40, 16384, 512, 4
+    sc = r.standard_normal((1, T, E)).astype(np.float32)
+    if ties:
+        sc = (np.round(sc * 2) / 2).astype(np.float32)
+    pos = np.linspace(2 * k * m, E * m - 1, T).astype(np.int64).reshape(1, T)
+    _topk_check(csa, orc, sc, pos, m, k)
+
+
+def test_topk_sample_miss_prefill(csa, orc):
+    """The largest keys sit exactly at the sampled positions, so the sampled
+    bound admits fewer than k keys and the exact whole-row selection runs."""
+    r = _np_rng(313)
+    T, E, k, m = 4, 16384, 512, 4
+    sc = r.standard_normal((1, T, E)).astype(np.float32)
+    hot = (np.arange(E) % 8) == 0              # the 2048 evenly spaced sample positions
+    sc[..., hot] = 100.0 + r.standard_normal((T, int(hot.sum()))).astype(np.float32)
+    pos = np.full((1, T), E * m - 1, np.int64)
+    _topk_check(csa, orc, sc, pos, m, k)
+
+
+def test_topk_sample_miss_decode(csa, orc):
+    """Decode rows whose largest keys sit exactly at the evenly spaced sample
+    positions: the long-row path falls back to the exact selection."""
+    r = _np_rng(317)
+    B, E, k, m = 2, 262144, 1024, 4
+    sc = r.standard_normal((B, 1, E)).astype(np.float32)
+    sc[..., ::64] = 100.0 + r.standard_normal((B, 1, E // 64)).astype(np.float32)
+    pos = np.full((B, 1), E * m - 1, np.int64)
+    _topk_check(csa, orc, sc, pos, m, k)
+
+
 # --------------------------------------------------------------- attention
 
 @pytest.mark.parametrize("dtype,B,T,H,c,E,k,m,n_win,r,derot", [
