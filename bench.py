@@ -125,6 +125,23 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
+# ------------------------------------------------------------ multi-rank
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest x over all ranks (x itself on one process)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank: float, world: int, ms_step: float) -> float:
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    return world * units_per_rank / (ms_step / 1e3)
+
+
 # --------------------------------------------------------------- workloads
 
 class Workload:
@@ -361,12 +378,8 @@ def run_ours(args, rank, world, dist):
     clocks.keep_busy(wl.step, 2)
     clk = clocks.stop()
     ms_total = ev0.elapsed_time(ev1)
-    ms_step = ms_total / args.steps
-    if dist is not None:
-        t = torch.tensor([ms_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = world * wl.units / (ms_step / 1e3)
+    ms_step = max_over_ranks(ms_total / args.steps, dist, "cuda")
+    value = job_value(wl.units, world, ms_step)
 
     # end to end through the public API with host buffers
     wl.e2e_setup()
@@ -378,12 +391,8 @@ def run_ours(args, rank, world, dist):
     for _ in range(k_e2e):
         wl.e2e_step()
     torch.cuda.synchronize()
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / k_e2e
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * wl.units / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / k_e2e, dist, "cuda")
+    e2e_value = job_value(wl.units, world, e2e_ms)
 
     # roofline of the dominant stage
     pk, pk_kind = peaks()

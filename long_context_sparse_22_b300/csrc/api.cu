@@ -198,10 +198,14 @@ csa_status do_indexer(csa_dtype dt, int64_t B, int64_t T, int hI, int dI, int64_
 }
 
 csa_status do_topk(int64_t B, int64_t T, int64_t E, int k, int m, const float *scores,
-                   const int64_t *q_pos, int32_t *idx, int32_t *cnt, void *scratch, cudaStream_t st) {
+                   const int64_t *q_pos, int32_t *idx, int32_t *cnt, void *scratch, cudaStream_t st,
+                   int phase = 0) {
     StageScope sc(CSA_STAGE_TOPK, st);
-    CSA_TRY_CUDA(launch_topk(B, T, E, k, m, scores, q_pos, idx, cnt, scratch, st),
-                 "topk_select launch");
+    if (phase == 0)
+        CSA_TRY_CUDA(launch_topk(B, T, E, k, m, scores, q_pos, idx, cnt, scratch, st), "topk_select launch");
+    else
+        CSA_TRY_CUDA(launch_topk_phase(phase, B, T, E, k, m, scores, q_pos, idx, cnt, scratch, st),
+                     "topk_select launch");
     return CSA_OK;
 }
 
@@ -653,37 +657,31 @@ csa_status hybrid_decode(csa_dtype dtype, int64_t B, int32_t H, int32_t c, int32
                   &asc, &asc2);
     if (idx_out) idx = idx_out;
     unsigned *status = (unsigned *)ws;
-    // The HCA layer's attention does not depend on the CSA layer: when both
-    // run on the tensor-core paths it goes to an auxiliary stream on a slice
-    // of the SMs while the CSA indexer streams kI on the rest.
-    const bool concurrent = hca && dtype == CSA_BF16 && attn_tc_supported(dtype, c) &&
-                            indexer_tc_supported(hI, dI, B, 1, E);
-    int idx_ctas = 0, hca_ctas = 0;
+    // The HCA layer's attention does not depend on the CSA layer.  The CSA
+    // indexer (which streams kI at the HBM rate) and the top-k's candidate
+    // collection run first on every SM; the HCA attention then runs on an
+    // auxiliary stream, on all but a few SMs, beside the rest of the CSA top-k
+    // and the sparse attention, which need few CTAs.
+    const bool concurrent = hca && dtype == CSA_BF16 && attn_tc_supported(dtype, c);
+    CSA_TRY(do_indexer(dtype, B, 1, hI, dI, E, params->m, qI, w, kIc, q_pos, (float *)sc, 0, status, st));
+    CSA_TRY(do_topk(B, 1, E, params->top_k, params->m, (const float *)sc, q_pos, (int32_t *)idx,
+                    (int32_t *)cnt, tks, st, 1));
+    AuxStreams *ax = nullptr;
     if (concurrent) {
-        AuxStreams *ax = nullptr;
         CSA_TRY(get_aux(&ax));
         const int sms = device_sms();
-        hca_ctas = sms / 4;
-        idx_ctas = sms - hca_ctas;
         CSA_TRY_CUDA(cudaEventRecord(ax->fork, st), "fork");
         CSA_TRY_CUDA(cudaStreamWaitEvent(ax->aux, ax->fork, 0), "fork wait");
         CSA_TRY(do_attn(dtype, B, 1, H, c, E2, 0, L, q2, q_pos, kvc2, nullptr, nullptr, kv_raw2,
-                        raw_pos0, sink2, out2, nullptr, params2, status, asc2, ax->aux, hca_ctas));
+                        raw_pos0, sink2, out2, nullptr, params2, status, asc2, ax->aux, sms - 24));
         CSA_TRY_CUDA(cudaEventRecord(ax->join, ax->aux), "join");
-        CSA_TRY(do_indexer(dtype, B, 1, hI, dI, E, params->m, qI, w, kIc, q_pos, (float *)sc, 0,
-                           status, st, idx_ctas));
-    } else {
-        CSA_TRY(do_indexer(dtype, B, 1, hI, dI, E, params->m, qI, w, kIc, q_pos, (float *)sc, 0,
-                           status, st));
     }
     CSA_TRY(do_topk(B, 1, E, params->top_k, params->m, (const float *)sc, q_pos, (int32_t *)idx,
-                    (int32_t *)cnt, tks, st));
+                    (int32_t *)cnt, tks, st, 2));
     CSA_TRY(do_attn(dtype, B, 1, H, c, E, params->top_k, L, q, q_pos, kvc, (const int32_t *)idx,
                     (const int32_t *)cnt, kv_raw, raw_pos0, sink, out, nullptr, params, status, asc,
                     st));
     if (concurrent) {
-        AuxStreams *ax = nullptr;
-        CSA_TRY(get_aux(&ax));
         CSA_TRY_CUDA(cudaStreamWaitEvent(st, ax->join, 0), "join wait");
     } else if (hca) {
         CSA_TRY(do_attn(dtype, B, 1, H, c, E2, 0, L, q2, q_pos, kvc2, nullptr, nullptr, kv_raw2,

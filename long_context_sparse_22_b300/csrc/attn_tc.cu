@@ -32,12 +32,13 @@
 // Warp roles (persistent CTAs, items dealt round-robin):
 //   warps 0-3  loaders: q tile (box TMA, then RoPE at t in place), the entry
 //              tiles (two buffers), the presence masks;
-//   warp 4     TMEM allocator and MMA issuer (one thread): QK and PV in
-//              whichever order their inputs become ready;
-//   warps 5-8  softmax (one head per thread), the O rescale, and the
-//              epilogue: normalise, de-rotate, stage a 128-dim chunk in
-//              shared memory and write it with one TMA store (or fp32
-//              partial outputs for a split-KV combine).
+//   warp 4     TMEM allocator and QK issuer (one thread);
+//   warps 5-8  softmax (a head's 64 logits spread over four threads), the
+//              O rescale, and the epilogue: normalise, de-rotate, stage 32
+//              heads x 128 dims at a time in shared memory and write each
+//              block with a TMA store that overlaps the next block's work
+//              (or fp32 partial outputs for a split-KV combine);
+//   warp 9     PV issuer (one thread).
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -666,7 +667,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (named_bar_or(1, 128, !ok)) break;
             tc::fence_after_sync();
             const int nh = a.H - h0 < 64 ? a.H - h0 : 64;
-            __nv_bfloat16 *stage = (__nv_bfloat16 *)sP;        // [64 heads][128 dims], P is free now
+            // stage: two [32 heads][128 dims] bf16 halves (P is free now); each half of
+            // a chunk leaves by its own TMA store, which overlaps the next half's work
+            __nv_bfloat16 *stage = (__nv_bfloat16 *)sP;
             for (int c = 0; c < Cfg::NC; c++) {
                 const int dl = quarter * 32 + lane;             // dim within the chunk
                 const int d = c * 128 + dl;
@@ -708,8 +711,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         }
                     }
                     if (tma_out) {
+                        __nv_bfloat16 *sb = stage + (hb >> 5) * (32 * 128);
 #pragma unroll
-                        for (int h = 0; h < 32; h++) stage[(hb + h) * 128 + dl] = __float2bfloat16_rn(o[h]);
+                        for (int h = 0; h < 32; h++) sb[h * 128 + dl] = __float2bfloat16_rn(o[h]);
+                        fence_proxy_async();
+                        // the store issued one half earlier has read its buffer (the one
+                        // the next half writes) before anyone passes the barrier
+                        if (st == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                        named_bar(1, 128);
+                        if (st == 0) {
+                            asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                                         ::"l"(reinterpret_cast<uint64_t>(&tm_o)), "r"(c * 128),
+                                         "r"((int)(f.bt * a.H + h0 + hb)), "r"(tc::smem_u32(sb))
+                                         : "memory");
+                            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                        }
                     } else {
                         __nv_bfloat16 *op = a.out + (f.bt * a.H + h0 + hb) * (int64_t)C + d;
 #pragma unroll
@@ -717,25 +733,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             if (hb + h < nh) op[(int64_t)h * C] = __float2bfloat16_rn(o[h]);
                     }
                 }
-                if (tma_out) {
-                    // the normalised chunk leaves shared memory by one TMA store
-                    fence_proxy_async();
-                    named_bar(1, 128);
-                    if (st == 0) {
-                        asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
-                                     ::"l"(reinterpret_cast<uint64_t>(&tm_o)), "r"(c * 128),
-                                     "r"((int)(f.bt * a.H + h0)), "r"(tc::smem_u32(stage))
-                                     : "memory");
-                        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                    }
-                    named_bar(1, 128);
-                }
             }
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(oempty);
-            named_bar(1, 128);                 // inv_den_s is rewritten by the next item
+            // the last store has read P's buffers; inv_den_s is rewritten by the next item
+            if (st == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            named_bar(1, 128);
             ii++;
         }
         if (st == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -840,9 +844,11 @@ size_t attn_tc_split_bytes(int64_t rows, int H, int c, int n_chunks) {
 int attn_tc_chunks(int64_t rows, int H, int64_t max_list) {
     const int64_t tiles = (max_list + 63) / 64 + 1;       // + 1: padding of the compressed part
     if (rows * ((H + 63) / 64) >= 2 * 148 || tiles <= 4) return 1;
-    int64_t ch = (tiles + 7) / 8;          // 8 tiles per chunk
-    if (ch > 64) ch = 64;
-    return (int)ch;
+    // at least 4 tiles per chunk and at most 16 chunks: a function of the list
+    // length alone
+    int64_t per = (tiles + 15) / 16;
+    if (per < 4) per = 4;
+    return (int)((tiles + per - 1) / per);
 }
 
 cudaError_t launch_attn_tc(int64_t B, const AttnArgs &g, const int32_t *cnt, int n_chunks,
@@ -882,7 +888,7 @@ cudaError_t launch_attn_tc(int64_t B, const AttnArgs &g, const int32_t *cnt, int
     using Cfg = AtCfg<512>;
     // tensor maps: q rows [B*T*H, C]; compressed entries [B*E, C] and raw
     // window rows [B*L, C] as 64-row boxes (a map that is never read points
-    // at q); out [B*T*H, C] for the epilogue's 64 x 128 stores.
+    // at q); out [B*T*H, C] for the epilogue's 32 x 128 stores.
     CUtensorMap tq, tcmp, tw, to;
     const bool have_c = g.E > 0 && g.kvc != nullptr;
     const bool have_w = g.L > 0 && g.kv_raw != nullptr;
@@ -891,7 +897,7 @@ cudaError_t launch_attn_tc(int64_t B, const AttnArgs &g, const int32_t *cnt, int
                            512, 64) ||
         !make_tmap_bf16_2d(&tw, have_w ? g.kv_raw : g.q, have_w ? (uint64_t)(B * g.L) : (uint64_t)(rows * g.H),
                            512, 64) ||
-        !make_tmap_bf16_2d_plain(&to, g.out, (uint64_t)(rows * g.H), 512, 128, 64))
+        !make_tmap_bf16_2d_plain(&to, g.out, (uint64_t)(rows * g.H), 512, 128, 32))
         return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {

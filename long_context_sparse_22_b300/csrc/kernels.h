@@ -58,6 +58,12 @@ size_t topk_scratch_bytes(int64_t rows, int64_t E);
 cudaError_t launch_topk(int64_t B, int64_t Tq, int64_t E, int k, int m, const float *scores,
                         const int64_t *q_pos, int32_t *idx, int32_t *cnt, void *scratch,
                         cudaStream_t st);
+// The same in two phases: 1 = everything, or for few long rows only the
+// candidate collection (every SM); 2 = the long rows' exact selection (one
+// CTA per row), nothing otherwise.
+cudaError_t launch_topk_phase(int phase, int64_t B, int64_t Tq, int64_t E, int k, int m,
+                              const float *scores, const int64_t *q_pos, int32_t *idx, int32_t *cnt,
+                              void *scratch, cudaStream_t st);
 
 cudaError_t launch_attn_simt(csa_dtype dt, int64_t B, const AttnArgs &a, cudaStream_t st);
 

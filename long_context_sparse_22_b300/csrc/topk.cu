@@ -20,10 +20,10 @@
 // sample.
 //
 // Many rows (prefill): one warp per row.
-// Few long rows (decode, up to 262144 entries): three launches: (1) one CTA
-// per row takes the sample, (2) the row's chunks are spread over many CTAs,
-// each keeping its keys >= lo in index order, (3) one CTA per row runs the
-// exact selection on the candidates.
+// Few long rows (decode, up to 262144 entries): two launches: (1) the row's
+// chunks are spread over many CTAs, each deriving the row's sampled bound and
+// keeping its keys >= lo in index order, (2) one CTA per row runs the exact
+// selection on the candidates.
 #include <mutex>
 
 #include "common.cuh"
@@ -462,7 +462,6 @@ topk_kernel(const float *__restrict__ scores, const int64_t *__restrict__ q_pos,
 struct TkLong {
     const float *scores;
     const int64_t *q_pos;
-    uint32_t *lo;          // [rows] lower bound on the k-th largest key
     uint32_t *chunk_cnt;   // [rows][CH]
     uint32_t *cand_key;    // [rows][E]: chunk c's candidates at [c*CS, ...)
     int32_t *cand_idx;     // [rows][E]
@@ -472,52 +471,110 @@ struct TkLong {
     int CH, k, m;
 };
 
-constexpr int TK_LSAMPLE = 4096;
+constexpr int TK_LSAMPLE = 4096;              // sample keys per long row (8 per thread)
+constexpr int TK_SEG = 256;                   // candidates a warp keeps per chunk
 
-// (1) per row: a bound lo below the k-th largest key, from an evenly spaced
-// sample of the row (0 = no bound: every key is a candidate)
-__global__ void __launch_bounds__(TK_THREADS) topk_sample_kernel(TkLong a) {
-    __shared__ TkShared sh;
-    __shared__ uint32_t samp[TK_LSAMPLE];
-    const int64_t row = blockIdx.x;
-    const int64_t nv = visible_count(a.q_pos[row], a.m, a.E);
-    if (nv <= a.k) return;
-    const int S = (int)(nv < TK_LSAMPLE ? nv : TK_LSAMPLE);
-    const float *s = a.scores + row * a.E;
-    for (int i = threadIdx.x; i < S; i += TK_THREADS) samp[i] = score_key(s[(int64_t)i * nv / S]);
+// Keys >= t among every thread's NK register keys, summed over the block
+// (512 threads); red holds two 16-word slots used alternately.
+template <int NK>
+__device__ __forceinline__ uint32_t block_count_ge(const uint32_t (&kr)[NK], uint32_t t, uint32_t *red,
+                                                   int slot) {
+    uint32_t c = 0;
+#pragma unroll
+    for (int i = 0; i < NK; i++) c += kr[i] >= t ? 1u : 0u;
+    c = __reduce_add_sync(0xffffffffu, c);
+    if ((threadIdx.x & 31) == 0) red[slot * 16 + (threadIdx.x >> 5)] = c;
     __syncthreads();
-    const int r = sample_rank(nv, a.k, S);
-    uint32_t lo = 0u;
-    if (r < S) lo = find_threshold(sh, S, r, [&](int64_t j) { return samp[j]; }).tau;
-    if (threadIdx.x == 0) a.lo[row] = lo;
+    uint32_t tot = 0;
+#pragma unroll
+    for (int w = 0; w < TK_THREADS / 32; w++) tot += red[slot * 16 + w];
+    return tot;
 }
 
-// (2) per chunk: the keys >= lo, in index order
+// (1) per chunk of a long row: the row's sampled bound lo (every chunk CTA
+// derives the same value from the same evenly spaced sample), then the
+// chunk's keys >= lo in index order.  Each warp compacts its own contiguous
+// slice into a shared-memory segment; one scan of the warp counts places the
+// segments.  chunk_cnt gets the chunk's count, or ~0u if a segment overflowed.
 __global__ void __launch_bounds__(TK_THREADS) topk_collect_kernel(TkLong a) {
-    __shared__ uint32_t wsum[32];
+    __shared__ uint32_t red[32];
+    __shared__ uint32_t wcount[TK_THREADS / 32];
+    __shared__ uint32_t skey[TK_THREADS / 32][TK_SEG];
+    __shared__ int32_t sidx[TK_THREADS / 32][TK_SEG];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int64_t row = blockIdx.y;
     const int64_t nv = visible_count(a.q_pos[row], a.m, a.E);
     if (nv <= a.k) return;
-    const uint32_t lo = a.lo[row];
+    const float *s = a.scores + row * a.E;
+    // the bound: top 24 bits of the r-th largest of TK_LSAMPLE evenly spaced keys
+    const int S = (int)(nv < TK_LSAMPLE ? nv : TK_LSAMPLE);
+    uint32_t sk[TK_LSAMPLE / TK_THREADS];
+#pragma unroll
+    for (int u = 0; u < TK_LSAMPLE / TK_THREADS; u++) {
+        const int i = u * TK_THREADS + tid;
+        const int64_t pos = S == TK_LSAMPLE ? (((int64_t)i * nv) >> 12) : i;   // TK_LSAMPLE = 2^12
+        sk[u] = i < S ? score_key(s[pos]) : 0u;
+    }
+    const int r = S < TK_LSAMPLE ? a.k : sample_rank(nv, a.k, S);
+    uint32_t lo = 0u;
+    if (r < S) {
+        uint32_t t = 0;
+#pragma unroll 1
+        for (int b = 31; b >= 8; b--) {
+            const uint32_t c = t | (1u << b);
+            if (block_count_ge(sk, c, red, b & 1) >= (uint32_t)r) t = c;
+        }
+        lo = t;
+    }
+    // this warp's slice of the chunk
     const int64_t c0 = (int64_t)blockIdx.x * a.CS;
     const int64_t c1 = c0 + a.CS < nv ? c0 + a.CS : nv;
-    const float *s = a.scores + row * a.E;
-    uint32_t *ok = a.cand_key + row * a.E + c0;
-    int32_t *oi = a.cand_idx + row * a.E + c0;
-    uint32_t run = 0;
-    for (int64_t base = c0; base < c1; base += TK_THREADS) {
-        const int64_t j = base + threadIdx.x;
-        const uint32_t kv = j < c1 ? score_key(__ldcs(s + j)) : 0u;
-        const uint32_t keep = (j < c1 && kv >= lo) ? 1u : 0u;
-        uint32_t tot;
-        const uint32_t pos = run + block_excl_scan(keep, wsum, &tot);
-        if (keep) {
-            ok[pos] = kv;
-            oi[pos] = (int32_t)j;
+    const int64_t per = (c1 - c0 + TK_THREADS / 32 - 1) / (TK_THREADS / 32);
+    const int64_t w0 = c0 + wid * per;
+    const int64_t w1 = w0 + per < c1 ? w0 + per : c1;
+    const unsigned lt = (1u << lane) - 1u;
+    uint32_t n = 0;
+    constexpr int NB = 16;
+    for (int64_t base = w0; base < w1; base += 32 * NB) {
+        uint32_t kv[NB];
+#pragma unroll
+        for (int u = 0; u < NB; u++) {
+            const int64_t j = base + 32 * u + lane;
+            kv[u] = j < w1 ? score_key(__ldcs(s + j)) : 0u;
         }
-        run += tot;
+#pragma unroll
+        for (int u = 0; u < NB; u++) {
+            const int64_t j = base + 32 * u + lane;
+            const bool in = j < w1 && kv[u] >= lo;
+            const unsigned bm = __ballot_sync(0xffffffffu, in);
+            const uint32_t p = n + (uint32_t)__popc(bm & lt);
+            if (in && p < (uint32_t)TK_SEG) {
+                skey[wid][p] = kv[u];
+                sidx[wid][p] = (int32_t)j;
+            }
+            n += (uint32_t)__popc(bm);
+        }
     }
-    if (threadIdx.x == 0) a.chunk_cnt[row * a.CH + blockIdx.x] = run;
+    if (lane == 0) wcount[wid] = n;
+    __syncthreads();
+    uint32_t before = 0, tot = 0;
+    bool over = false;
+#pragma unroll
+    for (int w = 0; w < TK_THREADS / 32; w++) {
+        const uint32_t v = wcount[w];
+        before += w < wid ? v : 0u;
+        tot += v;
+        over |= v > (uint32_t)TK_SEG;
+    }
+    if (!over) {
+        uint32_t *ok = a.cand_key + row * a.E + c0 + before;
+        int32_t *oi = a.cand_idx + row * a.E + c0 + before;
+        for (uint32_t i = lane; i < n; i += 32) {
+            ok[i] = skey[wid][i];
+            oi[i] = sidx[wid][i];
+        }
+    }
+    if (tid == 0) a.chunk_cnt[row * a.CH + blockIdx.x] = over ? 0xffffffffu : tot;
 }
 
 __global__ void __launch_bounds__(TK_THREADS) topk_final_kernel(TkLong a, int cap) {
@@ -533,20 +590,19 @@ __global__ void __launch_bounds__(TK_THREADS) topk_final_kernel(TkLong a, int ca
         if (tid == 0) a.cnt[row] = (int32_t)nv;
         return;
     }
-    if (tid == 0) {
-        uint32_t o = 0;
-        for (int c = 0; c < a.CH; c++) {
-            offs[c] = o;
-            o += a.chunk_cnt[row * a.CH + c];
-        }
-        offs[a.CH] = o;
-    }
+    // chunk offsets: one block scan of the chunk counts (CH <= TK_THREADS)
+    const uint32_t mine = tid < a.CH ? a.chunk_cnt[row * a.CH + tid] : 0u;
+    const bool bad = __syncthreads_or(mine == 0xffffffffu);
+    uint32_t tot_all;
+    const uint32_t ex = block_excl_scan(bad ? 0u : mine, sh.wsum, &tot_all);
+    if (tid <= a.CH && tid < 257) offs[tid] = ex;
     __syncthreads();
-    const int64_t n = offs[a.CH];
+    const int64_t n = bad ? -1 : (int64_t)tot_all;
     const uint32_t *gk = a.cand_key + row * a.E;
     const int32_t *gi = a.cand_idx + row * a.E;
     if (n < a.k) {
-        // the sampled bound missed (fewer than k keys reach it): exact over the row
+        // the sampled bound missed (fewer than k keys reach it, or a warp's
+        // segment overflowed): exact over the row
         const float *s = a.scores + row * a.E;
         select_core(sh, nv, a.k, [&](int64_t j) { return score_key(s[j]); },
                     [](int64_t j) { return (int32_t)j; }, orow);
@@ -566,8 +622,49 @@ __global__ void __launch_bounds__(TK_THREADS) topk_final_kernel(TkLong a, int ca
             si[j] = gi[src];
         }
         __syncthreads();
-        select_core(sh, n, a.k, [&](int64_t j) { return smc[j]; }, [&](int64_t j) { return si[j]; },
-                    orow);
+        if (n <= 8 * TK_THREADS) {
+            // exact k-th largest bit by bit over the candidates in registers,
+            // thread t holding candidates 8t .. 8t+7 (index order)
+            uint32_t ck[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                const int64_t j = (int64_t)tid * 8 + u;
+                ck[u] = j < n ? smc[j] : 0u;
+            }
+            __shared__ uint32_t red[32];
+            uint32_t t = 0;
+#pragma unroll 1
+            for (int b = 31; b >= 0; b--) {
+                const uint32_t c = t | (1u << b);
+                if (block_count_ge(ck, c, red, b & 1) >= (uint32_t)a.k) t = c;
+            }
+            const uint32_t gt = t == 0xffffffffu ? 0u : block_count_ge(ck, t + 1u, red, 0);
+            const uint32_t need_eq = (uint32_t)a.k - gt;
+            // ordered emit: one scan of the per-thread counts of kept and of tied keys
+            uint32_t n_gt = 0, n_eq = 0;
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                n_gt += ck[u] > t ? 1u : 0u;
+                n_eq += ck[u] == t && (int64_t)tid * 8 + u < n ? 1u : 0u;
+            }
+            uint32_t tot2;
+            const uint32_t ex2 = block_excl_scan((n_eq << 16) | n_gt, sh.wsum, &tot2);
+            uint32_t eq_before = ex2 >> 16, gt_before = ex2 & 0xffffu;
+            uint32_t pos = gt_before + (eq_before < need_eq ? eq_before : need_eq);
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                const int64_t j = (int64_t)tid * 8 + u;
+                bool sel = false;
+                if (j < n) {
+                    if (ck[u] > t) sel = true;
+                    else if (ck[u] == t) sel = eq_before++ < need_eq;
+                }
+                if (sel) orow[pos++] = si[j];
+            }
+        } else {
+            select_core(sh, n, a.k, [&](int64_t j) { return smc[j]; }, [&](int64_t j) { return si[j]; },
+                        orow);
+        }
     } else {
         // many candidates (heavy ties): read them in place, chunk by chunk
         auto where = [&](int64_t j) {
@@ -601,12 +698,14 @@ static size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t topk_scratch_bytes(int64_t rows, int64_t E) {
     if (!topk_use_long(rows, E)) return 0;
     const int ch = topk_chunks(rows, E);
-    return a256((size_t)rows * 4) + a256((size_t)rows * ch * 4) + 2 * a256((size_t)rows * E * 4);
+    return a256((size_t)rows * ch * 4) + 2 * a256((size_t)rows * E * 4);
 }
 
-cudaError_t launch_topk(int64_t B, int64_t Tq, int64_t E, int k, int m, const float *scores,
-                        const int64_t *q_pos, int32_t *idx, int32_t *cnt, void *scratch,
-                        cudaStream_t st) {
+// phase 1: everything, or for long rows only the candidate collection;
+// phase 2: for long rows, the exact selection (nothing otherwise).
+cudaError_t launch_topk_phase(int phase, int64_t B, int64_t Tq, int64_t E, int k, int m,
+                              const float *scores, const int64_t *q_pos, int32_t *idx, int32_t *cnt,
+                              void *scratch, cudaStream_t st) {
     const int64_t rows = B * Tq;
     if (rows == 0) return cudaSuccess;
     if (topk_use_long(rows, E)) {
@@ -614,8 +713,6 @@ cudaError_t launch_topk(int64_t B, int64_t Tq, int64_t E, int k, int m, const fl
         TkLong a;
         const int ch = topk_chunks(rows, E);
         char *p = (char *)scratch;
-        a.lo = (uint32_t *)p;
-        p += a256((size_t)rows * 4);
         a.chunk_cnt = (uint32_t *)p;
         p += a256((size_t)rows * ch * 4);
         a.cand_key = (uint32_t *)p;
@@ -623,9 +720,12 @@ cudaError_t launch_topk(int64_t B, int64_t Tq, int64_t E, int k, int m, const fl
         a.cand_idx = (int32_t *)p;
         a.scores = scores; a.q_pos = q_pos; a.idx = idx; a.cnt = cnt;
         a.E = E; a.CH = ch; a.CS = (E + ch - 1) / ch; a.k = k; a.m = m;
-        dim3 g((unsigned)ch, (unsigned)rows);
-        topk_sample_kernel<<<(unsigned)rows, TK_THREADS, 0, st>>>(a);
-        topk_collect_kernel<<<g, TK_THREADS, 0, st>>>(a);
+        if (phase == 1) {
+            dim3 g((unsigned)ch, (unsigned)rows);
+            topk_collect_kernel<<<g, TK_THREADS, 0, st>>>(a);
+            count_launches(1);
+            return cudaGetLastError();
+        }
         if (!g_final_smem_set) {
             cudaError_t e = cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  CAND_CAP * 8);
@@ -633,9 +733,10 @@ cudaError_t launch_topk(int64_t B, int64_t Tq, int64_t E, int k, int m, const fl
             g_final_smem_set = 1;
         }
         topk_final_kernel<<<(unsigned)rows, TK_THREADS, CAND_CAP * 8, st>>>(a, CAND_CAP);
-        count_launches(3);
+        count_launches(1);
         return cudaGetLastError();
     }
+    if (phase != 1) return cudaSuccess;
     static int tw_attr = 0;
     const size_t smem = TW_WARPS * sizeof(TwShared);
     if (!tw_attr) {
@@ -651,13 +752,21 @@ cudaError_t launch_topk(int64_t B, int64_t Tq, int64_t E, int k, int m, const fl
     return cudaGetLastError();
 }
 
+cudaError_t launch_topk(int64_t B, int64_t Tq, int64_t E, int k, int m, const float *scores,
+                        const int64_t *q_pos, int32_t *idx, int32_t *cnt, void *scratch,
+                        cudaStream_t st) {
+    cudaError_t e = launch_topk_phase(1, B, Tq, E, k, m, scores, q_pos, idx, cnt, scratch, st);
+    if (e != cudaSuccess) return e;
+    return launch_topk_phase(2, B, Tq, E, k, m, scores, q_pos, idx, cnt, scratch, st);
+}
+
 // -------------------------------------------------- allocation-free selection
 //
 // Callers that cannot allocate device memory (code running where cudaMalloc
 // is not available or not allowed, e.g. inside an allocator-free serving loop
 // or a host that only hands over pre-registered buffers) can still select
-// over long rows: topk_select_noalloc keeps its scratch (histograms, chunk
-// counts, candidates) in the file-scope device array below instead of a
+// over long rows: topk_select_noalloc keeps its scratch (chunk counts and
+// candidates) in the file-scope device array below instead of a
 // caller workspace.  Limits: at most NOALLOC_MAX_ROWS rows and
 // NOALLOC_MAX_ENTRIES = rows x E entries when the long-row path is taken.
 constexpr int64_t NOALLOC_MAX_ROWS = 64;
