@@ -471,24 +471,106 @@ struct TkLong {
     int CH, k, m;
 };
 
-constexpr int TK_LSAMPLE = 4096;              // sample keys per long row (8 per thread)
+constexpr int TK_LSAMPLE = 1024;              // sample keys per long row (32 per lane of warp 0)
 constexpr int TK_SEG = 256;                   // candidates a warp keeps per chunk
 
-// Keys >= t among every thread's NK register keys, summed over the block
-// (512 threads); red holds two 16-word slots used alternately.
+// The k-th largest of the valid keys held in registers by the block's
+// TK_THREADS threads (the first nk[t] of thread t's NK keys are valid):
+// radix select with digits of at most 8 bits, over the bits in which the
+// keys differ only; three barriers per digit.
 template <int NK>
-__device__ __forceinline__ uint32_t block_count_ge(const uint32_t (&kr)[NK], uint32_t t, uint32_t *red,
-                                                   int slot) {
-    uint32_t c = 0;
+__device__ Thr block_threshold(const uint32_t (&kr)[NK], int nk, int k, uint32_t *hist, uint32_t *red) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    constexpr int NW = TK_THREADS / 32;
+    uint32_t a1 = 0xffffffffu, o1 = 0u;
 #pragma unroll
-    for (int i = 0; i < NK; i++) c += kr[i] >= t ? 1u : 0u;
-    c = __reduce_add_sync(0xffffffffu, c);
-    if ((threadIdx.x & 31) == 0) red[slot * 16 + (threadIdx.x >> 5)] = c;
+    for (int i = 0; i < NK; i++)
+        if (i < nk) {
+            a1 &= kr[i];
+            o1 |= kr[i];
+        }
+    a1 = __reduce_and_sync(0xffffffffu, a1);
+    o1 = __reduce_or_sync(0xffffffffu, o1);
+    if (lane == 0) {
+        red[wid] = a1;
+        red[NW + wid] = o1;
+    }
     __syncthreads();
-    uint32_t tot = 0;
+    a1 = 0xffffffffu;
+    o1 = 0u;
 #pragma unroll
-    for (int w = 0; w < TK_THREADS / 32; w++) tot += red[slot * 16 + w];
-    return tot;
+    for (int w = 0; w < NW; w++) {
+        a1 &= red[w];
+        o1 |= red[NW + w];
+    }
+    const uint32_t vary = a1 ^ o1;
+    uint32_t prefix = a1 & ~vary, pmask = ~vary, remaining = (uint32_t)k, n_eq = 0;
+    int hi = vary ? 31 - __clz(vary) : -1;
+    if (hi < 0) {
+        // all keys equal: count them
+        uint32_t c = 0;
+#pragma unroll
+        for (int i = 0; i < NK; i++) c += i < nk ? 1u : 0u;
+        c = __reduce_add_sync(0xffffffffu, c);
+        __syncthreads();
+        if (lane == 0) red[wid] = c;
+        __syncthreads();
+        for (int w = 0; w < NW; w++) n_eq += red[w];
+    }
+#pragma unroll 1
+    while (hi >= 0) {
+        const int lo_bit = hi >= 7 ? hi - 7 : 0;
+        const uint32_t dmask = (2u << (hi - lo_bit)) - 1u;
+        if (tid < 256) hist[tid] = 0u;
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < NK; i++) {
+            const bool in = i < nk && (kr[i] & pmask) == prefix;
+            const uint32_t bin = (kr[i] >> lo_bit) & dmask;
+            const unsigned m_in = __ballot_sync(0xffffffffu, in);
+            if (in) {
+                const unsigned peers = __match_any_sync(m_in, bin);
+                if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+            }
+        }
+        __syncthreads();
+        if (wid == 0) {
+            uint32_t h[8], c = 0;
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                h[i] = hist[lane * 8 + i];
+                c += h[i];
+            }
+            uint32_t sfx = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t t = __shfl_down_sync(0xffffffffu, sfx, o);
+                if (lane + o < 32) sfx += t;
+            }
+            uint32_t above = sfx - c;
+#pragma unroll
+            for (int i = 7; i >= 0; i--) {
+                if (above < remaining && above + h[i] >= remaining) {
+                    red[2 * NW] = (uint32_t)(lane * 8 + i);
+                    red[2 * NW + 1] = above;
+                    red[2 * NW + 2] = h[i];
+                }
+                above += h[i];
+            }
+        }
+        __syncthreads();
+        prefix |= red[2 * NW] << lo_bit;
+        remaining -= red[2 * NW + 1];
+        n_eq = red[2 * NW + 2];
+        pmask |= dmask << lo_bit;
+        hi = lo_bit - 1;
+    }
+    __syncthreads();
+    Thr t;
+    t.tau = prefix;
+    t.need_eq = remaining;
+    t.all_eq = remaining == n_eq;
+    return t;
 }
 
 // (1) per chunk of a long row: the row's sampled bound lo (every chunk CTA
@@ -497,7 +579,6 @@ __device__ __forceinline__ uint32_t block_count_ge(const uint32_t (&kr)[NK], uin
 // slice into a shared-memory segment; one scan of the warp counts places the
 // segments.  chunk_cnt gets the chunk's count, or ~0u if a segment overflowed.
 __global__ void __launch_bounds__(TK_THREADS) topk_collect_kernel(TkLong a) {
-    __shared__ uint32_t red[32];
     __shared__ uint32_t wcount[TK_THREADS / 32];
     __shared__ uint32_t skey[TK_THREADS / 32][TK_SEG];
     __shared__ int32_t sidx[TK_THREADS / 32][TK_SEG];
@@ -506,41 +587,47 @@ __global__ void __launch_bounds__(TK_THREADS) topk_collect_kernel(TkLong a) {
     const int64_t nv = visible_count(a.q_pos[row], a.m, a.E);
     if (nv <= a.k) return;
     const float *s = a.scores + row * a.E;
-    // the bound: top 24 bits of the r-th largest of TK_LSAMPLE evenly spaced keys
-    const int S = (int)(nv < TK_LSAMPLE ? nv : TK_LSAMPLE);
-    uint32_t sk[TK_LSAMPLE / TK_THREADS];
+    // the bound: top 24 bits of the r-th largest of TK_LSAMPLE evenly spaced
+    // keys, found by warp 0 alone (32 keys per lane, bit by bit)
+    __shared__ uint32_t lo_s;
+    if (wid == 0) {
+        const int S = (int)(nv < TK_LSAMPLE ? nv : TK_LSAMPLE);
+        uint32_t sk[TK_LSAMPLE / 32];
 #pragma unroll
-    for (int u = 0; u < TK_LSAMPLE / TK_THREADS; u++) {
-        const int i = u * TK_THREADS + tid;
-        const int64_t pos = S == TK_LSAMPLE ? (((int64_t)i * nv) >> 12) : i;   // TK_LSAMPLE = 2^12
-        sk[u] = i < S ? score_key(s[pos]) : 0u;
-    }
-    const int r = S < TK_LSAMPLE ? a.k : sample_rank(nv, a.k, S);
-    uint32_t lo = 0u;
-    if (r < S) {
-        uint32_t t = 0;
-#pragma unroll 1
-        for (int b = 31; b >= 8; b--) {
-            const uint32_t c = t | (1u << b);
-            if (block_count_ge(sk, c, red, b & 1) >= (uint32_t)r) t = c;
+        for (int u = 0; u < TK_LSAMPLE / 32; u++) {
+            const int i = 32 * u + lane;
+            const int64_t pos = S == TK_LSAMPLE ? (((int64_t)i * nv) >> 10) : i;   // TK_LSAMPLE = 2^10
+            sk[u] = i < S ? score_key(s[pos]) : 0u;
         }
-        lo = t;
+        const int r = S < TK_LSAMPLE ? a.k : sample_rank(nv, a.k, S);
+        const uint32_t lo = r < S ? warp_kth(sk, r, 24) : 0u;
+        if (lane == 0) lo_s = lo;
     }
-    // this warp's slice of the chunk
+    // this warp's slice of the chunk; its first keys are loaded before the
+    // bound is known, so the loads overlap warp 0's work
     const int64_t c0 = (int64_t)blockIdx.x * a.CS;
     const int64_t c1 = c0 + a.CS < nv ? c0 + a.CS : nv;
     const int64_t per = (c1 - c0 + TK_THREADS / 32 - 1) / (TK_THREADS / 32);
     const int64_t w0 = c0 + wid * per;
     const int64_t w1 = w0 + per < c1 ? w0 + per : c1;
     const unsigned lt = (1u << lane) - 1u;
-    uint32_t n = 0;
     constexpr int NB = 16;
-    for (int64_t base = w0; base < w1; base += 32 * NB) {
-        uint32_t kv[NB];
+    uint32_t kv[NB];
 #pragma unroll
-        for (int u = 0; u < NB; u++) {
-            const int64_t j = base + 32 * u + lane;
-            kv[u] = j < w1 ? score_key(__ldcs(s + j)) : 0u;
+    for (int u = 0; u < NB; u++) {
+        const int64_t j = w0 + 32 * u + lane;
+        kv[u] = j < w1 ? score_key(__ldcs(s + j)) : 0u;
+    }
+    __syncthreads();
+    const uint32_t lo = lo_s;
+    uint32_t n = 0;
+    for (int64_t base = w0; base < w1; base += 32 * NB) {
+        if (base != w0) {
+#pragma unroll
+            for (int u = 0; u < NB; u++) {
+                const int64_t j = base + 32 * u + lane;
+                kv[u] = j < w1 ? score_key(__ldcs(s + j)) : 0u;
+            }
         }
 #pragma unroll
         for (int u = 0; u < NB; u++) {
@@ -622,40 +709,39 @@ __global__ void __launch_bounds__(TK_THREADS) topk_final_kernel(TkLong a, int ca
             si[j] = gi[src];
         }
         __syncthreads();
-        if (n <= 8 * TK_THREADS) {
-            // exact k-th largest bit by bit over the candidates in registers,
-            // thread t holding candidates 8t .. 8t+7 (index order)
-            uint32_t ck[8];
+        constexpr int PT = 16;                 // candidates per thread in registers
+        if (n <= PT * TK_THREADS) {
+            // exact k-th largest over the candidates in registers, thread t
+            // holding candidates PT t .. PT t + PT-1 (index order)
+            uint32_t ck[PT];
 #pragma unroll
-            for (int u = 0; u < 8; u++) {
-                const int64_t j = (int64_t)tid * 8 + u;
+            for (int u = 0; u < PT; u++) {
+                const int64_t j = (int64_t)tid * PT + u;
                 ck[u] = j < n ? smc[j] : 0u;
             }
-            __shared__ uint32_t red[32];
-            uint32_t t = 0;
-#pragma unroll 1
-            for (int b = 31; b >= 0; b--) {
-                const uint32_t c = t | (1u << b);
-                if (block_count_ge(ck, c, red, b & 1) >= (uint32_t)a.k) t = c;
-            }
-            const uint32_t gt = t == 0xffffffffu ? 0u : block_count_ge(ck, t + 1u, red, 0);
-            const uint32_t need_eq = (uint32_t)a.k - gt;
+            __shared__ uint32_t red[40];
+            __shared__ uint32_t hist[256];
+            const int64_t left = n - (int64_t)tid * PT;
+            const int nk = (int)(left < 0 ? 0 : (left > PT ? PT : left));
+            const Thr th = block_threshold(ck, nk, a.k, hist, red);
+            const uint32_t t = th.tau;
+            const uint32_t need_eq = th.need_eq;
             // ordered emit: one scan of the per-thread counts of kept and of tied keys
             uint32_t n_gt = 0, n_eq = 0;
 #pragma unroll
-            for (int u = 0; u < 8; u++) {
+            for (int u = 0; u < PT; u++) {
                 n_gt += ck[u] > t ? 1u : 0u;
-                n_eq += ck[u] == t && (int64_t)tid * 8 + u < n ? 1u : 0u;
+                n_eq += ck[u] == t && u < nk ? 1u : 0u;
             }
             uint32_t tot2;
             const uint32_t ex2 = block_excl_scan((n_eq << 16) | n_gt, sh.wsum, &tot2);
             uint32_t eq_before = ex2 >> 16, gt_before = ex2 & 0xffffu;
             uint32_t pos = gt_before + (eq_before < need_eq ? eq_before : need_eq);
 #pragma unroll
-            for (int u = 0; u < 8; u++) {
-                const int64_t j = (int64_t)tid * 8 + u;
+            for (int u = 0; u < PT; u++) {
+                const int64_t j = (int64_t)tid * PT + u;
                 bool sel = false;
-                if (j < n) {
+                if (u < nk) {
                     if (ck[u] > t) sel = true;
                     else if (ck[u] == t) sel = eq_before++ < need_eq;
                 }

@@ -11,6 +11,7 @@ Cases:
   compress          csa_compress, n = 65536, c = 512, m = 4 (bf16, with raw rows)
   sparse_attn       sparse_attn, 4096 queries, 64 heads x 512, k = 512 + window
   hca_decode        hca_attn, 8 sequences x 8192 entries, 128 heads x 512
+  hca_prefill       hca_attn, 8192 queries over 64 entries (m' = 128) + window, 64 heads x 512
   csa_prefill       csa_prefill, n = 16384, Flash shapes
 """
 from __future__ import annotations
@@ -88,6 +89,20 @@ def case_hca_decode():
     return lambda: csa.hca_attn(q, pos, kvc, raw, rp0, sink, p, out=out)
 
 
+def case_hca_prefill():
+    T, H, c, m = 8192, 64, 512, 128
+    q = _bf16(1, T, H, c)
+    E = T // m
+    kvc = _bf16(1, E, c)
+    raw = _bf16(1, T, c)
+    pos = torch.arange(T, device="cuda").view(1, T)
+    rp0 = torch.zeros(1, dtype=torch.int64, device="cuda")
+    sink = torch.randn(H, device="cuda")
+    out = torch.empty_like(q)
+    p = csa.params(m=m, n_win=128, rope_dims=64)
+    return lambda: csa.hca_attn(q, pos, kvc, raw, rp0, sink, p, out=out)
+
+
 def case_csa_prefill():
     n, H, c = 16384, 64, 512
     C, Z = _bf16(1, n, c), _bf16(1, n, c)
@@ -110,6 +125,7 @@ CASES = {
     "compress": case_compress,
     "sparse_attn": case_sparse_attn,
     "hca_decode": case_hca_decode,
+    "hca_prefill": case_hca_prefill,
     "csa_prefill": case_csa_prefill,
 }
 
