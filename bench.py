@@ -38,6 +38,18 @@ METRIC = "CSA/HCA query-tokens/s (decode & prefill), % of HBM/tensor roofline, 1
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
+# DRAM bytes (read + write) per unit of the stage's work, from one ncu capture
+# of the same kernel on a smaller case of the same shape (files in profiles/):
+# attention per query token (attn_tc_sparse_attn_4096q.md,
+# attn_tc_hca_prefill_8192q.md), decode indexer per visible entry
+# (indexer_tc_decode_8x262144.md).  Traffic per launch = this x the launch's units.
+TRAFFIC_PER_UNIT = {
+    ("sparse_attn", "prefill"): (302.361856e6 + 234.920960e6) / 4096,
+    ("hca_attn", "prefill"): (546.020096e6 + 492.930816e6) / 8192,
+    ("indexer", "decode"): (537.122048e6 + 9.713664e6) / (8 * 262144),
+}
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -415,8 +427,20 @@ def run_ours(args, rank, world, dist):
         bound, unit = "hbm", "GB/s"
         achieved = w.get(byte_key, 0) / launches_per_step / (per_launch_ms / 1e3) / 1e9
         peak = pk["hbm_gbs"]
+    phase = "decode" if decode else "prefill"
+    # the captures are of the tensor-core kernels (bf16, c = 512)
+    tc_path = wl.s["dtype"] == "bf16" and wl.s["c"] == 512
+    per_unit = TRAFFIC_PER_UNIT.get((dom, phase)) if tc_path else None
+    traffic = None
+    if per_unit is not None:
+        if decode:
+            launch_units = wl.s["B"] * wl.s["E"]                 # visible entries per launch
+        else:
+            launch_units = wl.s["B"] * wl.s["n"] / launches_per_step   # query tokens per launch
+        traffic = per_unit * launch_units
     roof = {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": unit,
-            "frac": achieved / peak, "peak_source": pk_kind, "traffic": None,
+            "frac": achieved / peak, "peak_source": pk_kind, "traffic": traffic,
+            "traffic_unit": "bytes per launch",
             "stage_ms_per_step": {k: round(v, 4) for k, v in stage_ms.items()},
             "stage_launches": launches}
 
