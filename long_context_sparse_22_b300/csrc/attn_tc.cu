@@ -1,6 +1,7 @@
 // Core attention on the 5th-generation tensor cores (bf16 in, fp32 in tensor
 // memory): shared-KV MQA over a per-query list of entries (selected or
 // visible compressed entries, then the window rows) plus a sink logit.
+// Head dims c = 512 and c = 128.
 //
 // [DeepSeek-V4 book ch.6 "Shared key-value MQA"; ch.7 "The sliding window",
 // "Partial rotary position embeddings", "Why the output is de-rotated",
@@ -61,9 +62,9 @@ struct AtCfg {
     static constexpr int OFF_MISC = OFF_P + 2 * P_BYTES;
     static constexpr int MISC_BYTES = 6144;
     static constexpr int SMEM = OFF_MISC + MISC_BYTES + 1024;   // + alignment slack
-    static constexpr int TMEM_COLS = 512;
     static constexpr int S_COL = 0;               // two S buffers: cols 0, 64
     static constexpr int O_COL = 128;             // O^T chunks: 128 + 64 c
+    static constexpr int TMEM_COLS = O_COL + NC * 64 <= 256 ? 256 : 512;   // a power of two
     static constexpr int LOAD_WARPS = 4;          // warps 0-3: loaders
     static constexpr int NLOAD = LOAD_WARPS * 32;
     static constexpr int MMA_WARP = 4;            // warp 4: TMEM allocation, QK issue
@@ -831,7 +832,7 @@ int device_sms() {
     return n;
 }
 
-bool attn_tc_supported(csa_dtype dt, int c) { return dt == CSA_BF16 && c == 512; }
+bool attn_tc_supported(csa_dtype dt, int c) { return dt == CSA_BF16 && (c == 512 || c == 128); }
 
 size_t attn_tc_split_bytes(int64_t rows, int H, int c, int n_chunks) {
     const int64_t items = rows * ((H + 63) / 64) * n_chunks;
@@ -851,9 +852,9 @@ int attn_tc_chunks(int64_t rows, int H, int64_t max_list) {
     return (int)((tiles + per - 1) / per);
 }
 
-cudaError_t launch_attn_tc(int64_t B, const AttnArgs &g, const int32_t *cnt, int n_chunks,
-                           void *split_ws, int max_ctas, cudaStream_t st) {
-    if (B * g.Tq == 0) return cudaSuccess;
+template <int C>
+static cudaError_t launch_attn_tc_c(int64_t B, const AttnArgs &g, const int32_t *cnt, int n_chunks,
+                                    void *split_ws, int max_ctas, cudaStream_t st) {
     AttnTcArgs a;
     a.kvc = (const __nv_bfloat16 *)g.kvc;
     a.zsrc = g.q;
@@ -877,7 +878,7 @@ cudaError_t launch_attn_tc(int64_t B, const AttnArgs &g, const int32_t *cnt, int
         a.n_chunks = n_chunks;
         a.chunk_tiles = (int)((max_tiles + n_chunks - 1) / n_chunks);
         a.part_o = (float *)split_ws;
-        a.part_ml = (float *)((char *)split_ws + (size_t)rows * a.n_hg * n_chunks * 64 * 512 * 4);
+        a.part_ml = (float *)((char *)split_ws + (size_t)rows * a.n_hg * n_chunks * 64 * C * 4);
     } else {
         a.n_chunks = 1;
         a.chunk_tiles = 0;
@@ -885,36 +886,44 @@ cudaError_t launch_attn_tc(int64_t B, const AttnArgs &g, const int32_t *cnt, int
         a.part_ml = nullptr;
     }
     a.n_items = rows * a.n_hg * a.n_chunks;
-    using Cfg = AtCfg<512>;
+    using Cfg = AtCfg<C>;
     // tensor maps: q rows [B*T*H, C]; compressed entries [B*E, C] and raw
     // window rows [B*L, C] as 64-row boxes (a map that is never read points
     // at q); out [B*T*H, C] for the epilogue's 32 x 128 stores.
     CUtensorMap tq, tcmp, tw, to;
     const bool have_c = g.E > 0 && g.kvc != nullptr;
     const bool have_w = g.L > 0 && g.kv_raw != nullptr;
-    if (!make_tmap_bf16_2d(&tq, g.q, (uint64_t)(rows * g.H), 512, 64) ||
+    if (!make_tmap_bf16_2d(&tq, g.q, (uint64_t)(rows * g.H), C, 64) ||
         !make_tmap_bf16_2d(&tcmp, have_c ? g.kvc : g.q, have_c ? (uint64_t)(B * g.E) : (uint64_t)(rows * g.H),
-                           512, 64) ||
+                           C, 64) ||
         !make_tmap_bf16_2d(&tw, have_w ? g.kv_raw : g.q, have_w ? (uint64_t)(B * g.L) : (uint64_t)(rows * g.H),
-                           512, 64) ||
-        !make_tmap_bf16_2d_plain(&to, g.out, (uint64_t)(rows * g.H), 512, 128, 32))
+                           C, 64) ||
+        !make_tmap_bf16_2d_plain(&to, g.out, (uint64_t)(rows * g.H), C, 128, 32))
         return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Cfg::SMEM);
         if (e != cudaSuccess) return e;
         attr = true;
     }
     const int sms = max_ctas > 0 && max_ctas < device_sms() ? max_ctas : device_sms();
     const int grid = (int)(a.n_items < sms ? a.n_items : sms);
-    attn_tc_kernel<512><<<grid, Cfg::THREADS, Cfg::SMEM, st>>>(tq, tcmp, tw, to, a);
+    attn_tc_kernel<C><<<grid, Cfg::THREADS, Cfg::SMEM, st>>>(tq, tcmp, tw, to, a);
     count_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.chunk_tiles == 0) return e;
-    attn_combine_kernel<512><<<dim3((unsigned)rows, (unsigned)g.H), 128, 0, st>>>(a);
+    attn_combine_kernel<C><<<dim3((unsigned)rows, (unsigned)g.H), 128, 0, st>>>(a);
     count_launches(1);
     return cudaGetLastError();
+}
+
+cudaError_t launch_attn_tc(int64_t B, const AttnArgs &g, const int32_t *cnt, int n_chunks,
+                           void *split_ws, int max_ctas, cudaStream_t st) {
+    if (B * g.Tq == 0) return cudaSuccess;
+    if (g.c == 128) return launch_attn_tc_c<128>(B, g, cnt, n_chunks, split_ws, max_ctas, st);
+    if (g.c == 512) return launch_attn_tc_c<512>(B, g, cnt, n_chunks, split_ws, max_ctas, st);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace csa

@@ -103,6 +103,74 @@ compress_kernel(const T *__restrict__ C, const T *__restrict__ Z, const float *_
     Vec<T>::store(out + (b * E + e) * c + ch0, o);
 }
 
+// Long blocks (m >= 16, one branch): one CTA per (sequence, block).  Thread
+// (g, v) owns channel vector v and the slots s = g, g + G, ... of the block;
+// each keeps a partial online softmax, and the G partials of a vector are
+// merged through shared memory (max, rescaled denominators and sums).
+constexpr int CW_THREADS = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(CW_THREADS)
+compress_wide_kernel(const T *__restrict__ C, const T *__restrict__ Z, const float *__restrict__ bias,
+                     T *__restrict__ out, T *__restrict__ raw_out, int64_t n, int c, int m, int64_t E,
+                     int64_t Eg, RopeFreqs rope) {
+    constexpr int N = Vec<T>::N;
+    __shared__ float part[CW_THREADS][3][N];
+    const int V = c / N;                  // vectors per row (<= CW_THREADS)
+    const int G = CW_THREADS / V;         // row groups
+    const int tid = threadIdx.x;
+    const int v = tid % V, grp = tid / V;
+    const int64_t e = blockIdx.x % Eg, b = blockIdx.x / Eg;
+    const int ch0 = v * N;
+    const T *Cs = C + b * n * c;
+    const T *Zs = Z + b * n * c;
+    const int64_t row0 = e * m;
+    const int slots = (int)((n - row0) < m ? (n - row0) : m);
+    float mx[N], den[N], acc[N];
+#pragma unroll
+    for (int i = 0; i < N; i++) { mx[i] = -INFINITY; den[i] = 0.f; acc[i] = 0.f; }
+    if (grp < G) {
+        for (int s = grp; s < slots; s += G) {
+            float z[N], x[N], bs[N];
+            const int64_t row = row0 + s;
+            Vec<T>::load_stream(Zs + row * c + ch0, z);
+            Vec<T>::load_stream(Cs + row * c + ch0, x);
+            Vec<float>::load(bias + (int64_t)s * c + ch0, bs);
+            if constexpr (N == 8) Vec<float>::load(bias + (int64_t)s * c + ch0 + 4, bs + 4);
+#pragma unroll
+            for (int i = 0; i < N; i++) softmax_step<T>(z[i] + bs[i], x[i], mx[i], den[i], acc[i]);
+            if (raw_out != nullptr) {
+                rotate_vec<T>(x, ch0, row, rope);
+                Vec<T>::store(raw_out + (b * n + row) * c + ch0, x);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < N; i++) {
+        part[tid][0][i] = mx[i];
+        part[tid][1][i] = den[i];
+        part[tid][2][i] = acc[i];
+    }
+    __syncthreads();
+    if (grp != 0 || e >= E) return;       // one thread per vector merges; tail block: raw rows only
+#pragma unroll
+    for (int i = 0; i < N; i++) {
+        float M = -INFINITY;
+        for (int q = 0; q < G; q++) M = fmaxf(M, part[q * V + v][0][i]);
+        float d = 0.f, a = 0.f;
+        for (int q = 0; q < G; q++) {
+            const float mq = part[q * V + v][0][i];
+            if (mq == -INFINITY) continue;
+            const float sc = __expf(mq - M);
+            d = fmaf(part[q * V + v][1][i], sc, d);
+            a = fmaf(part[q * V + v][2][i], sc, a);
+        }
+        mx[i] = a / d;
+    }
+    rotate_vec<T>(mx, ch0, (e + 1) * m - 1, rope);
+    Vec<T>::store(out + (b * E + e) * c + ch0, mx);
+}
+
 cudaError_t launch_compress(csa_dtype dt, int64_t B, int64_t n, int c, int m, int overlap,
                             const void *C, const void *Z, const float *bias, const void *Cb,
                             const void *Zb, const float *biasb, void *out, void *raw_out,
@@ -112,6 +180,19 @@ cudaError_t launch_compress(csa_dtype dt, int64_t B, int64_t n, int c, int m, in
     const int N = dt == CSA_BF16 ? 8 : 4;
     const int64_t threads = B * Eg * (c / N);
     if (threads == 0) return cudaSuccess;
+    if (m >= 16 && !overlap && c / N <= CW_THREADS) {
+        const int64_t blocks = B * Eg;
+        if (dt == CSA_BF16) {
+            using T = __nv_bfloat16;
+            compress_wide_kernel<T><<<(unsigned)blocks, CW_THREADS, 0, st>>>(
+                (const T *)C, (const T *)Z, bias, (T *)out, (T *)raw_out, n, c, m, E, Eg, rope);
+        } else {
+            compress_wide_kernel<float><<<(unsigned)blocks, CW_THREADS, 0, st>>>(
+                (const float *)C, (const float *)Z, bias, (float *)out, (float *)raw_out, n, c, m, E, Eg, rope);
+        }
+        count_launches(1);
+        return cudaGetLastError();
+    }
     const int tpb = 256;
     const int64_t blocks = (threads + tpb - 1) / tpb;
     if (dt == CSA_BF16) {

@@ -67,7 +67,7 @@ cudaError_t launch_topk_phase(int phase, int64_t B, int64_t Tq, int64_t E, int k
 
 cudaError_t launch_attn_simt(csa_dtype dt, int64_t B, const AttnArgs &a, cudaStream_t st);
 
-// Tensor-core attention (bf16, c = 512).  n_chunks > 1 splits each query's
+// Tensor-core attention (bf16, c = 128 or 512).  n_chunks > 1 splits each query's
 // entry list over several CTAs (decode) and needs attn_tc_split_bytes of
 // scratch; cnt (nullable) gives the number of valid leading slots of idx.
 bool attn_tc_supported(csa_dtype dt, int c);
