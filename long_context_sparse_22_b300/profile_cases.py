@@ -9,6 +9,8 @@ Cases:
   topk_prefill      topk_select over [16384, 4096] fp32 scores, k = 512
   topk_decode       topk_select over [8, 262144] fp32 scores, k = 1024
   compress          csa_compress, n = 65536, c = 512, m = 4 (bf16, with raw rows)
+  compress_hca      csa_compress, n = 65536, c = 512, m' = 128 (bf16, with raw rows)
+  hca_prefill_c128  hca_attn, 8192 queries, 16 heads x 128, m' = 128 + window
   sparse_attn       sparse_attn, 4096 queries, 64 heads x 512, k = 512 + window
   hca_decode        hca_attn, 8 sequences x 8192 entries, 128 heads x 512
   hca_prefill       hca_attn, 8192 queries over 64 entries (m' = 128) + window, 64 heads x 512
@@ -50,13 +52,13 @@ def case_topk(T, E, B, k, m=4):
     return lambda: csa.topk_select(sc, pos, m, k, idx=idx, cnt=cnt)
 
 
-def case_compress():
+def case_compress(m=4):
     n, c = 65536, 512
     C, Z = _bf16(1, n, c), _bf16(1, n, c)
-    bias = torch.randn(4, c, device="cuda") * 0.1
-    out = torch.empty(1, n // 4, c, device="cuda", dtype=torch.bfloat16)
+    bias = torch.randn(m, c, device="cuda") * 0.1
+    out = torch.empty(1, n // m, c, device="cuda", dtype=torch.bfloat16)
     raw = torch.empty_like(C)
-    return lambda: csa.csa_compress(C, Z, bias, m=4, rope_dims=64, want_raw=True, out=out, raw_out=raw)
+    return lambda: csa.csa_compress(C, Z, bias, m=m, rope_dims=64, want_raw=True, out=out, raw_out=raw)
 
 
 def case_sparse_attn():
@@ -89,8 +91,8 @@ def case_hca_decode():
     return lambda: csa.hca_attn(q, pos, kvc, raw, rp0, sink, p, out=out)
 
 
-def case_hca_prefill():
-    T, H, c, m = 8192, 64, 512, 128
+def case_hca_prefill(H=64, c=512):
+    T, m = 8192, 128
     q = _bf16(1, T, H, c)
     E = T // m
     kvc = _bf16(1, E, c)
@@ -123,6 +125,8 @@ CASES = {
     "topk_prefill": lambda: case_topk(16384, 4096, 1, 512),
     "topk_decode": lambda: case_topk(1, 262144, 8, 1024),
     "compress": case_compress,
+    "compress_hca": lambda: case_compress(128),
+    "hca_prefill_c128": lambda: case_hca_prefill(16, 128),
     "sparse_attn": case_sparse_attn,
     "hca_decode": case_hca_decode,
     "hca_prefill": case_hca_prefill,
