@@ -35,10 +35,10 @@
 //              tiles (two buffers), the presence masks;
 //   warp 4     TMEM allocator and QK issuer (one thread);
 //   warps 5-8  softmax (a head's 64 logits spread over four threads), the
-//              O rescale, and the epilogue: normalise, de-rotate, stage 32
-//              heads x 128 dims at a time in shared memory and write each
-//              block with a TMA store that overlaps the next block's work
-//              (or fp32 partial outputs for a split-KV combine);
+//              O rescale, and the epilogue: normalise, de-rotate and store
+//              straight from registers, a warp writing 64 contiguous bytes
+//              of one head's row per instruction (or fp32 partial outputs
+//              for a split-KV combine);
 //   warp 9     PV issuer (one thread).
 #include "common.cuh"
 #include "kernels.h"
@@ -104,7 +104,22 @@ struct ItemInfo {
     int j0, j1;              // tile range of this item
 };
 
-__device__ __forceinline__ void item_info(const AttnTcArgs &a, int64_t it, ItemInfo &f) {
+// The query row of item `it`, and the two values an item reads from global
+// memory: its position and its kept count of selected indices.
+__device__ __forceinline__ int64_t item_bt(const AttnTcArgs &a, int64_t it) {
+    if (a.chunk_tiles > 0) it /= a.n_chunks;
+    return it / a.n_hg;
+}
+
+__device__ __forceinline__ void item_loads(const AttnTcArgs &a, int64_t it, int64_t *pre) {
+    const int64_t bt = item_bt(a, it);
+    pre[0] = a.q_pos[bt];
+    pre[1] = a.idx ? (a.cnt ? a.cnt[bt] : a.k) : 0;
+}
+
+// pre: the item's item_loads values if already fetched, else nullptr.
+__device__ __forceinline__ void item_info(const AttnTcArgs &a, int64_t it, ItemInfo &f,
+                                          const int64_t *pre = nullptr) {
     int64_t r = it;
     f.chunk = 0;
     if (a.chunk_tiles > 0) {
@@ -114,8 +129,8 @@ __device__ __forceinline__ void item_info(const AttnTcArgs &a, int64_t it, ItemI
     f.hg = (int)(r % a.n_hg);
     f.bt = r / a.n_hg;
     f.b = f.bt / a.T;
-    f.t = a.q_pos[f.bt];
-    if (a.idx) f.ncomp = a.cnt ? a.cnt[f.bt] : a.k;
+    f.t = pre ? pre[0] : a.q_pos[f.bt];
+    if (a.idx) f.ncomp = pre ? pre[1] : (a.cnt ? a.cnt[f.bt] : a.k);
     else f.ncomp = visible_count(f.t, a.m, a.E);
     if (f.ncomp < 0) f.ncomp = 0;
     int64_t p0 = f.t - a.n_win + 1;
@@ -216,7 +231,7 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32
 template <int C>
 __global__ void __launch_bounds__(AtCfg<C>::THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
-               const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_o,
+               const __grid_constant__ CUtensorMap tm_w,
                const __grid_constant__ AttnTcArgs a) {
     using Cfg = AtCfg<C>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -260,7 +275,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tc::prefetch_tmap(&tm_q);
         tc::prefetch_tmap(&tm_c);
         tc::prefetch_tmap(&tm_w);
-        tc::prefetch_tmap(&tm_o);
     }
     if (warp == Cfg::MMA_WARP) tc::tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
     tc::fence_before_sync();
@@ -289,9 +303,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                              "r"(tid * 64), "r"(y)
                              : "memory");
             }
-            // this item's q rows (box TMA) and the cos / sin of its angle.  Waits
-            // are warp-uniform and the four loader warps agree on a failure
-            // through a barrier reduction, so none is left at a named barrier.
+            // the cos / sin of this item's angle and its first selected indices,
+            // worked out while the previous item's last QK still reads q
+            for (int pi = tid; pi < a.rope.pairs; pi += Cfg::NLOAD) {
+                float c_, s_;
+                rope_cos_sin((double)f.t, a.rope.w[pi], c_, s_);
+                cs_s[pi] = c_;
+                cs_s[256 + pi] = s_;
+            }
+            int32_t iv = -1;                     // selected index of this thread's slot, next tile
+            if (a.idx && tid < 64 && f.j0 < f.ntc) {
+                const int64_t pos = (int64_t)f.j0 * 64 + tid;
+                iv = pos < f.ncomp ? a.idx[f.bt * a.k + pos] : -1;
+            }
+            // this item's q rows (box TMA).  Waits are warp-uniform and the four
+            // loader warps agree on a failure through a barrier reduction, so none
+            // is left at a named barrier; the barrier also publishes cs_s.
             if (named_bar_or(2, Cfg::NLOAD, !warp_wait(qempty, (ii & 1) ^ 1, a.status, abort_flag, lane))) {
                 ok = false;
                 break;
@@ -303,19 +330,47 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                     (int)(f.bt * a.H + f.hg * Cfg::HG), qland);
                 q_pending = 1;
             }
-            for (int pi = tid; pi < a.rope.pairs; pi += Cfg::NLOAD) {
-                float c_, s_;
-                rope_cos_sin((double)f.t, a.rope.w[pi], c_, s_);
-                cs_s[pi] = c_;
-                cs_s[256 + pi] = s_;
-            }
-            named_bar(2, Cfg::NLOAD);
-            const int q_after = (f.j1 - f.j0 > 1 ? f.j0 + 1 : f.j0);
-            int32_t iv = -1;                     // selected index of this thread's slot, next tile
-            if (a.idx && tid < 64 && f.j0 < f.ntc) {
-                const int64_t pos = (int64_t)f.j0 * 64 + tid;
-                iv = pos < f.ncomp ? a.idx[f.bt * a.k + pos] : -1;
-            }
+            // q~ = RoPE(q, t): once q has landed, rotate the rotary pairs in place and
+            // hand q to the MMA.  Runs while the item's first tile is in flight.
+            auto rope_q = [&]() -> bool {
+                if (named_bar_or(2, Cfg::NLOAD, !warp_wait(qland, ii & 1, a.status, abort_flag, lane)))
+                    return false;
+                if (tid == 0) q_pending = 0;
+                const int np = a.rope.pairs;
+                if (np == 32) {
+                    // one pair per lane, heads warp, warp + 4, ...: all loads in flight at once
+                    const int d = a.rope.first + 2 * lane;
+                    const float c_ = cs_s[lane], s_ = cs_s[256 + lane];
+                    uint8_t *qa = sQ + (d >> 6) * (Cfg::HG * 128);
+                    __nv_bfloat162 x[Cfg::HG / 4];
+#pragma unroll
+                    for (int k = 0; k < Cfg::HG / 4; k++) {
+                        const int h = warp + 4 * k;
+                        x[k] = *(const __nv_bfloat162 *)(qa + (h >> 3) * 1024 + swz128(h, (d & 63) * 2));
+                    }
+#pragma unroll
+                    for (int k = 0; k < Cfg::HG / 4; k++) {
+                        const int h = warp + 4 * k;
+                        const float2 v = __bfloat1622float2(x[k]);
+                        *(__nv_bfloat162 *)(qa + (h >> 3) * 1024 + swz128(h, (d & 63) * 2)) =
+                            __floats2bfloat162_rn(v.x * c_ - v.y * s_, v.x * s_ + v.y * c_);
+                    }
+                } else {
+                    for (int i = tid; i < Cfg::HG * np; i += Cfg::NLOAD) {
+                        const int h = i / np, pi = i - h * np;
+                        const int d = a.rope.first + 2 * pi;
+                        __nv_bfloat162 *pv = (__nv_bfloat162 *)(sQ + (d >> 6) * (Cfg::HG * 128) +
+                                                                (h >> 3) * 1024 + swz128(h, (d & 63) * 2));
+                        const float2 v = __bfloat1622float2(*pv);
+                        const float c_ = cs_s[pi], s_ = cs_s[256 + pi];
+                        *pv = __floats2bfloat162_rn(v.x * c_ - v.y * s_, v.x * s_ + v.y * c_);
+                    }
+                }
+                fence_proxy_async();
+                named_bar(2, Cfg::NLOAD);
+                if (tid == 0) tc::mbar_arrive(qfull);
+                return true;
+            };
             for (int j = f.j0; j < f.j1; j++, g++) {
                 const int buf = g & 1;
                 if (named_bar_or(2, Cfg::NLOAD,
@@ -351,6 +406,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         cp_async16(dst, src ? (const void *)(src + gr * 8) : a.zsrc, src ? 16u : 0u);
                     }
                     asm volatile("cp.async.commit_group;" ::: "memory");
+                    if (j == f.j0 && !rope_q()) {
+                        ok = false;
+                        break;
+                    }
                     asm volatile("cp.async.wait_group 0;" ::: "memory");
                     fence_proxy_async();
                     tc::mbar_arrive(&kfull[buf]);
@@ -390,27 +449,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     } else {
                         tc::mbar_arrive(&kfull[buf]);
                     }
-                }
-                if (j == q_after) {
-                    // q~ = RoPE(q, t): rotate the rotary pairs in place, then hand q to the MMA
-                    if (named_bar_or(2, Cfg::NLOAD, !warp_wait(qland, ii & 1, a.status, abort_flag, lane))) {
+                    if (j == f.j0 && !rope_q()) {
                         ok = false;
                         break;
                     }
-                    if (tid == 0) q_pending = 0;
-                    const int np = a.rope.pairs;
-                    for (int i = tid; i < Cfg::HG * np; i += Cfg::NLOAD) {
-                        const int h = i / np, pi = i - h * np;
-                        const int d = a.rope.first + 2 * pi;
-                        __nv_bfloat162 *pv = (__nv_bfloat162 *)(sQ + (d >> 6) * (Cfg::HG * 128) +
-                                                                (h >> 3) * 1024 + swz128(h, (d & 63) * 2));
-                        const float2 x = __bfloat1622float2(*pv);
-                        const float c_ = cs_s[pi], s_ = cs_s[256 + pi];
-                        *pv = __floats2bfloat162_rn(x.x * c_ - x.y * s_, x.x * s_ + x.y * c_);
-                    }
-                    fence_proxy_async();
-                    named_bar(2, Cfg::NLOAD);
-                    if (tid == 0) tc::mbar_arrive(qfull);
                 }
             }
             ii++;
@@ -520,11 +562,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int t4 = lane & 3;
         const int hr[2] = {quarter * 16 + (lane >> 2), quarter * 16 + (lane >> 2) + 8};
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        const bool tma_out = a.chunk_tiles == 0 && (a.H % Cfg::HG) == 0;
         uint32_t g = 0, ii = 0;
+        int64_t pre[2] = {0, 0};                 // the next item's item_loads values
+        bool have_pre = false;
         for (int64_t it = blockIdx.x; it < a.n_items; it += G) {
             ItemInfo f;
-            item_info(a, it, f);
+            item_info(a, it, f, have_pre ? pre : nullptr);
+            have_pre = false;
             if (f.j0 >= f.j1) continue;
             const int h0 = f.hg * Cfg::HG;
             bool real[2];
@@ -557,6 +601,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                           "=r"(raw[30]), "=r"(raw[31])
                         : "r"(tmem + lane_base + Cfg::S_COL + buf * 64));
                     tc::tmem_ld_wait();
+                    tc::tmem_regs_ready<32>(raw);
                     tc::fence_before_sync();
                 }
                 __syncwarp();
@@ -629,6 +674,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             uint32_t o[16];
                             tmem_ld16(to, o);
                             tc::tmem_ld_wait();
+                            tc::tmem_regs_ready<16>(o);
                             const float *alc = al + (cb & 63);
 #pragma unroll
                             for (int q = 0; q < 16; q++) o[q] = __float_as_uint(__uint_as_float(o[q]) * alc[q]);
@@ -642,6 +688,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (lane == 0) tc::mbar_arrive(&pfull[buf]);
             }
             if (fail) break;
+            // the next item's position and count on their way, and the cos / sin of
+            // -t for this thread's dim in the last chunk, while the last PV runs
+            if (it + G < a.n_items) {
+                item_loads(a, it + G, pre);
+                have_pre = true;
+            }
+            float dcr = 1.f, dsr = 0.f;
+            {
+                const int dlast = (Cfg::NC - 1) * 128 + quarter * 32 + lane;
+                if (a.chunk_tiles == 0 && a.derotate && dlast >= a.rope.first)
+                    rope_cos_sin(-(double)f.t, a.rope.w[(dlast - a.rope.first) >> 1], dcr, dsr);
+            }
             // item end: the four threads of a head add their partial sums
 #pragma unroll
             for (int u = 0; u < 2; u++) {
@@ -668,23 +726,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (named_bar_or(1, 128, !ok)) break;
             tc::fence_after_sync();
             const int nh = a.H - h0 < 64 ? a.H - h0 : 64;
-            // stage: two [32 heads][128 dims] bf16 halves (P is free now); each half of
-            // a chunk leaves by its own TMA store, which overlaps the next half's work
-            __nv_bfloat16 *stage = (__nv_bfloat16 *)sP;
+            const int dl = quarter * 32 + lane;                 // dim within a chunk
             for (int c = 0; c < Cfg::NC; c++) {
-                const int dl = quarter * 32 + lane;             // dim within the chunk
                 const int d = c * 128 + dl;
                 const uint32_t to = tmem + lane_base + Cfg::O_COL + c * 64;
                 float cr = 1.f, sr = 0.f;
-                const bool rot = a.chunk_tiles == 0 && a.derotate && d >= a.rope.first;
-                if (rot) rope_cos_sin(-(double)f.t, a.rope.w[(d - a.rope.first) >> 1], cr, sr);
-                const bool rot_w = a.chunk_tiles == 0 && a.derotate &&
-                                   c * 128 + quarter * 32 + 31 >= a.rope.first;   // warp-uniform
+                const bool rot_w = a.chunk_tiles == 0 && a.derotate && c * 128 + quarter * 32 + 31 >= a.rope.first;
+                const bool rot = d >= a.rope.first;
+                if (rot_w && rot) {
+                    if (c == Cfg::NC - 1) {
+                        cr = dcr;
+                        sr = dsr;
+                    } else {
+                        rope_cos_sin(-(double)f.t, a.rope.w[(d - a.rope.first) >> 1], cr, sr);
+                    }
+                }
+                const float sgn = (lane & 1) ? sr : -sr;
 #pragma unroll 1
-                for (int hb = 0; hb < 64; hb += 32) {           // 32 heads at a time
+                for (int hb = 0; hb < 64; hb += 32) {
                     float o[32];
                     tc::tmem_ld32(to + hb, o);
                     tc::tmem_ld_wait();
+                    tc::tmem_regs_ready<32>(o);
                     if (a.chunk_tiles > 0) {
                         float *po = a.part_o + (it * 64 + hb) * (int64_t)C + d;
 #pragma unroll
@@ -702,33 +765,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         o[4 * q4 + 3] *= iv4.w;
                     }
                     if (rot_w) {
-                        float op[32];
 #pragma unroll
-                        for (int h = 0; h < 32; h++) op[h] = __shfl_xor_sync(0xffffffffu, o[h], 1);
-                        if (rot) {
-#pragma unroll
-                            for (int h = 0; h < 32; h++)
-                                o[h] = (lane & 1) ? (op[h] * sr + o[h] * cr) : (o[h] * cr - op[h] * sr);
+                        for (int h = 0; h < 32; h++) {
+                            const float op = __shfl_xor_sync(0xffffffffu, o[h], 1);
+                            if (rot) o[h] = o[h] * cr + op * sgn;
                         }
                     }
-                    if (tma_out) {
-                        __nv_bfloat16 *sb = stage + (hb >> 5) * (32 * 128);
+                    __nv_bfloat16 *op = a.out + (f.bt * a.H + h0 + hb) * (int64_t)C + d;
+                    if (nh == 64) {
 #pragma unroll
-                        for (int h = 0; h < 32; h++) sb[h * 128 + dl] = __float2bfloat16_rn(o[h]);
-                        fence_proxy_async();
-                        // the store issued one half earlier has read its buffer (the one
-                        // the next half writes) before anyone passes the barrier
-                        if (st == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                        named_bar(1, 128);
-                        if (st == 0) {
-                            asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
-                                         ::"l"(reinterpret_cast<uint64_t>(&tm_o)), "r"(c * 128),
-                                         "r"((int)(f.bt * a.H + h0 + hb)), "r"(tc::smem_u32(sb))
-                                         : "memory");
-                            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                        for (int h = 0; h < 32; h += 2) {
+                            const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[h], o[h + 1]);
+                            op[(int64_t)h * C] = v2.x;
+                            op[(int64_t)(h + 1) * C] = v2.y;
                         }
                     } else {
-                        __nv_bfloat16 *op = a.out + (f.bt * a.H + h0 + hb) * (int64_t)C + d;
 #pragma unroll
                         for (int h = 0; h < 32; h++)
                             if (hb + h < nh) op[(int64_t)h * C] = __float2bfloat16_rn(o[h]);
@@ -738,12 +789,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(oempty);
-            // the last store has read P's buffers; inv_den_s is rewritten by the next item
-            if (st == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-            named_bar(1, 128);
+            named_bar(1, 128);                   // inv_den_s is rewritten by the next item
             ii++;
         }
-        if (st == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -889,16 +937,15 @@ static cudaError_t launch_attn_tc_c(int64_t B, const AttnArgs &g, const int32_t 
     using Cfg = AtCfg<C>;
     // tensor maps: q rows [B*T*H, C]; compressed entries [B*E, C] and raw
     // window rows [B*L, C] as 64-row boxes (a map that is never read points
-    // at q); out [B*T*H, C] for the epilogue's 32 x 128 stores.
-    CUtensorMap tq, tcmp, tw, to;
+    // at q).
+    CUtensorMap tq, tcmp, tw;
     const bool have_c = g.E > 0 && g.kvc != nullptr;
     const bool have_w = g.L > 0 && g.kv_raw != nullptr;
     if (!make_tmap_bf16_2d(&tq, g.q, (uint64_t)(rows * g.H), C, 64) ||
         !make_tmap_bf16_2d(&tcmp, have_c ? g.kvc : g.q, have_c ? (uint64_t)(B * g.E) : (uint64_t)(rows * g.H),
                            C, 64) ||
         !make_tmap_bf16_2d(&tw, have_w ? g.kv_raw : g.q, have_w ? (uint64_t)(B * g.L) : (uint64_t)(rows * g.H),
-                           C, 64) ||
-        !make_tmap_bf16_2d_plain(&to, g.out, (uint64_t)(rows * g.H), C, 128, 32))
+                           C, 64))
         return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
@@ -909,7 +956,7 @@ static cudaError_t launch_attn_tc_c(int64_t B, const AttnArgs &g, const int32_t 
     }
     const int sms = max_ctas > 0 && max_ctas < device_sms() ? max_ctas : device_sms();
     const int grid = (int)(a.n_items < sms ? a.n_items : sms);
-    attn_tc_kernel<C><<<grid, Cfg::THREADS, Cfg::SMEM, st>>>(tq, tcmp, tw, to, a);
+    attn_tc_kernel<C><<<grid, Cfg::THREADS, Cfg::SMEM, st>>>(tq, tcmp, tw, a);
     count_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.chunk_tiles == 0) return e;

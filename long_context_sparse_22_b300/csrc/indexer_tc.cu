@@ -279,6 +279,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     tc::tmem_ld32(taddr, v0);
                     tc::tmem_ld32(taddr + 32, v1);
                     tc::tmem_ld_wait();
+                    tc::tmem_regs_ready<32>(v0);
+                    tc::tmem_regs_ready<32>(v1);
                     const float *wt = w_s + u * Cfg::HI;
                     float s0 = 0.f, s1 = 0.f;
 #pragma unroll
@@ -347,21 +349,6 @@ bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
-// 2D bf16 tensor map without swizzle, box [box_rows, box_cols] (box_cols <= 256).
-bool make_tmap_bf16_2d_plain(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
-                             uint32_t box_cols, uint32_t box_rows) {
-    auto enc = get_encode();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {box_cols, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 

@@ -160,6 +160,20 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Ties registers written by tcgen05.ld to the tcgen05.wait::ld issued before
+// this call: they are rewritten here as far as the compiler knows, so no use
+// of them can be scheduled ahead of the wait.
+template <int N>
+__device__ __forceinline__ void tmem_regs_ready(float *v) {
+#pragma unroll
+    for (int i = 0; i < N; i++) asm volatile("" : "+f"(v[i]));
+}
+template <int N>
+__device__ __forceinline__ void tmem_regs_ready(uint32_t *v) {
+#pragma unroll
+    for (int i = 0; i < N; i++) asm volatile("" : "+r"(v[i]));
+}
+
 // Shared-memory matrix descriptor for a K-major operand stored with the
 // 128-byte swizzle: rows of 128 bytes (64 bf16), 8-row groups 1024 bytes
 // apart.  `addr` is the shared address of the first element of the K slice.
@@ -189,8 +203,5 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 // 128-byte swizzle (defined with the indexer kernels).
 bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                        uint32_t box_rows);
-// The same without swizzle, box [box_rows, box_cols] (box_cols <= 256).
-bool make_tmap_bf16_2d_plain(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
-                             uint32_t box_cols, uint32_t box_rows);
 
 }  // namespace csa
