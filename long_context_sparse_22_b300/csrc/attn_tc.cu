@@ -104,22 +104,7 @@ struct ItemInfo {
     int j0, j1;              // tile range of this item
 };
 
-// The query row of item `it`, and the two values an item reads from global
-// memory: its position and its kept count of selected indices.
-__device__ __forceinline__ int64_t item_bt(const AttnTcArgs &a, int64_t it) {
-    if (a.chunk_tiles > 0) it /= a.n_chunks;
-    return it / a.n_hg;
-}
-
-__device__ __forceinline__ void item_loads(const AttnTcArgs &a, int64_t it, int64_t *pre) {
-    const int64_t bt = item_bt(a, it);
-    pre[0] = a.q_pos[bt];
-    pre[1] = a.idx ? (a.cnt ? a.cnt[bt] : a.k) : 0;
-}
-
-// pre: the item's item_loads values if already fetched, else nullptr.
-__device__ __forceinline__ void item_info(const AttnTcArgs &a, int64_t it, ItemInfo &f,
-                                          const int64_t *pre = nullptr) {
+__device__ __forceinline__ void item_info(const AttnTcArgs &a, int64_t it, ItemInfo &f) {
     int64_t r = it;
     f.chunk = 0;
     if (a.chunk_tiles > 0) {
@@ -129,8 +114,8 @@ __device__ __forceinline__ void item_info(const AttnTcArgs &a, int64_t it, ItemI
     f.hg = (int)(r % a.n_hg);
     f.bt = r / a.n_hg;
     f.b = f.bt / a.T;
-    f.t = pre ? pre[0] : a.q_pos[f.bt];
-    if (a.idx) f.ncomp = pre ? pre[1] : (a.cnt ? a.cnt[f.bt] : a.k);
+    f.t = a.q_pos[f.bt];
+    if (a.idx) f.ncomp = a.cnt ? a.cnt[f.bt] : a.k;
     else f.ncomp = visible_count(f.t, a.m, a.E);
     if (f.ncomp < 0) f.ncomp = 0;
     int64_t p0 = f.t - a.n_win + 1;
@@ -563,23 +548,27 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int hr[2] = {quarter * 16 + (lane >> 2), quarter * 16 + (lane >> 2) + 8};
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         uint32_t g = 0, ii = 0;
-        int64_t pre[2] = {0, 0};                 // the next item's item_loads values
-        bool have_pre = false;
+        ItemInfo fn;                             // the next item, worked out during the last PV
+        bool have_fn = false;
+        int zl_hg = -1;                          // head group whose sink logits zl2 holds
+        float zl2[2] = {-INFINITY, -INFINITY};
         for (int64_t it = blockIdx.x; it < a.n_items; it += G) {
             ItemInfo f;
-            item_info(a, it, f, have_pre ? pre : nullptr);
-            have_pre = false;
+            if (have_fn) f = fn;
+            else item_info(a, it, f);
+            have_fn = false;
             if (f.j0 >= f.j1) continue;
             const int h0 = f.hg * Cfg::HG;
             bool real[2];
-            float zl2[2], m_run[2], l_run[2];
+            float m_run[2], l_run[2];
 #pragma unroll
             for (int u = 0; u < 2; u++) {
                 real[u] = h0 + hr[u] < a.H;
-                zl2[u] = real[u] ? a.sink[h0 + hr[u]] * 1.4426950408889634f : -INFINITY;
+                if (f.hg != zl_hg) zl2[u] = real[u] ? a.sink[h0 + hr[u]] * 1.4426950408889634f : -INFINITY;
                 m_run[u] = a.chunk_tiles > 0 ? -INFINITY : zl2[u];
                 l_run[u] = 0.f;
             }
+            zl_hg = f.hg;
             const uint32_t gfirst = g;
             bool fail = false;
             for (int j = f.j0; j < f.j1; j++, g++) {
@@ -688,11 +677,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (lane == 0) tc::mbar_arrive(&pfull[buf]);
             }
             if (fail) break;
-            // the next item's position and count on their way, and the cos / sin of
-            // -t for this thread's dim in the last chunk, while the last PV runs
+            // the next item's description, and the cos / sin of -t for this thread's
+            // dim in the last chunk, worked out while the last PV runs
             if (it + G < a.n_items) {
-                item_loads(a, it + G, pre);
-                have_pre = true;
+                item_info(a, it + G, fn);
+                have_fn = true;
             }
             float dcr = 1.f, dsr = 0.f;
             {
