@@ -200,12 +200,14 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr, uint32_t lbo, uint
     return d;
 }
 
-// Wait by lane 0 of a warp, result broadcast to the warp.
+// Wait by the whole warp, failure agreed by the warp.  Every lane polls the
+// barrier: when lane 0 polled alone while the others waited at a shuffle, the
+// warp's next burst of copies issued several times slower after a wait that
+// had blocked.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, unsigned *status,
-                                          volatile int *abort_flag, int lane) {
-    bool ok = true;
-    if (lane == 0) ok = tc::mbar_wait(bar, parity, status, abort_flag);
-    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                                          volatile int *abort_flag) {
+    const bool ok = tc::mbar_wait(bar, parity, status, abort_flag);
+    return __all_sync(0xffffffffu, ok);
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t bytes) {
@@ -304,7 +306,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // this item's q rows (box TMA).  Waits are warp-uniform and the four
             // loader warps agree on a failure through a barrier reduction, so none
             // is left at a named barrier; the barrier also publishes cs_s.
-            if (named_bar_or(2, Cfg::NLOAD, !warp_wait(qempty, (ii & 1) ^ 1, a.status, abort_flag, lane))) {
+            if (named_bar_or(2, Cfg::NLOAD, !warp_wait(qempty, (ii & 1) ^ 1, a.status, abort_flag))) {
                 ok = false;
                 break;
             }
@@ -318,7 +320,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // q~ = RoPE(q, t): once q has landed, rotate the rotary pairs in place and
             // hand q to the MMA.  Runs while the item's first tile is in flight.
             auto rope_q = [&]() -> bool {
-                if (named_bar_or(2, Cfg::NLOAD, !warp_wait(qland, ii & 1, a.status, abort_flag, lane)))
+                if (named_bar_or(2, Cfg::NLOAD, !warp_wait(qland, ii & 1, a.status, abort_flag)))
                     return false;
                 if (tid == 0) q_pending = 0;
                 const int np = a.rope.pairs;
@@ -359,7 +361,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int j = f.j0; j < f.j1; j++, g++) {
                 const int buf = g & 1;
                 if (named_bar_or(2, Cfg::NLOAD,
-                                 !warp_wait(&kempty[buf], ((g >> 1) & 1) ^ 1, a.status, abort_flag, lane))) {
+                                 !warp_wait(&kempty[buf], ((g >> 1) & 1) ^ 1, a.status, abort_flag))) {
                     ok = false;
                     break;
                 }
@@ -574,7 +576,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int j = f.j0; j < f.j1; j++, g++) {
                 const int buf = g & 1;
                 const uint32_t par = (g >> 1) & 1;
-                bool ok = warp_wait(&sfull[buf], par, a.status, abort_flag, lane);
+                bool ok = warp_wait(&sfull[buf], par, a.status, abort_flag);
                 uint32_t raw[32];
                 if (ok) {
                     tc::fence_after_sync();
@@ -597,7 +599,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (lane == 0) tc::mbar_arrive(&sempty[buf]);
                 // the loaders' presence mask for this tile (its kfull phase has
                 // completed and cannot advance again before this tile's PV)
-                ok = ok && warp_wait(&kfull[buf], par, a.status, abort_flag, lane);
+                ok = ok && warp_wait(&kfull[buf], par, a.status, abort_flag);
                 const uint32_t mlo = ok ? vmask32[buf * 2] : 0u, mhi = ok ? vmask32[buf * 2 + 1] : 0u;
                 // v[u][2i + e]: head hr[u], entry 8i + 2 t4 + e  (raw[4i + 2u + e])
                 float v[2][16];
@@ -626,7 +628,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     alpha[u] = need[u] ? ex2(m_run[u] - m_new) : 1.0f;
                     if (need[u]) m_run[u] = m_new;
                 }
-                ok = ok && warp_wait(&pempty[buf], par ^ 1, a.status, abort_flag, lane);
+                ok = ok && warp_wait(&pempty[buf], par ^ 1, a.status, abort_flag);
                 // P rows (bf16): this thread's two entries of chunk i are 4 bytes
                 // at byte 4 t4 of the row's (swizzled) 16-byte chunk i
 #pragma unroll
@@ -654,7 +656,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     // some head's max grew: O^T was accumulated with older maxima,
                     // scale column h by alpha[h]
                     const uint32_t gp = g - 1;
-                    if (warp_wait(&pempty[gp & 1], (gp >> 1) & 1, a.status, abort_flag, lane)) {
+                    if (warp_wait(&pempty[gp & 1], (gp >> 1) & 1, a.status, abort_flag)) {
                         tc::fence_after_sync();
                         const float *al = alpha_s + buf * 64;
 #pragma unroll 1
@@ -711,7 +713,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     }
                 }
             }
-            const bool ok = warp_wait(ofull, ii & 1, a.status, abort_flag, lane);
+            const bool ok = warp_wait(ofull, ii & 1, a.status, abort_flag);
             if (named_bar_or(1, 128, !ok)) break;
             tc::fence_after_sync();
             const int nh = a.H - h0 < 64 ? a.H - h0 : 64;
