@@ -457,11 +457,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
     } else if (warp == Cfg::MMA_WARP || warp == Cfg::PV_WARP) {
         // --------------------------------------------------------------- MMA
-        // Two issuing threads: QK on warp 4, PV on warp 9.  A tcgen05.mma of
-        // these small shapes costs more to issue than to execute, so the two
-        // streams are issued side by side; the barriers order them.
-        if (lane == 0) {
+        // Two issuing warps: QK on warp 4, PV on warp 9.  The whole warp runs
+        // the loop and waits on the barriers; one lane issues the MMAs and
+        // commits.  A tcgen05.mma of these small shapes costs more to issue
+        // than to execute, so the two streams are issued side by side; the
+        // barriers order them.
+        {
             const bool is_qk = warp == Cfg::MMA_WARP;
+            const bool leader = lane == 0;
             constexpr uint32_t idQK = tc::idesc_bf16_f32(64, 64);
             constexpr uint32_t idPV = tc::idesc_bf16_f32(128, 64) | (1u << 15);   // A MN-major
             // descriptors at the buffer bases; a byte offset o adds o >> 4
@@ -480,55 +483,62 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (f.j0 >= f.j1) continue;
                 const int nt = f.j1 - f.j0;
                 if (is_qk) {
-                    if (!tc::mbar_wait(qfull, ii & 1, a.status, abort_flag)) break;
+                    if (!warp_wait(qfull, ii & 1, a.status, abort_flag)) break;
                     for (int n = 0; n < nt; n++) {
                         const uint32_t gq = g + n;
                         const int buf = gq & 1;
-                        if (!tc::mbar_wait(&kfull[buf], (gq >> 1) & 1, a.status, abort_flag) ||
-                            !tc::mbar_wait(&sempty[buf], ((gq >> 1) & 1) ^ 1, a.status, abort_flag)) {
+                        if (!warp_wait(&kfull[buf], (gq >> 1) & 1, a.status, abort_flag) ||
+                            !warp_wait(&sempty[buf], ((gq >> 1) & 1) ^ 1, a.status, abort_flag)) {
                             ok = false;
                             break;
                         }
                         tc::fence_after_sync();
+                        if (leader) {
 #pragma unroll
-                        for (int at = 0; at < Cfg::NA; at++)
+                            for (int at = 0; at < Cfg::NA; at++)
 #pragma unroll
-                            for (int kk = 0; kk < 4; kk++)
-                                tc::mma_bf16(tmem + Cfg::S_COL + buf * 64,
-                                             dq + (uint64_t)((at * (Cfg::HG * 128) + kk * 32) >> 4),
-                                             dk[buf] + (uint64_t)((at * Cfg::ATOM + kk * 32) >> 4), idQK,
-                                             (at | kk) != 0);
-                        tc::mma_commit(&sfull[buf]);
-                        if (n == nt - 1) tc::mma_commit(qempty);
+                                for (int kk = 0; kk < 4; kk++)
+                                    tc::mma_bf16(tmem + Cfg::S_COL + buf * 64,
+                                                 dq + (uint64_t)((at * (Cfg::HG * 128) + kk * 32) >> 4),
+                                                 dk[buf] + (uint64_t)((at * Cfg::ATOM + kk * 32) >> 4), idQK,
+                                                 (at | kk) != 0);
+                            tc::mma_commit(&sfull[buf]);
+                            if (n == nt - 1) tc::mma_commit(qempty);
+                        }
+                        __syncwarp();
                     }
                 } else {
                     for (int n = 0; n < nt; n++) {
                         const uint32_t gp = g + n;
                         const int bp = gp & 1;
-                        if (!tc::mbar_wait(&pfull[bp], (gp >> 1) & 1, a.status, abort_flag) ||
-                            (n == 0 && !tc::mbar_wait(oempty, (ii & 1) ^ 1, a.status, abort_flag))) {
+                        if (!warp_wait(&pfull[bp], (gp >> 1) & 1, a.status, abort_flag) ||
+                            (n == 0 && !warp_wait(oempty, (ii & 1) ^ 1, a.status, abort_flag))) {
                             ok = false;
                             break;
                         }
                         tc::fence_after_sync();
+                        if (leader) {
 #pragma unroll
-                        for (int c = 0; c < Cfg::NC; c++)
+                            for (int c = 0; c < Cfg::NC; c++)
 #pragma unroll
-                            for (int ks = 0; ks < 4; ks++)
-                                tc::mma_bf16(tmem + Cfg::O_COL + c * 64,
-                                             dv[bp] + (uint64_t)(((2 * c) * Cfg::ATOM + ks * 2048) >> 4),
-                                             dp[bp] + (uint64_t)((ks * 32) >> 4), idPV,
-                                             (n == 0 && ks == 0) ? 0u : 1u);
-                        tc::mma_commit(&pempty[bp]);
-                        tc::mma_commit(&kempty[bp]);
+                                for (int ks = 0; ks < 4; ks++)
+                                    tc::mma_bf16(tmem + Cfg::O_COL + c * 64,
+                                                 dv[bp] + (uint64_t)(((2 * c) * Cfg::ATOM + ks * 2048) >> 4),
+                                                 dp[bp] + (uint64_t)((ks * 32) >> 4), idPV,
+                                                 (n == 0 && ks == 0) ? 0u : 1u);
+                            tc::mma_commit(&pempty[bp]);
+                            tc::mma_commit(&kempty[bp]);
+                        }
+                        __syncwarp();
                     }
-                    if (ok) tc::mma_commit(ofull);
+                    if (ok && leader) tc::mma_commit(ofull);
                 }
                 g += nt;
                 ii++;
             }
             // every MMA issued above has completed before TMEM is released
-            tc::mma_commit(mdone);
+            if (leader) tc::mma_commit(mdone);
+            __syncwarp();
             if (is_qk)
                 for (long long i = 0; i < tc::SPIN_LIMIT; i++)
                     if (tc::mbar_test(mdone, 0)) break;

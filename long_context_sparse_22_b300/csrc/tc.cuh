@@ -48,10 +48,26 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
                  : "memory");
 }
 
+// Non-blocking probe: has the phase of the given parity completed?
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // Wait for the phase of the given parity to complete.  Returns false (and
 // sets the timeout bit) if the cap runs out, or if *abort is already set.
+// A phase that has already completed is seen by the non-blocking probe,
+// which answers faster than a potentially blocking try_wait.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *status,
                                           volatile int *abort) {
+    if (mbar_test(bar, parity)) return true;
     const uint32_t a = smem_u32(bar);
     for (long long i = 0; i < SPIN_LIMIT; i++) {
         uint32_t done;
@@ -68,19 +84,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
     atomicOr(status, ST_TIMEOUT);
     *abort = 1;
     return false;
-}
-
-// Non-blocking probe: has the phase of the given parity completed?
-__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return done != 0;
 }
 
 // ----------------------------------------------------------------------- TMA
