@@ -360,24 +360,29 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             };
             for (int j = f.j0; j < f.j1; j++, g++) {
                 const int buf = g & 1;
+                const bool gather = j < f.ntc && a.idx;
+                // a gathered tile's row addresses go to shared memory before the wait
+                // for its buffer (the barrier that ends the wait publishes them; the
+                // gather two tiles back, the last reader of this slot, has been issued)
+                uint32_t bal = 0;
+                if (gather && tid < 64) {
+                    const int64_t pos = (int64_t)j * 64 + tid;
+                    const bool in = pos < f.ncomp;
+                    const bool v = in && iv >= 0 && iv < a.E;
+                    if (in && !v && iv != -1) atomicOr(a.status, ST_BAD_INDEX);
+                    rowp[buf * 64 + tid] = v ? a.kvc + (f.b * a.E + iv) * (int64_t)C : nullptr;
+                    bal = __ballot_sync(0xffffffffu, v);
+                }
                 if (named_bar_or(2, Cfg::NLOAD,
                                  !warp_wait(&kempty[buf], ((g >> 1) & 1) ^ 1, a.status, abort_flag))) {
                     ok = false;
                     break;
                 }
                 const uint32_t kb = kb0 + buf * Cfg::K_BYTES;
-                if (j < f.ntc && a.idx) {
-                    // gather of selected entries: cp.async, 16 bytes per thread and instruction
-                    if (tid < 64) {
-                        const int64_t pos = (int64_t)j * 64 + tid;
-                        const bool in = pos < f.ncomp;
-                        const bool v = in && iv >= 0 && iv < a.E;
-                        if (in && !v && iv != -1) atomicOr(a.status, ST_BAD_INDEX);
-                        rowp[buf * 64 + tid] = v ? a.kvc + (f.b * a.E + iv) * (int64_t)C : nullptr;
-                        const uint32_t bal = __ballot_sync(0xffffffffu, v);
-                        if (lane == 0) vmask32[buf * 2 + warp] = bal;
-                    }
-                    named_bar(2, Cfg::NLOAD);
+                if (gather) {
+                    // gather of selected entries: cp.async, 16 bytes per thread and instruction;
+                    // the presence mask is written once the softmax two tiles back is done with it
+                    if (tid < 64 && lane == 0) vmask32[buf * 2 + warp] = bal;
                     // the next tile's selected indices, fetched while this one loads
                     if (tid < 64 && j + 1 < f.j1 && j + 1 < f.ntc) {
                         const int64_t pos = (int64_t)(j + 1) * 64 + tid;
@@ -586,7 +591,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int j = f.j0; j < f.j1; j++, g++) {
                 const int buf = g & 1;
                 const uint32_t par = (g >> 1) & 1;
-                bool ok = warp_wait(&sfull[buf], par, a.status, abort_flag);
+                // the loaders' presence mask for this tile (its kfull phase has
+                // completed and cannot advance again before this tile's PV) and the
+                // P buffer (the PV of two tiles back has read it): both are ready
+                // before this tile's logits, so they are checked first
+                bool ok = warp_wait(&kfull[buf], par, a.status, abort_flag) &&
+                          warp_wait(&pempty[buf], par ^ 1, a.status, abort_flag);
+                const uint32_t mlo = ok ? vmask32[buf * 2] : 0u, mhi = ok ? vmask32[buf * 2 + 1] : 0u;
+                ok = ok && warp_wait(&sfull[buf], par, a.status, abort_flag);
                 uint32_t raw[32];
                 if (ok) {
                     tc::fence_after_sync();
@@ -603,14 +615,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         : "r"(tmem + lane_base + Cfg::S_COL + buf * 64));
                     tc::tmem_ld_wait();
                     tc::tmem_regs_ready<32>(raw);
-                    tc::fence_before_sync();
                 }
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&sempty[buf]);
-                // the loaders' presence mask for this tile (its kfull phase has
-                // completed and cannot advance again before this tile's PV)
-                ok = ok && warp_wait(&kfull[buf], par, a.status, abort_flag);
-                const uint32_t mlo = ok ? vmask32[buf * 2] : 0u, mhi = ok ? vmask32[buf * 2 + 1] : 0u;
                 // v[u][2i + e]: head hr[u], entry 8i + 2 t4 + e  (raw[4i + 2u + e])
                 float v[2][16];
 #pragma unroll
@@ -638,7 +643,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     alpha[u] = need[u] ? ex2(m_run[u] - m_new) : 1.0f;
                     if (need[u]) m_run[u] = m_new;
                 }
-                ok = ok && warp_wait(&pempty[buf], par ^ 1, a.status, abort_flag);
                 // P rows (bf16): this thread's two entries of chunk i are 4 bytes
                 // at byte 4 t4 of the row's (swizzled) 16-byte chunk i
 #pragma unroll
@@ -684,9 +688,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         tmem_st_wait();
                     }
                 }
+                // S buffer free for the QK two tiles on, P ready for this tile's PV
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&pfull[buf]);
+                if (lane == 0) {
+                    tc::mbar_arrive(&sempty[buf]);
+                    tc::mbar_arrive(&pfull[buf]);
+                }
             }
             if (fail) break;
             // the next item's description, and the cos / sin of -t for this thread's
