@@ -44,8 +44,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # attn_tc_hca_prefill_8192q.md), decode indexer per visible entry
 # (indexer_tc_decode_8x262144.md).  Traffic per launch = this x the launch's units.
 TRAFFIC_PER_UNIT = {
-    ("sparse_attn", "prefill"): (301.558528e6 + 236.067584e6) / 4096,
-    ("hca_attn", "prefill"): (545.907456e6 + 491.415808e6) / 8192,
+    ("sparse_attn", "prefill"): (301.359616e6 + 236.104192e6) / 4096,
+    ("hca_attn", "prefill"): (545.660928e6 + 491.687424e6) / 8192,
     ("indexer", "decode"): (537.122048e6 + 9.713664e6) / (8 * 262144),
 }
 
