@@ -46,7 +46,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 TRAFFIC_PER_UNIT = {
     ("sparse_attn", "prefill"): (301.359616e6 + 236.104192e6) / 4096,
     ("hca_attn", "prefill"): (545.660928e6 + 491.687424e6) / 8192,
-    ("indexer", "decode"): (537.122048e6 + 9.713664e6) / (8 * 262144),
+    ("indexer", "decode"): (537.125120e6 + 9.781760e6) / (8 * 262144),
 }
 
 
