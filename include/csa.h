@@ -86,7 +86,11 @@ typedef struct csa_params {
     int32_t derotate;   /* 1: rotate the output's rotary dims by -t         */
     double rope_theta;  /* RoPE base (> 1)                                  */
     float scale;        /* attention logit scale; 0 means 1/sqrt(c)         */
-    int32_t reserved;   /* set to 0                                         */
+    int32_t batch_invariant; /* 1: a query's output and selection do not   *
+                         * depend on the batch around it at any batch size  *
+                         * (long lists are always split the same way); 0:   *
+                         * large batches may skip the split, which changes  *
+                         * the fp32 summation order                         */
 } csa_params;
 
 /* Supported sizes: c (main head dim) in {64, 128, 256, 512}; dI (indexer

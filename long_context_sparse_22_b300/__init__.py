@@ -32,13 +32,13 @@ class CsaError(RuntimeError):
 class CsaParams(C.Structure):
     _fields_ = [("m", C.c_int32), ("overlap", C.c_int32), ("top_k", C.c_int32),
                 ("n_win", C.c_int32), ("rope_dims", C.c_int32), ("derotate", C.c_int32),
-                ("rope_theta", C.c_double), ("scale", C.c_float), ("reserved", C.c_int32)]
+                ("rope_theta", C.c_double), ("scale", C.c_float), ("batch_invariant", C.c_int32)]
 
 
 def params(m=4, overlap=0, top_k=512, n_win=128, rope_dims=64, derotate=1, rope_theta=10000.0,
-           scale=0.0) -> CsaParams:
+           scale=0.0, batch_invariant=0) -> CsaParams:
     return CsaParams(int(m), int(overlap), int(top_k), int(n_win), int(rope_dims), int(derotate),
-                     float(rope_theta), float(scale), 0)
+                     float(rope_theta), float(scale), int(batch_invariant))
 
 
 _SIGS = {

@@ -78,6 +78,8 @@ csa_status check_params(const csa_params *p, int c, bool attn) {
     if (p->rope_dims < 0 || (p->rope_dims & 1) || p->rope_dims > c || p->rope_dims / 2 > MAX_ROPE_PAIRS)
         return fail(CSA_ERR_UNSUPPORTED, "rope_dims=%d must be even and <= c", p->rope_dims);
     if (p->rope_dims > 0 && !(p->rope_theta > 1.0)) return fail(CSA_ERR_INVALID_ARG, "rope_theta must be > 1");
+    if (p->batch_invariant != 0 && p->batch_invariant != 1)
+        return fail(CSA_ERR_INVALID_ARG, "batch_invariant must be 0 or 1");
     if (attn) {
         if (p->n_win < 0 || p->n_win > 1024) return fail(CSA_ERR_UNSUPPORTED, "n_win=%d not in 0..1024", p->n_win);
         if (p->derotate != 0 && p->derotate != 1) return fail(CSA_ERR_INVALID_ARG, "derotate must be 0 or 1");
@@ -210,10 +212,11 @@ csa_status do_topk(int64_t B, int64_t T, int64_t E, int k, int m, const float *s
 }
 
 // scratch bytes an attention call needs beyond the status word
-size_t attn_scratch_bytes(csa_dtype dt, int64_t rows, int H, int c, int64_t E, int k, int n_win) {
+size_t attn_scratch_bytes(csa_dtype dt, int64_t rows, int H, int c, int64_t E, int k, int n_win,
+                          bool invariant) {
     if (!attn_tc_supported(dt, c)) return 0;
     const int64_t max_list = (k > 0 ? (int64_t)k : E) + n_win;
-    const int ch = attn_tc_chunks(rows, H, max_list);
+    const int ch = attn_tc_chunks(rows, H, max_list, invariant);
     return ch > 1 ? attn_tc_split_bytes(rows, H, c, ch) : 0;
 }
 
@@ -235,7 +238,7 @@ csa_status do_attn(csa_dtype dt, int64_t B, int64_t T, int H, int c, int64_t E, 
     const bool fits = B * T * H < lim && B * E < lim && B * L < lim;
     if (attn_tc_supported(dt, c) && fits) {
         const int64_t max_list = (idx ? (int64_t)k : E) + p->n_win;
-        int ch = attn_tc_chunks(B * T, H, max_list);
+        int ch = attn_tc_chunks(B * T, H, max_list, p->batch_invariant != 0);
         if (ch > 1 && scratch == nullptr) ch = 1;
         CSA_TRY_CUDA(launch_attn_tc(B, a, cnt, ch, scratch, max_ctas, st),
                      "attention launch (tensor cores)");
@@ -409,7 +412,7 @@ csa_status topk_select(int64_t B, int64_t T, int64_t E, int32_t k, int32_t m, co
 size_t attn_ws_size(csa_dtype dtype, int64_t B, int64_t T, int32_t H, int32_t c, int64_t E,
                     int32_t k, const csa_params *params) {
     if (params == nullptr || B < 0 || T < 0 || E < 0) return CSA_STATUS_BYTES;
-    return CSA_STATUS_BYTES + attn_scratch_bytes(dtype, B * T, H, c, E, k, params->n_win);
+    return CSA_STATUS_BYTES + attn_scratch_bytes(dtype, B * T, H, c, E, k, params->n_win, params->batch_invariant != 0);
 }
 
 csa_status sparse_attn(csa_dtype dtype, int64_t B, int64_t T, int32_t H, int32_t c, int64_t E,
@@ -460,7 +463,7 @@ static size_t csa_prefill_layout(Carve &cv, csa_dtype dt, int64_t B, int64_t n, 
     *idx = cv.take((size_t)B * n * p->top_k * 4);
     *cnt = cv.take((size_t)B * n * 4);
     *tks = cv.take(topk_scratch_bytes(B * n, E));
-    *asc = cv.take(attn_scratch_bytes(dt, B * n, H, c, E, p->top_k, p->n_win));
+    *asc = cv.take(attn_scratch_bytes(dt, B * n, H, c, E, p->top_k, p->n_win, p->batch_invariant != 0));
     return cv.off;
 }
 
@@ -533,7 +536,7 @@ static size_t hca_prefill_layout(Carve &cv, csa_dtype dt, int64_t B, int64_t n, 
     *rp0 = cv.take((size_t)B * 8);
     *kvc = cv.take((size_t)B * E * c * esize(dt));
     *raw = cv.take((size_t)B * n * c * esize(dt));
-    *asc = cv.take(attn_scratch_bytes(dt, B * n, H, c, E, 0, p->n_win));
+    *asc = cv.take(attn_scratch_bytes(dt, B * n, H, c, E, 0, p->n_win, p->batch_invariant != 0));
     return cv.off;
 }
 
@@ -583,8 +586,8 @@ static size_t decode_layout(Carve &cv, csa_dtype dt, int64_t B, int H, int c, in
     *idx = cv.take((size_t)B * p->top_k * 4);
     *cnt = cv.take((size_t)B * 4);
     *tks = cv.take(topk_scratch_bytes(B, E));
-    *asc = cv.take(attn_scratch_bytes(dt, B, H, c, E, p->top_k, p->n_win));
-    *asc2 = cv.take(p2 ? attn_scratch_bytes(dt, B, H, c, E2, 0, p2->n_win) : 0);
+    *asc = cv.take(attn_scratch_bytes(dt, B, H, c, E, p->top_k, p->n_win, p->batch_invariant != 0));
+    *asc2 = cv.take(p2 ? attn_scratch_bytes(dt, B, H, c, E2, 0, p2->n_win, p2->batch_invariant != 0) : 0);
     return cv.off;
 }
 

@@ -897,11 +897,13 @@ size_t attn_tc_split_bytes(int64_t rows, int H, int c, int n_chunks) {
 }
 
 // Number of split-KV chunks for rows of at most max_list entries: enough items
-// to cover the GPU, each at least 4 tiles; independent of the batch size when
-// rows are few, so a sequence's result does not depend on the batch around it.
-int attn_tc_chunks(int64_t rows, int H, int64_t max_list) {
+// to cover the GPU, each at least 4 tiles, as a function of the list length
+// alone, so a sequence's result does not depend on the batch around it.  When
+// the batch alone fills the GPU the split is skipped, unless `invariant` asks
+// for the same split (and so the same summation order) at every batch size.
+int attn_tc_chunks(int64_t rows, int H, int64_t max_list, bool invariant) {
     const int64_t tiles = (max_list + 63) / 64 + 1;       // + 1: padding of the compressed part
-    if (rows * ((H + 63) / 64) >= 2 * 148 || tiles <= 4) return 1;
+    if (tiles <= 4 || (!invariant && rows * ((H + 63) / 64) >= 2 * 148)) return 1;
     // at least 4 tiles per chunk and at most 16 chunks: a function of the list
     // length alone
     int64_t per = (tiles + 15) / 16;

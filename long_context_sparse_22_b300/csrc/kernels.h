@@ -71,7 +71,7 @@ cudaError_t launch_attn_simt(csa_dtype dt, int64_t B, const AttnArgs &a, cudaStr
 // entry list over several CTAs (decode) and needs attn_tc_split_bytes of
 // scratch; cnt (nullable) gives the number of valid leading slots of idx.
 bool attn_tc_supported(csa_dtype dt, int c);
-int attn_tc_chunks(int64_t rows, int H, int64_t max_list);
+int attn_tc_chunks(int64_t rows, int H, int64_t max_list, bool invariant);
 size_t attn_tc_split_bytes(int64_t rows, int H, int c, int n_chunks);
 cudaError_t launch_attn_tc(int64_t B, const AttnArgs &a, const int32_t *cnt, int n_chunks,
                            void *split_ws, int max_ctas, cudaStream_t st);

@@ -59,6 +59,11 @@ def test_validation_rejects_before_launch(csa):
     s = L.csa_compress(1, 1, 8, 64, C.c_void_p((1 << 20) + 2), fake, fake, None, None, None, fake,
                        None, C.byref(p), None)
     assert s == 1 and "aligned" in _err(csa, s)
+    # batch_invariant must be 0 or 1
+    p_bi = csa.params(m=4, rope_dims=64, batch_invariant=2)
+    s = L.hca_attn(1, 1, 1, 16, 128, 4, 4, fake, fake, fake, fake, fake, fake, fake, None,
+                   C.byref(p_bi), fake, 256, None)
+    assert s == 1 and "batch_invariant" in _err(csa, s)
     # odd rope dims
     p_bad = csa.params(m=4, rope_dims=3)
     s = L.csa_compress(1, 1, 8, 64, fake, fake, fake, None, None, None, fake, None, C.byref(p_bad), None)

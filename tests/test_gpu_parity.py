@@ -301,12 +301,12 @@ def test_hca_prefill_cfg2_full(csa, orc):
     check_close(host(out[0]), ref, "bf16", "hca_prefill out")
 
 
-def _decode_gpu(csa, s, x, hca):
+def _decode_gpu(csa, s, x, hca, batch_invariant=0):
     d = {k: dev(v) for k, v in x.items()}
     p = csa.params(m=s["m"], top_k=s["top_k"], n_win=s["n_win"], rope_dims=s["rope_dims"],
-                   rope_theta=s["theta"])
+                   rope_theta=s["theta"], batch_invariant=batch_invariant)
     p2 = csa.params(m=s.get("m2", 128), n_win=s["n_win"], rope_dims=s["rope_dims"],
-                    rope_theta=s["theta"])
+                    rope_theta=s["theta"], batch_invariant=batch_invariant)
     io = torch.empty((s["B"], 1, s["top_k"]), dtype=torch.int32, device="cuda")
     kw = dict(q2=d["q2"], kvc2=d["kvc2"], kv_raw2=d["kv_raw2"], sink2=d["sink2"], p2=p2) if hca else {}
     res = csa.hybrid_decode(d["q"], d["qI"], d["w"], d["kvc"], d["kIc"], d["kv_raw"], d["sink"],
@@ -387,6 +387,18 @@ def test_prefill_deterministic(csa):
     a, ia = _prefill_csa_gpu(csa, s, x)
     b, ib = _prefill_csa_gpu(csa, s, x)
     assert torch.equal(a, b) and torch.equal(ia, ib)
+
+
+def test_decode_batch_invariant_full_batch(csa):
+    """With batch_invariant set, a sequence decoded alone gives bitwise the same output as
+    inside a batch that fills the GPU by itself (300 sequences of 640 entries, where the
+    default would skip the split of each list into chunks)."""
+    s, x = synth.make_inputs("csa_decode_flash", B=300, t=2047)
+    res, io = _decode_gpu(csa, s, x, False, batch_invariant=1)
+    for b in (0, 299):
+        xb = {k: (v[b:b + 1] if k not in ("sink",) else v) for k, v in x.items()}
+        rb, ib = _decode_gpu(csa, dict(s, B=1), xb, False, batch_invariant=1)
+        assert torch.equal(rb[0], res[b]) and torch.equal(ib[0], io[b])
 
 
 def test_decode_batch_invariant(csa):
