@@ -31,15 +31,19 @@
 // out of the softmax by a per-tile presence mask.
 //
 // Warp roles (persistent CTAs, items dealt round-robin):
-//   warps 0-3  loaders: q tile (box TMA, then RoPE at t in place), the entry
-//              tiles (two buffers), the presence masks;
-//   warp 4     TMEM allocator and QK issuer (one thread);
+//   warps 0-3  loaders: q tile (box TMA, then RoPE at t in place while the
+//              item's first tile loads), the entry tiles (two buffers), the
+//              presence masks;
+//   warp 4     TMEM allocator and QK issuer (one lane issues);
 //   warps 5-8  softmax (a head's 64 logits spread over four threads), the
 //              O rescale, and the epilogue: normalise, de-rotate and store
 //              straight from registers, a warp writing 64 contiguous bytes
 //              of one head's row per instruction (or fp32 partial outputs
 //              for a split-KV combine);
-//   warp 9     PV issuer (one thread).
+//   warp 9     PV issuer (one lane issues).
+// Every wait is taken by a whole warp on an mbarrier (with an iteration cap
+// after which the kernel records a timeout and unwinds), and waits whose
+// phase must already have completed come before the one that can block.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
