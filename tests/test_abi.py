@@ -109,3 +109,34 @@ def test_no_cpu_fallback(csa):
         pytest.skip("a GPU is present")
     with pytest.raises(RuntimeError):
         csa._stream()
+
+
+def test_attention_split_rule(csa):
+    """Long lists are split into chunks of at least four 64-entry tiles (at most 16
+    chunks), as a function of the list length alone; a batch that fills the GPU by
+    itself skips the split unless batch_invariant is set.  Checked through the
+    workspace each call asks for (host arithmetic, no device)."""
+    L = csa.lib()
+    H, c, E = 64, 512, 4096
+
+    def ws(B, k, n_win, inv):
+        p = csa.params(top_k=k, n_win=n_win, batch_invariant=inv)
+        return L.attn_ws_size(1, B, 1, H, c, E, k, C.byref(p))
+
+    status = ws(1, 64, 0, 0)                           # two tiles: never split
+    per_item = 64 * c * 4 + 64 * 2 * 4                 # fp32 partial O and (max, sum) per head
+
+    def chunks(max_list):
+        tiles = -(-max_list // 64) + 1
+        if tiles <= 4:
+            return 1
+        per = max(4, -(-tiles // 16))
+        return -(-tiles // per)
+
+    for k, n_win in ((512, 128), (1024, 128), (2048, 0), (200, 0)):
+        ch = chunks(k + n_win)
+        for B in (1, 7, 296, 300):
+            want = 0 if ch == 1 else B * ch * per_item + 512
+            assert ws(B, k, n_win, 1) - status == want, (k, n_win, B)
+            small = B < 2 * 148
+            assert ws(B, k, n_win, 0) - status == (want if small else 0), (k, n_win, B)
