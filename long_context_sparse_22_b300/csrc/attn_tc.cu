@@ -815,7 +815,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 }
 
 // Split-KV combine: out[bt, h] = sum_c O_c e^(m_c - M) / (e^(z - M) + sum_c l_c e^(m_c - M)),
-// chunks in a fixed order, then de-rotation.  One CTA per (query, head).
+// over the chunks that hold some of the query's tiles, in a fixed order, then
+// de-rotation.  One CTA per (query, head).
 template <int C>
 __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnTcArgs a) {
     __shared__ float s_sc[64], s_red[4];
@@ -827,9 +828,14 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnTcArgs a) {
     const int64_t t = a.q_pos[bt];
     const int64_t base = (bt * a.n_hg + hg) * a.n_chunks;
     const float zl2 = a.sink[h] * 1.4426950408889634f;
-    // every chunk's (max, sum) loaded at once, one per thread
+    // chunks past this query's last tile hold no work and were never written
+    ItemInfo f;
+    item_info(a, base, f);
+    const int64_t nlive = (f.nt + a.chunk_tiles - 1) / a.chunk_tiles;
+    const int live = nlive < a.n_chunks ? (int)nlive : a.n_chunks;
+    // every live chunk's (max, sum) loaded at once, one per thread
     float mc = -INFINITY, lc = 0.f;
-    if (tid < a.n_chunks) {
+    if (tid < live) {
         mc = a.part_ml[((base + tid) * 64 + hl) * 2];
         lc = a.part_ml[((base + tid) * 64 + hl) * 2 + 1];
     }
@@ -841,7 +847,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnTcArgs a) {
     if (tid == 0) s_M = fmaxf(fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3])), zl2);
     __syncthreads();
     const float M = s_M;
-    const float sc = (tid < a.n_chunks && mc != -INFINITY) ? exp2f(mc - M) : 0.f;
+    const float sc = (tid < live && mc != -INFINITY) ? exp2f(mc - M) : 0.f;
     if (tid < 64) s_sc[tid] = sc;
     float dl = lc * sc;
 #pragma unroll
@@ -859,7 +865,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnTcArgs a) {
     for (int d = tid * 2; d < C; d += blockDim.x * 2) {
         float y0 = 0.f, y1 = 0.f;
 #pragma unroll 4
-        for (int c = 0; c < a.n_chunks; c++) {
+        for (int c = 0; c < live; c++) {
             const float2 v = *reinterpret_cast<const float2 *>(a.part_o + ((base + c) * 64 + hl) * (int64_t)C + d);
             y0 = fmaf(v.x, s_sc[c], y0);
             y1 = fmaf(v.y, s_sc[c], y1);

@@ -174,11 +174,23 @@ def test_topk_sample_miss_decode(csa, orc):
 
 # --------------------------------------------------------------- attention
 
+def _nan_ws(csa, nbytes=1 << 26):
+    """A workspace whose scratch bytes all hold NaN, so that a read of a split-KV
+    partial that was never written shows in the output instead of passing on
+    whatever an earlier call left there."""
+    ws = csa.Workspace(nbytes)
+    ws.buf[256:].fill_(0xFF)
+    return ws
+
+
 @pytest.mark.parametrize("dtype,B,T,H,c,E,k,m,n_win,r,derot", [
     ("f32", 1, 200, 4, 64, 60, 16, 4, 128, 32, 1),
     ("bf16", 2, 3, 64, 512, 3000, 512, 4, 128, 64, 1),
     ("bf16", 1, 17, 16, 128, 100, 8, 4, 5, 64, 0),
     ("bf16", 1, 300, 96, 512, 200, 64, 4, 128, 64, 1),    # two head groups, one partial
+    ("bf16", 1, 40, 64, 512, 400, 128, 4, 128, 32, 1),    # 16 rotary pairs
+    ("bf16", 1, 40, 64, 512, 400, 128, 4, 128, 192, 1),   # rotary dims across two chunks
+    ("bf16", 1, 20, 64, 512, 100, 64, 4, 16, 0, 1),       # no rotary dims
 ])
 def test_sparse_attn(csa, orc, dtype, B, T, H, c, E, k, m, n_win, r, derot):
     seed = 400 + E
@@ -202,7 +214,7 @@ def test_sparse_attn(csa, orc, dtype, B, T, H, c, E, k, m, n_win, r, derot):
     p = csa.params(m=m, top_k=k, n_win=n_win, rope_dims=r, derotate=derot)
     lse = torch.empty((B, T, H), dtype=torch.float32, device="cuda")
     out = csa.sparse_attn(dev(q), dev(pos), dev(kvc), dev(idx), dev(kv_raw), dev(raw_pos0),
-                          dev(sink), p, lse=lse)
+                          dev(sink), p, lse=lse, ws=_nan_ws(csa))
     g, gl = host(out), host(lse)
     for b in range(B):
         ro, rl = orc.attend(q[b], pos[b], kvc[b], m, kv_raw[b], int(raw_pos0[b]), sink, idx=idx[b],
@@ -229,7 +241,8 @@ def test_hca_attn(csa, orc, dtype, B, T, H, c, E, m, n_win, r):
     pos = np.tile(t_last - T + 1 + np.arange(T, dtype=np.int64), (B, 1))
     raw_pos0 = np.full(B, t_last - L + 1, np.int64)
     p = csa.params(m=m, n_win=n_win, rope_dims=r)
-    out = csa.hca_attn(dev(q), dev(pos), dev(kvc), dev(kv_raw), dev(raw_pos0), dev(sink), p)
+    out = csa.hca_attn(dev(q), dev(pos), dev(kvc), dev(kv_raw), dev(raw_pos0), dev(sink), p,
+                       ws=_nan_ws(csa))
     g = host(out)
     for b in range(B):
         ro = orc.attend(q[b], pos[b], kvc[b], m, kv_raw[b], int(raw_pos0[b]), sink, idx=None,
