@@ -307,6 +307,29 @@ def test_rope_matches_complex_form_and_relative(orc):
     np.testing.assert_allclose(orc.rope(orc.rope(x, 123, rd), -123, rd), x, atol=1e-13)
 
 
+@pytest.mark.parametrize("pos0", [0, 1, 127, 4093, (1 << 20) - 128])
+def test_rope_rows_rotates_row_l_at_pos0_plus_l(orc, pos0):
+    """Stored raw rows: row l of a block starting at pos0 is rotated at
+    pos0 + l ([Book] ch.7 "Partial rotary position embeddings": a key is
+    rotated at its own position).  Checked row by row against the complex
+    form at the row's own position, so an off-by-one in the row position
+    (pos0 + l + 1, or pos0 for every row) fails."""
+    r = rng(pos0 % 1000 + 17)
+    L, c, rd = 6, 16, 8
+    x = r.standard_normal((L, c))
+    got = orc.rope_rows(x, pos0, rd, 10000.0, "f64")
+    for l in range(L):
+        np.testing.assert_allclose(got[l], rope_complex(x[l], pos0 + l, rd), atol=1e-9)
+    # a neighbouring position is distinguishable at these sizes
+    assert np.abs(got[1] - rope_complex(x[1], pos0 + 2, rd)).max() > 1e-3
+    # rounding to the storage dtype happens after the rotation, once
+    gb = orc.rope_rows(x, pos0, rd, 10000.0, "bf16")
+    for l in range(L):
+        want = synth.widen(synth.to_storage(rope_complex(x[l], pos0 + l, rd), "bf16"), "bf16")
+        ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(want), 1e-30))) - 7)
+        assert np.all(np.abs(gb[l] - want) <= ulp)
+
+
 def test_sink_mass_example(orc):
     """Book ch.7 'Attention sinks': real mass 4, sink mass 6 -> real weights 0.4."""
     g = gold("sink_mass_example.json")
