@@ -14,6 +14,11 @@ Under torchrun each rank runs its own replica of the workload (the layer
 does not shard for one sequence); value = all ranks' query-tokens / the
 slowest rank's time.  `--impl reference` times the fp64 CPU oracle on a
 bounded sample of the same workload (rank 0 only).
+
+The line also carries `workloads`: every one of the five workloads timed in
+the same run (the headline's numbers, then the other four), each with its
+per-stage roofline, its SM clocks and the whole step's algorithmic bytes
+against HBM (8 TB/s and the measured copy rate).  `--no-all` skips them.
 """
 from __future__ import annotations
 
@@ -171,14 +176,9 @@ class Workload:
         elif self.kind in ("csa_decode", "hybrid_decode"):
             self.work = accounting.decode(s, self.kind == "hybrid_decode")
         elif self.kind == "csa_prefill":
-            w = accounting.hybrid_prefill(dict(s, m2=s["m"]))
-            w["flops"] -= w["hca_attn_flops"]
-            self.work = w
+            self.work = accounting.csa_layer_prefill(s)
         else:
-            w = accounting.hybrid_prefill(dict(s, hI=1, dI=0, top_k=0, m2=s["m"]))
-            self.work = {"flops": w["hca_attn_flops"], "query_tokens": w["query_tokens"],
-                         "hca_attn_flops": w["hca_attn_flops"], "hca_attn_bytes": w["hca_attn_bytes"],
-                         "compress_bytes": 0}
+            self.work = accounting.hca_layer_prefill(s, s["m"])
         self.units = self.work["query_tokens"]
         self.in_keys = [k for k in self.x]
         self.d = {k: self._dev(v) for k, v in self.x.items()}
@@ -350,25 +350,20 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, rank, world, dist):
-    import torch
-
-    import long_context_sparse_22_b300 as csa
-    local = int(os.environ.get("LOCAL_RANK", 0))
-    torch.cuda.set_device(local)
-    csa.lib()
-    wl = Workload(args.workload, csa, torch)
+def measure(wl, steps, warmup, local, dist, torch):
+    """Device time of `steps` steps of a workload (CUDA events on the launching
+    stream, barrier and synchronise on both sides), with the library's
+    per-stage times and the SM clocks sampled during the timed region."""
+    csa = wl.csa
     dev_stream = torch.cuda.current_stream()
 
     def barrier():
         if dist is not None:
             dist.barrier()
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         wl.step()
     torch.cuda.synchronize()
-
-    # per-stage device times of the same steps (library timing hooks)
     csa.timing_enable(True)
     clocks = ClockSampler(local)
     clocks.start()
@@ -379,7 +374,7 @@ def run_ours(args, rank, world, dist):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n_launch0 = csa.launch_count()
     ev0.record(dev_stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         wl.step()
     ev1.record(dev_stream)
     n_launches = csa.launch_count() - n_launch0
@@ -389,30 +384,19 @@ def run_ours(args, rank, world, dist):
     stages = csa.timing_read()
     clocks.keep_busy(wl.step, 2)
     clk = clocks.stop()
-    ms_total = ev0.elapsed_time(ev1)
-    ms_step = max_over_ranks(ms_total / args.steps, dist, "cuda")
-    value = job_value(wl.units, world, ms_step)
+    ms_step = max_over_ranks(ev0.elapsed_time(ev1) / steps, dist, "cuda")
+    return {"ms_step": ms_step, "stages": stages, "clocks": clk, "launches": n_launches}
 
-    # end to end through the public API with host buffers
-    wl.e2e_setup()
-    wl.e2e_step()
-    torch.cuda.synchronize()
-    k_e2e = max(1, min(args.steps, 3))
-    barrier()
-    t0 = time.perf_counter()
-    for _ in range(k_e2e):
-        wl.e2e_step()
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / k_e2e, dist, "cuda")
-    e2e_value = job_value(wl.units, world, e2e_ms)
 
-    # roofline of the dominant stage
+def roofline(wl, stages, steps):
+    """The dominant stage against its roofline: achieved = the stage's
+    algorithmic FLOPs or bytes per launch / its average launch time."""
     pk, pk_kind = peaks()
-    stage_ms = {k: v[0] / max(1, args.steps) for k, v in stages.items()}
+    stage_ms = {k: v[0] / max(1, steps) for k, v in stages.items()}
     launches = {k: v[1] for k, v in stages.items()}
     dom = max(stage_ms, key=lambda k: stage_ms[k])
     per_launch_ms = stages[dom][0] / max(1, stages[dom][1])
-    launches_per_step = max(1, stages[dom][1] // max(1, args.steps))
+    launches_per_step = max(1, stages[dom][1] // max(1, steps))
     w = wl.work
     flop_key = {"indexer": "indexer_flops", "sparse_attn": "csa_attn_flops",
                 "hca_attn": "hca_attn_flops"}.get(dom)
@@ -438,11 +422,52 @@ def run_ours(args, rank, world, dist):
         else:
             launch_units = wl.s["B"] * wl.s["n"] / launches_per_step   # query tokens per launch
         traffic = per_unit * launch_units
-    roof = {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": unit,
+    return {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak, "peak_source": pk_kind, "traffic": traffic,
             "traffic_unit": "bytes per launch",
             "stage_ms_per_step": {k: round(v, 4) for k, v in stage_ms.items()},
             "stage_launches": launches}
+
+
+def step_hbm(wl, ms_step):
+    """The whole step's algorithmic bytes against HBM: against the nominal
+    8 TB/s and against the measured copy rate."""
+    pk, pk_kind = peaks()
+    gbs = wl.work["bytes"] / (ms_step / 1e3) / 1e9
+    return {"bytes": wl.work["bytes"], "achieved_gbs": gbs, "frac_of_8tbs": gbs / 8000.0,
+            "frac_of_measured": gbs / pk["hbm_gbs"], "measured_gbs": pk["hbm_gbs"],
+            "peak_source": pk_kind}
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+
+    import long_context_sparse_22_b300 as csa
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    csa.lib()
+    wl = Workload(args.workload, csa, torch)
+    m = measure(wl, args.steps, args.warmup, local, dist, torch)
+    ms_step = m["ms_step"]
+    value = job_value(wl.units, world, ms_step)
+
+    # end to end through the public API with host buffers
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    wl.e2e_setup()
+    wl.e2e_step()
+    torch.cuda.synchronize()
+    k_e2e = max(1, min(args.steps, 3))
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(k_e2e):
+        wl.e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / k_e2e, dist, "cuda")
+    e2e_value = job_value(wl.units, world, e2e_ms)
+    roof = roofline(wl, m["stages"], args.steps)
 
     line = {"metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -452,14 +477,37 @@ def run_ours(args, rank, world, dist):
                        "seq_len": wl.s.get("n", wl.s.get("t")),
                        "parallelism": f"replicas{world}",
                        "l2": "inputs larger than L2 (126 MB) each step, no flush needed"},
-            "gpu_launches": int(n_launches),
+            "gpu_launches": int(m["launches"]),
             "e2e": {"value": e2e_value, "unit": "query-tokens/s", "h2d_bytes_per_step": wl.e2e_h2d,
                     "d2h_bytes_per_step": wl.e2e_d2h, "ms_per_step": e2e_ms},
-            "roofline": roof, "clocks": clk}
+            "roofline": roof, "clocks": m["clocks"]}
     if rank == 0 and world == 1 and not args.no_cpu:
         v, thr, desc = oracle_sample(args.workload, budget_s=args.ref_budget, x=wl.x, s=wl.s)
         line["cpu_baseline"] = {"value": v, "unit": "query-tokens/s", "cores": thr, "kind": "oracle",
                                 "sample": desc}
+
+    # every workload in the same run, each with its own clocks: the headline's
+    # numbers again, then the other four (decode included)
+    if not args.no_all:
+        allw = {args.workload: {"ms_per_step": ms_step, "value": value, "roofline": roof,
+                                "clocks": m["clocks"], "steps": args.steps,
+                                "step_hbm": step_hbm(wl, ms_step)}}
+        del wl
+        torch.cuda.empty_cache()
+        for name in sorted(synth.WORKLOADS):
+            if name == args.workload:
+                continue
+            w2 = Workload(name, csa, torch)
+            k2 = args.all_steps if w2.kind in ("csa_decode", "hybrid_decode") else max(3, min(args.steps, 10))
+            m2 = measure(w2, k2, args.warmup, local, dist, torch)
+            allw[name] = {"ms_per_step": m2["ms_step"],
+                          "value": job_value(w2.units, world, m2["ms_step"]),
+                          "roofline": roofline(w2, m2["stages"], k2), "clocks": m2["clocks"],
+                          "steps": k2, "dtype": w2.s["dtype"],
+                          "step_hbm": step_hbm(w2, m2["ms_step"])}
+            del w2
+            torch.cuda.empty_cache()
+        line["workloads"] = allw
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -473,6 +521,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-all", action="store_true", help="time only the selected workload")
+    ap.add_argument("--all-steps", type=int, default=200,
+                    help="timed steps of each decode workload in the all-workloads record")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -91,6 +91,10 @@ typedef struct csa_params {
                          * (long lists are always split the same way); 0:   *
                          * large batches may skip the split, which changes  *
                          * the fp32 summation order                         */
+    int64_t spin_limit; /* polls a kernel's wait on another of its warps    *
+                         * may take before it gives up, records a timeout   *
+                         * in the status word and unwinds; 0 = 2^24 (about  *
+                         * a second)                                        */
 } csa_params;
 
 /* Supported sizes: c (main head dim) in {64, 128, 256, 512}; dI (indexer
@@ -113,6 +117,17 @@ csa_status csa_stream_status(void *ws, void *stream);
 
 /* Zero the status word of a fresh workspace (enqueued on stream). */
 csa_status csa_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Check of the bounded-wait path every tensor-core kernel uses between its
+ * warps (the pages have no counterpart; this is a property of the library).
+ * Enqueues one small kernel whose thread waits on a shared-memory barrier
+ * that nothing completes, polling at most spin_limit times (0: the default
+ * of csa_params), then records the timeout bit in the status word of `ws`
+ * and returns.  csa_stream_status() then reports CSA_ERR_TIMEOUT and the
+ * context stays usable.  Nothing is copied or multiplied while it waits.
+ */
+csa_status csa_wait_probe(int64_t spin_limit, void *ws, size_t ws_bytes, void *stream);
 
 /*
  * Per-stage device timing, for profiling.  While enabled, every entry point
@@ -213,6 +228,9 @@ csa_status topk_select(int64_t B, int64_t T, int64_t E, int32_t k, int32_t m,
  *    streams, or two threads) race and corrupt each other.  Serialise them.
  *  - It allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  *    call.
+ *  - The looked-up address is kept for the life of the process: a device
+ *    reset (cudaDeviceReset) after the first call on that device is not
+ *    supported, because the array may then live at another address.
  */
 csa_status topk_select_noalloc(int64_t B, int64_t T, int64_t E, int32_t k, int32_t m,
                                const float *scores, const int64_t *q_pos,

@@ -9,7 +9,6 @@ raise.
 from __future__ import annotations
 
 import ctypes as C
-import math
 import os
 
 import torch
@@ -32,13 +31,14 @@ class CsaError(RuntimeError):
 class CsaParams(C.Structure):
     _fields_ = [("m", C.c_int32), ("overlap", C.c_int32), ("top_k", C.c_int32),
                 ("n_win", C.c_int32), ("rope_dims", C.c_int32), ("derotate", C.c_int32),
-                ("rope_theta", C.c_double), ("scale", C.c_float), ("batch_invariant", C.c_int32)]
+                ("rope_theta", C.c_double), ("scale", C.c_float), ("batch_invariant", C.c_int32),
+                ("spin_limit", C.c_int64)]
 
 
 def params(m=4, overlap=0, top_k=512, n_win=128, rope_dims=64, derotate=1, rope_theta=10000.0,
-           scale=0.0, batch_invariant=0) -> CsaParams:
+           scale=0.0, batch_invariant=0, spin_limit=0) -> CsaParams:
     return CsaParams(int(m), int(overlap), int(top_k), int(n_win), int(rope_dims), int(derotate),
-                     float(rope_theta), float(scale), int(batch_invariant))
+                     float(rope_theta), float(scale), int(batch_invariant), int(spin_limit))
 
 
 _SIGS = {
@@ -47,6 +47,7 @@ _SIGS = {
     "csa_launch_count": ([], C.c_int64),
     "csa_stream_status": ([C.c_void_p, C.c_void_p], C.c_int),
     "csa_workspace_init": ([C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
+    "csa_wait_probe": ([C.c_int64, C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
     "csa_timing_enable": ([C.c_int32], C.c_int),
     "csa_timing_read": ([C.POINTER(C.c_double), C.POINTER(C.c_int64), C.c_int32], C.c_int),
     "csa_compress": ([C.c_int, C.c_int64, C.c_int64, C.c_int32] + [C.c_void_p] * 8
@@ -169,6 +170,12 @@ def _ws(nbytes: int, ws: Workspace | None):
         cur = Workspace(nbytes)
         _ws_cache[dev] = cur
     return cur
+
+
+def wait_probe(spin_limit: int, ws: Workspace):
+    """Enqueue the bounded-wait check: a kernel waits on a barrier nothing
+    completes for at most spin_limit polls and records a timeout in ws."""
+    _check(lib().csa_wait_probe(int(spin_limit), ws.ptr, ws.nbytes, _stream()), "csa_wait_probe")
 
 
 # ------------------------------------------------------------------ steps
@@ -340,6 +347,3 @@ def timing_read() -> dict:
     _check(lib().csa_timing_read(ms, cnt, n), "timing read")
     return {STAGES[i]: (ms[i], cnt[i]) for i in range(n)}
 
-
-def default_scale(c: int) -> float:
-    return 1.0 / math.sqrt(c)

@@ -60,36 +60,61 @@ def sum_selected(n: int, m: int, k: int) -> int:
     return sum_visible(n, m, min(n // m, k))
 
 
-def hybrid_prefill(s: dict) -> dict:
-    """Per-step work of the interleaved CSA + HCA prefill (one sequence batch)."""
+def csa_layer_prefill(s: dict) -> dict:
+    """Per-step work of one CSA layer's prefill (compression of KV and indexer
+    keys, indexer, top-k, sparse attention)."""
     B, n, H, c, hI, dI, k, W = s["B"], s["n"], s["H"], s["c"], s["hI"], s["dI"], s["top_k"], s["n_win"]
-    m, m2 = s["m"], s.get("m2", s["m"])
+    m = s["m"]
     es = 2 if s["dtype"] == "bf16" else 4
-    E, E2 = n // m, n // m2
+    E = n // m
     vis = sum_visible(n, m)
     sel = sum_selected(n, m, k)
     win = sum_window(n, W)
-    vis2 = sum_visible(n, m2)
-    out = {}
-    out["indexer_pairs"] = B * vis
-    out["indexer_flops"] = B * 2 * dI * hI * vis
-    out["csa_attn_flops"] = B * 4 * c * H * (sel + win)
-    out["hca_attn_flops"] = B * 4 * c * H * (vis2 + win)
-    out["flops"] = out["indexer_flops"] + out["csa_attn_flops"] + out["hca_attn_flops"]
-    # bytes: compress reads C, Z (+ keys), writes entries and rotated raw rows
-    csa_in = B * n * (2 * c + 2 * dI) * es
-    csa_out = B * (E * c + E * dI + n * c) * es
-    hca_in = B * n * 2 * c * es
-    hca_out = B * (E2 * c + n * c) * es
     q_bytes = B * n * H * c * es
-    out["compress_bytes"] = csa_in + csa_out + hca_in + hca_out
-    out["indexer_bytes"] = B * (n * hI * dI * es + n * hI * 4 + E * dI * es)
-    out["topk_bytes"] = B * (vis * 4 + n * k * 4)
-    out["csa_attn_bytes"] = B * (2 * q_bytes // B + (sel + win) * c * es + n * k * 4)
-    out["hca_attn_bytes"] = B * (2 * q_bytes // B + (vis2 + win) * c * es)
+    out = {"indexer_pairs": B * vis,
+           "indexer_flops": B * 2 * dI * hI * vis,
+           "csa_attn_flops": B * 4 * c * H * (sel + win),
+           # compress reads C, Z (+ key C, Z), writes entries, keys and rotated raw rows
+           "compress_bytes": B * n * (2 * c + 2 * dI) * es + B * (E * c + E * dI + n * c) * es,
+           "indexer_bytes": B * (n * hI * dI * es + n * hI * 4 + E * dI * es),
+           "topk_bytes": B * (vis * 4 + n * k * 4),
+           "csa_attn_bytes": 2 * q_bytes + B * ((sel + win) * c * es + n * k * 4)}
+    out["flops"] = out["indexer_flops"] + out["csa_attn_flops"]
     out["bytes"] = (out["compress_bytes"] + out["indexer_bytes"] + out["topk_bytes"]
-                    + out["csa_attn_bytes"] + out["hca_attn_bytes"])
+                    + out["csa_attn_bytes"])
     out["query_tokens"] = B * n
+    return out
+
+
+def hca_layer_prefill(s: dict, m: int) -> dict:
+    """Per-step work of one HCA layer's prefill with rate m (compression,
+    dense attention over every visible entry)."""
+    B, n, H, c, W = s["B"], s["n"], s["H"], s["c"], s["n_win"]
+    es = 2 if s["dtype"] == "bf16" else 4
+    E2 = n // m
+    vis2 = sum_visible(n, m)
+    win = sum_window(n, W)
+    q_bytes = B * n * H * c * es
+    out = {"hca_attn_flops": B * 4 * c * H * (vis2 + win),
+           "compress_bytes": B * n * 2 * c * es + B * (E2 * c + n * c) * es,
+           "hca_attn_bytes": 2 * q_bytes + B * (vis2 + win) * c * es}
+    out["flops"] = out["hca_attn_flops"]
+    out["bytes"] = out["compress_bytes"] + out["hca_attn_bytes"]
+    out["query_tokens"] = B * n
+    return out
+
+
+def hybrid_prefill(s: dict) -> dict:
+    """Per-step work of the interleaved CSA + HCA prefill (one CSA layer with
+    rate m, one HCA layer with rate m2, over the same tokens)."""
+    a = csa_layer_prefill(s)
+    h = hca_layer_prefill(s, s.get("m2", s["m"]))
+    out = dict(a)
+    out["hca_attn_flops"] = h["hca_attn_flops"]
+    out["hca_attn_bytes"] = h["hca_attn_bytes"]
+    out["compress_bytes"] = a["compress_bytes"] + h["compress_bytes"]
+    out["flops"] = a["flops"] + h["flops"]
+    out["bytes"] = a["bytes"] + h["bytes"]
     return out
 
 

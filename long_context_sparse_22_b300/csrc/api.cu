@@ -10,6 +10,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
 
 using namespace csa;
 
@@ -80,6 +81,7 @@ csa_status check_params(const csa_params *p, int c, bool attn) {
     if (p->rope_dims > 0 && !(p->rope_theta > 1.0)) return fail(CSA_ERR_INVALID_ARG, "rope_theta must be > 1");
     if (p->batch_invariant != 0 && p->batch_invariant != 1)
         return fail(CSA_ERR_INVALID_ARG, "batch_invariant must be 0 or 1");
+    if (p->spin_limit < 0) return fail(CSA_ERR_INVALID_ARG, "spin_limit must be >= 0");
     if (attn) {
         if (p->n_win < 0 || p->n_win > 1024) return fail(CSA_ERR_UNSUPPORTED, "n_win=%d not in 0..1024", p->n_win);
         if (p->derotate != 0 && p->derotate != 1) return fail(CSA_ERR_INVALID_ARG, "derotate must be 0 or 1");
@@ -184,12 +186,12 @@ csa_status do_compress(csa_dtype dt, int64_t B, int64_t n, int c, const void *C,
 
 csa_status do_indexer(csa_dtype dt, int64_t B, int64_t T, int hI, int dI, int64_t E, int m,
                       const void *qI, const float *w, const void *kI, const int64_t *q_pos,
-                      float *scores, int write_masked, unsigned *status, cudaStream_t st,
-                      int max_ctas = 0) {
+                      float *scores, int write_masked, unsigned *status, int64_t spin_limit,
+                      cudaStream_t st, int max_ctas = 0) {
     StageScope sc(CSA_STAGE_INDEXER, st);
     if (dt == CSA_BF16 && indexer_tc_supported(hI, dI, B, T, E)) {
         CSA_TRY_CUDA(launch_indexer_tc(B, T, E, m, qI, w, kI, q_pos, scores, write_masked, status,
-                                       max_ctas, st),
+                                       max_ctas, spin_limit_of(spin_limit), st),
                      "indexer_score launch (tensor cores)");
         return CSA_OK;
     }
@@ -231,6 +233,7 @@ csa_status do_attn(csa_dtype dt, int64_t B, int64_t T, int H, int c, int64_t E, 
     a.Tq = T; a.H = H; a.c = c; a.E = E; a.k = k; a.L = L;
     a.m = p->m; a.n_win = p->n_win; a.derotate = p->derotate;
     a.scale = p->scale > 0.f ? p->scale : (float)(1.0 / sqrt((double)c));
+    a.spin = spin_limit_of(p->spin_limit);
     a.rope = make_rope(c, p->rope_dims, p->rope_theta);
     StageScope sc(idx ? CSA_STAGE_SPARSE_ATTN : CSA_STAGE_HCA_ATTN, st);
     // the tensor-core path addresses rows of q, kvc and kv_raw with 32-bit TMA coordinates
@@ -239,7 +242,13 @@ csa_status do_attn(csa_dtype dt, int64_t B, int64_t T, int H, int c, int64_t E, 
     if (attn_tc_supported(dt, c) && fits) {
         const int64_t max_list = (idx ? (int64_t)k : E) + p->n_win;
         int ch = attn_tc_chunks(B * T, H, max_list, p->batch_invariant != 0);
-        if (ch > 1 && scratch == nullptr) ch = 1;
+        if (ch > 1 && scratch == nullptr) {
+            // without split scratch the list runs unsplit, which changes the
+            // summation order: not allowed when batch invariance was asked for
+            if (p->batch_invariant)
+                return fail(CSA_ERR_WORKSPACE, "batch_invariant needs the split-KV scratch of attn_ws_size");
+            ch = 1;
+        }
         CSA_TRY_CUDA(launch_attn_tc(B, a, cnt, ch, scratch, max_ctas, st),
                      "attention launch (tensor cores)");
         return CSA_OK;
@@ -272,6 +281,28 @@ csa_status check_attn_common(csa_dtype dt, int64_t B, int64_t T, int H, int c, i
 }
 
 }  // namespace
+
+namespace csa {
+
+// One thread waits on a barrier whose single expected arrival never comes;
+// the bounded wait gives up after `spin` polls and records ST_TIMEOUT.
+__global__ void wait_probe_kernel(unsigned *status, long long spin) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    tc::mbar_init(&bar, 1);
+    abort_flag = 0;
+    tc::fence_barrier_init();
+    tc::mbar_wait(&bar, 0, status, (volatile int *)&abort_flag, spin);
+}
+
+cudaError_t launch_wait_probe(unsigned *status, long long spin, cudaStream_t st) {
+    wait_probe_kernel<<<1, 32, 0, st>>>(status, spin);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace csa
 
 // ====================================================================== ABI
 
@@ -340,6 +371,14 @@ csa_status csa_stream_status(void *ws, void *stream) {
                 (word & ST_NO_WINDOW_ROW) ? "window position missing from kv_raw; " : "", word);
 }
 
+csa_status csa_wait_probe(int64_t spin_limit, void *ws, size_t ws_bytes, void *stream) {
+    if (spin_limit < 0) return fail(CSA_ERR_INVALID_ARG, "spin_limit must be >= 0");
+    CSA_TRY(check_ws(ws, ws_bytes, CSA_STATUS_BYTES));
+    CSA_TRY_CUDA(launch_wait_probe((unsigned *)ws, spin_limit_of(spin_limit), (cudaStream_t)stream),
+                 "wait probe launch");
+    return CSA_OK;
+}
+
 csa_status csa_compress(csa_dtype dtype, int64_t B, int64_t n, int32_t c, const void *C,
                         const void *Z, const float *bias, const void *Cb, const void *Zb,
                         const float *biasb, void *out, void *raw_out, const csa_params *params,
@@ -382,7 +421,7 @@ csa_status indexer_score(csa_dtype dtype, int64_t B, int64_t T, int32_t hI, int3
     CSA_TRY(need_ptr(kI, "kI"));
     CSA_TRY(need_ptr(q_pos, "q_pos"));
     CSA_TRY(need_ptr(scores, "scores"));
-    return do_indexer(dtype, B, T, hI, dI, E, m, qI, w, kI, q_pos, scores, 1, (unsigned *)ws,
+    return do_indexer(dtype, B, T, hI, dI, E, m, qI, w, kI, q_pos, scores, 1, (unsigned *)ws, 0,
                       (cudaStream_t)stream);
 }
 
@@ -517,7 +556,7 @@ csa_status csa_prefill(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t
                         params->rope_dims, st));
     CSA_TRY(do_compress(dtype, B, n, dI, Ck, Zk, biask, Ckb, Zkb, biaskb, kic, nullptr, params, 0, st));
     CSA_TRY(do_indexer(dtype, B, n, hI, dI, E, params->m, qI, w, kic, (const int64_t *)pos,
-                       (float *)sc, 0, status, st));
+                       (float *)sc, 0, status, params->spin_limit, st));
     CSA_TRY(do_topk(B, n, E, params->top_k, params->m, (const float *)sc, (const int64_t *)pos,
                     (int32_t *)idx, (int32_t *)cnt, tks, st));
     return do_attn(dtype, B, n, H, c, E, params->top_k, n, q, (const int64_t *)pos, kvc,
@@ -591,28 +630,49 @@ static size_t decode_layout(Carve &cv, csa_dtype dt, int64_t B, int H, int c, in
     return cv.off;
 }
 
-// One auxiliary stream and two events per device, created on the first
-// hybrid_decode call that has an HCA layer, kept until the process exits.
-// They let the HCA layer's attention run beside the CSA indexer.
-struct AuxStreams {
+// Auxiliary stream sets, one per concurrent hybrid_decode call: a call takes
+// a set (stream + fork/join events) from its device's pool, records fork on
+// its own stream, runs the HCA layer's attention on the set's stream after
+// fork, records join there and makes its own stream wait on join; then it
+// returns the set.  A set is never shared by two calls in flight, so every
+// call's auxiliary work waits on its own stream.  Sets are created on demand
+// and kept until the process exits.
+struct AuxSet {
     cudaStream_t aux = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
 };
-static AuxStreams g_aux[64];
+static std::vector<AuxSet> g_aux_free[MAX_DEVICES];
 static std::mutex g_aux_mu;
 
-static csa_status get_aux(AuxStreams **out) {
+struct AuxLease {
+    int dev = -1;
+    AuxSet set;
+    ~AuxLease() {
+        if (dev < 0) return;
+        std::lock_guard<std::mutex> g(g_aux_mu);
+        g_aux_free[dev].push_back(set);
+    }
+};
+
+static csa_status take_aux(AuxLease &lease) {
     int dev = 0;
     CSA_TRY_CUDA(cudaGetDevice(&dev), "get device");
-    if (dev < 0 || dev >= 64) return fail(CSA_ERR_UNSUPPORTED, "device index %d", dev);
-    std::lock_guard<std::mutex> g(g_aux_mu);
-    AuxStreams &a = g_aux[dev];
-    if (!a.aux) {
-        CSA_TRY_CUDA(cudaStreamCreateWithFlags(&a.aux, cudaStreamNonBlocking), "aux stream");
-        CSA_TRY_CUDA(cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming), "fork event");
-        CSA_TRY_CUDA(cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming), "join event");
+    if (dev < 0 || dev >= MAX_DEVICES) return fail(CSA_ERR_UNSUPPORTED, "device index %d", dev);
+    {
+        std::lock_guard<std::mutex> g(g_aux_mu);
+        if (!g_aux_free[dev].empty()) {
+            lease.set = g_aux_free[dev].back();
+            g_aux_free[dev].pop_back();
+            lease.dev = dev;
+            return CSA_OK;
+        }
     }
-    *out = &a;
+    AuxSet a;
+    CSA_TRY_CUDA(cudaStreamCreateWithFlags(&a.aux, cudaStreamNonBlocking), "aux stream");
+    CSA_TRY_CUDA(cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming), "fork event");
+    CSA_TRY_CUDA(cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming), "join event");
+    lease.set = a;
+    lease.dev = dev;
     return CSA_OK;
 }
 
@@ -666,27 +726,33 @@ csa_status hybrid_decode(csa_dtype dtype, int64_t B, int32_t H, int32_t c, int32
     // auxiliary stream, on all but a few SMs, beside the rest of the CSA top-k
     // and the sparse attention, which need few CTAs.
     const bool concurrent = hca && dtype == CSA_BF16 && attn_tc_supported(dtype, c);
-    CSA_TRY(do_indexer(dtype, B, 1, hI, dI, E, params->m, qI, w, kIc, q_pos, (float *)sc, 0, status, st));
+    CSA_TRY(do_indexer(dtype, B, 1, hI, dI, E, params->m, qI, w, kIc, q_pos, (float *)sc, 0, status,
+                       params->spin_limit, st));
     CSA_TRY(do_topk(B, 1, E, params->top_k, params->m, (const float *)sc, q_pos, (int32_t *)idx,
                     (int32_t *)cnt, tks, st, 1));
-    AuxStreams *ax = nullptr;
+    AuxLease ax;
     if (concurrent) {
-        CSA_TRY(get_aux(&ax));
+        CSA_TRY(take_aux(ax));
         const int sms = device_sms();
-        CSA_TRY_CUDA(cudaEventRecord(ax->fork, st), "fork");
-        CSA_TRY_CUDA(cudaStreamWaitEvent(ax->aux, ax->fork, 0), "fork wait");
-        CSA_TRY(do_attn(dtype, B, 1, H, c, E2, 0, L, q2, q_pos, kvc2, nullptr, nullptr, kv_raw2,
-                        raw_pos0, sink2, out2, nullptr, params2, status, asc2, ax->aux, sms - 24));
-        CSA_TRY_CUDA(cudaEventRecord(ax->join, ax->aux), "join");
+        CSA_TRY_CUDA(cudaEventRecord(ax.set.fork, st), "fork");
+        CSA_TRY_CUDA(cudaStreamWaitEvent(ax.set.aux, ax.set.fork, 0), "fork wait");
+        csa_status s2 = do_attn(dtype, B, 1, H, c, E2, 0, L, q2, q_pos, kvc2, nullptr, nullptr,
+                                kv_raw2, raw_pos0, sink2, out2, nullptr, params2, status, asc2,
+                                ax.set.aux, sms - 24);
+        // the join is recorded and waited on even if the launch failed, so
+        // the set goes back to the pool with nothing of this call pending
+        cudaError_t e1 = cudaEventRecord(ax.set.join, ax.set.aux);
+        cudaError_t e2 = cudaStreamWaitEvent(st, ax.set.join, 0);
+        if (s2 != CSA_OK) return s2;
+        CSA_TRY_CUDA(e1, "join");
+        CSA_TRY_CUDA(e2, "join wait");
     }
     CSA_TRY(do_topk(B, 1, E, params->top_k, params->m, (const float *)sc, q_pos, (int32_t *)idx,
                     (int32_t *)cnt, tks, st, 2));
     CSA_TRY(do_attn(dtype, B, 1, H, c, E, params->top_k, L, q, q_pos, kvc, (const int32_t *)idx,
                     (const int32_t *)cnt, kv_raw, raw_pos0, sink, out, nullptr, params, status, asc,
                     st));
-    if (concurrent) {
-        CSA_TRY_CUDA(cudaStreamWaitEvent(st, ax->join, 0), "join wait");
-    } else if (hca) {
+    if (!concurrent && hca) {
         CSA_TRY(do_attn(dtype, B, 1, H, c, E2, 0, L, q2, q_pos, kvc2, nullptr, nullptr, kv_raw2,
                         raw_pos0, sink2, out2, nullptr, params2, status, asc2, st));
     }

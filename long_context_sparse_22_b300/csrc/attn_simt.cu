@@ -201,7 +201,7 @@ attn_simt_kernel(AttnArgs a) {
     }
 }
 
-static int g_attn_smem_set[2] = {0, 0};
+static PerDevice g_attn_smem[2];
 
 cudaError_t launch_attn_simt(csa_dtype dt, int64_t B, const AttnArgs &a, cudaStream_t st) {
     if (B * a.Tq == 0 || a.H == 0) return cudaSuccess;
@@ -209,12 +209,11 @@ cudaError_t launch_attn_simt(csa_dtype dt, int64_t B, const AttnArgs &a, cudaStr
     const size_t smem = ((size_t)AT_HG * a.c + (size_t)AT_TE * a.c + AT_HG * AT_TE) * 4;
     const size_t smem_max = ((size_t)AT_HG * 512 + (size_t)AT_TE * 512 + AT_HG * AT_TE) * 4;
     const int di = dt == CSA_BF16 ? 1 : 0;
-    if (!g_attn_smem_set[di]) {
+    {
         cudaError_t e = dt == CSA_BF16
-            ? cudaFuncSetAttribute(attn_simt_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max)
-            : cudaFuncSetAttribute(attn_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
+            ? smem_limit_once(g_attn_smem[di], (const void *)attn_simt_kernel<__nv_bfloat16>, (int)smem_max)
+            : smem_limit_once(g_attn_smem[di], (const void *)attn_simt_kernel<float>, (int)smem_max);
         if (e != cudaSuccess) return e;
-        g_attn_smem_set[di] = 1;
     }
     if (dt == CSA_BF16) attn_simt_kernel<__nv_bfloat16><<<grid, AT_THREADS, smem, st>>>(a);
     else attn_simt_kernel<float><<<grid, AT_THREADS, smem, st>>>(a);

@@ -95,6 +95,7 @@ struct AttnTcArgs {
     int chunk_tiles;         // > 0: split mode with this many tiles per item
     int n_chunks;
     int64_t n_items;
+    long long spin;          // polls before a wait between roles gives up
     float scale_log2;        // logit scale * log2(e)
     RopeFreqs rope;
 };
@@ -209,8 +210,8 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr, uint32_t lbo, uint
 // warp's next burst of copies issued several times slower after a wait that
 // had blocked.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, unsigned *status,
-                                          volatile int *abort_flag) {
-    const bool ok = tc::mbar_wait(bar, parity, status, abort_flag);
+                                          volatile int *abort_flag, long long limit) {
+    const bool ok = tc::mbar_wait(bar, parity, status, abort_flag, limit);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -310,7 +311,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // this item's q rows (box TMA).  Waits are warp-uniform and the four
             // loader warps agree on a failure through a barrier reduction, so none
             // is left at a named barrier; the barrier also publishes cs_s.
-            if (named_bar_or(2, Cfg::NLOAD, !warp_wait(qempty, (ii & 1) ^ 1, a.status, abort_flag))) {
+            if (named_bar_or(2, Cfg::NLOAD, !warp_wait(qempty, (ii & 1) ^ 1, a.status, abort_flag, a.spin))) {
                 ok = false;
                 break;
             }
@@ -324,7 +325,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // q~ = RoPE(q, t): once q has landed, rotate the rotary pairs in place and
             // hand q to the MMA.  Runs while the item's first tile is in flight.
             auto rope_q = [&]() -> bool {
-                if (named_bar_or(2, Cfg::NLOAD, !warp_wait(qland, ii & 1, a.status, abort_flag)))
+                if (named_bar_or(2, Cfg::NLOAD, !warp_wait(qland, ii & 1, a.status, abort_flag, a.spin)))
                     return false;
                 if (tid == 0) q_pending = 0;
                 const int np = a.rope.pairs;
@@ -378,7 +379,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     bal = __ballot_sync(0xffffffffu, v);
                 }
                 if (named_bar_or(2, Cfg::NLOAD,
-                                 !warp_wait(&kempty[buf], ((g >> 1) & 1) ^ 1, a.status, abort_flag))) {
+                                 !warp_wait(&kempty[buf], ((g >> 1) & 1) ^ 1, a.status, abort_flag, a.spin))) {
                     ok = false;
                     break;
                 }
@@ -458,10 +459,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // let every copy issued by TMA land before the CTA exits
             for (int s = 0; s < 2; s++)
                 if (tma_issued & (1u << s))
-                    for (long long i = 0; i < tc::SPIN_LIMIT; i++)
+                    for (long long i = 0; i < tc::DRAIN_LIMIT; i++)
                         if (tc::mbar_test(&kfull[s], (last_g[s] >> 1) & 1)) break;
             if (q_pending)
-                for (long long i = 0; i < tc::SPIN_LIMIT; i++)
+                for (long long i = 0; i < tc::DRAIN_LIMIT; i++)
                     if (tc::mbar_test(qland, (ii & 1))) break;
         }
     } else if (warp == Cfg::MMA_WARP || warp == Cfg::PV_WARP) {
@@ -492,12 +493,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (f.j0 >= f.j1) continue;
                 const int nt = f.j1 - f.j0;
                 if (is_qk) {
-                    if (!warp_wait(qfull, ii & 1, a.status, abort_flag)) break;
+                    if (!warp_wait(qfull, ii & 1, a.status, abort_flag, a.spin)) break;
                     for (int n = 0; n < nt; n++) {
                         const uint32_t gq = g + n;
                         const int buf = gq & 1;
-                        if (!warp_wait(&kfull[buf], (gq >> 1) & 1, a.status, abort_flag) ||
-                            !warp_wait(&sempty[buf], ((gq >> 1) & 1) ^ 1, a.status, abort_flag)) {
+                        if (!warp_wait(&kfull[buf], (gq >> 1) & 1, a.status, abort_flag, a.spin) ||
+                            !warp_wait(&sempty[buf], ((gq >> 1) & 1) ^ 1, a.status, abort_flag, a.spin)) {
                             ok = false;
                             break;
                         }
@@ -520,8 +521,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     for (int n = 0; n < nt; n++) {
                         const uint32_t gp = g + n;
                         const int bp = gp & 1;
-                        if (!warp_wait(&pfull[bp], (gp >> 1) & 1, a.status, abort_flag) ||
-                            (n == 0 && !warp_wait(oempty, (ii & 1) ^ 1, a.status, abort_flag))) {
+                        if (!warp_wait(&pfull[bp], (gp >> 1) & 1, a.status, abort_flag, a.spin) ||
+                            (n == 0 && !warp_wait(oempty, (ii & 1) ^ 1, a.status, abort_flag, a.spin))) {
                             ok = false;
                             break;
                         }
@@ -549,7 +550,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (leader) tc::mma_commit(mdone);
             __syncwarp();
             if (is_qk)
-                for (long long i = 0; i < tc::SPIN_LIMIT; i++)
+                for (long long i = 0; i < tc::DRAIN_LIMIT; i++)
                     if (tc::mbar_test(mdone, 0)) break;
         }
     } else {
@@ -599,10 +600,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 // completed and cannot advance again before this tile's PV) and the
                 // P buffer (the PV of two tiles back has read it): both are ready
                 // before this tile's logits, so they are checked first
-                bool ok = warp_wait(&kfull[buf], par, a.status, abort_flag) &&
-                          warp_wait(&pempty[buf], par ^ 1, a.status, abort_flag);
+                bool ok = warp_wait(&kfull[buf], par, a.status, abort_flag, a.spin) &&
+                          warp_wait(&pempty[buf], par ^ 1, a.status, abort_flag, a.spin);
                 const uint32_t mlo = ok ? vmask32[buf * 2] : 0u, mhi = ok ? vmask32[buf * 2 + 1] : 0u;
-                ok = ok && warp_wait(&sfull[buf], par, a.status, abort_flag);
+                ok = ok && warp_wait(&sfull[buf], par, a.status, abort_flag, a.spin);
                 uint32_t raw[32];
                 if (ok) {
                     tc::fence_after_sync();
@@ -674,7 +675,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     // some head's max grew: O^T was accumulated with older maxima,
                     // scale column h by alpha[h]
                     const uint32_t gp = g - 1;
-                    if (warp_wait(&pempty[gp & 1], (gp >> 1) & 1, a.status, abort_flag)) {
+                    if (warp_wait(&pempty[gp & 1], (gp >> 1) & 1, a.status, abort_flag, a.spin)) {
                         tc::fence_after_sync();
                         const float *al = alpha_s + buf * 64;
 #pragma unroll 1
@@ -735,7 +736,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     }
                 }
             }
-            const bool ok = warp_wait(ofull, ii & 1, a.status, abort_flag);
+            const bool ok = warp_wait(ofull, ii & 1, a.status, abort_flag, a.spin);
             if (named_bar_or(1, 128, !ok)) break;
             tc::fence_after_sync();
             const int nh = a.H - h0 < 64 ? a.H - h0 : 64;
@@ -889,14 +890,27 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnTcArgs a) {
 // ------------------------------------------------------------------- host
 
 int device_sms() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 148;
+    static std::atomic<int> n[MAX_DEVICES];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return 148;
+    int v = n[dev].load();
+    if (v <= 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+        n[dev].store(v);
     }
-    return n;
+    return v;
+}
+
+cudaError_t smem_limit_once(PerDevice &once, const void *kernel, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
+    const unsigned long long bit = 1ull << dev;
+    if (once.done.load() & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) once.done |= bit;
+    return e;
 }
 
 bool attn_tc_supported(csa_dtype dt, int c) { return dt == CSA_BF16 && (c == 512 || c == 128); }
@@ -938,6 +952,7 @@ static cudaError_t launch_attn_tc_c(int64_t B, const AttnArgs &g, const int32_t 
     a.T = g.Tq; a.E = g.E; a.L = g.L;
     a.H = g.H; a.k = g.k; a.m = g.m; a.n_win = g.n_win; a.derotate = g.derotate;
     a.n_hg = (g.H + 63) / 64;
+    a.spin = g.spin;
     a.scale_log2 = g.scale * 1.4426950408889634f;
     a.rope = g.rope;
     const int64_t max_list = (g.idx ? (int64_t)g.k : g.E) + g.n_win;
@@ -968,12 +983,10 @@ static cudaError_t launch_attn_tc_c(int64_t B, const AttnArgs &g, const int32_t 
         !make_tmap_bf16_2d(&tw, have_w ? g.kv_raw : g.q, have_w ? (uint64_t)(B * g.L) : (uint64_t)(rows * g.H),
                            C, 64))
         return cudaErrorInvalidValue;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Cfg::SMEM);
+    static PerDevice attr;
+    {
+        cudaError_t e = smem_limit_once(attr, (const void *)attn_tc_kernel<C>, Cfg::SMEM);
         if (e != cudaSuccess) return e;
-        attr = true;
     }
     const int sms = max_ctas > 0 && max_ctas < device_sms() ? max_ctas : device_sms();
     const int grid = (int)(a.n_items < sms ? a.n_items : sms);

@@ -42,6 +42,7 @@ struct IdxArgs {
     int64_t E;
     int m;
     int write_masked;
+    long long spin;          // polls before a wait between roles gives up
 };
 
 template <int QT>
@@ -126,7 +127,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     uint64_t *bempty = bfull + 1;
     uint64_t *accfull = bempty + 1;                        // [2]
     uint64_t *accempty = accfull + 2;                      // [2]
-    uint32_t *tmem_slot = (uint32_t *)(accempty + 2);
+    uint64_t *mdone = accempty + 2;                        // every issued MMA has completed
+    uint32_t *tmem_slot = (uint32_t *)(mdone + 1);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -143,6 +145,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tc::mbar_init(&accfull[i], 1);
             tc::mbar_init(&accempty[i], Cfg::EPI_WARPS);
         }
+        tc::mbar_init(mdone, 1);
         *abort_flag = 0;
         tc::fence_barrier_init();
         tc::prefetch_tmap(&tm_q);
@@ -159,19 +162,20 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0, bphase = 0;
-            uint32_t issued_mask = 0, last_par = 0, b_issued = 0;
+            uint32_t issued_mask = 0, last_par = 0, b_issued = 0, b_par = 0;
             Item it;
             for (int r = 0; idx_item<QT>(a, cta, G, r, it); r++) {
                 if (it.jt0 >= it.jt1) continue;
-                if (!tc::mbar_wait(bempty, bphase ^ 1, a.status, abort_flag)) break;
+                if (!tc::mbar_wait(bempty, bphase ^ 1, a.status, abort_flag, a.spin)) break;
                 tc::mbar_expect_tx(bfull, Cfg::B_BYTES);
                 const int qrow = (int)(((int64_t)it.b * a.T + (int64_t)it.qb * QT) * Cfg::HI);
                 for (int kh = 0; kh < Cfg::KH; kh++)
                     tc::tma_load_2d(sB + kh * Cfg::N * 128, &tm_q, kh * 64, qrow, bfull);
                 b_issued = 1;
+                b_par = bphase;
                 bool ok = true;
                 for (int jt = it.jt0; jt < it.jt1; jt++) {
-                    if (!tc::mbar_wait(&empty[stage], phase ^ 1, a.status, abort_flag)) { ok = false; break; }
+                    if (!tc::mbar_wait(&empty[stage], phase ^ 1, a.status, abort_flag, a.spin)) { ok = false; break; }
                     tc::mbar_expect_tx(&full[stage], Cfg::A_BYTES);
                     const int krow = (int)((int64_t)it.b * a.E + (int64_t)jt * 128);
                     uint8_t *dst = sA + stage * Cfg::A_BYTES;
@@ -187,15 +191,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (*abort_flag) {
                 // let every copy this thread issued land before the CTA exits
                 for (int s = 0; s < Cfg::STAGES; s++)
-                    if (issued_mask & (1u << s)) {
-                        for (int i = 0; i < (1 << 16); i++) {
-                            uint32_t done;
-                            asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-                                         : "=r"(done) : "r"(tc::smem_u32(&full[s])), "r"((last_par >> s) & 1u) : "memory");
-                            if (done) break;
-                        }
-                    }
-                (void)b_issued;
+                    if (issued_mask & (1u << s))
+                        for (long long i = 0; i < tc::DRAIN_LIMIT; i++)
+                            if (tc::mbar_test(&full[s], (last_par >> s) & 1u)) break;
+                if (b_issued)
+                    for (long long i = 0; i < tc::DRAIN_LIMIT; i++)
+                        if (tc::mbar_test(bfull, b_par)) break;
             }
         }
     } else if (warp == 1) {
@@ -208,12 +209,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             Item it;
             for (int r = 0; idx_item<QT>(a, cta, G, r, it); r++) {
                 if (it.jt0 >= it.jt1) continue;
-                if (!tc::mbar_wait(bfull, bphase, a.status, abort_flag)) break;
+                if (!tc::mbar_wait(bfull, bphase, a.status, abort_flag, a.spin)) break;
                 tc::fence_after_sync();
                 bool ok = true;
                 for (int jt = it.jt0; jt < it.jt1; jt++) {
-                    if (!tc::mbar_wait(&full[stage], phase, a.status, abort_flag) ||
-                        !tc::mbar_wait(&accempty[acc], accphase ^ 1, a.status, abort_flag)) {
+                    if (!tc::mbar_wait(&full[stage], phase, a.status, abort_flag, a.spin) ||
+                        !tc::mbar_wait(&accempty[acc], accphase ^ 1, a.status, abort_flag, a.spin)) {
                         ok = false;
                         break;
                     }
@@ -237,6 +238,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tc::mma_commit(bempty);
                 bphase ^= 1;
             }
+            // every MMA issued above has completed before TMEM is released
+            tc::mma_commit(mdone);
+            for (long long i = 0; i < tc::DRAIN_LIMIT; i++)
+                if (tc::mbar_test(mdone, 0)) break;
         }
     } else {
         // ---------------------------------------------------------- epilogue
@@ -267,7 +272,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 nvt[u] = t < a.T ? visible_count(a.q_pos[(int64_t)it.b * a.T + t], a.m, a.E) : -1;
             }
             for (int jt = it.jt0; jt < it.jt1; jt++) {
-                if (!tc::mbar_wait(&accfull[acc], accphase, a.status, abort_flag)) { ok = false; break; }
+                if (!tc::mbar_wait(&accfull[acc], accphase, a.status, abort_flag, a.spin)) { ok = false; break; }
                 tc::fence_after_sync();
                 const int64_t j = (int64_t)jt * 128 + row;
 #pragma unroll
@@ -352,18 +357,6 @@ bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64
     return r == CUDA_SUCCESS;
 }
 
-static int g_num_sms = 0;
-
-static int num_sms() {
-    if (g_num_sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (g_num_sms <= 0) g_num_sms = 148;
-    }
-    return g_num_sms;
-}
-
 bool indexer_tc_supported(int hI, int dI, int64_t B, int64_t T, int64_t E) {
     return hI == 64 && dI == 128 && B * T * 64 < (1LL << 31) && B * E < (1LL << 31) && E > 0;
 }
@@ -372,12 +365,10 @@ template <int QT>
 static cudaError_t launch_tc(const CUtensorMap &tq, const CUtensorMap &tk, const IdxArgs &a,
                              int grid, cudaStream_t st) {
     using Cfg = IdxCfg<QT>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<QT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    static PerDevice attr;
+    {
+        cudaError_t e = smem_limit_once(attr, (const void *)indexer_tc_kernel<QT>, Cfg::SMEM);
         if (e != cudaSuccess) return e;
-        attr = true;
     }
     indexer_tc_kernel<QT><<<grid, Cfg::THREADS, Cfg::SMEM, st>>>(tq, tk, a);
     count_launches(1);
@@ -386,11 +377,13 @@ static cudaError_t launch_tc(const CUtensorMap &tq, const CUtensorMap &tk, const
 
 cudaError_t launch_indexer_tc(int64_t B, int64_t T, int64_t E, int m, const void *qI,
                               const float *w, const void *kI, const int64_t *q_pos, float *scores,
-                              int write_masked, unsigned *status, int max_ctas, cudaStream_t st) {
+                              int write_masked, unsigned *status, int max_ctas, long long spin,
+                              cudaStream_t st) {
     if (B * T == 0 || E == 0) return cudaSuccess;
     IdxArgs a;
     a.w = w; a.q_pos = q_pos; a.scores = scores; a.status = status;
     a.B = (int)B; a.T = (int)T; a.E = E; a.m = m; a.write_masked = write_masked;
+    a.spin = spin;
     a.tps = (int)((E + 127) / 128);
     const bool decode = T < 4;
     const int QT = decode ? 1 : 4;
@@ -399,7 +392,7 @@ cudaError_t launch_indexer_tc(int64_t B, int64_t T, int64_t E, int m, const void
     if (!make_tmap_bf16_2d(&tq, qI, (uint64_t)(B * T * 64), 128, decode ? 64 : 256) ||
         !make_tmap_bf16_2d(&tk, kI, (uint64_t)(B * E), 128, 128))
         return cudaErrorInvalidValue;
-    const int sms = max_ctas > 0 && max_ctas < num_sms() ? max_ctas : num_sms();
+    const int sms = max_ctas > 0 && max_ctas < device_sms() ? max_ctas : device_sms();
     cudaError_t e;
     if (decode) {
         long long tiles = (long long)B * T * a.tps;

@@ -3,6 +3,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/csa.h"
 #include "common.cuh"
 
@@ -13,6 +15,24 @@ void count_launches(int n);
 
 // Record a failure message for csa_last_error() and return s.
 csa_status report_error(csa_status s, const char *msg);
+
+// Devices a process may address (device ordinals 0 .. MAX_DEVICES-1).
+constexpr int MAX_DEVICES = 64;
+
+// One-time set-up done separately on every device: bit d is set once the
+// set-up has run with device d current.
+struct PerDevice {
+    std::atomic<unsigned long long> done{0};
+};
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, the first time this kernel is launched there (the attribute is per
+// device).
+cudaError_t smem_limit_once(PerDevice &once, const void *kernel, int bytes);
+
+// Polls of a bounded wait: params->spin_limit, or the default when it is 0.
+constexpr long long DEFAULT_SPIN_LIMIT = 1LL << 24;
+inline long long spin_limit_of(int64_t v) { return v > 0 ? (long long)v : DEFAULT_SPIN_LIMIT; }
 
 struct AttnArgs {
     const void *q;
@@ -32,6 +52,7 @@ struct AttnArgs {
     int64_t L;
     int m, n_win, derotate;
     float scale;
+    long long spin;        // polls before a bounded wait gives up
     RopeFreqs rope;
 };
 
@@ -50,7 +71,8 @@ bool indexer_tc_supported(int hI, int dI, int64_t B, int64_t T, int64_t E);
 // max_ctas > 0 caps the persistent grid (to leave SMs to a concurrent kernel)
 cudaError_t launch_indexer_tc(int64_t B, int64_t T, int64_t E, int m, const void *qI,
                               const float *w, const void *kI, const int64_t *q_pos, float *scores,
-                              int write_masked, unsigned *status, int max_ctas, cudaStream_t st);
+                              int write_masked, unsigned *status, int max_ctas, long long spin,
+                              cudaStream_t st);
 
 // scratch: topk_scratch_bytes(B*Tq, E) bytes of device memory (0 for the
 // one-CTA-per-row path, used for rows of at most 16384 entries or many rows)
@@ -75,6 +97,11 @@ int attn_tc_chunks(int64_t rows, int H, int64_t max_list, bool invariant);
 size_t attn_tc_split_bytes(int64_t rows, int H, int c, int n_chunks);
 cudaError_t launch_attn_tc(int64_t B, const AttnArgs &a, const int32_t *cnt, int n_chunks,
                            void *split_ws, int max_ctas, cudaStream_t st);
+// SM count of the current device (cached per device).
 int device_sms();
+
+// A kernel that waits on a barrier nothing completes, for at most `spin`
+// polls, then records ST_TIMEOUT in *status.
+cudaError_t launch_wait_probe(unsigned *status, long long spin, cudaStream_t st);
 
 }  // namespace csa

@@ -11,9 +11,11 @@
 namespace csa {
 namespace tc {
 
-// Iteration cap of every wait loop: about a second of try_wait polling,
-// after which the kernel records ST_TIMEOUT and unwinds instead of hanging.
-constexpr long long SPIN_LIMIT = 1LL << 24;
+// Polls of the loops that let a CTA's own copies and MMAs retire before it
+// exits (these wait on the hardware, not on another thread): about a second.
+// The waits between roles take their cap from the caller (csa_params
+// spin_limit) and record ST_TIMEOUT when it runs out.
+constexpr long long DRAIN_LIMIT = 1LL << 24;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -61,15 +63,16 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
     return done != 0;
 }
 
-// Wait for the phase of the given parity to complete.  Returns false (and
-// sets the timeout bit) if the cap runs out, or if *abort is already set.
+// Wait for the phase of the given parity to complete, polling at most
+// `limit` times.  Returns false (and sets the timeout bit) if the cap runs
+// out, or if *abort is already set.
 // A phase that has already completed is seen by the non-blocking probe,
 // which answers faster than a potentially blocking try_wait.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *status,
-                                          volatile int *abort) {
+                                          volatile int *abort, long long limit) {
     if (mbar_test(bar, parity)) return true;
     const uint32_t a = smem_u32(bar);
-    for (long long i = 0; i < SPIN_LIMIT; i++) {
+    for (long long i = 0; i < limit; i++) {
         uint32_t done;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"

@@ -766,7 +766,7 @@ __global__ void __launch_bounds__(TK_THREADS) topk_final_kernel(TkLong a, int ca
 
 // -------------------------------------------------------------------- host
 
-static int g_final_smem_set = 0;
+static PerDevice g_final_smem;
 constexpr int CAND_CAP = 24576;      // candidates cached per row (192 KB)
 
 bool topk_use_long(int64_t rows, int64_t E) { return rows < 256 && E > 16384; }
@@ -812,23 +812,20 @@ cudaError_t launch_topk_phase(int phase, int64_t B, int64_t Tq, int64_t E, int k
             count_launches(1);
             return cudaGetLastError();
         }
-        if (!g_final_smem_set) {
-            cudaError_t e = cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 CAND_CAP * 8);
+        {
+            cudaError_t e = smem_limit_once(g_final_smem, (const void *)topk_final_kernel, CAND_CAP * 8);
             if (e != cudaSuccess) return e;
-            g_final_smem_set = 1;
         }
         topk_final_kernel<<<(unsigned)rows, TK_THREADS, CAND_CAP * 8, st>>>(a, CAND_CAP);
         count_launches(1);
         return cudaGetLastError();
     }
     if (phase != 1) return cudaSuccess;
-    static int tw_attr = 0;
+    static PerDevice tw_attr;
     const size_t smem = TW_WARPS * sizeof(TwShared);
-    if (!tw_attr) {
-        cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    {
+        cudaError_t e = smem_limit_once(tw_attr, (const void *)topk_kernel, (int)smem);
         if (e != cudaSuccess) return e;
-        tw_attr = 1;
     }
     int64_t blocks = (rows + TW_WARPS - 1) / TW_WARPS;
     const int64_t cap = (int64_t)device_sms();           // one resident CTA per SM

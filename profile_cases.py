@@ -1,7 +1,7 @@
 """Small, self-contained launches of one stage each, sized for an ncu capture
 (inputs larger than L2 so DRAM counters mean something, a few GB at most).
 
-    python -m long_context_sparse_22_b300.profile_cases CASE [--reps R]
+    python profile_cases.py CASE [--reps R]
 
 Cases:
   indexer_prefill   indexer_score, 16384 queries x 4096 entries, 64 x 128 (bf16)
@@ -15,14 +15,22 @@ Cases:
   hca_decode        hca_attn, 8 sequences x 8192 entries, 128 heads x 512
   hca_prefill       hca_attn, 8192 queries over 64 entries (m' = 128) + window, 64 heads x 512
   csa_prefill       csa_prefill, n = 16384, Flash shapes
+  sparse_attn_decode  sparse_attn, 8 sequences x 1 query, 128 heads x 512, k = 1024 +
+                    window (lists split over CTAs: the split-KV combine runs)
+  attn_simt         sparse_attn in fp32, 2048 queries, 4 heads x 64, k = 64 + window
+  indexer_simt      indexer_score in fp32, 2048 queries x 512 entries, 4 x 32
 """
 from __future__ import annotations
 
 import argparse
+import os
+import sys
 
 import torch
 
-import long_context_sparse_22_b300 as csa
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+
+import long_context_sparse_22_b300 as csa  # noqa: E402
 
 
 def _bf16(*shape, scale=1.0):
@@ -38,6 +46,15 @@ def case_indexer(T, E, B, m=4):
     else:
         pos = (torch.arange(T, device="cuda") + (E * m - T)).repeat(B, 1)
     scores = torch.empty(B, T, E, device="cuda")
+    return lambda: csa.indexer_score(qI, w, kI, pos, m, scores=scores)
+
+
+def case_indexer_f32(T=2048, E=512, hI=4, dI=32, m=4):
+    qI = torch.randn(1, T, hI, dI, device="cuda")
+    w = torch.softmax(torch.randn(1, T, hI, device="cuda"), -1)
+    kI = torch.randn(1, E, dI, device="cuda")
+    pos = torch.arange(T, device="cuda").view(1, T)
+    scores = torch.empty(1, T, E, device="cuda")
     return lambda: csa.indexer_score(qI, w, kI, pos, m, scores=scores)
 
 
@@ -74,6 +91,41 @@ def case_sparse_attn():
     sink = torch.randn(H, device="cuda")
     out = torch.empty_like(q)
     p = csa.params(m=m, top_k=k, n_win=128, rope_dims=64)
+    return lambda: csa.sparse_attn(q, pos, kvc, idx, raw, rp0, sink, p, out=out)
+
+
+def case_sparse_attn_decode():
+    B, H, c, E, k, m = 8, 128, 512, 262144, 1024, 4
+    t = E * m - 1
+    q = _bf16(B, 1, H, c)
+    kvc = _bf16(B, E, c)
+    raw = _bf16(B, 128, c)
+    pos = torch.full((B, 1), t, dtype=torch.int64, device="cuda")
+    rp0 = torch.full((B,), t - 127, dtype=torch.int64, device="cuda")
+    idx = torch.sort(torch.stack([torch.randperm(E, device="cuda")[:k] for _ in range(B)]), -1)[0]
+    idx = idx.to(torch.int32).view(B, 1, k).contiguous()
+    sink = torch.randn(H, device="cuda")
+    out = torch.empty_like(q)
+    p = csa.params(m=m, top_k=k, n_win=128, rope_dims=64)
+    return lambda: csa.sparse_attn(q, pos, kvc, idx, raw, rp0, sink, p, out=out)
+
+
+def case_attn_simt():
+    T, H, c, E, k, m = 2048, 4, 64, 512, 64, 4
+    q = torch.randn(1, T, H, c, device="cuda")
+    kvc = torch.randn(1, E, c, device="cuda")
+    raw = torch.randn(1, T, c, device="cuda")
+    pos = torch.arange(T, device="cuda").view(1, T)
+    nv = ((pos + 1) // m).clamp(max=E)                   # visible entries per query
+    j = torch.arange(E, device="cuda").view(1, 1, E)
+    r = torch.where(j < nv.view(1, T, 1), torch.rand(1, T, E, device="cuda"), -1.0)
+    top = torch.topk(r, k, -1)                           # invisible entries never win
+    sel = torch.sort(torch.where(top.values >= 0, top.indices, E), -1).values
+    idx = torch.where(sel == E, -1, sel).to(torch.int32).contiguous()   # ascending, -1 padded
+    rp0 = torch.zeros(1, dtype=torch.int64, device="cuda")
+    sink = torch.randn(H, device="cuda")
+    out = torch.empty_like(q)
+    p = csa.params(m=m, top_k=k, n_win=128, rope_dims=32)
     return lambda: csa.sparse_attn(q, pos, kvc, idx, raw, rp0, sink, p, out=out)
 
 
@@ -131,6 +183,9 @@ CASES = {
     "hca_decode": case_hca_decode,
     "hca_prefill": case_hca_prefill,
     "csa_prefill": case_csa_prefill,
+    "sparse_attn_decode": case_sparse_attn_decode,
+    "attn_simt": case_attn_simt,
+    "indexer_simt": case_indexer_f32,
 }
 
 

@@ -64,6 +64,15 @@ def test_validation_rejects_before_launch(csa):
     s = L.hca_attn(1, 1, 1, 16, 128, 4, 4, fake, fake, fake, fake, fake, fake, fake, None,
                    C.byref(p_bi), fake, 256, None)
     assert s == 1 and "batch_invariant" in _err(csa, s)
+    # spin_limit must not be negative
+    p_sp = csa.params(m=4, rope_dims=64, spin_limit=-1)
+    s = L.hca_attn(1, 1, 1, 16, 128, 4, 4, fake, fake, fake, fake, fake, fake, fake, None,
+                   C.byref(p_sp), fake, 256, None)
+    assert s == 1 and "spin_limit" in _err(csa, s)
+    s = L.csa_wait_probe(-5, fake, 256, None)
+    assert s == 1 and "spin_limit" in _err(csa, s)
+    s = L.csa_wait_probe(100, None, 0, None)
+    assert s == 3
     # odd rope dims
     p_bad = csa.params(m=4, rope_dims=3)
     s = L.csa_compress(1, 1, 8, 64, fake, fake, fake, None, None, None, fake, None, C.byref(p_bad), None)

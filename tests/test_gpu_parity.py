@@ -357,12 +357,29 @@ def test_decode_cfg5_pro(csa, orc):
     _check_decode(orc, s, x, res, io, [0, 5], True)
 
 
+def _cfg4_rows(n):
+    """Query rows checked at full size: the first and last query blocks of
+    the indexer (4 queries each), every row around the top-k transition
+    (|V| = k at t = 2047 .. 2050, k + 1 from t = 2051), and a stratified
+    sample of 14 rows from each of the 16 bands of 4096 queries, so every
+    region of the indexer's block schedule and of the attention work list is
+    reached."""
+    r = _np_rng(44)
+    rows = [np.arange(0, 8), np.arange(n - 8, n), np.arange(2040, 2060)]
+    for band in range(16):
+        lo = band * (n // 16)
+        rows.append(lo + r.choice(n // 16, 14, replace=False))
+    rows.append(np.array([4095, 4096, 16383, 16384, 32767, 32768, 49151, 49152]))
+    return np.unique(np.concatenate(rows))
+
+
 def test_prefill_cfg4_flash_sampled(csa, orc):
     """Flash-shaped interleaved CSA + HCA prefill at the full n = 65536, in the
     launch configuration the bench times; oracle on sampled query rows."""
     s, x = synth.make_inputs("hybrid_prefill_flash")
     out, io = _prefill_csa_gpu(csa, s, x)
-    q_sel = np.array([0, 3, 4, 2047, 2048, 2051, 30000, 65535])
+    q_sel = _cfg4_rows(s["n"])
+    assert q_sel.size >= 256
     _check_csa_prefill(orc, s, x, out, io, q_sel)
     d = {k: dev(v) for k, v in x.items() if k.endswith("2")}
     p2 = csa.params(m=s["m2"], n_win=s["n_win"], rope_dims=s["rope_dims"], rope_theta=s["theta"])
@@ -402,12 +419,13 @@ def test_prefill_deterministic(csa):
     assert torch.equal(a, b) and torch.equal(ia, ib)
 
 
-def test_decode_batch_invariant_full_batch(csa):
+def test_decode_batch_invariant_full_batch(csa, orc):
     """With batch_invariant set, a sequence decoded alone gives bitwise the same output as
     inside a batch that fills the GPU by itself (300 sequences of 640 entries, where the
     default would skip the split of each list into chunks)."""
     s, x = synth.make_inputs("csa_decode_flash", B=300, t=2047)
     res, io = _decode_gpu(csa, s, x, False, batch_invariant=1)
+    _check_decode(orc, s, x, res, io, [0, 299], False)      # and the batch run is right
     for b in (0, 299):
         xb = {k: (v[b:b + 1] if k not in ("sink",) else v) for k, v in x.items()}
         rb, ib = _decode_gpu(csa, dict(s, B=1), xb, False, batch_invariant=1)
@@ -423,3 +441,74 @@ def test_decode_batch_invariant(csa):
         sb = dict(s, B=1)
         rb, ib = _decode_gpu(csa, sb, xb, False)
         assert torch.equal(rb[0], res[b]) and torch.equal(ib[0], io[b])
+
+
+def test_wait_probe_reports_timeout(csa):
+    """A bounded wait that nothing completes gives up after spin_limit polls,
+    sets the timeout bit, and the context stays usable for the next call."""
+    ws = csa.Workspace(1 << 16)
+    csa.wait_probe(2000, ws)
+    with pytest.raises(csa.CsaError) as e:
+        ws.status()
+    assert e.value.status == 5
+    ws.status()                                     # cleared
+    s, x = synth.make_inputs("hybrid_decode_pro", B=1, t=1023)
+    res, io = _decode_gpu(csa, s, x, True)
+    torch.cuda.synchronize()
+    assert torch.isfinite(res[0]).all() and torch.isfinite(res[1]).all()
+
+
+def test_hybrid_decode_two_threads_two_streams(csa):
+    """Two host threads, each on its own stream and workspace, issue 20
+    Pro-shaped hybrid decode calls each (the HCA layer runs on an auxiliary
+    stream inside every call); q2 is rewritten on the caller's stream right
+    before each call.  Every output equals, bit for bit, the same call made
+    serially afterwards."""
+    import threading
+    sets = []
+    for j in range(4):
+        s, x = synth.make_inputs("hybrid_decode_pro", B=2, t=4095 + 128 * j, seed=40 + j)
+        sets.append((s, {k: dev(v) for k, v in x.items()}))
+    s0 = sets[0][0]
+    p = csa.params(m=4, top_k=s0["top_k"], n_win=128, rope_dims=64)
+    p2 = csa.params(m=128, n_win=128, rope_dims=64)
+    N = 20
+    results = {}
+    errors = []
+
+    def one(d, q2buf, ws, out, out2):
+        q2buf.copy_(d["q2"])
+        csa.hybrid_decode(d["q"], d["qI"], d["w"], d["kvc"], d["kIc"], d["kv_raw"], d["sink"],
+                          d["q_pos"], d["raw_pos0"], p, q2=q2buf, kvc2=d["kvc2"],
+                          kv_raw2=d["kv_raw2"], sink2=d["sink2"], p2=p2, out=out, out2=out2, ws=ws)
+
+    def worker(j):
+        try:
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                ws = csa.Workspace(1 << 26)
+                q2buf = torch.empty_like(sets[0][1]["q2"])
+                for i in range(N):
+                    d = sets[(i + j) % 4][1]
+                    out, out2 = torch.empty_like(d["q"]), torch.empty_like(d["q2"])
+                    one(d, q2buf, ws, out, out2)
+                    results[(j, i)] = (out, out2)
+                st.synchronize()
+        except Exception as e:  # surfaced below
+            errors.append(e)
+
+    th = [threading.Thread(target=worker, args=(j,)) for j in range(2)]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    ws = csa.Workspace(1 << 26)
+    q2buf = torch.empty_like(sets[0][1]["q2"])
+    for (j, i), (out, out2) in sorted(results.items()):
+        d = sets[(i + j) % 4][1]
+        o, o2 = torch.empty_like(d["q"]), torch.empty_like(d["q2"])
+        one(d, q2buf, ws, o, o2)
+        torch.cuda.synchronize()
+        assert torch.equal(o, out) and torch.equal(o2, out2), (j, i)
