@@ -161,20 +161,27 @@ def job_value(units_per_rank: float, world: int, ms_step: float) -> float:
 
 # --------------------------------------------------------------- workloads
 
+# decode workloads on the low-precision caches (FP8 KV records, MXFP4 indexer
+# keys, BF16 scores): the same inputs, caches quantised on the device once
+LOWP = {"csa_decode_flash_lowp": "csa_decode_flash", "hybrid_decode_pro_lowp": "hybrid_decode_pro"}
+ALL_WORKLOADS = sorted(synth.WORKLOADS) + sorted(LOWP)
+
+
 class Workload:
     """Device buffers and the step of one workload through the public API."""
 
     def __init__(self, name: str, csa, torch):
         self.name, self.csa, self.torch = name, csa, torch
+        self.lowp = name in LOWP
         t0 = time.time()
-        self.s, self.x = synth.make_inputs(name)
+        self.s, self.x = synth.make_inputs(LOWP.get(name, name))
         self.gen_s = time.time() - t0
         self.kind = self.s["kind"]
         s = self.s
         if self.kind == "hybrid_prefill":
             self.work = accounting.hybrid_prefill(s)
         elif self.kind in ("csa_decode", "hybrid_decode"):
-            self.work = accounting.decode(s, self.kind == "hybrid_decode")
+            self.work = accounting.decode(s, self.kind == "hybrid_decode", lowp=self.lowp)
         elif self.kind == "csa_prefill":
             self.work = accounting.csa_layer_prefill(s)
         else:
@@ -184,10 +191,18 @@ class Workload:
         self.d = {k: self._dev(v) for k, v in self.x.items()}
         self.h2d_bytes = sum(v.nbytes for v in self.x.values())
         p = csa.params
+        cf = 1 if self.lowp else 0
         self.p = p(m=s["m"], overlap=s.get("overlap", 0), top_k=s.get("top_k", 1),
-                   n_win=s["n_win"], rope_dims=s["rope_dims"], rope_theta=s["theta"])
+                   n_win=s["n_win"], rope_dims=s["rope_dims"], rope_theta=s["theta"], cache_format=cf)
         self.p2 = p(m=s.get("m2", s["m"]), n_win=s["n_win"], rope_dims=s["rope_dims"],
-                    rope_theta=s["theta"])
+                    rope_theta=s["theta"], cache_format=cf)
+        if self.lowp:
+            # the stored caches in their low-precision formats (resident state, as in serving)
+            self.d["kvc"] = csa.quantize_kv_fp8(self.d["kvc"])
+            self.d["kIc"] = csa.quantize_index_fp4(self.d["kIc"])
+            if "kvc2" in self.d:
+                self.d["kvc2"] = csa.quantize_kv_fp8(self.d["kvc2"])
+            torch.cuda.synchronize()
         self._alloc()
 
     def _dev(self, a):
@@ -329,13 +344,14 @@ def oracle_sample(name: str, budget_s: float = 15.0, x=None, s=None):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    s, x = synth.make_inputs(args.workload)
+    # the low-precision decode variants share their inputs with the dtype workloads
+    s, x = synth.make_inputs(LOWP.get(args.workload, args.workload))
     vals = []
     for _ in range(args.warmup):
-        oracle_sample(args.workload, budget_s=2.0, x=x, s=s)
+        oracle_sample(s["name"], budget_s=2.0, x=x, s=s)
     desc = threads = None
     for _ in range(args.steps):
-        v, threads, desc = oracle_sample(args.workload, budget_s=args.ref_budget, x=x, s=s)
+        v, threads, desc = oracle_sample(s["name"], budget_s=args.ref_budget, x=x, s=s)
         vals.append(v)
     value = float(statistics.median(vals))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "query-tokens/s",
@@ -352,8 +368,10 @@ def run_reference(args, rank, world):
 
 def measure(wl, steps, warmup, local, dist, torch):
     """Device time of `steps` steps of a workload (CUDA events on the launching
-    stream, barrier and synchronise on both sides), with the library's
-    per-stage times and the SM clocks sampled during the timed region."""
+    stream, barrier and synchronise on both sides) with the SM clocks sampled
+    during the timed region; then the library's per-stage times from the same
+    number of steps run again with its event hooks on (kept out of the timed
+    region, where the extra events would lengthen short decode steps)."""
     csa = wl.csa
     dev_stream = torch.cuda.current_stream()
 
@@ -364,11 +382,9 @@ def measure(wl, steps, warmup, local, dist, torch):
     for _ in range(warmup):
         wl.step()
     torch.cuda.synchronize()
-    csa.timing_enable(True)
     clocks = ClockSampler(local)
     clocks.start()
     clocks.keep_busy(wl.step, 2)
-    csa.timing_read()            # drop the stage times of the untimed steps
     barrier()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -380,11 +396,16 @@ def measure(wl, steps, warmup, local, dist, torch):
     n_launches = csa.launch_count() - n_launch0
     torch.cuda.synchronize()
     barrier()
-    csa.timing_enable(False)
-    stages = csa.timing_read()
     clocks.keep_busy(wl.step, 2)
     clk = clocks.stop()
     ms_step = max_over_ranks(ev0.elapsed_time(ev1) / steps, dist, "cuda")
+    csa.timing_enable(True)
+    csa.timing_read()
+    for _ in range(steps):
+        wl.step()
+    torch.cuda.synchronize()
+    csa.timing_enable(False)
+    stages = csa.timing_read()
     return {"ms_step": ms_step, "stages": stages, "clocks": clk, "launches": n_launches}
 
 
@@ -482,7 +503,7 @@ def run_ours(args, rank, world, dist):
                     "d2h_bytes_per_step": wl.e2e_d2h, "ms_per_step": e2e_ms},
             "roofline": roof, "clocks": m["clocks"]}
     if rank == 0 and world == 1 and not args.no_cpu:
-        v, thr, desc = oracle_sample(args.workload, budget_s=args.ref_budget, x=wl.x, s=wl.s)
+        v, thr, desc = oracle_sample(wl.s["name"], budget_s=args.ref_budget, x=wl.x, s=wl.s)
         line["cpu_baseline"] = {"value": v, "unit": "query-tokens/s", "cores": thr, "kind": "oracle",
                                 "sample": desc}
 
@@ -494,7 +515,7 @@ def run_ours(args, rank, world, dist):
                                 "step_hbm": step_hbm(wl, ms_step)}}
         del wl
         torch.cuda.empty_cache()
-        for name in sorted(synth.WORKLOADS):
+        for name in ALL_WORKLOADS:
             if name == args.workload:
                 continue
             w2 = Workload(name, csa, torch)
@@ -517,7 +538,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="hybrid_prefill_flash", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default="hybrid_prefill_flash", choices=ALL_WORKLOADS)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu", action="store_true")

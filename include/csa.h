@@ -95,7 +95,25 @@ typedef struct csa_params {
                          * may take before it gives up, records a timeout   *
                          * in the status word and unwinds; 0 = 2^24 (about  *
                          * a second)                                        */
+    int32_t cache_format; /* CSA_CACHE_DTYPE or CSA_CACHE_LOWP (section 6)  */
+    /* RMSNorm gains (device pointers to c floats, or NULL for no norm)
+     * [book ch.7 "Query and KV normalization"]: y = x / sqrt(mean(x^2) +
+     * norm_eps) * g over the c coordinates of a vector, applied to the vector
+     * as produced, before RoPE.  q_norm: each query head (shared by the
+     * heads), in every attention entry point.  kv_norm: each compressed KV
+     * entry after pooling and each stored raw row, in csa_compress,
+     * csa_prefill, hca_prefill and decode_append (caches passed to attention
+     * are already stored normalised). */
+    const float *q_norm;
+    const float *kv_norm;
+    float norm_eps;     /* 0 means 1e-6                                     */
 } csa_params;
+
+/* Storage of the compressed caches an entry point reads (section 6). */
+typedef enum {
+    CSA_CACHE_DTYPE = 0, /* entries and indexer keys in the call's dtype; fp32 scores */
+    CSA_CACHE_LOWP = 1   /* FP8 KV records, MXFP4 indexer keys, BF16 scores      */
+} csa_cache_format;
 
 /* Supported sizes: c (main head dim) in {64, 128, 256, 512}; dI (indexer
  * dim) in {32, 64, 128}; H (query heads) 1 .. 128; hI (indexer heads)
@@ -329,6 +347,131 @@ csa_status hybrid_decode(csa_dtype dtype, int64_t B, int32_t H, int32_t c, int32
                          void *out, void *out2, int32_t *idx_out,
                          const csa_params *params, const csa_params *params2,
                          void *ws, size_t ws_bytes, void *stream);
+
+/* --------------------------------------------------------------------- */
+/* 5. Incremental decode state.                                           */
+/* --------------------------------------------------------------------- */
+/*
+ * [DeepSeek-V4 book ch.5 "What is retained during decode"; ch.13 "Bounded
+ * state per request": when a token arrives the window advances and the
+ * compression state changes; when a block completes, its summary moves into
+ * the growing cache.]
+ *
+ * decode_append takes one new token per sequence, at position t[b] (the
+ * number of tokens the sequence held before it), for one compressed layer:
+ *   - its raw row C, rotated at t, goes into the window ring `win` at row
+ *     t mod n_win;
+ *   - its compressor inputs (C, Z; the indexer keys' Ck, Zk when Ck is not
+ *     NULL; the second-branch rows Cb, Zb, Ckb, Zkb when overlap = 1) go into
+ *     the tail, which holds the current block's rows (and, for overlap = 1,
+ *     the previous block's second-branch rows);
+ *   - when t+1 is a multiple of m, block i = (t+1)/m - 1 is compressed
+ *     exactly as csa_compress compresses it (same arithmetic, bitwise the
+ *     same entry), rotated at (i+1)*m-1 and stored at kvc[b, i] (and the
+ *     key, without rotation, at kIc[b, i]).
+ * Sizes: C, Z, Cb, Zb [B, c]; Ck, Zk, Ckb, Zkb [B, dI]; bias, biasb [m, c];
+ * biask, biaskb [m, dI]; win [B, n_win, c]; tail: decode_tail_bytes();
+ * kvc [B, E_cap, c]; kIc [B, E_cap, dI]; all in dtype.  Uses params->m,
+ * overlap, n_win, rope_dims, rope_theta.  The tail needs no initialisation:
+ * every slot is written before it is read.  A block past E_cap sets the
+ * range bit of the status word and is not stored.
+ *
+ * The ring is the window hybrid_decode reads: pass kv_raw = win, L = n_win
+ * and raw_pos0[b] = max(0, t - n_win + 1) for the query at t.  While
+ * t < n_win - 1, row l holds position l, as raw_pos0 = 0 says; once the
+ * window is full every row of the ring is in it, in rotated rather than
+ * positional order, which attention does not depend on (it sums over the
+ * set, and stored rows carry their own rotation).  Pass E = E_cap: entries
+ * past the visible prefix are never read.
+ */
+size_t decode_tail_bytes(csa_dtype dtype, int64_t B, int32_t c, int32_t dI,
+                         const csa_params *params);
+csa_status decode_append(csa_dtype dtype, int64_t B, int32_t c, int32_t dI, const int64_t *t,
+                         const void *C, const void *Z, const float *bias,
+                         const void *Cb, const void *Zb, const float *biasb,
+                         const void *Ck, const void *Zk, const float *biask,
+                         const void *Ckb, const void *Zkb, const float *biaskb,
+                         void *win, void *tail, void *kvc, void *kIc, int64_t E_cap,
+                         const csa_params *params, void *ws, size_t ws_bytes, void *stream);
+
+/* --------------------------------------------------------------------- */
+/* 6. Low-precision caches.                                               */
+/* --------------------------------------------------------------------- */
+/*
+ * [DeepSeek-V4 book ch.8 "The main compressed-entry payload": an entry keeps
+ * its non-rotary dims in FP8 and its 64 rotary dims in BF16, 576 bytes at
+ * c = 512; ch.16 "The two main FP4 targets", "Why use fine-grained scales?":
+ * indexer queries and keys in FP4 with one scale per 1 x 32 tile; "BF16
+ * index scores".]
+ *
+ * FP8 KV record, one per entry of c = 512 with rope_dims = 64, KV_FP8_BYTES
+ * bytes: bytes 0..447 the E4M3 codes of dims 0..447 (finite variant,
+ * largest 448, nearest-even, saturating); bytes 448..575 dims 448..511 in
+ * BF16; bytes 576..591 four fp32 scales for dims [0,128), [128,256),
+ * [256,384), [384,448): scale = amax / 448 (1 for an all-zero group), code =
+ * E4M3(x / scale) with the quotient formed in fp32.  A cache of E entries
+ * per sequence is [B, E, KV_FP8_BYTES].
+ *
+ * MXFP4 rows of 128 values, planar over `rows` rows (rows = B * E for a key
+ * cache), index_fp4_bytes(rows) bytes: first the codes, 64 bytes a row,
+ * value 2i in the low nibble of byte i and 2i+1 in the high nibble (E2M1:
+ * sign bit 3, magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6; nearest-even,
+ * saturating); then the scales, 4 bytes a row (one per block of 32 values,
+ * the row count rounded up to a multiple of 4): the exponent e + 127 of the
+ * block's scale 2^e, e = floor(log2 amax) - 2 clipped to [-127, 127] (0 for
+ * an all-zero block).
+ *
+ * With params->cache_format = CSA_CACHE_LOWP:
+ *   - sparse_attn, hca_attn and hybrid_decode read kvc (and kvc2) as FP8
+ *     records (dtype bf16, c = 512, rope_dims = 64); the window rows stay in
+ *     dtype.  A record's codes are dequantised to bf16 (code * scale rounded
+ *     once) for the tensor-core products;
+ *   - hybrid_decode reads kIc as MXFP4 keys (hI = 64, dI = 128), quantises
+ *     the query qI to MXFP4 the same way, and ranks BF16 scores
+ *     bf16(sum_h w * ReLU(q4 . k4)): equal BF16 scores tie and the lower
+ *     index wins.
+ * csa_prefill and hca_prefill take CSA_CACHE_DTYPE only.
+ */
+#define KV_FP8_BYTES 592
+size_t index_fp4_bytes(int64_t rows);
+/* src [rows, 512] in dtype -> dst [rows, KV_FP8_BYTES] */
+csa_status quantize_kv_fp8(csa_dtype dtype, int64_t rows, int32_t c, int32_t rope_dims,
+                           const void *src, void *dst, void *stream);
+/* src [rows, 128] in dtype -> dst (index_fp4_bytes(rows) bytes) */
+csa_status quantize_index_fp4(csa_dtype dtype, int64_t rows, int32_t d, const void *src, void *dst,
+                              void *stream);
+/*
+ * Decode index scores over MXFP4 keys: one query per sequence, qI [B, 1, 64,
+ * 128] bf16 (quantised to MXFP4 inside), w [B, 1, 64] f32, kI4 the MXFP4
+ * cache of B * E keys, q_pos [B, 1]; scores [B, 1, E] f32 holding BF16
+ * values for visible entries and -inf past them.  ws: the status word.
+ */
+csa_status indexer_score_fp4(int64_t B, int64_t E, int32_t m, const void *qI, const float *w,
+                             const void *kI4, const int64_t *q_pos, float *scores, void *ws,
+                             size_t ws_bytes, void *stream);
+
+/* --------------------------------------------------------------------- */
+/* 7. Grouped output projection.                                          */
+/* --------------------------------------------------------------------- */
+/*
+ * [DeepSeek-V4 book ch.6 "Why output projection is a large cost": the heads
+ * are split into groups, each group's concatenated outputs are projected to
+ * a width d_g, and the concatenation of the group results is projected to
+ * the hidden width d; "DeepSeek-V4 technical preview" blog: 16 groups for
+ * Pro.]  For token t, G = H / heads_per_group groups:
+ *   u[t, g*d_g + j] = sum_i o[t, g*hg*c + i] * w_g[g, j, i]     (hg = heads_per_group)
+ *   y[t, n]         = sum_i u[t, i] * w_o[n, i]
+ * o [T, H, c] bf16 (the attention output, de-rotated); w_g [G, d_g, hg*c]
+ * and w_o [d, G*d_g] bf16 in the out-features-major layout of a linear
+ * layer; y [T, d] bf16.  u is kept in bf16 in the workspace, after the
+ * status word (out_proj_ws_size bytes in all).  Both products run on the
+ * tensor cores with fp32 accumulation.  d_g and d must be multiples of 256,
+ * hg*c a multiple of 64.
+ */
+size_t out_proj_ws_size(int64_t T, int32_t H, int32_t heads_per_group, int32_t d_g);
+csa_status out_proj(int64_t T, int32_t H, int32_t c, int32_t heads_per_group, int32_t d_g,
+                    int32_t d, const void *o, const void *w_g, const void *w_o, void *y,
+                    void *ws, size_t ws_bytes, void *stream);
 
 #if defined(__GNUC__)
 #pragma GCC visibility pop

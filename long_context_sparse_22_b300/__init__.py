@@ -32,13 +32,21 @@ class CsaParams(C.Structure):
     _fields_ = [("m", C.c_int32), ("overlap", C.c_int32), ("top_k", C.c_int32),
                 ("n_win", C.c_int32), ("rope_dims", C.c_int32), ("derotate", C.c_int32),
                 ("rope_theta", C.c_double), ("scale", C.c_float), ("batch_invariant", C.c_int32),
-                ("spin_limit", C.c_int64)]
+                ("spin_limit", C.c_int64), ("cache_format", C.c_int32),
+                ("q_norm", C.c_void_p), ("kv_norm", C.c_void_p), ("norm_eps", C.c_float)]
+
+CACHE_DTYPE, CACHE_LOWP = 0, 1
+KV_FP8_BYTES = 592
 
 
 def params(m=4, overlap=0, top_k=512, n_win=128, rope_dims=64, derotate=1, rope_theta=10000.0,
-           scale=0.0, batch_invariant=0, spin_limit=0) -> CsaParams:
+           scale=0.0, batch_invariant=0, spin_limit=0, cache_format=0, q_norm=None, kv_norm=None,
+           norm_eps=0.0) -> CsaParams:
+    """Layer parameters; q_norm / kv_norm are float32 device tensors of c gains
+    (kept alive by the caller while the parameters are in use) or None."""
     return CsaParams(int(m), int(overlap), int(top_k), int(n_win), int(rope_dims), int(derotate),
-                     float(rope_theta), float(scale), int(batch_invariant), int(spin_limit))
+                     float(rope_theta), float(scale), int(batch_invariant), int(spin_limit),
+                     int(cache_format), _p(q_norm), _p(kv_norm), float(norm_eps))
 
 
 _SIGS = {
@@ -84,6 +92,20 @@ _SIGS = {
                        C.c_int64, C.c_int64] + [C.c_void_p] * 16
                       + [C.POINTER(CsaParams), C.POINTER(CsaParams), C.c_void_p, C.c_size_t,
                          C.c_void_p], C.c_int),
+    "index_fp4_bytes": ([C.c_int64], C.c_size_t),
+    "quantize_kv_fp8": ([C.c_int, C.c_int64, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p],
+                        C.c_int),
+    "quantize_index_fp4": ([C.c_int, C.c_int64, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
+    "indexer_score_fp4": ([C.c_int64, C.c_int64, C.c_int32] + [C.c_void_p] * 5
+                          + [C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
+    "out_proj_ws_size": ([C.c_int64, C.c_int32, C.c_int32, C.c_int32], C.c_size_t),
+    "out_proj": ([C.c_int64, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32] + [C.c_void_p] * 4
+                 + [C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
+    "decode_tail_bytes": ([C.c_int, C.c_int64, C.c_int32, C.c_int32, C.POINTER(CsaParams)],
+                          C.c_size_t),
+    "decode_append": ([C.c_int, C.c_int64, C.c_int32, C.c_int32] + [C.c_void_p] * 17
+                      + [C.c_int64, C.POINTER(CsaParams), C.c_void_p, C.c_size_t, C.c_void_p],
+                      C.c_int),
 }
 
 
@@ -181,11 +203,13 @@ def wait_probe(spin_limit: int, ws: Workspace):
 # ------------------------------------------------------------------ steps
 
 def csa_compress(C_, Z, bias, *, m, overlap=0, Cb=None, Zb=None, biasb=None, rope_dims=0,
-                 rope_theta=10000.0, want_raw=False, out=None, raw_out=None):
+                 rope_theta=10000.0, want_raw=False, out=None, raw_out=None, kv_norm=None,
+                 norm_eps=0.0):
     """[B, n, c] content and logits -> entries [B, n // m, c] (and the raw rows
-    rotated at their positions when want_raw)."""
+    rotated at their positions when want_raw); kv_norm: RMSNorm gains [c]."""
     B, n, c = C_.shape
-    p = params(m=m, overlap=overlap, rope_dims=rope_dims, rope_theta=rope_theta)
+    p = params(m=m, overlap=overlap, rope_dims=rope_dims, rope_theta=rope_theta, kv_norm=kv_norm,
+               norm_eps=norm_eps)
     if out is None:
         out = torch.empty((B, n // m, c), dtype=C_.dtype, device=C_.device)
     if want_raw and raw_out is None:
@@ -325,6 +349,78 @@ def hybrid_decode(q, qI, w, kvc, kIc, kv_raw, sink, q_pos, raw_pos0, p: CsaParam
                                _p(idx_out), C.byref(p), C.byref(p2), ws.ptr, ws.nbytes,
                                _stream()), "hybrid_decode")
     return (out, out2) if q2 is not None else out
+
+
+# -------------------------------------------------------- low precision
+
+def quantize_kv_fp8(x, out=None):
+    """[..., 512] entries (64 rotary dims) -> [..., KV_FP8_BYTES] uint8 FP8 records."""
+    rows = x.numel() // x.shape[-1]
+    if out is None:
+        out = torch.empty(tuple(x.shape[:-1]) + (KV_FP8_BYTES,), dtype=torch.uint8, device=x.device)
+    _check(lib().quantize_kv_fp8(_dt(x), rows, x.shape[-1], 64, _p(x), _p(out), _stream()),
+           "quantize_kv_fp8")
+    return out
+
+
+def quantize_index_fp4(x, out=None):
+    """[..., 128] rows -> uint8 buffer of index_fp4_bytes(rows): codes, then scale bytes."""
+    rows = x.numel() // x.shape[-1]
+    if out is None:
+        out = torch.empty(lib().index_fp4_bytes(rows), dtype=torch.uint8, device=x.device)
+    _check(lib().quantize_index_fp4(_dt(x), rows, x.shape[-1], _p(x), _p(out), _stream()),
+           "quantize_index_fp4")
+    return out
+
+
+def indexer_score_fp4(qI, w, kI4, q_pos, E, m, scores=None, ws=None):
+    """Decode scores over MXFP4 keys: qI [B,1,64,128] bf16, w [B,1,64], kI4 the
+    MXFP4 cache of B*E keys -> scores [B,1,E] (BF16 values; -inf past the
+    visible prefix)."""
+    B = qI.shape[0]
+    if scores is None:
+        scores = torch.empty((B, 1, E), dtype=torch.float32, device=qI.device)
+    ws = _ws(256, ws)
+    _check(lib().indexer_score_fp4(B, E, m, _p(qI), _p(w), _p(kI4), _p(q_pos), _p(scores), ws.ptr,
+                                   ws.nbytes, _stream()), "indexer_score_fp4")
+    return scores
+
+
+# ------------------------------------------------- grouped output projection
+
+def out_proj(o, w_g, w_o, heads_per_group=8, y=None, ws=None):
+    """o [T, H, c] bf16; w_g [G, d_g, hg*c]; w_o [d, G*d_g] -> y [T, d] bf16."""
+    T, H, c = o.shape[0], o.shape[-2], o.shape[-1]
+    T = o.numel() // (H * c)
+    d_g, d = w_g.shape[1], w_o.shape[0]
+    if y is None:
+        y = torch.empty((T, d), dtype=torch.bfloat16, device=o.device)
+    ws = _ws(lib().out_proj_ws_size(T, H, heads_per_group, d_g), ws)
+    _check(lib().out_proj(T, H, c, heads_per_group, d_g, d, _p(o), _p(w_g), _p(w_o), _p(y), ws.ptr,
+                          ws.nbytes, _stream()), "out_proj")
+    return y
+
+
+# ------------------------------------------------------- incremental decode
+
+def decode_tail_bytes(dtype, B, c, dI, p: CsaParams) -> int:
+    return lib().decode_tail_bytes(dtype, B, c, dI, C.byref(p))
+
+
+def decode_append(t, C_, Z, bias, win, tail, kvc, p: CsaParams, *, Cb=None, Zb=None, biasb=None,
+                  Ck=None, Zk=None, biask=None, Ckb=None, Zkb=None, biaskb=None, kIc=None, ws=None):
+    """One new token per sequence at positions t [B] (int64): C, Z [B, c]
+    (Ck, Zk [B, dI] for a CSA layer's indexer keys) into the window ring win
+    [B, n_win, c] and the tail; a completed block is compressed into kvc
+    [B, E_cap, c] (and kIc [B, E_cap, dI])."""
+    B, c = C_.shape
+    dI = Ck.shape[1] if Ck is not None else 0
+    E_cap = kvc.shape[1]
+    ws = _ws(256, ws)
+    _check(lib().decode_append(_dt(C_), B, c, dI, _p(t), _p(C_), _p(Z), _p(bias), _p(Cb), _p(Zb),
+                               _p(biasb), _p(Ck), _p(Zk), _p(biask), _p(Ckb), _p(Zkb), _p(biaskb),
+                               _p(win), _p(tail), _p(kvc), _p(kIc), E_cap, C.byref(p), ws.ptr,
+                               ws.nbytes, _stream()), "decode_append")
 
 
 STAGES = ["compress", "indexer", "topk", "sparse_attn", "hca_attn"]

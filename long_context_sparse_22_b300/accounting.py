@@ -118,18 +118,23 @@ def hybrid_prefill(s: dict) -> dict:
     return out
 
 
-def decode(s: dict, hca: bool) -> dict:
-    """Per-step work of one decode step (one query per sequence)."""
+def decode(s: dict, hca: bool, lowp: bool = False) -> dict:
+    """Per-step work of one decode step (one query per sequence).  lowp: the
+    low-precision caches (an FP8 KV record of (c - 64) + 64 * 2 bytes plus
+    four fp32 scales per entry, an MXFP4 key of dI / 2 bytes plus dI / 32
+    scale bytes); window rows, queries and outputs stay in the dtype."""
     B, H, c, hI, dI, k, W, t = s["B"], s["H"], s["c"], s["hI"], s["dI"], s["top_k"], s["n_win"], s["t"]
     es = 2 if s["dtype"] == "bf16" else 4
     E = s.get("E", (t + 1) // s["m"])
     nv = visible(t, s["m"], E)
     sel = min(k, nv)
     win = _window(t, W)
+    ent_b = (c - 64) + 64 * 2 + 16 if lowp else c * es        # bytes of one stored entry
+    key_b = dI // 2 + dI // 32 if lowp else dI * es            # bytes of one indexer key
     out = {"indexer_flops": B * 2 * dI * hI * nv,
-           "indexer_bytes": B * (nv * dI * es + hI * dI * es + hI * 4),
+           "indexer_bytes": B * (nv * key_b + hI * dI * es + hI * 4),
            "csa_attn_flops": B * 4 * c * H * (sel + win),
-           "csa_attn_bytes": B * ((sel + win) * c * es + 2 * H * c * es + k * 4)}
+           "csa_attn_bytes": B * (sel * ent_b + win * c * es + 2 * H * c * es + k * 4)}
     out["topk_bytes"] = B * (nv * 4 + k * 4)
     flops = out["indexer_flops"] + out["csa_attn_flops"]
     byts = out["indexer_bytes"] + out["csa_attn_bytes"]
@@ -137,7 +142,7 @@ def decode(s: dict, hca: bool) -> dict:
         E2 = s.get("E2", (t + 1) // s["m2"])
         nv2 = visible(t, s["m2"], E2)
         out["hca_attn_flops"] = B * 4 * c * H * (nv2 + win)
-        out["hca_attn_bytes"] = B * ((nv2 + win) * c * es + 2 * H * c * es)
+        out["hca_attn_bytes"] = B * (nv2 * ent_b + win * c * es + 2 * H * c * es)
         flops += out["hca_attn_flops"]
         byts += out["hca_attn_bytes"]
     out["flops"] = flops

@@ -82,6 +82,11 @@ csa_status check_params(const csa_params *p, int c, bool attn) {
     if (p->batch_invariant != 0 && p->batch_invariant != 1)
         return fail(CSA_ERR_INVALID_ARG, "batch_invariant must be 0 or 1");
     if (p->spin_limit < 0) return fail(CSA_ERR_INVALID_ARG, "spin_limit must be >= 0");
+    if (p->cache_format != CSA_CACHE_DTYPE && p->cache_format != CSA_CACHE_LOWP)
+        return fail(CSA_ERR_INVALID_ARG, "cache_format must be CSA_CACHE_DTYPE or CSA_CACHE_LOWP");
+    if (!(p->norm_eps >= 0.f) || std::isinf(p->norm_eps)) return fail(CSA_ERR_INVALID_ARG, "norm_eps must be finite and >= 0");
+    if ((p->q_norm && !al16(p->q_norm)) || (p->kv_norm && !al16(p->kv_norm)))
+        return fail(CSA_ERR_INVALID_ARG, "norm gains must be 16-byte aligned");
     if (attn) {
         if (p->n_win < 0 || p->n_win > 1024) return fail(CSA_ERR_UNSUPPORTED, "n_win=%d not in 0..1024", p->n_win);
         if (p->derotate != 0 && p->derotate != 1) return fail(CSA_ERR_INVALID_ARG, "derotate must be 0 or 1");
@@ -172,14 +177,18 @@ struct StageScope {
 
 // --------------------------------------------------------------- launchers
 
+// gain: the KV RMSNorm gains (params->kv_norm for the KV; nullptr for the
+// indexer keys, which carry no norm)
 csa_status do_compress(csa_dtype dt, int64_t B, int64_t n, int c, const void *C, const void *Z,
                        const float *bias, const void *Cb, const void *Zb, const float *biasb,
                        void *out, void *raw_out, const csa_params *p, int rope_dims,
-                       cudaStream_t st) {
+                       const float *gain, cudaStream_t st) {
     RopeFreqs rf = make_rope(c, rope_dims, p->rope_theta);
     StageScope sc(CSA_STAGE_COMPRESS, st);
+    if (gain && c / (dt == CSA_BF16 ? 8 : 4) > 256)
+        return fail(CSA_ERR_UNSUPPORTED, "the KV norm takes c <= %d", dt == CSA_BF16 ? 2048 : 1024);
     CSA_TRY_CUDA(launch_compress(dt, B, n, c, p->m, p->overlap, C, Z, bias, Cb, Zb, biasb, out,
-                                 raw_out, rf, st),
+                                 raw_out, rf, gain, p->norm_eps > 0.f ? p->norm_eps : 1e-6f, st),
                  "csa_compress launch");
     return CSA_OK;
 }
@@ -234,6 +243,9 @@ csa_status do_attn(csa_dtype dt, int64_t B, int64_t T, int H, int c, int64_t E, 
     a.m = p->m; a.n_win = p->n_win; a.derotate = p->derotate;
     a.scale = p->scale > 0.f ? p->scale : (float)(1.0 / sqrt((double)c));
     a.spin = spin_limit_of(p->spin_limit);
+    a.kv8 = p->cache_format == CSA_CACHE_LOWP;
+    a.q_norm = p->q_norm;
+    a.norm_eps = p->norm_eps > 0.f ? p->norm_eps : 1e-6f;
     a.rope = make_rope(c, p->rope_dims, p->rope_theta);
     StageScope sc(idx ? CSA_STAGE_SPARSE_ATTN : CSA_STAGE_HCA_ATTN, st);
     // the tensor-core path addresses rows of q, kvc and kv_raw with 32-bit TMA coordinates
@@ -253,6 +265,7 @@ csa_status do_attn(csa_dtype dt, int64_t B, int64_t T, int H, int c, int64_t E, 
                      "attention launch (tensor cores)");
         return CSA_OK;
     }
+    if (a.kv8) return fail(CSA_ERR_UNSUPPORTED, "FP8 entries need the tensor-core path");
     CSA_TRY_CUDA(launch_attn_simt(dt, B, a, st), "attention launch");
     return CSA_OK;
 }
@@ -266,6 +279,8 @@ csa_status check_attn_common(csa_dtype dt, int64_t B, int64_t T, int H, int c, i
     CSA_TRY(check_params(p, c, true));
     if (B < 0 || T < 0 || E < 0 || L < 0) return fail(CSA_ERR_INVALID_ARG, "negative size");
     if (H < 1 || H > 128) return fail(CSA_ERR_UNSUPPORTED, "H=%d not in 1..128", H);
+    if (p->cache_format == CSA_CACHE_LOWP && (dt != CSA_BF16 || c != 512 || p->rope_dims != 64))
+        return fail(CSA_ERR_UNSUPPORTED, "FP8 entries need bf16, c = 512 and rope_dims = 64");
     if (B * T == 0) return CSA_OK;
     CSA_TRY(need_ptr(q, "q"));
     CSA_TRY(need_ptr(q_pos, "q_pos"));
@@ -399,7 +414,7 @@ csa_status csa_compress(csa_dtype dtype, int64_t B, int64_t n, int32_t c, const 
     if (n / params->m > 0) CSA_TRY(need_ptr(out, "out"));
     if (raw_out != nullptr && !al16(raw_out)) return fail(CSA_ERR_INVALID_ARG, "raw_out is not 16-byte aligned");
     return do_compress(dtype, B, n, c, C, Z, bias, Cb, Zb, biasb, out, raw_out, params,
-                       params->rope_dims, (cudaStream_t)stream);
+                       params->rope_dims, params->kv_norm, (cudaStream_t)stream);
 }
 
 size_t indexer_score_ws_size(void) { return CSA_STATUS_BYTES; }
@@ -531,6 +546,7 @@ csa_status csa_prefill(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t
     if (hI < 1 || hI > 64) return fail(CSA_ERR_UNSUPPORTED, "hI=%d not in 1..64", hI);
     if (dI != 32 && dI != 64 && dI != 128) return fail(CSA_ERR_UNSUPPORTED, "dI=%d not in {32,64,128}", dI);
     if (params->top_k < 1 || params->top_k > 2048) return fail(CSA_ERR_UNSUPPORTED, "top_k=%d not in 1..2048", params->top_k);
+    if (params->cache_format != CSA_CACHE_DTYPE) return fail(CSA_ERR_UNSUPPORTED, "csa_prefill stores caches in dtype");
     CSA_TRY(check_ws(ws, ws_bytes, csa_prefill_ws_size(dtype, B, n, H, c, hI, dI, params)));
     if (B * n == 0) return CSA_OK;
     const char *names[] = {"C", "Z", "bias", "Ck", "Zk", "biask", "q", "qI", "w", "sink", "out"};
@@ -553,8 +569,9 @@ csa_status csa_prefill(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t
     CSA_TRY_CUDA(fill_positions((int64_t *)pos, B, n, st), "positions");
     CSA_TRY_CUDA(cudaMemsetAsync(rp0, 0, (size_t)B * 8, st), "raw_pos0");
     CSA_TRY(do_compress(dtype, B, n, c, C, Z, bias, Cb, Zb, biasb, kvc, raw, params,
-                        params->rope_dims, st));
-    CSA_TRY(do_compress(dtype, B, n, dI, Ck, Zk, biask, Ckb, Zkb, biaskb, kic, nullptr, params, 0, st));
+                        params->rope_dims, params->kv_norm, st));
+    CSA_TRY(do_compress(dtype, B, n, dI, Ck, Zk, biask, Ckb, Zkb, biaskb, kic, nullptr, params, 0,
+                        nullptr, st));
     CSA_TRY(do_indexer(dtype, B, n, hI, dI, E, params->m, qI, w, kic, (const int64_t *)pos,
                        (float *)sc, 0, status, params->spin_limit, st));
     CSA_TRY(do_topk(B, n, E, params->top_k, params->m, (const float *)sc, (const int64_t *)pos,
@@ -595,6 +612,7 @@ csa_status hca_prefill(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t
     CSA_TRY(check_c(c));
     CSA_TRY(check_params(params, c, true));
     if (params->overlap) return fail(CSA_ERR_UNSUPPORTED, "HCA compression has one branch (overlap = 0)");
+    if (params->cache_format != CSA_CACHE_DTYPE) return fail(CSA_ERR_UNSUPPORTED, "hca_prefill stores caches in dtype");
     if (B < 0 || n < 0) return fail(CSA_ERR_INVALID_ARG, "negative size");
     if (H < 1 || H > 128) return fail(CSA_ERR_UNSUPPORTED, "H=%d not in 1..128", H);
     CSA_TRY(check_ws(ws, ws_bytes, hca_prefill_ws_size(dtype, B, n, H, c, params)));
@@ -610,7 +628,7 @@ csa_status hca_prefill(csa_dtype dtype, int64_t B, int64_t n, int32_t H, int32_t
     CSA_TRY_CUDA(fill_positions((int64_t *)pos, B, n, st), "positions");
     CSA_TRY_CUDA(cudaMemsetAsync(rp0, 0, (size_t)B * 8, st), "raw_pos0");
     CSA_TRY(do_compress(dtype, B, n, c, C, Z, bias, nullptr, nullptr, nullptr, kvc, raw, params,
-                        params->rope_dims, st));
+                        params->rope_dims, params->kv_norm, st));
     return do_attn(dtype, B, n, H, c, E, 0, n, q, (const int64_t *)pos, kvc, nullptr, nullptr, raw,
                    (const int64_t *)rp0, sink, out, nullptr, params, (unsigned *)ws, asc, st);
 }
@@ -699,6 +717,8 @@ csa_status hybrid_decode(csa_dtype dtype, int64_t B, int32_t H, int32_t c, int32
     if (dI != 32 && dI != 64 && dI != 128) return fail(CSA_ERR_UNSUPPORTED, "dI=%d not in {32,64,128}", dI);
     if (params->top_k < 1 || params->top_k > 2048) return fail(CSA_ERR_UNSUPPORTED, "top_k=%d not in 1..2048", params->top_k);
     if (E > 2147483647LL) return fail(CSA_ERR_UNSUPPORTED, "E too large");
+    if (params->cache_format == CSA_CACHE_LOWP && (hI != 64 || dI != 128 || B * E > 2147483647LL))
+        return fail(CSA_ERR_UNSUPPORTED, "MXFP4 keys need hI = 64 and dI = 128");
     const bool hca = q2 != nullptr;
     if (hca) {
         CSA_TRY(check_attn_common(dtype, B, 1, H, c, E2, L, q2, q_pos, kvc2, kv_raw2, raw_pos0,
@@ -726,8 +746,15 @@ csa_status hybrid_decode(csa_dtype dtype, int64_t B, int32_t H, int32_t c, int32
     // auxiliary stream, on all but a few SMs, beside the rest of the CSA top-k
     // and the sparse attention, which need few CTAs.
     const bool concurrent = hca && dtype == CSA_BF16 && attn_tc_supported(dtype, c);
-    CSA_TRY(do_indexer(dtype, B, 1, hI, dI, E, params->m, qI, w, kIc, q_pos, (float *)sc, 0, status,
-                       params->spin_limit, st));
+    if (params->cache_format == CSA_CACHE_LOWP) {
+        StageScope si(CSA_STAGE_INDEXER, st);
+        CSA_TRY_CUDA(launch_indexer_fp4(B, E, params->m, qI, w, kIc, q_pos, (float *)sc, status,
+                                        spin_limit_of(params->spin_limit), 0, st),
+                     "indexer launch (MXFP4 keys)");
+    } else {
+        CSA_TRY(do_indexer(dtype, B, 1, hI, dI, E, params->m, qI, w, kIc, q_pos, (float *)sc, 0, status,
+                           params->spin_limit, st));
+    }
     CSA_TRY(do_topk(B, 1, E, params->top_k, params->m, (const float *)sc, q_pos, (int32_t *)idx,
                     (int32_t *)cnt, tks, st, 1));
     AuxLease ax;
@@ -756,6 +783,158 @@ csa_status hybrid_decode(csa_dtype dtype, int64_t B, int32_t H, int32_t c, int32
         CSA_TRY(do_attn(dtype, B, 1, H, c, E2, 0, L, q2, q_pos, kvc2, nullptr, nullptr, kv_raw2,
                         raw_pos0, sink2, out2, nullptr, params2, status, asc2, st));
     }
+    return CSA_OK;
+}
+
+// ------------------------------------------------------ low-precision caches
+
+size_t index_fp4_bytes(int64_t rows) { return rows < 0 ? 0 : mxfp4_bytes(rows); }
+
+csa_status quantize_kv_fp8(csa_dtype dtype, int64_t rows, int32_t c, int32_t rope_dims, const void *src,
+                           void *dst, void *stream) {
+    CSA_TRY(check_dtype(dtype));
+    if (c != 512 || rope_dims != 64) return fail(CSA_ERR_UNSUPPORTED, "FP8 records hold c = 512 with 64 rotary dims");
+    if (rows < 0) return fail(CSA_ERR_INVALID_ARG, "negative size");
+    if (rows == 0) return CSA_OK;
+    if (rows > ((int64_t)1 << 40)) return fail(CSA_ERR_UNSUPPORTED, "rows too large");
+    CSA_TRY(need_ptr(src, "src"));
+    CSA_TRY(need_ptr(dst, "dst"));
+    CSA_TRY_CUDA(launch_quant_kv_fp8(dtype, rows, src, dst, (cudaStream_t)stream), "quantize_kv_fp8 launch");
+    return CSA_OK;
+}
+
+csa_status quantize_index_fp4(csa_dtype dtype, int64_t rows, int32_t d, const void *src, void *dst,
+                              void *stream) {
+    CSA_TRY(check_dtype(dtype));
+    if (d != 128) return fail(CSA_ERR_UNSUPPORTED, "MXFP4 rows hold d = 128 values");
+    if (rows < 0) return fail(CSA_ERR_INVALID_ARG, "negative size");
+    if (rows == 0) return CSA_OK;
+    if (rows > ((int64_t)1 << 40)) return fail(CSA_ERR_UNSUPPORTED, "rows too large");
+    CSA_TRY(need_ptr(src, "src"));
+    CSA_TRY(need_ptr(dst, "dst"));
+    CSA_TRY_CUDA(launch_quant_mxfp4(dtype, rows, src, dst, (cudaStream_t)stream), "quantize_index_fp4 launch");
+    return CSA_OK;
+}
+
+csa_status indexer_score_fp4(int64_t B, int64_t E, int32_t m, const void *qI, const float *w,
+                             const void *kI4, const int64_t *q_pos, float *scores, void *ws,
+                             size_t ws_bytes, void *stream) {
+    if (B < 0 || E < 0) return fail(CSA_ERR_INVALID_ARG, "negative size");
+    if (m < 1) return fail(CSA_ERR_INVALID_ARG, "m must be >= 1");
+    if (B * E > 2147483647LL) return fail(CSA_ERR_UNSUPPORTED, "B x E too large");
+    CSA_TRY(check_ws(ws, ws_bytes, CSA_STATUS_BYTES));
+    if (B == 0 || E == 0) return CSA_OK;
+    const char *names[] = {"qI", "w", "kI4", "q_pos", "scores"};
+    const void *ptrs[] = {qI, w, kI4, q_pos, scores};
+    for (int i = 0; i < 5; i++) CSA_TRY(need_ptr(ptrs[i], names[i]));
+    cudaStream_t st = (cudaStream_t)stream;
+    StageScope sc(CSA_STAGE_INDEXER, st);
+    CSA_TRY_CUDA(launch_indexer_fp4(B, E, m, qI, w, kI4, q_pos, scores, (unsigned *)ws, DEFAULT_SPIN_LIMIT,
+                                    0, st),
+                 "indexer_score_fp4 launch");
+    CSA_TRY_CUDA(launch_mask_tail(scores, q_pos, B, E, m, st), "mask launch");
+    return CSA_OK;
+}
+
+// ------------------------------------------------- grouped output projection
+
+size_t out_proj_ws_size(int64_t T, int32_t H, int32_t heads_per_group, int32_t d_g) {
+    if (T < 0 || H < 1 || heads_per_group < 1 || d_g < 0 || H % heads_per_group) return CSA_STATUS_BYTES;
+    return CSA_STATUS_BYTES + align256((size_t)T * (H / heads_per_group) * d_g * 2);
+}
+
+csa_status out_proj(int64_t T, int32_t H, int32_t c, int32_t heads_per_group, int32_t d_g, int32_t d,
+                    const void *o, const void *w_g, const void *w_o, void *y, void *ws, size_t ws_bytes,
+                    void *stream) {
+    if (T < 0) return fail(CSA_ERR_INVALID_ARG, "negative size");
+    if (H < 1 || c < 1 || heads_per_group < 1 || H % heads_per_group)
+        return fail(CSA_ERR_INVALID_ARG, "H=%d must be a multiple of heads_per_group=%d", H, heads_per_group);
+    const int G = H / heads_per_group;
+    const int64_t kin = (int64_t)heads_per_group * c;
+    if (d_g < 256 || d_g % 256 || d < 256 || d % 256)
+        return fail(CSA_ERR_UNSUPPORTED, "d_g=%d and d=%d must be positive multiples of 256", d_g, d);
+    if (kin % 64 || kin > (1 << 20) || (int64_t)G * d_g > (1 << 20))
+        return fail(CSA_ERR_UNSUPPORTED, "heads_per_group * c = %lld must be a multiple of 64", (long long)kin);
+    CSA_TRY(check_ws(ws, ws_bytes, out_proj_ws_size(T, H, heads_per_group, d_g)));
+    if (T == 0) return CSA_OK;
+    const char *names[] = {"o", "w_g", "w_o", "y"};
+    const void *ptrs[] = {o, w_g, w_o, y};
+    for (int i = 0; i < 4; i++) CSA_TRY(need_ptr(ptrs[i], names[i]));
+    cudaStream_t st = (cudaStream_t)stream;
+    void *u = (char *)ws + CSA_STATUS_BYTES;
+    unsigned *status = (unsigned *)ws;
+    CSA_TRY_CUDA(launch_gemm_bf16(T, d_g, (int)kin, G, o, w_g, u, status, DEFAULT_SPIN_LIMIT, st),
+                 "out_proj group stage");
+    CSA_TRY_CUDA(launch_gemm_bf16(T, d, G * d_g, 1, u, w_o, y, status, DEFAULT_SPIN_LIMIT, st),
+                 "out_proj final stage");
+    return CSA_OK;
+}
+
+// ------------------------------------------------------ incremental decode
+
+size_t decode_tail_bytes(csa_dtype dtype, int64_t B, int32_t c, int32_t dI,
+                         const csa_params *params) {
+    if (params == nullptr || B < 0 || c < 0 || dI < 0 || params->m < 1) return 0;
+    return (size_t)B * decode_tail_slots(params->m, params->overlap) *
+           decode_tail_width(c, dI, params->overlap) * esize(dtype);
+}
+
+csa_status decode_append(csa_dtype dtype, int64_t B, int32_t c, int32_t dI, const int64_t *t,
+                         const void *C, const void *Z, const float *bias, const void *Cb,
+                         const void *Zb, const float *biasb, const void *Ck, const void *Zk,
+                         const float *biask, const void *Ckb, const void *Zkb,
+                         const float *biaskb, void *win, void *tail, void *kvc, void *kIc,
+                         int64_t E_cap, const csa_params *params, void *ws, size_t ws_bytes,
+                         void *stream) {
+    CSA_TRY(check_dtype(dtype));
+    const int vec = dtype == CSA_BF16 ? 8 : 4;
+    if (c < vec || c % vec != 0 || c / vec > 256)
+        return fail(CSA_ERR_UNSUPPORTED, "c=%d must be a multiple of %d, at most %d", c, vec, 256 * vec);
+    CSA_TRY(check_params(params, c, false));
+    if (params->m > 128) return fail(CSA_ERR_UNSUPPORTED, "m=%d: the tail holds at most 128 slots", params->m);
+    if (params->n_win < 0 || params->n_win > 1024) return fail(CSA_ERR_UNSUPPORTED, "n_win=%d not in 0..1024", params->n_win);
+    const bool keys = Ck != nullptr;
+    if (keys && (dI < vec || dI % vec != 0 || dI / vec > 256))
+        return fail(CSA_ERR_UNSUPPORTED, "dI=%d must be a multiple of %d, at most %d", dI, vec, 256 * vec);
+    if (!keys) dI = 0;
+    if (B < 0 || E_cap < 0) return fail(CSA_ERR_INVALID_ARG, "negative size");
+    if (B > 2147483647LL) return fail(CSA_ERR_UNSUPPORTED, "B too large");
+    CSA_TRY(check_ws(ws, ws_bytes, CSA_STATUS_BYTES));
+    if (B == 0) return CSA_OK;
+    const char *names[] = {"t", "C", "Z", "bias", "tail", "kvc"};
+    const void *ptrs[] = {t, C, Z, bias, tail, kvc};
+    for (int i = 0; i < 6; i++) CSA_TRY(need_ptr(ptrs[i], names[i]));
+    if (params->n_win > 0) CSA_TRY(need_ptr(win, "win"));
+    if (keys) {
+        CSA_TRY(need_ptr(Zk, "Zk"));
+        CSA_TRY(need_ptr(biask, "biask"));
+        CSA_TRY(need_ptr(kIc, "kIc"));
+    }
+    if (params->overlap) {
+        CSA_TRY(need_ptr(Cb, "Cb"));
+        CSA_TRY(need_ptr(Zb, "Zb"));
+        CSA_TRY(need_ptr(biasb, "biasb"));
+        if (keys) {
+            CSA_TRY(need_ptr(Ckb, "Ckb"));
+            CSA_TRY(need_ptr(Zkb, "Zkb"));
+            CSA_TRY(need_ptr(biaskb, "biaskb"));
+        }
+    }
+    DecodeAppend d;
+    d.C = C; d.Z = Z; d.Cb = params->overlap ? Cb : nullptr; d.Zb = params->overlap ? Zb : nullptr;
+    d.Ck = keys ? Ck : nullptr; d.Zk = keys ? Zk : nullptr;
+    d.Ckb = keys && params->overlap ? Ckb : nullptr; d.Zkb = keys && params->overlap ? Zkb : nullptr;
+    d.bias = bias; d.biasb = biasb; d.biask = biask; d.biaskb = biaskb;
+    d.t = t; d.win = win; d.tail = tail; d.kvc = kvc; d.kIc = kIc;
+    d.status = (unsigned *)ws;
+    d.E_cap = E_cap; d.c = c; d.dI = dI; d.m = params->m; d.overlap = params->overlap;
+    d.n_win = params->n_win;
+    d.kv_norm = params->kv_norm;
+    d.norm_eps = params->norm_eps > 0.f ? params->norm_eps : 1e-6f;
+    d.rope = make_rope(c, params->rope_dims, params->rope_theta);
+    cudaStream_t st = (cudaStream_t)stream;
+    StageScope sc(CSA_STAGE_COMPRESS, st);
+    CSA_TRY_CUDA(launch_decode_append(dtype, B, d, st), "decode_append launch");
     return CSA_OK;
 }
 

@@ -39,8 +39,21 @@ attn_simt_kernel(AttnArgs a) {
     const int64_t t = a.q_pos[bt];
     const T *q = (const T *)a.q + (bt * a.H + h0) * (int64_t)c;
 
-    // q rows -> shared float, rotated at t and scaled
-    for (int i = tid; i < hg * c; i += AT_THREADS) qs[i] = to_f(q[i]) * a.scale;
+    // q rows -> shared float (RMSNorm per head when asked), rotated at t and scaled
+    if (a.q_norm) {
+        for (int i = tid; i < hg * c; i += AT_THREADS) qs[i] = to_f(q[i]);
+        __syncthreads();
+        for (int h = warp; h < hg; h += AT_THREADS / 32) {
+            float ss = 0.f;
+            for (int ch = lane; ch < c; ch += 32) ss = fmaf(qs[h * c + ch], qs[h * c + ch], ss);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            const float rs = 1.0f / sqrtf(ss / (float)c + a.norm_eps);
+            for (int ch = lane; ch < c; ch += 32) qs[h * c + ch] = qs[h * c + ch] * rs * a.q_norm[ch] * a.scale;
+        }
+    } else {
+        for (int i = tid; i < hg * c; i += AT_THREADS) qs[i] = to_f(q[i]) * a.scale;
+    }
     __syncthreads();
     const int pairs = a.rope.pairs;
     for (int i = tid; i < hg * pairs; i += AT_THREADS) {

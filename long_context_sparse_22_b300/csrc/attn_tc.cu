@@ -64,7 +64,7 @@ struct AtCfg {
     static constexpr int OFF_Q = OFF_K + 2 * K_BYTES;
     static constexpr int OFF_P = OFF_Q + Q_BYTES;
     static constexpr int OFF_MISC = OFF_P + 2 * P_BYTES;
-    static constexpr int MISC_BYTES = 6144;
+    static constexpr int MISC_BYTES = 8192;
     static constexpr int SMEM = OFF_MISC + MISC_BYTES + 1024;   // + alignment slack
     static constexpr int S_COL = 0;               // two S buffers: cols 0, 64
     static constexpr int O_COL = 128;             // O^T chunks: 128 + 64 c
@@ -79,6 +79,7 @@ struct AtCfg {
 
 struct AttnTcArgs {
     const __nv_bfloat16 *kvc;
+    const uint8_t *kv8;      // FP8 records of the compressed entries (the KV8 variant), or nullptr
     const void *zsrc;        // any valid 16-byte-aligned address (source of zero-filled copies)
     const int64_t *q_pos;
     const int32_t *idx;      // [B,T,k] or nullptr: every visible entry
@@ -95,13 +96,19 @@ struct AttnTcArgs {
     int chunk_tiles;         // > 0: split mode with this many tiles per item
     int n_chunks;
     int64_t n_items;
+    int qpi;                 // queries packed into one item's 64 rows (64 / H; 1 = one query)
+    int64_t tq_blocks;       // query blocks per sequence: ceil(T / qpi)
     long long spin;          // polls before a wait between roles gives up
+    const float *q_norm;     // RMSNorm gains of q (C floats) or nullptr
+    float norm_eps;
     float scale_log2;        // logit scale * log2(e)
     RopeFreqs rope;
 };
 
 struct ItemInfo {
-    int64_t bt, b, t;
+    int64_t bt, b, t;        // first query row of the item, its sequence, its largest position
+    int64_t tmin;            // smallest query position of the item
+    int nq;                  // queries in the item (> 1 only when queries are packed)
     int hg, chunk;
     int64_t ncomp;           // compressed slots (tiles 0 .. ntc-1)
     int64_t p0, nwin;        // window rows p0 .. p0+nwin-1 (tiles ntc ..)
@@ -117,13 +124,30 @@ __device__ __forceinline__ void item_info(const AttnTcArgs &a, int64_t it, ItemI
         r /= a.n_chunks;
     }
     f.hg = (int)(r % a.n_hg);
-    f.bt = r / a.n_hg;
-    f.b = f.bt / a.T;
-    f.t = a.q_pos[f.bt];
+    if (a.qpi == 1) {
+        f.bt = r / a.n_hg;
+        f.b = f.bt / a.T;
+        f.t = a.q_pos[f.bt];
+        f.tmin = f.t;
+        f.nq = 1;
+    } else {
+        // qpi consecutive queries of one sequence share the item (dense lists only)
+        const int64_t qb = r / a.n_hg;
+        f.b = qb / a.tq_blocks;
+        const int64_t i0 = (qb % a.tq_blocks) * a.qpi;
+        f.bt = f.b * a.T + i0;
+        f.nq = (int)(a.T - i0 < a.qpi ? a.T - i0 : a.qpi);
+        f.t = f.tmin = a.q_pos[f.bt];
+        for (int q = 1; q < f.nq; q++) {
+            const int64_t tq = a.q_pos[f.bt + q];
+            f.t = tq > f.t ? tq : f.t;
+            f.tmin = tq < f.tmin ? tq : f.tmin;
+        }
+    }
     if (a.idx) f.ncomp = a.cnt ? a.cnt[f.bt] : a.k;
     else f.ncomp = visible_count(f.t, a.m, a.E);
     if (f.ncomp < 0) f.ncomp = 0;
-    int64_t p0 = f.t - a.n_win + 1;
+    int64_t p0 = f.tmin - a.n_win + 1;     // the union of the item's windows
     if (p0 < 0) p0 = 0;
     f.p0 = p0;
     f.nwin = a.n_win > 0 && f.t >= 0 ? f.t - p0 + 1 : 0;
@@ -220,7 +244,37 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32
                  : "memory");
 }
 
-template <int C>
+// 16 E4M3 codes times their group scale -> two 16-byte chunks of 8 bf16 each
+// (the code is exact in f16; the scaled value is rounded once to bf16).
+__device__ __forceinline__ void fp8x16_to_bf16(const uint4 g, float sc, uint32_t *o) {
+    const uint32_t w[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+    for (int q = 0; q < 4; q++)
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+            const uint16_t pair = (uint16_t)(w[q] >> (16 * hh));
+            uint32_t h2;
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+            o[2 * q + hh] = *reinterpret_cast<const uint32_t *>(&b2);
+        }
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+template <int C, bool KV8, bool PACK>
 __global__ void __launch_bounds__(AtCfg<C>::THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
                const __grid_constant__ CUtensorMap tm_w,
@@ -244,6 +298,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     float *inv_den_s = (float *)(misc + 1024);         // [64]
     float *cs_s = (float *)(misc + 2048);              // [2][256]: cos, sin of the query angle
     const __nv_bfloat16 **rowp = (const __nv_bfloat16 **)(misc + 4096);   // [2][64] gathered rows
+    float *gain_s = (float *)(misc + 6144);            // [C] RMSNorm gains of q
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x;
@@ -269,6 +324,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tc::prefetch_tmap(&tm_w);
     }
     if (warp == Cfg::MMA_WARP) tc::tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    if (a.q_norm)
+        for (int i = threadIdx.x; i < C; i += Cfg::THREADS) gain_s[i] = a.q_norm[i];
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -297,11 +354,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             // the cos / sin of this item's angle and its first selected indices,
             // worked out while the previous item's last QK still reads q
-            for (int pi = tid; pi < a.rope.pairs; pi += Cfg::NLOAD) {
+            // (one set of angles per packed query: query q's pair pi at q * pairs + pi)
+            for (int i = tid; i < a.qpi * a.rope.pairs; i += Cfg::NLOAD) {
+                const int q = i / a.rope.pairs, pi = i - q * a.rope.pairs;
+                const int64_t tq = q == 0 ? (a.qpi == 1 ? f.t : a.q_pos[f.bt]) : (q < f.nq ? a.q_pos[f.bt + q] : f.t);
                 float c_, s_;
-                rope_cos_sin((double)f.t, a.rope.w[pi], c_, s_);
-                cs_s[pi] = c_;
-                cs_s[256 + pi] = s_;
+                rope_cos_sin((double)tq, a.rope.w[pi], c_, s_);
+                cs_s[i] = c_;
+                cs_s[256 + i] = s_;
             }
             int32_t iv = -1;                     // selected index of this thread's slot, next tile
             if (a.idx && tid < 64 && f.j0 < f.ntc) {
@@ -328,11 +388,46 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (named_bar_or(2, Cfg::NLOAD, !warp_wait(qland, ii & 1, a.status, abort_flag, a.spin)))
                     return false;
                 if (tid == 0) q_pending = 0;
+                if (a.q_norm) {
+                    // RMSNorm of each head's row before its rotation: two threads per
+                    // head (adjacent lanes), each over half of the row's 16-byte chunks
+                    const int h = tid >> 1, hf = tid & 1;
+                    constexpr int CH = C / 16;           // chunks per half row
+                    uint8_t *hb = sQ + (h >> 3) * 1024;
+                    float ss = 0.f;
+#pragma unroll 4
+                    for (int k = 0; k < CH; k++) {
+                        const int d0 = (hf * CH + k) * 8;
+                        const uint4 u = *reinterpret_cast<const uint4 *>(hb + (d0 >> 6) * (Cfg::HG * 128) +
+                                                                         swz128(h, (d0 & 63) * 2));
+                        float f[8];
+                        Vec<__nv_bfloat16>::unpack(u, f);
+#pragma unroll
+                        for (int e = 0; e < 8; e++) ss = fmaf(f[e], f[e], ss);
+                    }
+                    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                    const float rs = 1.0f / sqrtf(ss / (float)C + a.norm_eps);
+#pragma unroll 4
+                    for (int k = 0; k < CH; k++) {
+                        const int d0 = (hf * CH + k) * 8;
+                        uint4 *pu = reinterpret_cast<uint4 *>(hb + (d0 >> 6) * (Cfg::HG * 128) +
+                                                              swz128(h, (d0 & 63) * 2));
+                        float f[8];
+                        Vec<__nv_bfloat16>::unpack(*pu, f);
+#pragma unroll
+                        for (int e = 0; e < 8; e++) f[e] = f[e] * rs * gain_s[d0 + e];
+                        uint4 o;
+                        __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(&o);
+#pragma unroll
+                        for (int e = 0; e < 4; e++) o2[e] = __floats2bfloat162_rn(f[2 * e], f[2 * e + 1]);
+                        *pu = o;
+                    }
+                    named_bar(2, Cfg::NLOAD);
+                }
                 const int np = a.rope.pairs;
                 if (np == 32) {
                     // one pair per lane, heads warp, warp + 4, ...: all loads in flight at once
                     const int d = a.rope.first + 2 * lane;
-                    const float c_ = cs_s[lane], s_ = cs_s[256 + lane];
                     uint8_t *qa = sQ + (d >> 6) * (Cfg::HG * 128);
                     __nv_bfloat162 x[Cfg::HG / 4];
 #pragma unroll
@@ -343,6 +438,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                     for (int k = 0; k < Cfg::HG / 4; k++) {
                         const int h = warp + 4 * k;
+                        const int ci = PACK && a.qpi > 1 ? (h / a.H) * 32 + lane : lane;
+                        const float c_ = cs_s[ci], s_ = cs_s[256 + ci];
                         const float2 v = __bfloat1622float2(x[k]);
                         *(__nv_bfloat162 *)(qa + (h >> 3) * 1024 + swz128(h, (d & 63) * 2)) =
                             __floats2bfloat162_rn(v.x * c_ - v.y * s_, v.x * s_ + v.y * c_);
@@ -354,7 +451,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         __nv_bfloat162 *pv = (__nv_bfloat162 *)(sQ + (d >> 6) * (Cfg::HG * 128) +
                                                                 (h >> 3) * 1024 + swz128(h, (d & 63) * 2));
                         const float2 v = __bfloat1622float2(*pv);
-                        const float c_ = cs_s[pi], s_ = cs_s[256 + pi];
+                        const int ci = (PACK && a.qpi > 1 ? (h / a.H) * np : 0) + pi;
+                        const float c_ = cs_s[ci], s_ = cs_s[256 + ci];
                         *pv = __floats2bfloat162_rn(v.x * c_ - v.y * s_, v.x * s_ + v.y * c_);
                     }
                 }
@@ -365,7 +463,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             };
             for (int j = f.j0; j < f.j1; j++, g++) {
                 const int buf = g & 1;
-                const bool gather = j < f.ntc && a.idx;
+                // compressed tiles are gathered row by row: selected entries, and with
+                // FP8 entries every compressed tile (its rows are dequantised here)
+                const bool gather = j < f.ntc && (a.idx || KV8);
                 // a gathered tile's row addresses go to shared memory before the wait
                 // for its buffer (the barrier that ends the wait publishes them; the
                 // gather two tiles back, the last reader of this slot, has been issued)
@@ -373,9 +473,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (gather && tid < 64) {
                     const int64_t pos = (int64_t)j * 64 + tid;
                     const bool in = pos < f.ncomp;
-                    const bool v = in && iv >= 0 && iv < a.E;
-                    if (in && !v && iv != -1) atomicOr(a.status, ST_BAD_INDEX);
-                    rowp[buf * 64 + tid] = v ? a.kvc + (f.b * a.E + iv) * (int64_t)C : nullptr;
+                    const int64_t ent = a.idx ? (int64_t)iv : pos;
+                    const bool v = in && ent >= 0 && ent < a.E;
+                    if (a.idx && in && !v && iv != -1) atomicOr(a.status, ST_BAD_INDEX);
+                    if constexpr (KV8)
+                        rowp[buf * 64 + tid] = v ? reinterpret_cast<const __nv_bfloat16 *>(
+                                                       a.kv8 + (f.b * a.E + ent) * (int64_t)KV8_BYTES)
+                                                 : nullptr;
+                    else
+                        rowp[buf * 64 + tid] = v ? a.kvc + (f.b * a.E + ent) * (int64_t)C : nullptr;
                     bal = __ballot_sync(0xffffffffu, v);
                 }
                 if (named_bar_or(2, Cfg::NLOAD,
@@ -389,9 +495,49 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     // the presence mask is written once the softmax two tiles back is done with it
                     if (tid < 64 && lane == 0) vmask32[buf * 2 + warp] = bal;
                     // the next tile's selected indices, fetched while this one loads
-                    if (tid < 64 && j + 1 < f.j1 && j + 1 < f.ntc) {
+                    if (a.idx && tid < 64 && j + 1 < f.j1 && j + 1 < f.ntc) {
                         const int64_t pos = (int64_t)(j + 1) * 64 + tid;
                         iv = pos < f.ncomp ? a.idx[f.bt * a.k + pos] : -1;
+                    }
+                    if constexpr (KV8) {
+                        // FP8 records: two threads per row, each loading 14 granules of
+                        // codes, 4 of rotary BF16 values and the group scales, then writing
+                        // the row's bf16 chunks into the swizzled tile (zeros for rows
+                        // that are not in the list)
+                        const int r = tid >> 1, half = tid & 1;
+                        const uint8_t *src = reinterpret_cast<const uint8_t *>(rowp[buf * 64 + r]);
+                        uint4 g8[14], g16[4], gs = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                        for (int q = 0; q < 14; q++)
+                            g8[q] = src ? ld_nc_v4(src + (half * 14 + q) * 16) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                        for (int q = 0; q < 4; q++)
+                            g16[q] = src ? ld_nc_v4(src + KV8_NR + (half * 4 + q) * 16) : make_uint4(0, 0, 0, 0);
+                        if (src) gs = ld_nc_v4(src + KV8_NR + 128);
+                        if (j == f.j0 && !rope_q()) {
+                            ok = false;
+                            break;
+                        }
+                        const float scl[4] = {__uint_as_float(gs.x), __uint_as_float(gs.y),
+                                              __uint_as_float(gs.z), __uint_as_float(gs.w)};
+                        const uint32_t rb = kb + (r >> 3) * 1024;
+#pragma unroll
+                        for (int q = 0; q < 14; q++) {
+                            const int gidx = half * 14 + q;      // dims 16 gidx .. 16 gidx + 15
+                            uint32_t o[8];
+                            fp8x16_to_bf16(g8[q], scl[gidx >> 3], o);
+                            const uint32_t ab = rb + (gidx >> 2) * Cfg::ATOM;
+                            const int c0 = (gidx & 3) * 2;
+                            sts_v4(ab + swz128(r, c0 * 16), o[0], o[1], o[2], o[3]);
+                            sts_v4(ab + swz128(r, (c0 + 1) * 16), o[4], o[5], o[6], o[7]);
+                        }
+#pragma unroll
+                        for (int q = 0; q < 4; q++)      // dims 448 + 8 k .. : chunk k of the last atom
+                            sts_v4(rb + (Cfg::NA - 1) * Cfg::ATOM + swz128(r, (half * 4 + q) * 16), g16[q].x,
+                                   g16[q].y, g16[q].z, g16[q].w);
+                        fence_proxy_async();
+                        tc::mbar_arrive(&kfull[buf]);
+                        continue;
                     }
                     constexpr int GR = C / 8;            // 16-byte granules per row
                     const int gr = tid % GR;
@@ -581,16 +727,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             have_fn = false;
             if (f.j0 >= f.j1) continue;
             const int h0 = f.hg * Cfg::HG;
+            const bool packed = PACK && a.qpi > 1;   // rows are (query, head) pairs of f.nq queries
             bool real[2];
             float m_run[2], l_run[2];
+            int64_t t_r[2], nv_r[2];             // packed: the row's query position and visible entries
 #pragma unroll
             for (int u = 0; u < 2; u++) {
-                real[u] = h0 + hr[u] < a.H;
-                if (f.hg != zl_hg) zl2[u] = real[u] ? a.sink[h0 + hr[u]] * 1.4426950408889634f : -INFINITY;
+                if (packed) {
+                    const int q = hr[u] / a.H;
+                    real[u] = q < f.nq;
+                    t_r[u] = real[u] ? a.q_pos[f.bt + q] : f.t;
+                    nv_r[u] = visible_count(t_r[u], a.m, a.E);
+                    zl2[u] = a.sink[hr[u] % a.H] * 1.4426950408889634f;
+                } else {
+                    real[u] = h0 + hr[u] < a.H;
+                    t_r[u] = f.t;
+                    nv_r[u] = 0;
+                    if (f.hg != zl_hg) zl2[u] = real[u] ? a.sink[h0 + hr[u]] * 1.4426950408889634f : -INFINITY;
+                }
                 m_run[u] = a.chunk_tiles > 0 ? -INFINITY : zl2[u];
                 l_run[u] = 0.f;
             }
-            zl_hg = f.hg;
+            zl_hg = packed ? -1 : f.hg;
             const uint32_t gfirst = g;
             bool fail = false;
             for (int j = f.j0; j < f.j1; j++, g++) {
@@ -630,8 +788,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         const int ent = 8 * i + 2 * t4 + e;
                         const uint32_t bit = ent < 32 ? (mlo >> ent) & 1u : (mhi >> (ent - 32)) & 1u;
 #pragma unroll
-                        for (int u = 0; u < 2; u++)
-                            v[u][2 * i + e] = bit ? __uint_as_float(raw[4 * i + 2 * u + e]) * a.scale_log2 : -INFINITY;
+                        for (int u = 0; u < 2; u++) {
+                            bool vis = bit != 0;
+                            if (packed) {        // the row's own list: its visible entries, its window
+                                if (j < f.ntc) {
+                                    vis = vis && (int64_t)j * 64 + ent < nv_r[u];
+                                } else {
+                                    const int64_t pw = f.p0 + (int64_t)(j - f.ntc) * 64 + ent;
+                                    vis = vis && pw <= t_r[u] && pw > t_r[u] - a.n_win;
+                                }
+                            }
+                            v[u][2 * i + e] = vis ? __uint_as_float(raw[4 * i + 2 * u + e]) * a.scale_log2 : -INFINITY;
+                        }
                     }
                 bool need[2];
                 float alpha[2];
@@ -711,7 +879,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             float dcr = 1.f, dsr = 0.f;
             {
                 const int dlast = (Cfg::NC - 1) * 128 + quarter * 32 + lane;
-                if (a.chunk_tiles == 0 && a.derotate && dlast >= a.rope.first)
+                if (!packed && a.chunk_tiles == 0 && a.derotate && dlast >= a.rope.first)
                     rope_cos_sin(-(double)f.t, a.rope.w[(dlast - a.rope.first) >> 1], dcr, dsr);
             }
             // item end: the four threads of a head add their partial sums
@@ -739,7 +907,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const bool ok = warp_wait(ofull, ii & 1, a.status, abort_flag, a.spin);
             if (named_bar_or(1, 128, !ok)) break;
             tc::fence_after_sync();
-            const int nh = a.H - h0 < 64 ? a.H - h0 : 64;
+            const int nh = packed ? f.nq * a.H : (a.H - h0 < 64 ? a.H - h0 : 64);
             const int dl = quarter * 32 + lane;                 // dim within a chunk
             for (int c = 0; c < Cfg::NC; c++) {
                 const int d = c * 128 + dl;
@@ -747,7 +915,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 float cr = 1.f, sr = 0.f;
                 const bool rot_w = a.chunk_tiles == 0 && a.derotate && c * 128 + quarter * 32 + 31 >= a.rope.first;
                 const bool rot = d >= a.rope.first;
-                if (rot_w && rot) {
+                if (rot_w && rot && !packed) {
                     if (c == Cfg::NC - 1) {
                         cr = dcr;
                         sr = dsr;
@@ -755,7 +923,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         rope_cos_sin(-(double)f.t, a.rope.w[(d - a.rope.first) >> 1], cr, sr);
                     }
                 }
-                const float sgn = (lane & 1) ? sr : -sr;
+                float sgn = (lane & 1) ? sr : -sr;
 #pragma unroll 1
                 for (int hb = 0; hb < 64; hb += 32) {
                     float o[32];
@@ -778,7 +946,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         o[4 * q4 + 2] *= iv4.z;
                         o[4 * q4 + 3] *= iv4.w;
                     }
-                    if (rot_w) {
+                    if (rot_w && packed) {
+                        // rows hb .. hb + 31 hold at most two queries (H >= 16): each
+                        // row is rotated back by its own query's position
+                        const int q0 = hb / a.H, q1 = (hb + 31) / a.H;
+                        float cr0 = 1.f, sr0 = 0.f, cr1 = 1.f, sr1 = 0.f;
+                        if (rot) {
+                            const double w_ = a.rope.w[(d - a.rope.first) >> 1];
+                            rope_cos_sin(-(double)(q0 < f.nq ? a.q_pos[f.bt + q0] : f.t), w_, cr0, sr0);
+                            rope_cos_sin(-(double)(q1 < f.nq ? a.q_pos[f.bt + q1] : f.t), w_, cr1, sr1);
+                        }
+#pragma unroll
+                        for (int h = 0; h < 32; h++) {
+                            const float op = __shfl_xor_sync(0xffffffffu, o[h], 1);
+                            const bool second = (hb + h) / a.H != q0;
+                            const float crh = second ? cr1 : cr0, srh = second ? sr1 : sr0;
+                            if (rot) o[h] = o[h] * crh + op * ((lane & 1) ? srh : -srh);
+                        }
+                    } else if (rot_w) {
 #pragma unroll
                         for (int h = 0; h < 32; h++) {
                             const float op = __shfl_xor_sync(0xffffffffu, o[h], 1);
@@ -935,11 +1120,12 @@ int attn_tc_chunks(int64_t rows, int H, int64_t max_list, bool invariant) {
     return (int)((tiles + per - 1) / per);
 }
 
-template <int C>
+template <int C, bool KV8, bool PACK>
 static cudaError_t launch_attn_tc_c(int64_t B, const AttnArgs &g, const int32_t *cnt, int n_chunks,
                                     void *split_ws, int max_ctas, cudaStream_t st) {
     AttnTcArgs a;
-    a.kvc = (const __nv_bfloat16 *)g.kvc;
+    a.kvc = KV8 ? nullptr : (const __nv_bfloat16 *)g.kvc;
+    a.kv8 = KV8 ? (const uint8_t *)g.kvc : nullptr;
     a.zsrc = g.q;
     a.q_pos = g.q_pos;
     a.idx = g.idx;
@@ -953,10 +1139,19 @@ static cudaError_t launch_attn_tc_c(int64_t B, const AttnArgs &g, const int32_t 
     a.H = g.H; a.k = g.k; a.m = g.m; a.n_win = g.n_win; a.derotate = g.derotate;
     a.n_hg = (g.H + 63) / 64;
     a.spin = g.spin;
+    a.q_norm = g.q_norm;
+    a.norm_eps = g.norm_eps;
     a.scale_log2 = g.scale * 1.4426950408889634f;
     a.rope = g.rope;
-    const int64_t max_list = (g.idx ? (int64_t)g.k : g.E) + g.n_win;
     const int64_t rows = B * g.Tq;
+    // dense lists with 16 or 32 heads: 64 / H consecutive queries share an item,
+    // their (query, head) pairs on the 64 rows, the union of their lists read once
+    a.qpi = (PACK && !g.idx && (g.H == 16 || g.H == 32) && g.Tq >= 64 / g.H && n_chunks <= 1 &&
+             (64 / g.H) * g.rope.pairs <= 256)
+                ? 64 / g.H
+                : 1;
+    a.tq_blocks = (g.Tq + a.qpi - 1) / a.qpi;
+    const int64_t max_list = (g.idx ? (int64_t)g.k : g.E) + g.n_win + (a.qpi - 1);
     const int64_t max_tiles = (max_list + 63) / 64 + 1;
     if (n_chunks > 1 && split_ws) {
         a.n_chunks = n_chunks;
@@ -969,13 +1164,13 @@ static cudaError_t launch_attn_tc_c(int64_t B, const AttnArgs &g, const int32_t 
         a.part_o = nullptr;
         a.part_ml = nullptr;
     }
-    a.n_items = rows * a.n_hg * a.n_chunks;
+    a.n_items = (a.qpi > 1 ? B * a.tq_blocks : rows) * a.n_hg * a.n_chunks;
     using Cfg = AtCfg<C>;
     // tensor maps: q rows [B*T*H, C]; compressed entries [B*E, C] and raw
     // window rows [B*L, C] as 64-row boxes (a map that is never read points
     // at q).
     CUtensorMap tq, tcmp, tw;
-    const bool have_c = g.E > 0 && g.kvc != nullptr;
+    const bool have_c = g.E > 0 && g.kvc != nullptr && !KV8;
     const bool have_w = g.L > 0 && g.kv_raw != nullptr;
     if (!make_tmap_bf16_2d(&tq, g.q, (uint64_t)(rows * g.H), C, 64) ||
         !make_tmap_bf16_2d(&tcmp, have_c ? g.kvc : g.q, have_c ? (uint64_t)(B * g.E) : (uint64_t)(rows * g.H),
@@ -985,12 +1180,12 @@ static cudaError_t launch_attn_tc_c(int64_t B, const AttnArgs &g, const int32_t 
         return cudaErrorInvalidValue;
     static PerDevice attr;
     {
-        cudaError_t e = smem_limit_once(attr, (const void *)attn_tc_kernel<C>, Cfg::SMEM);
+        cudaError_t e = smem_limit_once(attr, (const void *)attn_tc_kernel<C, KV8, PACK>, Cfg::SMEM);
         if (e != cudaSuccess) return e;
     }
     const int sms = max_ctas > 0 && max_ctas < device_sms() ? max_ctas : device_sms();
     const int grid = (int)(a.n_items < sms ? a.n_items : sms);
-    attn_tc_kernel<C><<<grid, Cfg::THREADS, Cfg::SMEM, st>>>(tq, tcmp, tw, a);
+    attn_tc_kernel<C, KV8, PACK><<<grid, Cfg::THREADS, Cfg::SMEM, st>>>(tq, tcmp, tw, a);
     count_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.chunk_tiles == 0) return e;
@@ -1002,8 +1197,13 @@ static cudaError_t launch_attn_tc_c(int64_t B, const AttnArgs &g, const int32_t 
 cudaError_t launch_attn_tc(int64_t B, const AttnArgs &g, const int32_t *cnt, int n_chunks,
                            void *split_ws, int max_ctas, cudaStream_t st) {
     if (B * g.Tq == 0) return cudaSuccess;
-    if (g.c == 128) return launch_attn_tc_c<128>(B, g, cnt, n_chunks, split_ws, max_ctas, st);
-    if (g.c == 512) return launch_attn_tc_c<512>(B, g, cnt, n_chunks, split_ws, max_ctas, st);
+    if (g.kv8) {
+        if (g.c != 512) return cudaErrorInvalidValue;
+        return launch_attn_tc_c<512, true, false>(B, g, cnt, n_chunks, split_ws, max_ctas, st);
+    }
+    // queries are packed on the c = 128 kernel (the 16-head dense layer); c = 512 takes one query
+    if (g.c == 128) return launch_attn_tc_c<128, false, true>(B, g, cnt, n_chunks, split_ws, max_ctas, st);
+    if (g.c == 512) return launch_attn_tc_c<512, false, false>(B, g, cnt, n_chunks, split_ws, max_ctas, st);
     return cudaErrorInvalidValue;
 }
 

@@ -326,6 +326,14 @@ __global__ void mask_tail_kernel(float *scores, const int64_t *q_pos, int64_t ro
         scores[row * E + j] = -INFINITY;
 }
 
+cudaError_t launch_mask_tail(float *scores, const int64_t *q_pos, int64_t rows, int64_t E, int m, cudaStream_t st) {
+    if (rows == 0 || E == 0) return cudaSuccess;
+    dim3 g(8, (unsigned)(rows < 65535 ? rows : 65535), (unsigned)((rows + 65534) / 65535));
+    mask_tail_kernel<<<g, 256, 0, st>>>(scores, q_pos, rows, E, m);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------- host
 
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -404,11 +412,7 @@ cudaError_t launch_indexer_tc(int64_t B, int64_t T, int64_t E, int m, const void
         e = launch_tc<4>(tq, tk, a, grid, st);
     }
     if (e != cudaSuccess || !write_masked) return e;
-    const int64_t rows = B * T;
-    dim3 g(8, (unsigned)(rows < 65535 ? rows : 65535), (unsigned)((rows + 65534) / 65535));
-    mask_tail_kernel<<<g, 256, 0, st>>>(scores, q_pos, rows, E, m);
-    count_launches(1);
-    return cudaGetLastError();
+    return launch_mask_tail(scores, q_pos, B * T, E, m, st);
 }
 
 }  // namespace csa

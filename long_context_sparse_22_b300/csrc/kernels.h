@@ -53,13 +53,59 @@ struct AttnArgs {
     int m, n_win, derotate;
     float scale;
     long long spin;        // polls before a bounded wait gives up
+    int kv8;               // kvc holds FP8 records (c = 512, 64 rotary dims)
+    const float *q_norm;   // RMSNorm gains of q (c floats) or nullptr
+    float norm_eps;
     RopeFreqs rope;
 };
 
+// gain != nullptr: the KV RMSNorm of every stored raw row and entry, before
+// its rotation (one CTA per block).
 cudaError_t launch_compress(csa_dtype dt, int64_t B, int64_t n, int c, int m, int overlap,
                             const void *C, const void *Z, const float *bias, const void *Cb,
                             const void *Zb, const float *biasb, void *out, void *raw_out,
-                            const RopeFreqs &rope, cudaStream_t st);
+                            const RopeFreqs &rope, const float *gain, float eps, cudaStream_t st);
+
+// Low-precision caches.  FP8 KV record of a c = 512 entry with 64 rotary
+// dims: 448 E4M3 codes, 64 BF16 rotary values, 4 fp32 group scales.
+constexpr int KV8_BYTES = 592;
+constexpr int KV8_NR = 448;
+// MXFP4 rows of 128 values: codes (64 bytes a row) then scale bytes (4 a row,
+// the row count rounded up to a multiple of 4).
+size_t mxfp4_bytes(int64_t rows);
+cudaError_t launch_quant_kv_fp8(csa_dtype dt, int64_t rows, const void *src, void *dst, cudaStream_t st);
+cudaError_t launch_quant_mxfp4(csa_dtype dt, int64_t rows, const void *src, void *dst, cudaStream_t st);
+// -inf into every score past a row's visible prefix.
+cudaError_t launch_mask_tail(float *scores, const int64_t *q_pos, int64_t rows, int64_t E, int m, cudaStream_t st);
+// Decode scores (one query per sequence, 64 x 128 indexer) over MXFP4 keys,
+// rounded to BF16 (kept as fp32 values).
+cudaError_t launch_indexer_fp4(int64_t B, int64_t E, int m, const void *qI, const float *w, const void *kI4,
+                               const int64_t *q_pos, float *scores, unsigned *status, long long spin,
+                               int max_ctas, cudaStream_t st);
+
+// Y[:, g*N + n] = A[:, g*K : (g+1)*K] . W[g*N + n, :] for g < groups (bf16, fp32
+// accumulation): A [M, groups*K], W [groups*N, K], Y [M, groups*N] row-major.
+// N a multiple of 256, K of 64.
+cudaError_t launch_gemm_bf16(int64_t M, int N, int K, int groups, const void *A, const void *W, void *Y,
+                             unsigned *status, long long spin, cudaStream_t st);
+
+// Incremental decode: one arriving token per sequence into the window ring and
+// the compression tail; a completed block is compressed into the caches.
+struct DecodeAppend {
+    const void *C, *Z, *Cb, *Zb, *Ck, *Zk, *Ckb, *Zkb;
+    const float *bias, *biasb, *biask, *biaskb;
+    const int64_t *t;
+    void *win, *tail, *kvc, *kIc;
+    unsigned *status;
+    int64_t E_cap;
+    int c, dI, m, overlap, n_win;
+    const float *kv_norm;
+    float norm_eps;
+    RopeFreqs rope;
+};
+int decode_tail_slots(int m, int overlap);
+int decode_tail_width(int c, int dI, int overlap);
+cudaError_t launch_decode_append(csa_dtype dt, int64_t B, const DecodeAppend &d, cudaStream_t st);
 
 cudaError_t launch_indexer_simt(csa_dtype dt, int64_t B, int64_t Tq, int hI, int dI, int64_t E,
                                 int m, const void *qI, const float *w, const void *kI,

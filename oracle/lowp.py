@@ -24,6 +24,11 @@ design notes):
   FP8 recipe; the last group of the 448 non-rotary dims is 64 wide): scale =
   amax / 448, so the group's largest magnitude maps to the top of the range.
   An all-zero group gets scale 1.
+* The entry is quantised as the fp32 values a kernel holds it in: the scale
+  is rounded to fp32, and the quotient x / scale that the E4M3 rounding
+  decides on is formed in fp32 (the precision of the FP8 conversion), so a
+  quotient within an fp32 rounding of an E4M3 midpoint is decided as that
+  arithmetic decides it.  The rotary dims are rounded to BF16 from fp32.
 * MXFP4 follows the OCP microscaling rule: shared exponent =
   floor(log2(amax)) - 2 (2 is the largest E2M1 exponent), elements round to
   nearest, ties to even, and saturate at +-6; an all-zero block has scale 1.
@@ -106,18 +111,19 @@ def kv_entry_fp8(e, rope_dims: int = 64, group: int = 128) -> np.ndarray:
     """One stored KV entry (or rows of entries, last axis = c): the first
     c - rope_dims dims in FP8 E4M3 with one fp32 scale per `group` dims, the
     rotary dims in BF16.  Returns the dequantised entry."""
-    e = np.asarray(e, dtype=np.float64)
-    c = e.shape[-1]
+    e32 = np.asarray(e, dtype=np.float64).astype(np.float32)
+    c = e32.shape[-1]
     nr = c - rope_dims
-    out = np.empty_like(e)
+    out = np.empty(e32.shape, np.float64)
     for g0 in range(0, nr, group):
         g1 = min(g0 + group, nr)
-        part = e[..., g0:g1]
-        amax = np.max(np.abs(part), axis=-1, keepdims=True)
+        part = e32[..., g0:g1]
+        amax = np.max(np.abs(part), axis=-1, keepdims=True).astype(np.float64)
         # the scale itself is stored in fp32
-        scale = np.where(amax > 0, (amax / E4M3_MAX).astype(np.float32).astype(np.float64), 1.0)
-        out[..., g0:g1] = e4m3_round(part / scale) * scale
-    out[..., nr:] = bf16_round(e[..., nr:])
+        scale = np.where(amax > 0, amax / E4M3_MAX, 1.0).astype(np.float32)
+        quot = (part / scale).astype(np.float64)          # formed in fp32
+        out[..., g0:g1] = e4m3_round(quot) * scale.astype(np.float64)
+    out[..., nr:] = bf16_round(e32[..., nr:].astype(np.float64))
     return out
 
 

@@ -19,6 +19,10 @@ Cases:
                     window (lists split over CTAs: the split-KV combine runs)
   attn_simt         sparse_attn in fp32, 2048 queries, 4 heads x 64, k = 64 + window
   indexer_simt      indexer_score in fp32, 2048 queries x 512 entries, 4 x 32
+  indexer_fp4       indexer_score_fp4, 8 sequences x 262144 MXFP4 keys, 1 query each
+  hca_decode_fp8    hca_attn on FP8 entries, 8 sequences x 8192 entries, 128 heads x 512
+  out_proj          out_proj, 4096 tokens, 64 heads x 512 in 8 groups -> 1024 -> 4096
+  decode_append     decode_append, 64 sequences, c = 512, dI = 128, m = 4 (one step)
 """
 from __future__ import annotations
 
@@ -129,6 +133,51 @@ def case_attn_simt():
     return lambda: csa.sparse_attn(q, pos, kvc, idx, raw, rp0, sink, p, out=out)
 
 
+def case_indexer_fp4(B=8, E=262144, m=4):
+    qI = _bf16(B, 1, 64, 128)
+    w = torch.softmax(torch.randn(B, 1, 64, device="cuda"), -1)
+    kI4 = csa.quantize_index_fp4(_bf16(B, E, 128))
+    pos = torch.full((B, 1), E * m - 1, dtype=torch.int64, device="cuda")
+    scores = torch.empty(B, 1, E, device="cuda")
+    return lambda: csa.indexer_score_fp4(qI, w, kI4, pos, E, m, scores=scores)
+
+
+def case_hca_decode_fp8():
+    B, H, c, E, m = 8, 128, 512, 8192, 128
+    t = E * m
+    q = _bf16(B, 1, H, c)
+    kv8 = csa.quantize_kv_fp8(_bf16(B, E, c))
+    raw = _bf16(B, 128, c)
+    pos = torch.full((B, 1), t, dtype=torch.int64, device="cuda")
+    rp0 = torch.full((B,), t - 127, dtype=torch.int64, device="cuda")
+    sink = torch.randn(H, device="cuda")
+    out = torch.empty_like(q)
+    p = csa.params(m=m, n_win=128, rope_dims=64, cache_format=1)
+    return lambda: csa.hca_attn(q, pos, kv8, raw, rp0, sink, p, out=out)
+
+
+def case_out_proj(T=4096, H=64, c=512, hg=8, d_g=1024, d=4096):
+    G = H // hg
+    o = _bf16(T, H, c)
+    w_g = _bf16(G, d_g, hg * c, scale=(hg * c) ** -0.5)
+    w_o = _bf16(d, G * d_g, scale=(G * d_g) ** -0.5)
+    y = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    return lambda: csa.out_proj(o, w_g, w_o, heads_per_group=hg, y=y)
+
+
+def case_decode_append(B=64, c=512, dI=128, m=4):
+    p = csa.params(m=m, n_win=128, rope_dims=64)
+    C_, Z = _bf16(B, c), _bf16(B, c)
+    Ck, Zk = _bf16(B, dI), _bf16(B, dI)
+    bias = torch.randn(m, c, device="cuda") * 0.1
+    biask = torch.randn(m, dI, device="cuda") * 0.1
+    win = _bf16(B, 128, c)
+    tail = torch.zeros(csa.decode_tail_bytes(1, B, c, dI, p), dtype=torch.uint8, device="cuda")
+    kvc, kIc = _bf16(B, 4096, c), _bf16(B, 4096, dI)
+    t = torch.full((B,), 4 * 1000 + 3, dtype=torch.int64, device="cuda")   # completes block 1000
+    return lambda: csa.decode_append(t, C_, Z, bias, win, tail, kvc, p, Ck=Ck, Zk=Zk, biask=biask, kIc=kIc)
+
+
 def case_hca_decode():
     B, H, c, E, m = 8, 128, 512, 8192, 128
     t = E * m
@@ -186,6 +235,10 @@ CASES = {
     "sparse_attn_decode": case_sparse_attn_decode,
     "attn_simt": case_attn_simt,
     "indexer_simt": case_indexer_f32,
+    "indexer_fp4": case_indexer_fp4,
+    "hca_decode_fp8": case_hca_decode_fp8,
+    "out_proj": case_out_proj,
+    "decode_append": case_decode_append,
 }
 
 

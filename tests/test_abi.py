@@ -73,6 +73,27 @@ def test_validation_rejects_before_launch(csa):
     assert s == 1 and "spin_limit" in _err(csa, s)
     s = L.csa_wait_probe(100, None, 0, None)
     assert s == 3
+    # low-precision caches: FP8 records only for c = 512 with 64 rotary dims, MXFP4 rows of 128
+    s = L.quantize_kv_fp8(1, 4, 128, 64, fake, fake, None)
+    assert s == 2 and "c = 512" in _err(csa, s)
+    s = L.quantize_index_fp4(1, 4, 64, fake, fake, None)
+    assert s == 2
+    p_lp = csa.params(m=4, rope_dims=32, cache_format=1)
+    s = L.hca_attn(1, 1, 1, 16, 512, 4, 4, fake, fake, fake, fake, fake, fake, fake, None,
+                   C.byref(p_lp), fake, 256, None)
+    assert s == 2 and "FP8" in _err(csa, s)
+    p_cf = csa.params(m=4, rope_dims=64, cache_format=7)
+    s = L.hca_attn(1, 1, 1, 16, 512, 4, 4, fake, fake, fake, fake, fake, fake, fake, None,
+                   C.byref(p_cf), fake, 256, None)
+    assert s == 1 and "cache_format" in _err(csa, s)
+    p_lp64 = csa.params(m=4, rope_dims=64, cache_format=1, top_k=64)
+    s = L.csa_prefill(1, 1, 64, 16, 512, 64, 128, *([fake] * 18), C.byref(p_lp64), fake, 1 << 30, None)
+    assert s == 2 and "dtype" in _err(csa, s)
+    assert L.index_fp4_bytes(5) == 5 * 64 + 8 * 4
+    # decode_append: the tail holds at most 128 slots
+    p_big = csa.params(m=256, rope_dims=64)
+    s = L.decode_append(1, 1, 512, 128, *([fake] * 17), 4, C.byref(p_big), fake, 256, None)
+    assert s == 2 and "128 slots" in _err(csa, s)
     # odd rope dims
     p_bad = csa.params(m=4, rope_dims=3)
     s = L.csa_compress(1, 1, 8, 64, fake, fake, fake, None, None, None, fake, None, C.byref(p_bad), None)

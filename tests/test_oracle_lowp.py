@@ -131,14 +131,19 @@ def test_kv_entry_fp8():
     e = r.standard_normal((16, 512))
     q = lowp.kv_entry_fp8(e, rope_dims=64, group=128)
     # rotary dims: BF16
-    assert np.array_equal(q[:, 448:], lowp.bf16_round(e[:, 448:]))
+    assert np.array_equal(q[:, 448:], lowp.bf16_round(e[:, 448:].astype(np.float32)))
     # non-rotary dims: each group's largest magnitude maps onto the top of the E4M3 range,
     # every value within half a step (3 mantissa bits) of its scaled input
     for g0, g1 in ((0, 128), (128, 256), (256, 384), (384, 448)):
-        part = e[:, g0:g1]
-        scale = (np.abs(part).max(-1, keepdims=True) / 448.0).astype(np.float32).astype(np.float64)
+        p32 = e[:, g0:g1].astype(np.float32)
+        s32 = (np.abs(p32).max(-1, keepdims=True) / np.float32(448.0)).astype(np.float32)
+        part, scale = p32.astype(np.float64), s32.astype(np.float64)
         y = part / scale
-        assert np.array_equal(q[:, g0:g1], lowp.e4m3_round(y) * scale)
+        # the stored codes are those of the fp32 quotient; they differ from the exact
+        # quotient's only where the two straddle an E4M3 midpoint
+        y32 = (p32 / s32).astype(np.float64)
+        assert np.array_equal(q[:, g0:g1], lowp.e4m3_round(y32) * scale)
+        assert np.mean(lowp.e4m3_round(y32) != lowp.e4m3_round(y)) < 1e-3
         normal = np.abs(y) >= 2.0 ** -6
         assert np.all(np.abs(q[:, g0:g1] - part)[normal] <= (np.abs(part) * 2.0 ** -4)[normal] * (1 + 1e-12))
     # an all-zero group stays zero
