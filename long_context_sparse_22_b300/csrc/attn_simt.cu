@@ -5,233 +5,213 @@
 // "Partial rotary position embeddings", "Why the output is de-rotated",
 // "Attention sinks".]
 //
-// One CTA = one query and a group of up to HG heads.  Entries (selected or
-// every visible compressed entry, then the window rows) stream through
-// shared memory in tiles of TE rows; logits are warp-reduced dot products,
-// the softmax is online (running max and denominator per head, seeded with
-// the sink logit so the sink only enters the denominator), and each thread
-// accumulates HG x (c/128) output columns in registers.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace csa {
 
-constexpr int AT_THREADS = 128;
-constexpr int AT_HG = 16;   // heads per CTA
-constexpr int AT_TE = 16;   // entry rows per tile
-constexpr int AT_DMAX = 4;  // c / 128 columns per thread (c <= 512)
+// One warp per work item (query, group of WH heads).  The query rows live in
+// shared memory (normalised when asked, rotated at t, times the logit scale in
+// log2 units), read as broadcasts.  The list is walked 32 entries at a time:
+//   QK  lane l takes entry base + l and dots its whole row with the WH rows;
+//   softmax: the running max per head is agreed by a warp max; each lane
+//       keeps its own partial denominator (rescaled with the shared max);
+//   PV  lanes over dims: for each entry of the chunk, its probabilities come
+//       from the owning lane by shuffle and every lane adds p * row[d] for
+//       its dims d = lane + 32 i.
+// No CTA-wide barrier: a warp runs its item alone, start to end.  The sink
+// seeds the running max and enters only the denominator.
+constexpr int AW_WARPS = 4;    // warps (items) per CTA
+constexpr int AW_WH = 4;       // heads per item
 
-template <typename T>
-__global__ void __launch_bounds__(AT_THREADS)
-attn_simt_kernel(AttnArgs a) {
-    extern __shared__ float sm[];
-    const int c = a.c;
-    const int hg = min(AT_HG, a.H - (int)blockIdx.y * AT_HG);
-    const int h0 = blockIdx.y * AT_HG;
-    float *qs = sm;                       // [AT_HG][c]
-    float *ks = qs + AT_HG * c;           // [AT_TE][c]
-    float *lg = ks + AT_TE * c;           // [AT_HG][AT_TE]
-    __shared__ const T *rowp[AT_TE];
-    __shared__ float s_m[AT_HG], s_den[AT_HG], s_corr[AT_HG];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t bt = blockIdx.x;
+template <typename T, int C>
+__global__ void __launch_bounds__(AW_WARPS * 32)
+attn_warp_kernel(const AttnArgs a, int64_t n_items) {
+    constexpr int DPL = C / 32;                 // dims per lane in PV and the epilogue
+    constexpr int VN = Vec<T>::N;
+    extern __shared__ float smq[];              // [AW_WARPS][AW_WH][C]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t item = (int64_t)blockIdx.x * AW_WARPS + warp;
+    if (item >= n_items) return;                // warp-uniform; nothing below syncs the CTA
+    const int ng = (a.H + AW_WH - 1) / AW_WH;
+    const int64_t bt = item / ng;
+    const int h0 = (int)(item % ng) * AW_WH;
+    const int hg = a.H - h0 < AW_WH ? a.H - h0 : AW_WH;
     const int64_t b = bt / a.Tq;
     const int64_t t = a.q_pos[bt];
-    const T *q = (const T *)a.q + (bt * a.H + h0) * (int64_t)c;
+    float *qs = smq + warp * AW_WH * C;
+    const T *qg = (const T *)a.q + (bt * a.H + h0) * (int64_t)C;
+    const float sl2 = a.scale * 1.4426950408889634f;
 
-    // q rows -> shared float (RMSNorm per head when asked), rotated at t and scaled
-    if (a.q_norm) {
-        for (int i = tid; i < hg * c; i += AT_THREADS) qs[i] = to_f(q[i]);
-        __syncthreads();
-        for (int h = warp; h < hg; h += AT_THREADS / 32) {
+    // q rows: RMSNorm (when asked), RoPE at t, scale
+#pragma unroll 1
+    for (int h = 0; h < AW_WH; h++) {
+        float v[DPL];
+#pragma unroll
+        for (int i = 0; i < DPL; i++) v[i] = h < hg ? to_f(qg[h * C + lane + 32 * i]) : 0.f;
+        if (a.q_norm && h < hg) {
             float ss = 0.f;
-            for (int ch = lane; ch < c; ch += 32) ss = fmaf(qs[h * c + ch], qs[h * c + ch], ss);
+#pragma unroll
+            for (int i = 0; i < DPL; i++) ss = fmaf(v[i], v[i], ss);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            const float rs = 1.0f / sqrtf(ss / (float)c + a.norm_eps);
-            for (int ch = lane; ch < c; ch += 32) qs[h * c + ch] = qs[h * c + ch] * rs * a.q_norm[ch] * a.scale;
+            const float rs = 1.0f / sqrtf(ss / (float)C + a.norm_eps);
+#pragma unroll
+            for (int i = 0; i < DPL; i++) v[i] = v[i] * rs * a.q_norm[lane + 32 * i];
         }
-    } else {
-        for (int i = tid; i < hg * c; i += AT_THREADS) qs[i] = to_f(q[i]) * a.scale;
+#pragma unroll
+        for (int i = 0; i < DPL; i++) {
+            const int d = lane + 32 * i;       // d and d ^ 1 sit in lanes l and l ^ 1
+            const float pv = __shfl_xor_sync(0xffffffffu, v[i], 1);
+            if (d >= a.rope.first) {
+                float cs, sn;
+                rope_cos_sin((double)t, a.rope.w[(d - a.rope.first) >> 1], cs, sn);
+                v[i] = (d & 1) ? pv * sn + v[i] * cs : v[i] * cs - pv * sn;
+            }
+            qs[h * C + d] = v[i] * sl2;
+        }
     }
-    __syncthreads();
-    const int pairs = a.rope.pairs;
-    for (int i = tid; i < hg * pairs; i += AT_THREADS) {
-        const int h = i / pairs, p = i % pairs;
-        float cs, sn;
-        rope_cos_sin((double)t, a.rope.w[p], cs, sn);
-        float *v = qs + h * c + a.rope.first + 2 * p;
-        const float x0 = v[0], x1 = v[1];
-        v[0] = x0 * cs - x1 * sn;
-        v[1] = x0 * sn + x1 * cs;
-    }
-    if (tid < hg) {
-        const float z = a.sink[h0 + tid];
-        s_m[tid] = z;
-        s_den[tid] = (z == -INFINITY) ? 0.f : 1.f;
-    }
+    __syncwarp();
 
-    // entry list: compressed part then window part
     const int64_t nv = visible_count(t, a.m, a.E);
     const int64_t ncomp = a.idx ? (int64_t)a.k : nv;
     int64_t p0 = t - a.n_win + 1;
     if (p0 < 0) p0 = 0;
-    const int64_t nwin = a.n_win > 0 ? (t - p0 + 1) : 0;
-    const int64_t total = ncomp + (nwin > 0 ? nwin : 0);
+    const int64_t nwin = a.n_win > 0 ? t - p0 + 1 : 0;
+    const int64_t total = ncomp + nwin;
     const int64_t rp0 = a.raw_pos0[b];
 
-    float acc[AT_HG][AT_DMAX];
+    float m[AW_WH], z2[AW_WH], lsum[AW_WH], acc[AW_WH][DPL];
 #pragma unroll
-    for (int h = 0; h < AT_HG; h++)
+    for (int h = 0; h < AW_WH; h++) {
+        z2[h] = h < hg ? a.sink[h0 + h] * 1.4426950408889634f : -INFINITY;
+        m[h] = z2[h];
+        lsum[h] = 0.f;
 #pragma unroll
-        for (int i = 0; i < AT_DMAX; i++) acc[h][i] = 0.f;
-    __syncthreads();
-
-    for (int64_t base = 0; base < total; base += AT_TE) {
-        if (tid < AT_TE) {
-            const int64_t e = base + tid;
-            const T *p = nullptr;
-            if (e < ncomp) {
-                int64_t j = a.idx ? (int64_t)a.idx[bt * a.k + e] : e;
-                if (j >= 0 && j < a.E) {
-                    p = (const T *)a.kvc + (b * a.E + j) * (int64_t)c;
-                } else if (j != -1 || !a.idx) {
-                    atomicOr(a.status, ST_BAD_INDEX);
-                }
-            } else if (e < total) {
-                const int64_t row = p0 + (e - ncomp) - rp0;
-                if (row >= 0 && row < a.L) p = (const T *)a.kv_raw + (b * a.L + row) * (int64_t)c;
-                else atomicOr(a.status, ST_NO_WINDOW_ROW);
-            }
-            rowp[tid] = p;
+        for (int i = 0; i < DPL; i++) acc[h][i] = 0.f;
+    }
+    for (int64_t base = 0; base < total; base += 32) {
+        // this lane's entry of the chunk
+        const int64_t e = base + lane;
+        const T *row = nullptr;
+        if (e < ncomp) {
+            const int64_t j = a.idx ? (int64_t)a.idx[bt * a.k + e] : e;
+            if (j >= 0 && j < a.E) row = (const T *)a.kvc + (b * a.E + j) * (int64_t)C;
+            else if (j != -1 || !a.idx) atomicOr(a.status, ST_BAD_INDEX);
+        } else if (e < total) {
+            const int64_t r = p0 + (e - ncomp) - rp0;
+            if (r >= 0 && r < a.L) row = (const T *)a.kv_raw + (b * a.L + r) * (int64_t)C;
+            else atomicOr(a.status, ST_NO_WINDOW_ROW);
         }
-        __syncthreads();
-        // rows -> shared float (zeros for skipped rows)
-        constexpr int N = Vec<T>::N;
-        for (int i = tid; i < AT_TE * (c / N); i += AT_THREADS) {
-            const int r = i / (c / N), cc = (i % (c / N)) * N;
-            float v[N];
-            if (rowp[r]) Vec<T>::load(rowp[r] + cc, v);
-            else
+        float sc[AW_WH];
 #pragma unroll
-                for (int u = 0; u < N; u++) v[u] = 0.f;
+        for (int h = 0; h < AW_WH; h++) sc[h] = 0.f;
+        if (row) {
+#pragma unroll 2
+            for (int d = 0; d < C; d += VN) {
+                float x[VN];
+                Vec<T>::load(row + d, x);
 #pragma unroll
-            for (int u = 0; u < N; u++) ks[r * c + cc + u] = v[u];
-        }
-        __syncthreads();
-        // logits: warp w takes pairs w, w+4, ...
-        for (int pr = warp; pr < AT_HG * AT_TE; pr += AT_THREADS / 32) {
-            const int h = pr / AT_TE, e = pr % AT_TE;
-            float d = 0.f;
-            if (h < hg && rowp[e]) {
-                for (int ch = lane; ch < c; ch += 32) d = fmaf(qs[h * c + ch], ks[e * c + ch], d);
+                for (int h = 0; h < AW_WH; h++) {
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-            }
-            if (lane == 0) lg[h * AT_TE + e] = (h < hg && rowp[e]) ? d : -INFINITY;
-        }
-        __syncthreads();
-        // online softmax, one thread per head
-        if (tid < hg) {
-            const int h = tid;
-            float mt = s_m[h];
-            for (int e = 0; e < AT_TE; e++) mt = fmaxf(mt, lg[h * AT_TE + e]);
-            float corr = 1.f, den = s_den[h];
-            if (mt != -INFINITY) {
-                corr = __expf(s_m[h] - mt);
-                den *= corr;
-                for (int e = 0; e < AT_TE; e++) {
-                    const float p = __expf(lg[h * AT_TE + e] - mt);
-                    lg[h * AT_TE + e] = p;
-                    den += p;
-                }
-            } else {
-                for (int e = 0; e < AT_TE; e++) lg[h * AT_TE + e] = 0.f;
-            }
-            s_m[h] = mt;
-            s_den[h] = den;
-            s_corr[h] = corr;
-        }
-        __syncthreads();
-        // PV: this thread's columns d = tid + 128*i
-#pragma unroll
-        for (int h = 0; h < AT_HG; h++) {
-            if (h < hg) {
-                const float corr = s_corr[h];
-#pragma unroll
-                for (int i = 0; i < AT_DMAX; i++) acc[h][i] *= corr;
-            }
-        }
-        for (int e = 0; e < AT_TE; e++) {
-            float kv[AT_DMAX];
-#pragma unroll
-            for (int i = 0; i < AT_DMAX; i++) {
-                const int d = tid + i * AT_THREADS;
-                kv[i] = d < c ? ks[e * c + d] : 0.f;
-            }
-#pragma unroll
-            for (int h = 0; h < AT_HG; h++) {
-                if (h < hg) {
-                    const float p = lg[h * AT_TE + e];
-#pragma unroll
-                    for (int i = 0; i < AT_DMAX; i++) acc[h][i] = fmaf(p, kv[i], acc[h][i]);
+                    for (int u = 0; u < VN; u += 4) {
+                        const float4 qv = *reinterpret_cast<const float4 *>(qs + h * C + d + u);
+                        sc[h] = fmaf(qv.x, x[u], sc[h]);
+                        sc[h] = fmaf(qv.y, x[u + 1], sc[h]);
+                        sc[h] = fmaf(qv.z, x[u + 2], sc[h]);
+                        sc[h] = fmaf(qv.w, x[u + 3], sc[h]);
+                    }
                 }
             }
         }
-        __syncthreads();
-    }
-    // finish: out = acc / den, de-rotate, store
+        float p[AW_WH];
 #pragma unroll
-    for (int h = 0; h < AT_HG; h++) {
-        if (h < hg) {
-            const float den = s_den[h];
-            const float inv = den > 0.f ? 1.f / den : 0.f;
+        for (int h = 0; h < AW_WH; h++) {
+            const float sh = row ? sc[h] : -INFINITY;
+            float mx = sh;
 #pragma unroll
-            for (int i = 0; i < AT_DMAX; i++) {
-                const int d = tid + i * AT_THREADS;
-                if (d < c) qs[h * c + d] = acc[h][i] * inv;
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            const float mnew = fmaxf(m[h], mx);
+            if (mnew == -INFINITY) {            // nothing readable yet (warp-uniform)
+                p[h] = 0.f;
+                continue;
+            }
+            const float alpha = exp2f(m[h] - mnew);
+            p[h] = exp2f(sh - mnew);
+            lsum[h] = fmaf(lsum[h], alpha, p[h]);
+#pragma unroll
+            for (int i = 0; i < DPL; i++) acc[h][i] *= alpha;
+            m[h] = mnew;
+        }
+        const int nin = total - base < 32 ? (int)(total - base) : 32;
+        for (int jj = 0; jj < nin; jj++) {
+            const unsigned long long rj =
+                __shfl_sync(0xffffffffu, (unsigned long long)reinterpret_cast<uintptr_t>(row), jj);
+            if (rj == 0ull) continue;
+            const T *r = reinterpret_cast<const T *>(rj);
+            float pj[AW_WH];
+#pragma unroll
+            for (int h = 0; h < AW_WH; h++) pj[h] = __shfl_sync(0xffffffffu, p[h], jj);
+#pragma unroll
+            for (int i = 0; i < DPL; i++) {
+                const float x = to_f(r[lane + 32 * i]);
+#pragma unroll
+                for (int h = 0; h < AW_WH; h++) acc[h][i] = fmaf(pj[h], x, acc[h][i]);
             }
         }
     }
-    __syncthreads();
-    if (a.derotate) {
-        for (int i = tid; i < hg * pairs; i += AT_THREADS) {
-            const int h = i / pairs, p = i % pairs;
-            float cs, sn;
-            rope_cos_sin(-(double)t, a.rope.w[p], cs, sn);
-            float *v = qs + h * c + a.rope.first + 2 * p;
-            const float x0 = v[0], x1 = v[1];
-            v[0] = x0 * cs - x1 * sn;
-            v[1] = x0 * sn + x1 * cs;
+    // finish: normalise, de-rotate by -t, store
+    T *og = (T *)a.out + (bt * a.H + h0) * (int64_t)C;
+#pragma unroll
+    for (int h = 0; h < AW_WH; h++) {
+        if (h >= hg) continue;
+        float den = lsum[h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        if (z2[h] != -INFINITY) den += exp2f(z2[h] - m[h]);
+        const float inv = den > 0.f ? 1.0f / den : 0.f;
+#pragma unroll
+        for (int i = 0; i < DPL; i++) {
+            const int d = lane + 32 * i;
+            float o = acc[h][i] * inv;
+            const float po = __shfl_xor_sync(0xffffffffu, o, 1);
+            if (a.derotate && d >= a.rope.first) {
+                float cs, sn;
+                rope_cos_sin(-(double)t, a.rope.w[(d - a.rope.first) >> 1], cs, sn);
+                o = (d & 1) ? po * sn + o * cs : o * cs - po * sn;
+            }
+            from_f(og[h * C + d], o);
         }
-        __syncthreads();
-    }
-    T *o = (T *)a.out + (bt * a.H + h0) * (int64_t)c;
-    for (int i = tid; i < hg * c; i += AT_THREADS) from_f(o[i], qs[i]);
-    if (a.lse && tid < hg) {
-        const float den = s_den[tid];
-        a.lse[bt * a.H + h0 + tid] = den > 0.f ? s_m[tid] + logf(den) : -INFINITY;
+        if (a.lse && lane == 0)
+            a.lse[bt * a.H + h0 + h] = den > 0.f ? (m[h] + log2f(den)) * 0.6931471805599453f : -INFINITY;
     }
 }
 
-static PerDevice g_attn_smem[2];
+template <typename T, int C>
+static cudaError_t launch_warp_c(int64_t B, const AttnArgs &a, cudaStream_t st) {
+    const int64_t items = B * a.Tq * ((a.H + AW_WH - 1) / AW_WH);
+    const int64_t blocks = (items + AW_WARPS - 1) / AW_WARPS;
+    if (blocks > 2147483647LL) return cudaErrorInvalidValue;
+    const size_t smem = (size_t)AW_WARPS * AW_WH * C * sizeof(float);
+    attn_warp_kernel<T, C><<<(unsigned)blocks, AW_WARPS * 32, smem, st>>>(a, items);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_warp_t(int64_t B, const AttnArgs &a, cudaStream_t st) {
+    switch (a.c) {
+        case 64: return launch_warp_c<T, 64>(B, a, st);
+        case 128: return launch_warp_c<T, 128>(B, a, st);
+        case 256: return launch_warp_c<T, 256>(B, a, st);
+        case 512: return launch_warp_c<T, 512>(B, a, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
 
 cudaError_t launch_attn_simt(csa_dtype dt, int64_t B, const AttnArgs &a, cudaStream_t st) {
     if (B * a.Tq == 0 || a.H == 0) return cudaSuccess;
-    dim3 grid((unsigned)(B * a.Tq), (unsigned)((a.H + AT_HG - 1) / AT_HG));
-    const size_t smem = ((size_t)AT_HG * a.c + (size_t)AT_TE * a.c + AT_HG * AT_TE) * 4;
-    const size_t smem_max = ((size_t)AT_HG * 512 + (size_t)AT_TE * 512 + AT_HG * AT_TE) * 4;
-    const int di = dt == CSA_BF16 ? 1 : 0;
-    {
-        cudaError_t e = dt == CSA_BF16
-            ? smem_limit_once(g_attn_smem[di], (const void *)attn_simt_kernel<__nv_bfloat16>, (int)smem_max)
-            : smem_limit_once(g_attn_smem[di], (const void *)attn_simt_kernel<float>, (int)smem_max);
-        if (e != cudaSuccess) return e;
-    }
-    if (dt == CSA_BF16) attn_simt_kernel<__nv_bfloat16><<<grid, AT_THREADS, smem, st>>>(a);
-    else attn_simt_kernel<float><<<grid, AT_THREADS, smem, st>>>(a);
-    count_launches(1);
-    return cudaGetLastError();
+    return dt == CSA_BF16 ? launch_warp_t<__nv_bfloat16>(B, a, st) : launch_warp_t<float>(B, a, st);
 }
 
 }  // namespace csa

@@ -75,6 +75,9 @@ struct AtCfg {
     static constexpr int SM_WARP0 = 5;            // warps 5-8: softmax and epilogue
     static constexpr int PV_WARP = 9;             // warp 9: PV issue
     static constexpr int THREADS = (PV_WARP + 1) * 32;
+    // c = 128: two CTAs per SM (registers capped at 96, TMEM 2 x 256 columns, shared
+    // memory 2 x 75 KB), so one CTA's hand-off latencies overlap the other's work
+    static constexpr int MIN_BLOCKS = C == 128 ? 2 : 1;
 };
 
 struct AttnTcArgs {
@@ -275,7 +278,7 @@ __device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, ui
 }
 
 template <int C, bool KV8, bool PACK>
-__global__ void __launch_bounds__(AtCfg<C>::THREADS, 1)
+__global__ void __launch_bounds__(AtCfg<C>::THREADS, AtCfg<C>::MIN_BLOCKS)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
                const __grid_constant__ CUtensorMap tm_w,
                const __grid_constant__ AttnTcArgs a) {
@@ -337,6 +340,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const uint32_t kb0 = tc::smem_u32(sK);
         uint32_t g = 0, ii = 0;
         uint32_t tma_issued = 0, last_g[2] = {0, 0}, q_pending = 0;
+        // FP8 records of the next gathered tile, loaded while the current one is
+        // converted and multiplied (within an item)
+        uint4 pf8[KV8 ? 14 : 1], pf16[KV8 ? 4 : 1], pfs = make_uint4(0, 0, 0, 0);
+        bool pf = false;
+        uint32_t pf_bal = 0;
         bool ok = true;
         for (int64_t it = blockIdx.x; ok && it < a.n_items; it += G) {
             ItemInfo f;
@@ -469,8 +477,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 // a gathered tile's row addresses go to shared memory before the wait
                 // for its buffer (the barrier that ends the wait publishes them; the
                 // gather two tiles back, the last reader of this slot, has been issued)
-                uint32_t bal = 0;
-                if (gather && tid < 64) {
+                uint32_t bal = pf ? pf_bal : 0u;
+                if (gather && tid < 64 && !pf) {
                     const int64_t pos = (int64_t)j * 64 + tid;
                     const bool in = pos < f.ncomp;
                     const int64_t ent = a.idx ? (int64_t)iv : pos;
@@ -505,21 +513,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         // the row's bf16 chunks into the swizzled tile (zeros for rows
                         // that are not in the list)
                         const int r = tid >> 1, half = tid & 1;
-                        const uint8_t *src = reinterpret_cast<const uint8_t *>(rowp[buf * 64 + r]);
-                        uint4 g8[14], g16[4], gs = make_uint4(0, 0, 0, 0);
+                        auto load_rows = [&](int bsel) {
+                            const uint8_t *src = reinterpret_cast<const uint8_t *>(rowp[bsel * 64 + r]);
 #pragma unroll
-                        for (int q = 0; q < 14; q++)
-                            g8[q] = src ? ld_nc_v4(src + (half * 14 + q) * 16) : make_uint4(0, 0, 0, 0);
+                            for (int q = 0; q < 14; q++)
+                                pf8[q] = src ? ld_nc_v4(src + (half * 14 + q) * 16) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-                        for (int q = 0; q < 4; q++)
-                            g16[q] = src ? ld_nc_v4(src + KV8_NR + (half * 4 + q) * 16) : make_uint4(0, 0, 0, 0);
-                        if (src) gs = ld_nc_v4(src + KV8_NR + 128);
+                            for (int q = 0; q < 4; q++)
+                                pf16[q] = src ? ld_nc_v4(src + KV8_NR + (half * 4 + q) * 16) : make_uint4(0, 0, 0, 0);
+                            pfs = src ? ld_nc_v4(src + KV8_NR + 128) : make_uint4(0, 0, 0, 0);
+                        };
+                        if (!pf) load_rows(buf);
+                        pf = false;
                         if (j == f.j0 && !rope_q()) {
                             ok = false;
                             break;
                         }
-                        const float scl[4] = {__uint_as_float(gs.x), __uint_as_float(gs.y),
-                                              __uint_as_float(gs.z), __uint_as_float(gs.w)};
+                        const float scl[4] = {__uint_as_float(pfs.x), __uint_as_float(pfs.y),
+                                              __uint_as_float(pfs.z), __uint_as_float(pfs.w)};
+                        uint4 *g8 = pf8, *g16 = pf16;
                         const uint32_t rb = kb + (r >> 3) * 1024;
 #pragma unroll
                         for (int q = 0; q < 14; q++) {
@@ -537,6 +549,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                    g16[q].y, g16[q].z, g16[q].w);
                         fence_proxy_async();
                         tc::mbar_arrive(&kfull[buf]);
+                        if (j + 1 < f.j1 && j + 1 < f.ntc) {
+                            // the next gathered tile: its row addresses into the other slot
+                            // (its last reader, two tiles back, has finished), its presence
+                            // bits kept, its records on their way into registers
+                            const int nb = buf ^ 1;
+                            if (tid < 64) {
+                                const int64_t pos = (int64_t)(j + 1) * 64 + tid;
+                                const bool in = pos < f.ncomp;
+                                const int64_t ent = a.idx ? (int64_t)iv : pos;
+                                const bool v = in && ent >= 0 && ent < a.E;
+                                if (a.idx && in && !v && iv != -1) atomicOr(a.status, ST_BAD_INDEX);
+                                rowp[nb * 64 + tid] = v ? reinterpret_cast<const __nv_bfloat16 *>(
+                                                              a.kv8 + (f.b * a.E + ent) * (int64_t)KV8_BYTES)
+                                                        : nullptr;
+                                pf_bal = __ballot_sync(0xffffffffu, v);
+                            }
+                            named_bar(2, Cfg::NLOAD);
+                            load_rows(nb);
+                            pf = true;
+                        }
                         continue;
                     }
                     constexpr int GR = C / 8;            // 16-byte granules per row
@@ -1183,7 +1215,7 @@ static cudaError_t launch_attn_tc_c(int64_t B, const AttnArgs &g, const int32_t 
         cudaError_t e = smem_limit_once(attr, (const void *)attn_tc_kernel<C, KV8, PACK>, Cfg::SMEM);
         if (e != cudaSuccess) return e;
     }
-    const int sms = max_ctas > 0 && max_ctas < device_sms() ? max_ctas : device_sms();
+    const int sms = (max_ctas > 0 && max_ctas < device_sms() ? max_ctas : device_sms()) * Cfg::MIN_BLOCKS;
     const int grid = (int)(a.n_items < sms ? a.n_items : sms);
     attn_tc_kernel<C, KV8, PACK><<<grid, Cfg::THREADS, Cfg::SMEM, st>>>(tq, tcmp, tw, a);
     count_launches(1);

@@ -490,36 +490,42 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
                 ok = false;
                 break;
             }
-            for (int k = 0; k < 2; k++) {
-                const int u = ct + 128 * k, h = u >> 2, blk = u & 3;
-                const __nv_bfloat16 *src = a.qI + ((int64_t)b * 64 + h) * 128 + blk * 32;
-                float v[32];
+            if (ct < 64) {
+                // head h = ct: its 4 blocks of 32 values quantised in this thread
+                const int h = ct;
+                const __nv_bfloat16 *src = a.qI + ((int64_t)b * 64 + h) * 128;
+                float v[128];
 #pragma unroll
-                for (int q = 0; q < 32; q += 8) Vec<__nv_bfloat16>::load(src + q, v + q);
-                float am = 0.f;
+                for (int q = 0; q < 128; q += 8) Vec<__nv_bfloat16>::load(src + q, v + q);
+                int eb[4], E = -127;
 #pragma unroll
-                for (int q = 0; q < 32; q++) am = fmaxf(am, fabsf(v[q]));
-                const int e = mx_exponent(am);
-                int E = e;
-                E = max(E, __shfl_xor_sync(0xffffffffu, E, 1));
-                E = max(E, __shfl_xor_sync(0xffffffffu, E, 2));
-                const float inv = pow2f(-e);
-                uint4 cw;
-                uint32_t *cp = &cw.x;
+                for (int blk = 0; blk < 4; blk++) {
+                    float am = 0.f;
 #pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    uint32_t wv = 0;
-#pragma unroll
-                    for (int t = 0; t < 8; t++) wv |= e2m1_encode(v[8 * q + t] * inv) << (4 * t);
-                    cp[q] = wv;
+                    for (int q = 0; q < 32; q++) am = fmaxf(am, fabsf(v[32 * blk + q]));
+                    eb[blk] = mx_exponent(am);
+                    E = max(E, eb[blk]);
                 }
-                const uint32_t s1 = f16_pow2(e - E);
-                uint32_t o[16];
-                e2m1_to_f16(cw, s1 | (s1 << 16), o);
 #pragma unroll
-                for (int q = 0; q < 4; q++)
-                    st_shared_v4(bBase + (blk >> 1) * 8192 + swz_off(h, (blk & 1) * 4 + q), o + 4 * q);
-                if (blk == 0) wq[wb * 64 + h] = a.w[(int64_t)b * 64 + h] * pow2f(E);
+                for (int blk = 0; blk < 4; blk++) {
+                    const float inv = pow2f(-eb[blk]);
+                    uint4 cw;
+                    uint32_t *cp = &cw.x;
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        uint32_t wv = 0;
+#pragma unroll
+                        for (int t = 0; t < 8; t++) wv |= e2m1_encode(v[32 * blk + 8 * q + t] * inv) << (4 * t);
+                        cp[q] = wv;
+                    }
+                    const uint32_t s1 = f16_pow2(eb[blk] - E);
+                    uint32_t o[16];
+                    e2m1_to_f16(cw, s1 | (s1 << 16), o);
+#pragma unroll
+                    for (int q = 0; q < 4; q++)
+                        st_shared_v4(bBase + (blk >> 1) * 8192 + swz_off(h, (blk & 1) * 4 + q), o + 4 * q);
+                }
+                wq[wb * 64 + h] = a.w[(int64_t)b * 64 + h] * pow2f(E);
             }
             fence_proxy_async_shared();
             __syncwarp();
@@ -543,21 +549,31 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
                 const int64_t key0 = first + (int64_t)jt * 128;
                 const int sc0 = (int)(key0 & 3);          // key0's byte offset in its scale row / 4
                 const uint32_t aS = aBase + st * Cfg::A_BYTES;
+                {
+                    // key row rw = ct: its 64 code bytes and 4 scale bytes, all four
+                    // blocks converted in this thread (independent of one another);
+                    // stores of consecutive rows land in distinct banks (swizzle)
+                    const int rw = ct;
+                    const uint32_t sc4 = *reinterpret_cast<const uint32_t *>(stg + Cfg::CODE_BYTES + (sc0 + rw) * 4);
+                    uint4 cw[4];                          // cw[k]: the codes of block (k + rw) & 3, so
+#pragma unroll                                            // the lanes' loads spread over the banks
+                    for (int k = 0; k < 4; k++)
+                        cw[k] = *reinterpret_cast<const uint4 *>(stg + rw * 64 + ((k + rw) & 3) * 16);
+                    int E = -127;
 #pragma unroll
-                for (int k = 0; k < 4; k++) {
-                    const int u = ct + 128 * k, rw = u >> 2, blk = u & 3;
-                    const uint4 cw = *reinterpret_cast<const uint4 *>(stg + rw * 64 + blk * 16);
-                    const int e = (int)stg[Cfg::CODE_BYTES + (sc0 + rw) * 4 + blk] - 127;
-                    int E = e;
-                    E = max(E, __shfl_xor_sync(0xffffffffu, E, 1));
-                    E = max(E, __shfl_xor_sync(0xffffffffu, E, 2));
-                    const uint32_t s1 = f16_pow2(e - E);
-                    uint32_t o[16];
-                    e2m1_to_f16(cw, s1 | (s1 << 16), o);
+                    for (int blk = 0; blk < 4; blk++) E = max(E, (int)((sc4 >> (8 * blk)) & 0xFFu) - 127);
 #pragma unroll
-                    for (int q = 0; q < 4; q++)
-                        st_shared_v4(aS + (blk >> 1) * 16384 + swz_off(rw, (blk & 1) * 4 + q), o + 4 * q);
-                    if (blk == 0) ek[qe * 128 + rw] = E;
+                    for (int k = 0; k < 4; k++) {
+                        const int blk = (k + rw) & 3;
+                        const int e = (int)((sc4 >> (8 * blk)) & 0xFFu) - 127;
+                        const uint32_t s1 = f16_pow2(e - E);
+                        uint32_t o[16];
+                        e2m1_to_f16(cw[k], s1 | (s1 << 16), o);
+#pragma unroll
+                        for (int q = 0; q < 4; q++)
+                            st_shared_v4(aS + (blk >> 1) * 16384 + swz_off(rw, (blk & 1) * 4 + q), o + 4 * q);
+                    }
+                    ek[qe * 128 + rw] = E;
                 }
                 fence_proxy_async_shared();
                 __syncwarp();
