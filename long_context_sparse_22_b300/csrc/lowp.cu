@@ -223,8 +223,9 @@ struct Fp4Cfg {
     static constexpr int OFF_MISC = OFF_B + B_BYTES;
     static constexpr int MISC_BYTES = 4096;               // barriers, wq [2][64], ek [NEK][128]
     static constexpr int SMEM = OFF_MISC + MISC_BYTES + 1024;
-    static constexpr int THREADS = 320;
-    static constexpr int CONV0 = 6;                       // first converter warp
+    static constexpr int EPI0 = 2;                        // epilogue warps 2 .. 5
+    static constexpr int CONV0 = 6;                       // converter warps 6 .. 13 (two groups of 4)
+    static constexpr int THREADS = 448;
     static constexpr int TMEM_COLS = 128;
 };
 
@@ -300,7 +301,8 @@ __device__ __forceinline__ int swz_off(int row, int chunk) {   // K-major, 128-b
     return (row >> 3) * 1024 + (row & 7) * 128 + (((chunk ^ row) & 7) << 4);
 }
 
-__global__ void __launch_bounds__(Fp4Cfg::THREADS, 1)
+// (448 threads; 144 registers a thread fit the register file once)
+__global__ void __maxnreg__(144)
 indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_sc,
                    const __grid_constant__ Fp4IdxArgs a) {
     using Cfg = Fp4Cfg;
@@ -423,10 +425,9 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
         }
     } else if (warp < Cfg::CONV0) {
         // -------------------------------------------------------- epilogue
+        // each warp one TMEM lane quarter; the two accumulators alternate
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
-        int acc = 0;
-        uint32_t accph = 0;
         uint32_t g = 0, ii = 0;
         int b, jt0, jt1;
         bool ok = true;
@@ -437,6 +438,8 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
             const float *wt = wq + wb * 64;
             const int64_t nv = visible_count(a.q_pos[b], a.m, a.E);
             for (int jt = jt0; jt < jt1; jt++, g++) {
+                const int acc = (int)(g & 1);
+                const uint32_t accph = (g >> 1) & 1;
                 const int q = g % Cfg::NEK;
                 if (!tc::mbar_wait(&accfull[acc], accph, a.status, abort_flag, a.spin) ||
                     !tc::mbar_wait(&ekfull[q], (g / Cfg::NEK) & 1, a.status, abort_flag, a.spin)) {
@@ -445,17 +448,25 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
                 }
                 tc::fence_after_sync();
                 const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + acc * 64;
-                float v0[32], v1[32];
-                tc::tmem_ld32(taddr, v0);
-                tc::tmem_ld32(taddr + 32, v1);
-                tc::tmem_ld_wait();
-                tc::tmem_regs_ready<32>(v0);
-                tc::tmem_regs_ready<32>(v1);
+                // 32 columns (heads) at a time keeps the registers low
                 float s0 = 0.f, s1 = 0.f;
+                const float4 *wt4 = reinterpret_cast<const float4 *>(wt);
 #pragma unroll
-                for (int h = 0; h < 32; h++) {
-                    s0 = fmaf(wt[h], fmaxf(v0[h], 0.f), s0);
-                    s1 = fmaf(wt[32 + h], fmaxf(v1[h], 0.f), s1);
+                for (int half = 0; half < 2; half++) {
+                    float v[32];
+                    tc::tmem_ld32(taddr + 32 * half, v);
+                    tc::tmem_ld_wait();
+                    tc::tmem_regs_ready<32>(v);
+                    float sh = 0.f;
+#pragma unroll
+                    for (int h4 = 0; h4 < 8; h4++) {
+                        const float4 wa = wt4[8 * half + h4];
+                        sh = fmaf(wa.x, fmaxf(v[4 * h4], 0.f), sh);
+                        sh = fmaf(wa.y, fmaxf(v[4 * h4 + 1], 0.f), sh);
+                        sh = fmaf(wa.z, fmaxf(v[4 * h4 + 2], 0.f), sh);
+                        sh = fmaf(wa.w, fmaxf(v[4 * h4 + 3], 0.f), sh);
+                    }
+                    if (half == 0) s0 = sh; else s1 = sh;
                 }
                 const int64_t j = (int64_t)jt * 128 + row;
                 const float sc = (s0 + s1) * pow2f(ek[q * 128 + row]);
@@ -466,7 +477,6 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
                     tc::mbar_arrive(&accempty[acc]);
                     tc::mbar_arrive(&ekempty[q]);
                 }
-                if (++acc == 2) { acc = 0; accph ^= 1; }
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&wempty[wb]);
@@ -474,80 +484,88 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
         }
     } else {
         // ------------------------------------------------------ converters
-        const int ct = threadIdx.x - Cfg::CONV0 * 32;     // 0 .. 127
+        // two groups of four warps take alternate tiles; group 0 also converts
+        // each item's query (its 64 threads of one head each)
+        const int cgrp = (warp - Cfg::CONV0) >> 2;
+        const int ct = (threadIdx.x - Cfg::CONV0 * 32) & 127;   // the tile row this thread converts
         const uint32_t aBase = tc::smem_u32(sA), bBase = tc::smem_u32(sB);
-        int s = 0, st = 0;
-        uint32_t ph = 0, aph = 0, bph = 0;
+        uint32_t bph = 0;
         uint32_t g = 0, ii = 0;
         int b, jt0, jt1;
         bool ok = true;
         for (int r = 0; ok && fp4_item(a, cta, G, r, b, jt0, jt1); r++) {
             if (jt0 >= jt1) continue;
-            // the item's query: 64 heads x 4 blocks, two (head, block) units per thread
             const int wb = ii & 1;
-            if (!tc::mbar_wait(bempty, bph ^ 1, a.status, abort_flag, a.spin) ||
-                !tc::mbar_wait(&wempty[wb], ((ii >> 1) & 1) ^ 1, a.status, abort_flag, a.spin)) {
-                ok = false;
-                break;
-            }
-            if (ct < 64) {
-                // head h = ct: its 4 blocks of 32 values quantised in this thread
-                const int h = ct;
-                const __nv_bfloat16 *src = a.qI + ((int64_t)b * 64 + h) * 128;
-                float v[128];
-#pragma unroll
-                for (int q = 0; q < 128; q += 8) Vec<__nv_bfloat16>::load(src + q, v + q);
-                int eb[4], E = -127;
-#pragma unroll
-                for (int blk = 0; blk < 4; blk++) {
-                    float am = 0.f;
-#pragma unroll
-                    for (int q = 0; q < 32; q++) am = fmaxf(am, fabsf(v[32 * blk + q]));
-                    eb[blk] = mx_exponent(am);
-                    E = max(E, eb[blk]);
+            if (cgrp == 0) {
+                if (!tc::mbar_wait(bempty, bph ^ 1, a.status, abort_flag, a.spin) ||
+                    !tc::mbar_wait(&wempty[wb], ((ii >> 1) & 1) ^ 1, a.status, abort_flag, a.spin)) {
+                    ok = false;
+                    break;
                 }
+                if (ct < 64) {
+                    // head h = ct: block exponents from a first pass over its 128 values,
+                    // then each block quantised and expanded (second pass, from cache)
+                    const int h = ct;
+                    const __nv_bfloat16 *src = a.qI + ((int64_t)b * 64 + h) * 128;
+                    int eb[4], E = -127;
 #pragma unroll
-                for (int blk = 0; blk < 4; blk++) {
-                    const float inv = pow2f(-eb[blk]);
-                    uint4 cw;
-                    uint32_t *cp = &cw.x;
+                    for (int blk = 0; blk < 4; blk++) {
+                        float v[32];
 #pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        uint32_t wv = 0;
+                        for (int q = 0; q < 32; q += 8) Vec<__nv_bfloat16>::load(src + 32 * blk + q, v + q);
+                        float am = 0.f;
 #pragma unroll
-                        for (int t = 0; t < 8; t++) wv |= e2m1_encode(v[32 * blk + 8 * q + t] * inv) << (4 * t);
-                        cp[q] = wv;
+                        for (int q = 0; q < 32; q++) am = fmaxf(am, fabsf(v[q]));
+                        eb[blk] = mx_exponent(am);
+                        E = max(E, eb[blk]);
                     }
-                    const uint32_t s1 = f16_pow2(eb[blk] - E);
-                    uint32_t o[16];
-                    e2m1_to_f16(cw, s1 | (s1 << 16), o);
 #pragma unroll
-                    for (int q = 0; q < 4; q++)
-                        st_shared_v4(bBase + (blk >> 1) * 8192 + swz_off(h, (blk & 1) * 4 + q), o + 4 * q);
+                    for (int blk = 0; blk < 4; blk++) {
+                        float v[32];
+#pragma unroll
+                        for (int q = 0; q < 32; q += 8) Vec<__nv_bfloat16>::load(src + 32 * blk + q, v + q);
+                        const float inv = pow2f(-eb[blk]);
+                        uint4 cw;
+                        uint32_t *cp = &cw.x;
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            uint32_t wv = 0;
+#pragma unroll
+                            for (int t = 0; t < 8; t++) wv |= e2m1_encode(v[8 * q + t] * inv) << (4 * t);
+                            cp[q] = wv;
+                        }
+                        const uint32_t s1 = f16_pow2(eb[blk] - E);
+                        uint32_t o[16];
+                        e2m1_to_f16(cw, s1 | (s1 << 16), o);
+#pragma unroll
+                        for (int q = 0; q < 4; q++)
+                            st_shared_v4(bBase + (blk >> 1) * 8192 + swz_off(h, (blk & 1) * 4 + q), o + 4 * q);
+                    }
+                    wq[wb * 64 + h] = a.w[(int64_t)b * 64 + h] * pow2f(E);
                 }
-                wq[wb * 64 + h] = a.w[(int64_t)b * 64 + h] * pow2f(E);
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    tc::mbar_arrive(bfull);
+                    tc::mbar_arrive(&wfull[wb]);
+                }
+                bph ^= 1;
             }
-            fence_proxy_async_shared();
-            __syncwarp();
-            if (lane == 0) {
-                tc::mbar_arrive(bfull);
-                tc::mbar_arrive(&wfull[wb]);
-            }
-            bph ^= 1;
             ii++;
-            // the key tiles: 128 rows x 4 blocks, four (row, block) units per thread
+            // the key tiles of this group: 128 rows, one per thread
             const int64_t first = (int64_t)b * a.E;
             for (int jt = jt0; jt < jt1; jt++, g++) {
-                const int qe = g % Cfg::NEK;
-                if (!tc::mbar_wait(&sfull[s], ph, a.status, abort_flag, a.spin) ||
-                    !tc::mbar_wait(&aempty[st], aph ^ 1, a.status, abort_flag, a.spin) ||
+                if ((int)(g & 1) != cgrp) continue;
+                const int s = g % Cfg::SST, st = g % Cfg::AST, qe = g % Cfg::NEK;
+                if (!tc::mbar_wait(&sfull[s], (g / Cfg::SST) & 1, a.status, abort_flag, a.spin) ||
+                    !tc::mbar_wait(&aempty[st], ((g / Cfg::AST) & 1) ^ 1, a.status, abort_flag, a.spin) ||
                     !tc::mbar_wait(&ekempty[qe], ((g / Cfg::NEK) & 1) ^ 1, a.status, abort_flag, a.spin)) {
                     ok = false;
                     break;
                 }
                 const uint8_t *stg = sS + s * Cfg::STG_BYTES;
                 const int64_t key0 = first + (int64_t)jt * 128;
-                const int sc0 = (int)(key0 & 3);          // key0's byte offset in its scale row / 4
+                const int sc0 = (int)(key0 & 3);          // key0's place in its 16-byte scale row
                 const uint32_t aS = aBase + st * Cfg::A_BYTES;
                 {
                     // key row rw = ct: its 64 code bytes and 4 scale bytes, all four
@@ -555,20 +573,18 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
                     // stores of consecutive rows land in distinct banks (swizzle)
                     const int rw = ct;
                     const uint32_t sc4 = *reinterpret_cast<const uint32_t *>(stg + Cfg::CODE_BYTES + (sc0 + rw) * 4);
-                    uint4 cw[4];                          // cw[k]: the codes of block (k + rw) & 3, so
-#pragma unroll                                            // the lanes' loads spread over the banks
-                    for (int k = 0; k < 4; k++)
-                        cw[k] = *reinterpret_cast<const uint4 *>(stg + rw * 64 + ((k + rw) & 3) * 16);
                     int E = -127;
 #pragma unroll
                     for (int blk = 0; blk < 4; blk++) E = max(E, (int)((sc4 >> (8 * blk)) & 0xFFu) - 127);
 #pragma unroll
                     for (int k = 0; k < 4; k++) {
+                        // block (k + rw) & 3: the lanes' loads spread over the banks
                         const int blk = (k + rw) & 3;
+                        const uint4 cw = *reinterpret_cast<const uint4 *>(stg + rw * 64 + blk * 16);
                         const int e = (int)((sc4 >> (8 * blk)) & 0xFFu) - 127;
                         const uint32_t s1 = f16_pow2(e - E);
                         uint32_t o[16];
-                        e2m1_to_f16(cw[k], s1 | (s1 << 16), o);
+                        e2m1_to_f16(cw, s1 | (s1 << 16), o);
 #pragma unroll
                         for (int q = 0; q < 4; q++)
                             st_shared_v4(aS + (blk >> 1) * 16384 + swz_off(rw, (blk & 1) * 4 + q), o + 4 * q);
@@ -582,8 +598,6 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
                     tc::mbar_arrive(&sempty[s]);
                     tc::mbar_arrive(&ekfull[qe]);
                 }
-                if (++s == Cfg::SST) { s = 0; ph ^= 1; }
-                if (++st == Cfg::AST) { st = 0; aph ^= 1; }
             }
         }
     }
