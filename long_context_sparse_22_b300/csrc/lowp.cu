@@ -273,22 +273,19 @@ __device__ __forceinline__ uint32_t f16_pow2(int rel) {
     return 0u;
 }
 
-// 16 code bytes (32 E2M1 values) times 2^rel into four 16-byte f16 chunks.
-__device__ __forceinline__ void e2m1_to_f16(const uint4 c, uint32_t s2, uint32_t *o) {
-    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+// 4 code bytes (8 E2M1 values) times 2^rel into one 16-byte f16 chunk.
+__device__ __forceinline__ void e2m1x8_to_f16(uint32_t cw, uint32_t s2, uint32_t *o) {
 #pragma unroll
-    for (int q = 0; q < 4; q++)
-#pragma unroll
-        for (int u = 0; u < 4; u++) {
-            uint32_t h;
-            asm("{\n\t.reg .b8 t;\n\t"
-                "cvt.u8.u32 t, %1;\n\t"
-                "cvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-                : "=r"(h)
-                : "r"(cw[q] >> (8 * u)));
-            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(h) : "r"(h), "r"(s2));
-            o[4 * q + u] = h;
-        }
+    for (int u = 0; u < 4; u++) {
+        uint32_t h;
+        asm("{\n\t.reg .b8 t;\n\t"
+            "cvt.u8.u32 t, %1;\n\t"
+            "cvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+            : "=r"(h)
+            : "r"(cw >> (8 * u)));
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(h) : "r"(h), "r"(s2));
+        o[u] = h;
+    }
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint32_t *v) {
@@ -301,8 +298,7 @@ __device__ __forceinline__ int swz_off(int row, int chunk) {   // K-major, 128-b
     return (row >> 3) * 1024 + (row & 7) * 128 + (((chunk ^ row) & 7) << 4);
 }
 
-// (448 threads; 144 registers a thread fit the register file once)
-__global__ void __maxnreg__(144)
+__global__ void __launch_bounds__(Fp4Cfg::THREADS, 1)
 indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_sc,
                    const __grid_constant__ Fp4IdxArgs a) {
     using Cfg = Fp4Cfg;
@@ -510,36 +506,32 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
                     int eb[4], E = -127;
 #pragma unroll
                     for (int blk = 0; blk < 4; blk++) {
-                        float v[32];
-#pragma unroll
-                        for (int q = 0; q < 32; q += 8) Vec<__nv_bfloat16>::load(src + 32 * blk + q, v + q);
                         float am = 0.f;
 #pragma unroll
-                        for (int q = 0; q < 32; q++) am = fmaxf(am, fabsf(v[q]));
+                        for (int q = 0; q < 4; q++) {
+                            float v[8];
+                            Vec<__nv_bfloat16>::load(src + 32 * blk + 8 * q, v);
+#pragma unroll
+                            for (int t = 0; t < 8; t++) am = fmaxf(am, fabsf(v[t]));
+                        }
                         eb[blk] = mx_exponent(am);
                         E = max(E, eb[blk]);
                     }
-#pragma unroll
+#pragma unroll 1
                     for (int blk = 0; blk < 4; blk++) {
-                        float v[32];
-#pragma unroll
-                        for (int q = 0; q < 32; q += 8) Vec<__nv_bfloat16>::load(src + 32 * blk + q, v + q);
                         const float inv = pow2f(-eb[blk]);
-                        uint4 cw;
-                        uint32_t *cp = &cw.x;
+                        const uint32_t s1 = f16_pow2(eb[blk] - E);
 #pragma unroll
                         for (int q = 0; q < 4; q++) {
+                            float v[8];
+                            Vec<__nv_bfloat16>::load(src + 32 * blk + 8 * q, v);
                             uint32_t wv = 0;
 #pragma unroll
-                            for (int t = 0; t < 8; t++) wv |= e2m1_encode(v[8 * q + t] * inv) << (4 * t);
-                            cp[q] = wv;
+                            for (int t = 0; t < 8; t++) wv |= e2m1_encode(v[t] * inv) << (4 * t);
+                            uint32_t o[4];
+                            e2m1x8_to_f16(wv, s1 | (s1 << 16), o);
+                            st_shared_v4(bBase + (blk >> 1) * 8192 + swz_off(h, (blk & 1) * 4 + q), o);
                         }
-                        const uint32_t s1 = f16_pow2(eb[blk] - E);
-                        uint32_t o[16];
-                        e2m1_to_f16(cw, s1 | (s1 << 16), o);
-#pragma unroll
-                        for (int q = 0; q < 4; q++)
-                            st_shared_v4(bBase + (blk >> 1) * 8192 + swz_off(h, (blk & 1) * 4 + q), o + 4 * q);
                     }
                     wq[wb * 64 + h] = a.w[(int64_t)b * 64 + h] * pow2f(E);
                 }
@@ -583,11 +575,13 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
                         const uint4 cw = *reinterpret_cast<const uint4 *>(stg + rw * 64 + blk * 16);
                         const int e = (int)((sc4 >> (8 * blk)) & 0xFFu) - 127;
                         const uint32_t s1 = f16_pow2(e - E);
-                        uint32_t o[16];
-                        e2m1_to_f16(cw, s1 | (s1 << 16), o);
+                        const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
-                        for (int q = 0; q < 4; q++)
-                            st_shared_v4(aS + (blk >> 1) * 16384 + swz_off(rw, (blk & 1) * 4 + q), o + 4 * q);
+                        for (int q = 0; q < 4; q++) {
+                            uint32_t o[4];
+                            e2m1x8_to_f16(cws[q], s1 | (s1 << 16), o);
+                            st_shared_v4(aS + (blk >> 1) * 16384 + swz_off(rw, (blk & 1) * 4 + q), o);
+                        }
                     }
                     ek[qe * 128 + rw] = E;
                 }

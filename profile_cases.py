@@ -23,6 +23,8 @@ Cases:
   hca_decode_fp8    hca_attn on FP8 entries, 8 sequences x 8192 entries, 128 heads x 512
   out_proj          out_proj, 4096 tokens, 64 heads x 512 in 8 groups -> 1024 -> 4096
   decode_append     decode_append, 64 sequences, c = 512, dI = 128, m = 4 (one step)
+  compress_norm     csa_compress with the KV RMSNorm, n = 65536, c = 512, m = 4 (bf16, raw rows)
+  quantize          quantize_kv_fp8 of 262144 entries and quantize_index_fp4 of 2097152 keys
 """
 from __future__ import annotations
 
@@ -178,6 +180,29 @@ def case_decode_append(B=64, c=512, dI=128, m=4):
     return lambda: csa.decode_append(t, C_, Z, bias, win, tail, kvc, p, Ck=Ck, Zk=Zk, biask=biask, kIc=kIc)
 
 
+def case_compress_norm(m=4):
+    n, c = 65536, 512
+    C, Z = _bf16(1, n, c), _bf16(1, n, c)
+    bias = torch.randn(m, c, device="cuda") * 0.1
+    g = 1 + 0.1 * torch.randn(c, device="cuda")
+    out = torch.empty(1, n // m, c, device="cuda", dtype=torch.bfloat16)
+    raw = torch.empty_like(C)
+    return lambda: csa.csa_compress(C, Z, bias, m=m, rope_dims=64, want_raw=True, out=out, raw_out=raw,
+                                    kv_norm=g)
+
+
+def case_quantize():
+    kv = _bf16(262144, 512)
+    ki = _bf16(2097152, 128)
+    kv8 = torch.empty(262144, csa.KV_FP8_BYTES, dtype=torch.uint8, device="cuda")
+    ki4 = torch.empty(csa.lib().index_fp4_bytes(2097152), dtype=torch.uint8, device="cuda")
+
+    def run():
+        csa.quantize_kv_fp8(kv, out=kv8)
+        csa.quantize_index_fp4(ki, out=ki4)
+    return run
+
+
 def case_hca_decode():
     B, H, c, E, m = 8, 128, 512, 8192, 128
     t = E * m
@@ -239,6 +264,8 @@ CASES = {
     "hca_decode_fp8": case_hca_decode_fp8,
     "out_proj": case_out_proj,
     "decode_append": case_decode_append,
+    "compress_norm": case_compress_norm,
+    "quantize": case_quantize,
 }
 
 
