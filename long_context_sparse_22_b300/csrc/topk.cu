@@ -698,15 +698,35 @@ __global__ void __launch_bounds__(TK_THREADS) topk_final_kernel(TkLong a, int ca
         // every thread locates its items' chunks by binary search so all the
         // loads are in flight together
         int32_t *si = (int32_t *)(smc + cap);
-        for (int64_t j = tid; j < n; j += TK_THREADS) {
-            int lo = 0, hi = a.CH - 1;
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if ((int64_t)offs[mid] <= j) lo = mid; else hi = mid - 1;
+        // four items per thread per round: their sources first, then all eight
+        // loads in flight together, then the stores
+        for (int64_t j0 = tid; j0 < n; j0 += 4 * TK_THREADS) {
+            int64_t src[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const int64_t j = j0 + (int64_t)u * TK_THREADS;
+                int lo = 0, hi = a.CH - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if ((int64_t)offs[mid] <= j) lo = mid; else hi = mid - 1;
+                }
+                src[u] = j < n ? lo * a.CS + (j - offs[lo]) : -1;
             }
-            const int64_t src = lo * a.CS + (j - offs[lo]);
-            smc[j] = gk[src];
-            si[j] = gi[src];
+            uint32_t kv[4];
+            int32_t iv[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                kv[u] = src[u] >= 0 ? gk[src[u]] : 0u;
+                iv[u] = src[u] >= 0 ? gi[src[u]] : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const int64_t j = j0 + (int64_t)u * TK_THREADS;
+                if (j < n) {
+                    smc[j] = kv[u];
+                    si[j] = iv[u];
+                }
+            }
         }
         __syncthreads();
         constexpr int PT = 16;                 // candidates per thread in registers
