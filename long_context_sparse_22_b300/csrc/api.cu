@@ -100,7 +100,12 @@ RopeFreqs make_rope(int c, int r, double theta) {
     memset(&rf, 0, sizeof rf);
     rf.pairs = r / 2;
     rf.first = c - r;
-    for (int i = 0; i < r / 2; i++) rf.w[i] = pow(theta, -2.0 * i / (double)r);
+    for (int i = 0; i < r / 2; i++) {
+        rf.w[i] = pow(theta, -2.0 * i / (double)r);
+        const double f = rf.w[i] / (2.0 * 3.14159265358979323846);
+        rf.fh[i] = (float)f;
+        rf.fl[i] = (float)(f - (double)rf.fh[i]);
+    }
     return rf;
 }
 
@@ -665,8 +670,21 @@ static std::mutex g_aux_mu;
 struct AuxLease {
     int dev = -1;
     AuxSet set;
+    cudaStream_t waiter = nullptr;   // set once work was forked onto set.aux
+    // the join: record it on the auxiliary stream and make the caller's
+    // stream wait on it
+    cudaError_t join() {
+        cudaError_t e1 = cudaEventRecord(set.join, set.aux);
+        cudaError_t e2 = cudaStreamWaitEvent(waiter, set.join, 0);
+        waiter = nullptr;
+        return e1 != cudaSuccess ? e1 : e2;
+    }
     ~AuxLease() {
         if (dev < 0) return;
+        // an early return after the fork still joins, so the set goes back to
+        // the pool with nothing of this call pending that the caller's stream
+        // does not wait for
+        if (waiter != nullptr) (void)join();
         std::lock_guard<std::mutex> g(g_aux_mu);
         g_aux_free[dev].push_back(set);
     }
@@ -740,45 +758,46 @@ csa_status hybrid_decode(csa_dtype dtype, int64_t B, int32_t H, int32_t c, int32
                   &asc, &asc2);
     if (idx_out) idx = idx_out;
     unsigned *status = (unsigned *)ws;
-    // The HCA layer's attention does not depend on the CSA layer.  The CSA
-    // indexer (which streams kI at the HBM rate) and the top-k's candidate
-    // collection run first on every SM; the HCA attention then runs on an
-    // auxiliary stream, on all but a few SMs, beside the rest of the CSA top-k
-    // and the sparse attention, which need few CTAs.
+    // The HCA layer's attention does not depend on the CSA layer.  It starts
+    // first, on an auxiliary stream, on a third of the SMs; the CSA indexer
+    // (which streams kI at the HBM rate and needs few SMs to do so) runs
+    // beside it on the rest, then the CSA top-k and sparse attention.  (The
+    // Pro decode step, B = 8 at 1M positions, measured 0.237 / 0.193 / 0.193
+    // / 0.214 ms with 32 / 48 / 64 / 80 SMs for the HCA branch, against 0.246
+    // ms when the HCA attention waited for the CSA top-k's collection; the
+    // outputs are bitwise the same, since no kernel's result depends on its
+    // grid.)
     const bool concurrent = hca && dtype == CSA_BF16 && attn_tc_supported(dtype, c);
-    if (params->cache_format == CSA_CACHE_LOWP) {
-        StageScope si(CSA_STAGE_INDEXER, st);
-        CSA_TRY_CUDA(launch_indexer_fp4(B, E, params->m, qI, w, kIc, q_pos, (float *)sc, status,
-                                        spin_limit_of(params->spin_limit), 0, st),
-                     "indexer launch (MXFP4 keys)");
-    } else {
-        CSA_TRY(do_indexer(dtype, B, 1, hI, dI, E, params->m, qI, w, kIc, q_pos, (float *)sc, 0, status,
-                           params->spin_limit, st));
-    }
-    CSA_TRY(do_topk(B, 1, E, params->top_k, params->m, (const float *)sc, q_pos, (int32_t *)idx,
-                    (int32_t *)cnt, tks, st, 1));
     AuxLease ax;
+    int rest = 0;
     if (concurrent) {
         CSA_TRY(take_aux(ax));
         const int sms = device_sms();
+        const int hca_sms = sms / 3;
+        rest = sms - hca_sms;
         CSA_TRY_CUDA(cudaEventRecord(ax.set.fork, st), "fork");
         CSA_TRY_CUDA(cudaStreamWaitEvent(ax.set.aux, ax.set.fork, 0), "fork wait");
-        csa_status s2 = do_attn(dtype, B, 1, H, c, E2, 0, L, q2, q_pos, kvc2, nullptr, nullptr,
-                                kv_raw2, raw_pos0, sink2, out2, nullptr, params2, status, asc2,
-                                ax.set.aux, sms - 24);
-        // the join is recorded and waited on even if the launch failed, so
-        // the set goes back to the pool with nothing of this call pending
-        cudaError_t e1 = cudaEventRecord(ax.set.join, ax.set.aux);
-        cudaError_t e2 = cudaStreamWaitEvent(st, ax.set.join, 0);
-        if (s2 != CSA_OK) return s2;
-        CSA_TRY_CUDA(e1, "join");
-        CSA_TRY_CUDA(e2, "join wait");
+        ax.waiter = st;
+        CSA_TRY(do_attn(dtype, B, 1, H, c, E2, 0, L, q2, q_pos, kvc2, nullptr, nullptr, kv_raw2,
+                        raw_pos0, sink2, out2, nullptr, params2, status, asc2, ax.set.aux, hca_sms));
     }
+    if (params->cache_format == CSA_CACHE_LOWP) {
+        StageScope si(CSA_STAGE_INDEXER, st);
+        CSA_TRY_CUDA(launch_indexer_fp4(B, E, params->m, qI, w, kIc, q_pos, (float *)sc, status,
+                                        spin_limit_of(params->spin_limit), rest, st),
+                     "indexer launch (MXFP4 keys)");
+    } else {
+        CSA_TRY(do_indexer(dtype, B, 1, hI, dI, E, params->m, qI, w, kIc, q_pos, (float *)sc, 0, status,
+                           params->spin_limit, st, rest));
+    }
+    CSA_TRY(do_topk(B, 1, E, params->top_k, params->m, (const float *)sc, q_pos, (int32_t *)idx,
+                    (int32_t *)cnt, tks, st, 1));
     CSA_TRY(do_topk(B, 1, E, params->top_k, params->m, (const float *)sc, q_pos, (int32_t *)idx,
                     (int32_t *)cnt, tks, st, 2));
     CSA_TRY(do_attn(dtype, B, 1, H, c, E, params->top_k, L, q, q_pos, kvc, (const int32_t *)idx,
                     (const int32_t *)cnt, kv_raw, raw_pos0, sink, out, nullptr, params, status, asc,
                     st));
+    if (concurrent) CSA_TRY_CUDA(ax.join(), "join");
     if (!concurrent && hca) {
         CSA_TRY(do_attn(dtype, B, 1, H, c, E2, 0, L, q2, q_pos, kvc2, nullptr, nullptr, kv_raw2,
                         raw_pos0, sink2, out2, nullptr, params2, status, asc2, st));

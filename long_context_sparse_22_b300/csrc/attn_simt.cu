@@ -26,7 +26,7 @@ constexpr int AW_WH = 4;       // heads per item
 
 template <typename T, int C>
 __global__ void __launch_bounds__(AW_WARPS * 32)
-attn_warp_kernel(const AttnArgs a, int64_t n_items) {
+attn_warp_kernel(const __grid_constant__ AttnArgs a, int64_t n_items) {
     constexpr int DPL = C / 32;                 // dims per lane in PV and the epilogue
     constexpr int VN = Vec<T>::N;
     extern __shared__ float smq[];              // [AW_WARPS][AW_WH][C]
@@ -65,7 +65,7 @@ attn_warp_kernel(const AttnArgs a, int64_t n_items) {
             const float pv = __shfl_xor_sync(0xffffffffu, v[i], 1);
             if (d >= a.rope.first) {
                 float cs, sn;
-                rope_cos_sin((double)t, a.rope.w[(d - a.rope.first) >> 1], cs, sn);
+                rope_cos_sin(a.rope, t, (d - a.rope.first) >> 1, cs, sn);
                 v[i] = (d & 1) ? pv * sn + v[i] * cs : v[i] * cs - pv * sn;
             }
             qs[h * C + d] = v[i] * sl2;
@@ -177,7 +177,7 @@ attn_warp_kernel(const AttnArgs a, int64_t n_items) {
             const float po = __shfl_xor_sync(0xffffffffu, o, 1);
             if (a.derotate && d >= a.rope.first) {
                 float cs, sn;
-                rope_cos_sin(-(double)t, a.rope.w[(d - a.rope.first) >> 1], cs, sn);
+                rope_cos_sin(a.rope, -t, (d - a.rope.first) >> 1, cs, sn);
                 o = (d & 1) ? po * sn + o * cs : o * cs - po * sn;
             }
             from_f(og[h * C + d], o);

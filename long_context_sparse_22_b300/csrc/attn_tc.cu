@@ -367,7 +367,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 const int q = i / a.rope.pairs, pi = i - q * a.rope.pairs;
                 const int64_t tq = q == 0 ? (a.qpi == 1 ? f.t : a.q_pos[f.bt]) : (q < f.nq ? a.q_pos[f.bt + q] : f.t);
                 float c_, s_;
-                rope_cos_sin((double)tq, a.rope.w[pi], c_, s_);
+                rope_cos_sin(a.rope, tq, pi, c_, s_);
                 cs_s[i] = c_;
                 cs_s[256 + i] = s_;
             }
@@ -912,7 +912,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             {
                 const int dlast = (Cfg::NC - 1) * 128 + quarter * 32 + lane;
                 if (!packed && a.chunk_tiles == 0 && a.derotate && dlast >= a.rope.first)
-                    rope_cos_sin(-(double)f.t, a.rope.w[(dlast - a.rope.first) >> 1], dcr, dsr);
+                    rope_cos_sin(a.rope, -f.t, (dlast - a.rope.first) >> 1, dcr, dsr);
             }
             // item end: the four threads of a head add their partial sums
 #pragma unroll
@@ -952,7 +952,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         cr = dcr;
                         sr = dsr;
                     } else {
-                        rope_cos_sin(-(double)f.t, a.rope.w[(d - a.rope.first) >> 1], cr, sr);
+                        rope_cos_sin(a.rope, -f.t, (d - a.rope.first) >> 1, cr, sr);
                     }
                 }
                 float sgn = (lane & 1) ? sr : -sr;
@@ -984,9 +984,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         const int q0 = hb / a.H, q1 = (hb + 31) / a.H;
                         float cr0 = 1.f, sr0 = 0.f, cr1 = 1.f, sr1 = 0.f;
                         if (rot) {
-                            const double w_ = a.rope.w[(d - a.rope.first) >> 1];
-                            rope_cos_sin(-(double)(q0 < f.nq ? a.q_pos[f.bt + q0] : f.t), w_, cr0, sr0);
-                            rope_cos_sin(-(double)(q1 < f.nq ? a.q_pos[f.bt + q1] : f.t), w_, cr1, sr1);
+                            const int pi_ = (d - a.rope.first) >> 1;
+                            rope_cos_sin(a.rope, -(q0 < f.nq ? a.q_pos[f.bt + q0] : f.t), pi_, cr0, sr0);
+                            rope_cos_sin(a.rope, -(q1 < f.nq ? a.q_pos[f.bt + q1] : f.t), pi_, cr1, sr1);
                         }
 #pragma unroll
                         for (int h = 0; h < 32; h++) {
@@ -1036,7 +1036,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 // over the chunks that hold some of the query's tiles, in a fixed order, then
 // de-rotation.  One CTA per (query, head).
 template <int C>
-__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnTcArgs a) {
+__global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant__ AttnTcArgs a) {
     __shared__ float s_sc[64], s_red[4];
     __shared__ float s_M, s_den;
     const int64_t bt = blockIdx.x;
@@ -1092,7 +1092,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnTcArgs a) {
         y1 = den > 0.f ? y1 / den : 0.f;
         if (a.derotate && d >= a.rope.first) {
             float cr, sr;
-            rope_cos_sin(-(double)t, a.rope.w[(d - a.rope.first) >> 1], cr, sr);
+            rope_cos_sin(a.rope, -t, (d - a.rope.first) >> 1, cr, sr);
             const float r0 = y0 * cr - y1 * sr, r1 = y0 * sr + y1 * cr;
             y0 = r0;
             y1 = r1;

@@ -21,19 +21,38 @@ constexpr int MAX_ROPE_PAIRS = 256;
 struct RopeFreqs {
     int pairs;    // r / 2
     int first;    // c - r: first rotary channel
-    double w[MAX_ROPE_PAIRS];
+    double w[MAX_ROPE_PAIRS];       // theta^(-2i/r)
+    float fh[MAX_ROPE_PAIRS];       // w / (2 pi) as fh + fl (fh the float
+    float fl[MAX_ROPE_PAIRS];       // nearest to it, fl the float nearest the rest)
 };
 
-// Angle p * w reduced to [-pi, pi] in double (two-constant Cody-Waite style
-// reduction by 2*pi), then the float cosine and sine of the reduced angle.
-// Positions reach 2^20, where a float product p * w would already carry an
-// absolute error of several hundredths of a radian.
-__device__ __forceinline__ void rope_cos_sin(double p, double w, float &cs, float &sn) {
+// cos and sin of the angle p * w_i of rotary pair i.
+//
+// |p| < 2^24 (every position of a 16M-token context): the angle is reduced in
+// turns, in fp32 only.  With f = w / (2 pi) split as fh + fl, p * fh is split
+// exactly into hi + lo by one fma (the fma two-product of Ogita, Rump and
+// Oishi, 2005; p and fh are floats); hi - rint(hi) is
+// exact, so t = frac(p f) = (hi - rint(hi)) + (p * fl + lo) carries one
+// rounding of about 2^-25 turns, and sincospif gives sin / cos of 2 pi t.  (The
+// angle itself reaches 2^20 rad, where a float product p * w would already be
+// off by hundredths of a radian.)
+// Larger |p|: the same reduction in double, by 2 pi split in two parts
+// (Cody-Waite style), then the float sine and cosine of the reduced angle.
+__device__ __forceinline__ void rope_cos_sin(const RopeFreqs &rf, int64_t p, int i, float &cs, float &sn) {
+    if (p > -(1LL << 24) && p < (1LL << 24)) {
+        const float pf = (float)p;
+        const float fh = rf.fh[i];
+        const float hi = pf * fh;
+        const float lo = fmaf(pf, fh, -hi);
+        const float t = (hi - rintf(hi)) + fmaf(pf, rf.fl[i], lo);
+        sincospif(2.0f * t, &sn, &cs);
+        return;
+    }
     const double two_pi_hi = 6.283185307179586;           // 2*pi rounded to double
     const double two_pi_lo = 2.4492935982947064e-16;      // 2*pi - two_pi_hi
     const double inv_two_pi = 0.15915494309189535;
-    double a = p * w;
-    double k = rint(a * inv_two_pi);
+    const double a = (double)p * rf.w[i];
+    const double k = rint(a * inv_two_pi);
     double r = fma(-k, two_pi_hi, a);
     r = fma(-k, two_pi_lo, r);
     sincosf((float)r, &sn, &cs);

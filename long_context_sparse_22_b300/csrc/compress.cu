@@ -24,7 +24,7 @@ __device__ __forceinline__ void rotate_vec(float *v, int ch0, int64_t pos, const
         int ch = ch0 + 2 * q;
         if (ch < rf.first) continue;
         float cs, sn;
-        rope_cos_sin((double)pos, rf.w[(ch - rf.first) >> 1], cs, sn);
+        rope_cos_sin(rf, pos, (ch - rf.first) >> 1, cs, sn);
         float x0 = v[2 * q], x1 = v[2 * q + 1];
         v[2 * q] = x0 * cs - x1 * sn;
         v[2 * q + 1] = x0 * sn + x1 * cs;
@@ -46,11 +46,11 @@ __device__ __forceinline__ void softmax_step(float a, float v, float &mx, float 
 }
 
 template <typename T>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 3)
 compress_kernel(const T *__restrict__ C, const T *__restrict__ Z, const float *__restrict__ bias,
                 const T *__restrict__ Cb, const T *__restrict__ Zb, const float *__restrict__ biasb,
                 T *__restrict__ out, T *__restrict__ raw_out, int64_t B, int64_t n, int c, int m,
-                int overlap, int64_t E, int64_t Eg, RopeFreqs rope) {
+                int overlap, int64_t E, int64_t Eg, const __grid_constant__ RopeFreqs rope) {
     constexpr int N = Vec<T>::N;
     const int cv = c / N;
     int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -67,11 +67,20 @@ compress_kernel(const T *__restrict__ C, const T *__restrict__ Z, const float *_
 
     const int64_t row0 = e * m;
     const int slots = (int)((n - row0) < m ? (n - row0) : m);   // < m only for a partial tail
+    // the next slot's rows are loaded before this slot's arithmetic, so two
+    // slots' loads are in flight per thread
+    float z[N], v[N];
+    if (slots > 0) {
+        Vec<T>::load_stream(Zs + row0 * c + ch0, z);
+        Vec<T>::load_stream(Cs + row0 * c + ch0, v);
+    }
     for (int s = 0; s < slots; s++) {
-        float z[N], v[N], bs[N];
+        float zn[N], vn[N], bs[N];
         const int64_t row = row0 + s;
-        Vec<T>::load_stream(Zs + row * c + ch0, z);
-        Vec<T>::load_stream(Cs + row * c + ch0, v);
+        if (s + 1 < slots) {
+            Vec<T>::load_stream(Zs + (row + 1) * c + ch0, zn);
+            Vec<T>::load_stream(Cs + (row + 1) * c + ch0, vn);
+        }
         Vec<float>::load(bias + (int64_t)s * c + ch0, bs);
         if constexpr (N == 8) Vec<float>::load(bias + (int64_t)s * c + ch0 + 4, bs + 4);
 #pragma unroll
@@ -80,6 +89,8 @@ compress_kernel(const T *__restrict__ C, const T *__restrict__ Z, const float *_
             rotate_vec<T>(v, ch0, row, rope);
             Vec<T>::store(raw_out + (b * n + row) * c + ch0, v);
         }
+#pragma unroll
+        for (int i = 0; i < N; i++) { z[i] = zn[i]; v[i] = vn[i]; }
     }
     if (e >= E) return;                 // partial tail block: raw rows only
     if (overlap && e > 0) {
@@ -113,7 +124,7 @@ template <typename T>
 __global__ void __launch_bounds__(CW_THREADS)
 compress_wide_kernel(const T *__restrict__ C, const T *__restrict__ Z, const float *__restrict__ bias,
                      T *__restrict__ out, T *__restrict__ raw_out, int64_t n, int c, int m, int64_t E,
-                     int64_t Eg, RopeFreqs rope) {
+                     int64_t Eg, const __grid_constant__ RopeFreqs rope) {
     constexpr int N = Vec<T>::N;
     __shared__ float part[CW_THREADS][3][N];
     const int V = c / N;                  // vectors per row (<= CW_THREADS)
@@ -210,7 +221,7 @@ __global__ void __launch_bounds__(256)
 compress_norm_kernel(const T *__restrict__ C, const T *__restrict__ Z, const float *__restrict__ bias,
                      const T *__restrict__ Cb, const T *__restrict__ Zb, const float *__restrict__ biasb,
                      T *__restrict__ out, T *__restrict__ raw_out, int64_t n, int c, int m, int overlap,
-                     int64_t E, int64_t Eg, RopeFreqs rope, const float *__restrict__ gain, float eps) {
+                     int64_t E, int64_t Eg, const __grid_constant__ RopeFreqs rope, const float *__restrict__ gain, float eps) {
     constexpr int N = Vec<T>::N;
     __shared__ float red[8];
     const int V = c / N;
@@ -386,7 +397,7 @@ __device__ __forceinline__ void ld_tail(const __nv_bfloat16 *p, float *o) {
 template <typename T>
 __device__ void append_entry(const AppendArgs &a, const T *tl, int width, int offC, int offZ,
                              int offCb, int offZb, const float *bias, const float *biasb,
-                             int64_t i, int base, int prev_base, const RopeFreqs &rope, T *dst,
+                             int64_t i, int base, int prev_base, const RopeFreqs *rope, T *dst,
                              const float *gain, float (*part)[3][Vec<T>::N], float *red) {
     constexpr int N = Vec<T>::N;
     const int V = width / N;
@@ -429,7 +440,7 @@ __device__ void append_entry(const AppendArgs &a, const T *tl, int width, int of
         for (int q = 0; q < N; q++) o[q] = active ? acc[q] / den[q] : 0.f;
         rms_scale<N>(o, active, ch0, width, gain, a.norm_eps, red);
         if (!active) return;
-        rotate_vec<T>(o, ch0, (i + 1) * a.m - 1, rope);
+        if (rope) rotate_vec<T>(o, ch0, (i + 1) * a.m - 1, *rope);
         Vec<T>::store(dst + ch0, o);
         return;
     }
@@ -461,7 +472,7 @@ __device__ void append_entry(const AppendArgs &a, const T *tl, int width, int of
         float o[N];
 #pragma unroll
         for (int q = 0; q < N; q++) o[q] = acc[q] / den[q];
-        rotate_vec<T>(o, ch0, (i + 1) * a.m - 1, rope);
+        if (rope) rotate_vec<T>(o, ch0, (i + 1) * a.m - 1, *rope);
         Vec<T>::store(dst + ch0, o);
         return;
     }
@@ -504,7 +515,7 @@ __device__ void append_entry(const AppendArgs &a, const T *tl, int width, int of
             }
             mx[q] = s_ / d;
         }
-        rotate_vec<T>(mx, ch0, (i + 1) * a.m - 1, rope);
+        if (rope) rotate_vec<T>(mx, ch0, (i + 1) * a.m - 1, *rope);
         Vec<T>::store(dst + ch0, mx);
     }
     __syncthreads();
@@ -512,7 +523,7 @@ __device__ void append_entry(const AppendArgs &a, const T *tl, int width, int of
 
 // One CTA per sequence.
 template <typename T>
-__global__ void __launch_bounds__(CW_THREADS) decode_append_kernel(const AppendArgs a) {
+__global__ void __launch_bounds__(CW_THREADS) decode_append_kernel(const __grid_constant__ AppendArgs a) {
     constexpr int N = Vec<T>::N;
     __shared__ float part[CW_THREADS][3][N];
     __shared__ float red[CW_THREADS / 32];
@@ -567,15 +578,12 @@ __global__ void __launch_bounds__(CW_THREADS) decode_append_kernel(const AppendA
     const int base = (int)((i * a.m) % a.S);
     const int prev_base = (int)(((i + a.S / a.m - 1) * a.m) % a.S);
     append_entry<T>(a, tl, a.c, tail_off(a.c, a.dI, 0), tail_off(a.c, a.dI, 1), tail_off(a.c, a.dI, 4),
-                    tail_off(a.c, a.dI, 5), a.bias, a.biasb, i, base, prev_base, a.rope,
+                    tail_off(a.c, a.dI, 5), a.bias, a.biasb, i, base, prev_base, &a.rope,
                     (T *)a.kvc + (b * a.E_cap + i) * a.c, a.kv_norm, part, red);
     if (a.Ck == nullptr) return;
     __syncthreads();
-    RopeFreqs none;
-    none.pairs = 0;
-    none.first = a.dI;
     append_entry<T>(a, tl, a.dI, tail_off(a.c, a.dI, 2), tail_off(a.c, a.dI, 3), tail_off(a.c, a.dI, 6),
-                    tail_off(a.c, a.dI, 7), a.biask, a.biaskb, i, base, prev_base, none,
+                    tail_off(a.c, a.dI, 7), a.biask, a.biaskb, i, base, prev_base, nullptr,
                     (T *)a.kIc + (b * a.E_cap + i) * a.dI, nullptr, part, red);
 }
 

@@ -57,11 +57,9 @@ struct IdxCfg {
     static constexpr int B_BYTES = N * DI * 2;
     static constexpr int ACC_COLS = N;
     static constexpr int TMEM_COLS = QT == 4 ? 512 : 128;
-    // eight epilogue warps: for QT = 4, two column groups (tokens) over the four
-    // TMEM lane quarters; for QT = 1, two groups taking alternate tiles
-    static constexpr int EPI_WARPS = 8;
+    static constexpr int EPI_WARPS = QT == 4 ? 8 : 4;
     static constexpr int THREADS = 64 + EPI_WARPS * 32;
-    static constexpr int TOK_PER_WARP = QT == 1 ? 1 : QT * 4 / EPI_WARPS;
+    static constexpr int TOK_PER_WARP = QT * 4 / EPI_WARPS;
     static constexpr int W_FLOATS = EPI_WARPS * TOK_PER_WARP * HI;
     static constexpr int SMEM = STAGES * A_BYTES + B_BYTES + W_FLOATS * 4 + 256 + 1024;
 };
@@ -145,7 +143,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tc::mbar_init(bempty, 1);
         for (int i = 0; i < 2; i++) {
             tc::mbar_init(&accfull[i], 1);
-            tc::mbar_init(&accempty[i], QT == 1 ? Cfg::EPI_WARPS / 2 : Cfg::EPI_WARPS);
+            tc::mbar_init(&accempty[i], Cfg::EPI_WARPS);
         }
         tc::mbar_init(mdone, 1);
         *abort_flag = 0;
@@ -249,9 +247,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // ---------------------------------------------------------- epilogue
         const int ew = warp - 2;                 // 0 .. EPI_WARPS-1
         const int quarter = warp & 3;            // TMEM lanes this warp may read
-        constexpr bool ALT = QT == 1;            // the two groups take alternate tiles
-        const int egrp = ew >> 2;
-        const int cgroup = ALT ? 0 : egrp;       // column group
+        const int cgroup = ew >> 2;              // column group
         constexpr int TOK_PER_WARP = Cfg::TOK_PER_WARP;
         float *w_s = w_all + ew * TOK_PER_WARP * Cfg::HI;   // this warp's tokens only
         const int row = quarter * 32 + lane;     // entry row within the tile
@@ -276,10 +272,6 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 nvt[u] = t < a.T ? visible_count(a.q_pos[(int64_t)it.b * a.T + t], a.m, a.E) : -1;
             }
             for (int jt = it.jt0; jt < it.jt1; jt++) {
-                if (ALT && acc != egrp) {        // the other group's tile
-                    if (++acc == 2) { acc = 0; accphase ^= 1; }
-                    continue;
-                }
                 if (!tc::mbar_wait(&accfull[acc], accphase, a.status, abort_flag, a.spin)) { ok = false; break; }
                 tc::fence_after_sync();
                 const int64_t j = (int64_t)jt * 128 + row;

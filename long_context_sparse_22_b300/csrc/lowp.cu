@@ -223,10 +223,8 @@ struct Fp4Cfg {
     static constexpr int OFF_MISC = OFF_B + B_BYTES;
     static constexpr int MISC_BYTES = 4096;               // barriers, wq [2][64], ek [NEK][128]
     static constexpr int SMEM = OFF_MISC + MISC_BYTES + 1024;
-    static constexpr int EPI0 = 2;                        // epilogue warps 2 .. 9
-    static constexpr int EGROUPS = 2;                     // epilogue groups of 4 warps, alternate tiles
-    static constexpr int CONV0 = 10;                      // converter warps 10 .. 13
-    static constexpr int CGROUPS = 1;                     // converter groups of 4 warps
+    static constexpr int EPI0 = 2;                        // epilogue warps 2 .. 5
+    static constexpr int CONV0 = 6;                       // converter warps 6 .. 13 (two groups of 4)
     static constexpr int THREADS = 448;
     static constexpr int TMEM_COLS = 128;
 };
@@ -334,7 +332,7 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
         tc::mbar_init(bempty, 1);
         for (int i = 0; i < 2; i++) {
             tc::mbar_init(&wfull[i], 4);
-            tc::mbar_init(&wempty[i], 4 * Cfg::EGROUPS);
+            tc::mbar_init(&wempty[i], 4);
             tc::mbar_init(&accfull[i], 1);
             tc::mbar_init(&accempty[i], 4);
         }
@@ -423,8 +421,7 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
         }
     } else if (warp < Cfg::CONV0) {
         // -------------------------------------------------------- epilogue
-        // each warp one TMEM lane quarter; the groups take alternate tiles
-        const int egrp = (warp - Cfg::EPI0) >> 2;
+        // each warp one TMEM lane quarter; the two accumulators alternate
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         uint32_t g = 0, ii = 0;
@@ -437,7 +434,6 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
             const float *wt = wq + wb * 64;
             const int64_t nv = visible_count(a.q_pos[b], a.m, a.E);
             for (int jt = jt0; jt < jt1; jt++, g++) {
-                if ((int)(g % Cfg::EGROUPS) != egrp) continue;
                 const int acc = (int)(g & 1);
                 const uint32_t accph = (g >> 1) & 1;
                 const int q = g % Cfg::NEK;
@@ -484,8 +480,8 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
         }
     } else {
         // ------------------------------------------------------ converters
-        // CGROUPS groups of four warps take the tiles in turn; group 0 also
-        // converts each item's query (its 64 threads of one head each)
+        // two groups of four warps take alternate tiles; group 0 also converts
+        // each item's query (its 64 threads of one head each)
         const int cgrp = (warp - Cfg::CONV0) >> 2;
         const int ct = (threadIdx.x - Cfg::CONV0 * 32) & 127;   // the tile row this thread converts
         const uint32_t aBase = tc::smem_u32(sA), bBase = tc::smem_u32(sB);
@@ -551,7 +547,7 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
             // the key tiles of this group: 128 rows, one per thread
             const int64_t first = (int64_t)b * a.E;
             for (int jt = jt0; jt < jt1; jt++, g++) {
-                if ((int)(g % Cfg::CGROUPS) != cgrp) continue;
+                if ((int)(g & 1) != cgrp) continue;
                 const int s = g % Cfg::SST, st = g % Cfg::AST, qe = g % Cfg::NEK;
                 if (!tc::mbar_wait(&sfull[s], (g / Cfg::SST) & 1, a.status, abort_flag, a.spin) ||
                     !tc::mbar_wait(&aempty[st], ((g / Cfg::AST) & 1) ^ 1, a.status, abort_flag, a.spin) ||

@@ -225,16 +225,20 @@ def test_sparse_attn(csa, orc, dtype, B, T, H, c, E, k, m, n_win, r, derot):
         assert np.abs(gl[b] - rl).max() <= (1e-4 if dtype == "f32" else 1e-2)
 
 
-@pytest.mark.parametrize("dtype,B,T,H,c,E,m,n_win,r", [
-    ("bf16", 1, 70, 16, 128, 64, 128, 128, 64),
-    ("bf16", 2, 1, 128, 512, 700, 128, 128, 64),
-    ("f32", 1, 40, 4, 64, 30, 4, 16, 32),
+# t0 > 0: the last query sits at position t0 (past 2^24, where the kernels'
+# rotary angles take their double-precision reduction), with every entry visible
+@pytest.mark.parametrize("dtype,B,T,H,c,E,m,n_win,r,t0", [
+    ("bf16", 1, 70, 16, 128, 64, 128, 128, 64, 0),
+    ("bf16", 2, 1, 128, 512, 700, 128, 128, 64, 0),
+    ("f32", 1, 40, 4, 64, 30, 4, 16, 32, 0),
+    ("bf16", 1, 3, 64, 512, 200, 128, 128, 64, (1 << 25) + 77),
+    ("f32", 1, 5, 4, 64, 30, 4, 16, 32, (1 << 26) + 3),
 ])
-def test_hca_attn(csa, orc, dtype, B, T, H, c, E, m, n_win, r):
+def test_hca_attn(csa, orc, dtype, B, T, H, c, E, m, n_win, r, t0):
     seed = 500 + E
     q = synth.normal(seed, 1, (B, T, H, c), 1.0, dtype)
     kvc = synth.normal(seed, 2, (B, E, c), 1.0, dtype)
-    t_last = E * m + m // 2
+    t_last = t0 if t0 else E * m + m // 2
     L = n_win + T
     kv_raw = synth.normal(seed, 3, (B, L, c), 1.0, dtype)
     sink = synth.normal(seed, 4, (H,), 1.0, "f32")
