@@ -40,7 +40,7 @@ struct RopeFreqs {
 // (Cody-Waite style), then the float sine and cosine of the reduced angle.
 __device__ __forceinline__ void rope_cos_sin(const RopeFreqs &rf, int64_t p, int i, float &cs, float &sn) {
     if (p > -(1LL << 24) && p < (1LL << 24)) {
-        const float pf = (float)p;
+        const float pf = (float)(int)p;     // through int32: a 64-bit convert runs on the fp64 pipe
         const float fh = rf.fh[i];
         const float hi = pf * fh;
         const float lo = fmaf(pf, fh, -hi);

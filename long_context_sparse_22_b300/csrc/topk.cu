@@ -20,11 +20,16 @@
 // sample.
 //
 // Many rows (prefill): one warp per row.
-// Few long rows (decode, up to 262144 entries): two launches: (1) the row's
-// chunks are spread over many CTAs, each deriving the row's sampled bound and
-// keeping its keys >= lo in index order, (2) one CTA per row runs the exact
-// selection on the candidates.
+// Few long rows (decode, up to 262144 entries): one launch, a cluster of eight
+// CTAs per row, the row's keys in their registers; each CTA derives the row's
+// sampled bound and keeps its keys >= lo in index order in shared memory, and
+// the cluster's first CTA reads all of them through distributed shared memory
+// and runs the exact selection.  Longer rows: two launches, (1) the row's
+// chunks spread over many CTAs, each keeping its keys >= lo in global memory,
+// (2) one CTA per row running the exact selection on the candidates.
 #include <mutex>
+
+#include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -573,6 +578,38 @@ __device__ Thr block_threshold(const uint32_t (&kr)[NK], int nk, int k, uint32_t
     return t;
 }
 
+// The k largest of n > k candidates held in registers, thread t holding
+// candidates PT t .. PT t + PT - 1 in index order (nk of them valid), written
+// to orow in index order; id(u) gives the index of this thread's candidate u.
+// The threshold from block_threshold, then one block scan of the per-thread
+// counts of keys above it and of ties places every kept index.
+template <int PT, typename IdF>
+__device__ void select_registers(const uint32_t (&ck)[PT], int nk, int k, IdF id, uint32_t *hist,
+                                 uint32_t *red, uint32_t *wsum, int32_t *orow) {
+    const Thr th = block_threshold(ck, nk, k, hist, red);
+    const uint32_t t = th.tau;
+    const uint32_t need_eq = th.need_eq;
+    uint32_t n_gt = 0, n_eq = 0;
+#pragma unroll
+    for (int u = 0; u < PT; u++) {
+        n_gt += ck[u] > t && u < nk ? 1u : 0u;
+        n_eq += ck[u] == t && u < nk ? 1u : 0u;
+    }
+    uint32_t tot2;
+    const uint32_t ex2 = block_excl_scan((n_eq << 16) | n_gt, wsum, &tot2);
+    uint32_t eq_before = ex2 >> 16, gt_before = ex2 & 0xffffu;
+    uint32_t pos = gt_before + (eq_before < need_eq ? eq_before : need_eq);
+#pragma unroll
+    for (int u = 0; u < PT; u++) {
+        bool sel = false;
+        if (u < nk) {
+            if (ck[u] > t) sel = true;
+            else if (ck[u] == t) sel = eq_before++ < need_eq;
+        }
+        if (sel) orow[pos++] = id(u);
+    }
+}
+
 // (1) per chunk of a long row: the row's sampled bound lo (every chunk CTA
 // derives the same value from the same evenly spaced sample), then the
 // chunk's keys >= lo in index order.  Each warp compacts its own contiguous
@@ -743,30 +780,8 @@ __global__ void __launch_bounds__(TK_THREADS) topk_final_kernel(TkLong a, int ca
             __shared__ uint32_t hist[256];
             const int64_t left = n - (int64_t)tid * PT;
             const int nk = (int)(left < 0 ? 0 : (left > PT ? PT : left));
-            const Thr th = block_threshold(ck, nk, a.k, hist, red);
-            const uint32_t t = th.tau;
-            const uint32_t need_eq = th.need_eq;
-            // ordered emit: one scan of the per-thread counts of kept and of tied keys
-            uint32_t n_gt = 0, n_eq = 0;
-#pragma unroll
-            for (int u = 0; u < PT; u++) {
-                n_gt += ck[u] > t ? 1u : 0u;
-                n_eq += ck[u] == t && u < nk ? 1u : 0u;
-            }
-            uint32_t tot2;
-            const uint32_t ex2 = block_excl_scan((n_eq << 16) | n_gt, sh.wsum, &tot2);
-            uint32_t eq_before = ex2 >> 16, gt_before = ex2 & 0xffffu;
-            uint32_t pos = gt_before + (eq_before < need_eq ? eq_before : need_eq);
-#pragma unroll
-            for (int u = 0; u < PT; u++) {
-                const int64_t j = (int64_t)tid * PT + u;
-                bool sel = false;
-                if (u < nk) {
-                    if (ck[u] > t) sel = true;
-                    else if (ck[u] == t) sel = eq_before++ < need_eq;
-                }
-                if (sel) orow[pos++] = si[j];
-            }
+            select_registers(ck, nk, a.k, [&](int u) { return si[(int64_t)tid * PT + u]; }, hist, red,
+                             sh.wsum, orow);
         } else {
             select_core(sh, n, a.k, [&](int64_t j) { return smc[j]; }, [&](int64_t j) { return si[j]; },
                         orow);
@@ -782,6 +797,153 @@ __global__ void __launch_bounds__(TK_THREADS) topk_final_kernel(TkLong a, int ca
                     [&](int64_t j) { return gi[where(j)]; }, orow);
     }
     if (tid == 0) a.cnt[row] = a.k;
+}
+
+// Few long rows, one launch: a cluster of TC_CL CTAs per row.  CTA r of the
+// cluster holds the keys of the r-th slice of the row in registers (thread t
+// a contiguous run of KPT keys).  Every CTA derives the same sampled bound lo
+// from the same evenly spaced sample (block-wide, bit by bit); each keeps its
+// keys >= lo in index order in its own shared memory.  Rank 0 then reads the
+// cluster's candidates through distributed shared memory, rank by rank (so in
+// index order), into registers and runs the exact selection there.  If the
+// sample misses (fewer than k candidates) or a CTA's candidates overflow,
+// rank 0 runs the exact selection over the whole row from global memory.
+constexpr int TC_CL = 8;              // CTAs per row
+constexpr int TC_CAPL = 2048;         // candidates a CTA keeps
+constexpr int TC_PT = 16;             // candidates per thread in rank 0's selection
+
+template <int KPT>
+__global__ void __cluster_dims__(TC_CL, 1, 1) __launch_bounds__(TK_THREADS, 1)
+topk_cluster_kernel(const float *__restrict__ scores, const int64_t *__restrict__ q_pos,
+                    int32_t *__restrict__ idx, int32_t *__restrict__ cnt, int64_t E, int k, int m) {
+    __shared__ union {
+        struct {
+            uint32_t key[TC_CAPL];
+            int32_t id[TC_CAPL];
+        } c;
+        TkShared tk;                  // rank 0's whole-row fallback, after the candidates are dead
+    } u;
+    __shared__ uint32_t s_count;      // candidates kept here; ~0u: overflow
+    __shared__ uint32_t wsum[32];
+    __shared__ uint32_t hist[256];
+    __shared__ uint32_t red[40];
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    const unsigned rank = cl.block_rank();
+    const int tid = threadIdx.x;
+    const int64_t row = blockIdx.x / TC_CL;
+    const int64_t nv = visible_count(q_pos[row], m, E);
+    int32_t *orow = idx + row * (int64_t)k;
+    if (nv <= k) {                    // the same in every CTA of the cluster
+        if (rank == 0) {
+            for (int i = tid; i < k; i += TK_THREADS) orow[i] = i < nv ? i : -1;
+            if (tid == 0) cnt[row] = (int32_t)nv;
+        }
+        return;
+    }
+    const float *s = scores + row * E;
+    // this CTA's slice (a multiple of 4 keys long) and this thread's run
+    const int64_t per = (((nv + TC_CL - 1) / TC_CL) + 3) & ~(int64_t)3;
+    const int64_t c0 = (int64_t)rank * per;
+    const int64_t c1 = c0 + per < nv ? c0 + per : nv;
+    const int64_t j0 = c0 + (int64_t)tid * KPT;
+    const int64_t left = c1 - j0;
+    const int nk = (int)(left < 0 ? 0 : (left > KPT ? KPT : left));
+    uint32_t key[KPT];
+    const bool vec = (((uintptr_t)s) & 15) == 0;
+#pragma unroll
+    for (int q = 0; q < KPT / 4; q++) {
+        if (vec && 4 * q + 4 <= nk) {
+            const float4 v = __ldcs(reinterpret_cast<const float4 *>(s + j0 + 4 * q));
+            key[4 * q] = score_key(v.x);
+            key[4 * q + 1] = score_key(v.y);
+            key[4 * q + 2] = score_key(v.z);
+            key[4 * q + 3] = score_key(v.w);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; e++) key[4 * q + e] = 4 * q + e < nk ? score_key(__ldcs(s + j0 + 4 * q + e)) : 0u;
+        }
+    }
+    // the bound: the top 24 bits of the r-th largest of TK_LSAMPLE evenly
+    // spaced keys (two per thread), the largest 24-bit prefix that at least r
+    // sample keys reach
+    const int S = (int)(nv < TK_LSAMPLE ? nv : TK_LSAMPLE);
+    uint32_t sk[2];
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+        const int i = tid + h * TK_THREADS;
+        const int64_t pos = S == TK_LSAMPLE ? (((int64_t)i * nv) >> 10) : i;   // TK_LSAMPLE = 2^10
+        sk[h] = i < S ? score_key(s[pos]) : 0u;
+    }
+    const int r = S < TK_LSAMPLE ? k : sample_rank(nv, k, S);
+    uint32_t lo = 0;
+    if (r < S) {
+#pragma unroll 1
+        for (int b = 31; b >= 8; b--) {
+            const uint32_t c = lo | (1u << b);
+            const int n0 = __syncthreads_count(sk[0] >= c);
+            const int n1 = __syncthreads_count(sk[1] >= c);
+            if (n0 + n1 >= r) lo = c;
+        }
+    }
+    // this CTA's keys >= lo, in index order
+    uint32_t mine = 0;
+#pragma unroll
+    for (int q = 0; q < KPT; q++) mine += q < nk && key[q] >= lo ? 1u : 0u;
+    uint32_t tot;
+    uint32_t p = block_excl_scan(mine, wsum, &tot);
+    if (tot <= (uint32_t)TC_CAPL) {
+#pragma unroll
+        for (int q = 0; q < KPT; q++)
+            if (q < nk && key[q] >= lo) {
+                u.c.key[p] = key[q];
+                u.c.id[p] = (int32_t)(j0 + q);
+                p++;
+            }
+    }
+    if (tid == 0) s_count = tot <= (uint32_t)TC_CAPL ? tot : 0xffffffffu;
+    cl.sync();                        // every CTA's candidates are in place
+    if (rank != 0) {
+        cl.sync();                    // rank 0 has read them
+        return;
+    }
+    uint32_t off[TC_CL + 1];
+    bool bad = false;
+    off[0] = 0;
+#pragma unroll
+    for (int q = 0; q < TC_CL; q++) {
+        const uint32_t cq = *cl.map_shared_rank(&s_count, q);
+        bad |= cq == 0xffffffffu;
+        off[q + 1] = off[q] + (cq == 0xffffffffu ? 0u : cq);
+    }
+    const uint32_t n = off[TC_CL];
+    if (!bad && n >= (uint32_t)k && n <= (uint32_t)(TC_PT * TK_THREADS)) {
+        uint32_t ck[TC_PT];
+        int32_t ci[TC_PT];
+#pragma unroll
+        for (int q = 0; q < TC_PT; q++) {
+            const uint32_t g = (uint32_t)tid * TC_PT + q;
+            ck[q] = 0u;
+            ci[q] = 0;
+            if (g < n) {
+                int w = 0;
+#pragma unroll
+                for (int v = 1; v < TC_CL; v++) w += g >= off[v] ? 1 : 0;
+                ck[q] = cl.map_shared_rank(u.c.key, w)[g - off[w]];
+                ci[q] = cl.map_shared_rank(u.c.id, w)[g - off[w]];
+            }
+        }
+        cl.sync();                    // the other CTAs may leave
+        const int64_t l2 = (int64_t)n - (int64_t)tid * TC_PT;
+        const int nk2 = (int)(l2 < 0 ? 0 : (l2 > TC_PT ? TC_PT : l2));
+        select_registers(ck, nk2, k, [&](int q) { return ci[q]; }, hist, red, wsum, orow);
+    } else {
+        cl.sync();
+        __syncthreads();              // u.c is dead from here on
+        select_core(u.tk, nv, k, [&](int64_t j) { return score_key(s[j]); },
+                    [](int64_t j) { return (int32_t)j; }, orow);
+    }
+    if (tid == 0) cnt[row] = k;
 }
 
 // -------------------------------------------------------------------- host
@@ -801,8 +963,15 @@ int topk_chunks(int64_t rows, int64_t E) {
 
 static size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// keys per thread of the cluster kernel for rows of E entries (0: too long)
+static int topk_cluster_kpt(int64_t E) {
+    for (int kpt = 8; kpt <= 64; kpt *= 2)
+        if (E <= (int64_t)TC_CL * TK_THREADS * kpt) return kpt;
+    return 0;
+}
+
 size_t topk_scratch_bytes(int64_t rows, int64_t E) {
-    if (!topk_use_long(rows, E)) return 0;
+    if (!topk_use_long(rows, E) || topk_cluster_kpt(E) > 0) return 0;
     const int ch = topk_chunks(rows, E);
     return a256((size_t)rows * ch * 4) + 2 * a256((size_t)rows * E * 4);
 }
@@ -814,6 +983,19 @@ cudaError_t launch_topk_phase(int phase, int64_t B, int64_t Tq, int64_t E, int k
                               void *scratch, cudaStream_t st) {
     const int64_t rows = B * Tq;
     if (rows == 0) return cudaSuccess;
+    if (topk_use_long(rows, E) && topk_cluster_kpt(E) > 0) {
+        if (phase != 1) return cudaSuccess;
+        if (rows > 65535) return cudaErrorInvalidValue;
+        const dim3 g((unsigned)(rows * TC_CL));
+        switch (topk_cluster_kpt(E)) {
+        case 8: topk_cluster_kernel<8><<<g, TK_THREADS, 0, st>>>(scores, q_pos, idx, cnt, E, k, m); break;
+        case 16: topk_cluster_kernel<16><<<g, TK_THREADS, 0, st>>>(scores, q_pos, idx, cnt, E, k, m); break;
+        case 32: topk_cluster_kernel<32><<<g, TK_THREADS, 0, st>>>(scores, q_pos, idx, cnt, E, k, m); break;
+        default: topk_cluster_kernel<64><<<g, TK_THREADS, 0, st>>>(scores, q_pos, idx, cnt, E, k, m); break;
+        }
+        count_launches(1);
+        return cudaGetLastError();
+    }
     if (topk_use_long(rows, E)) {
         if (scratch == nullptr) return cudaErrorInvalidValue;
         TkLong a;

@@ -103,6 +103,7 @@ def test_indexer_score(csa, orc, dtype, B, T, hI, dI, E, m, pos0):
     (2, 5, 50000, 512, 1),        # beyond the shared-memory key cache
     (3, 4, 40000, 1024, 1),
     (1, 1, 262144, 1024, 4),
+    (1, 2, 300000, 1024, 1),      # longer than the cluster kernel takes: two launches
 ])
 def test_topk_exact(csa, orc, B, T, E, k, m):
     r = _np_rng(300 + E)
@@ -169,6 +170,16 @@ def test_topk_sample_miss_decode(csa, orc):
     sc = r.standard_normal((B, 1, E)).astype(np.float32)
     sc[..., ::64] = 100.0 + r.standard_normal((B, 1, E // 64)).astype(np.float32)
     pos = np.full((B, 1), E * m - 1, np.int64)
+    _topk_check(csa, orc, sc, pos, m, k)
+
+
+def test_topk_decode_all_ties(csa, orc):
+    """Decode rows whose visible keys are all equal: every CTA's candidates
+    overflow and the exact selection over the whole row runs (ties go to the
+    lowest indices)."""
+    B, E, k, m = 2, 262144, 1024, 4
+    sc = np.full((B, 1, E), 0.5, np.float32)
+    pos = np.array([[E * m - 1], [E * m // 2 + 5]], np.int64)
     _topk_check(csa, orc, sc, pos, m, k)
 
 
