@@ -218,12 +218,16 @@ __device__ void select_core(TkShared &sh, int64_t n, int k, KeyF key, IdF id, in
 
 // Rank in a sample of S keys (drawn from n) whose key lower-bounds the k-th
 // largest of all n with a margin of five standard deviations of the number of
-// sample keys above it; >= S means "no useful bound".
+// sample keys above it; >= S means "no useful bound".  In fp32 (B300's fp64
+// pipe is narrow, and every thread of a block evaluates this): the rank only
+// sets how far below the k-th largest key the bound falls, and any rank
+// leaves the selection exact.
 __device__ __forceinline__ int sample_rank(int64_t n, int k, int S) {
-    const double p = (double)k / (double)n;
-    const double mu = S * p;
-    const double sd = sqrt(S * p * (1.0 - p));
-    return (int)ceil(mu + 5.0 * sd + 2.0);
+    const float nf = n > 0x7fffffffLL ? 2147483648.0f : (float)(int)n;
+    const float p = (float)k / nf;
+    const float mu = (float)S * p;
+    const float sd = sqrtf(mu * (1.0f - p));
+    return (int)ceilf(mu + 5.0f * sd + 2.0f);
 }
 
 // ----------------------------------------------------------- one CTA per row
@@ -583,12 +587,13 @@ __device__ Thr block_threshold(const uint32_t (&kr)[NK], int nk, int k, uint32_t
 // to orow in index order; id(u) gives the index of this thread's candidate u.
 // The threshold from block_threshold, then one block scan of the per-thread
 // counts of keys above it and of ties places every kept index.
+// Writes, in index order, the id of every key above tau and of the first
+// need_eq keys equal to tau, from keys held in registers (thread t holds
+// keys PT t .. PT t + PT - 1, nk of them valid): one block scan of the
+// per-thread counts of keys above tau and of ties places every kept index.
 template <int PT, typename IdF>
-__device__ void select_registers(const uint32_t (&ck)[PT], int nk, int k, IdF id, uint32_t *hist,
-                                 uint32_t *red, uint32_t *wsum, int32_t *orow) {
-    const Thr th = block_threshold(ck, nk, k, hist, red);
-    const uint32_t t = th.tau;
-    const uint32_t need_eq = th.need_eq;
+__device__ void emit_registers(const uint32_t (&ck)[PT], int nk, uint32_t t, uint32_t need_eq, IdF id,
+                               uint32_t *wsum, int32_t *orow) {
     uint32_t n_gt = 0, n_eq = 0;
 #pragma unroll
     for (int u = 0; u < PT; u++) {
@@ -608,6 +613,15 @@ __device__ void select_registers(const uint32_t (&ck)[PT], int nk, int k, IdF id
         }
         if (sel) orow[pos++] = id(u);
     }
+}
+
+// The k largest of n > k candidates held in registers (see emit_registers
+// for the layout), written to orow in index order.
+template <int PT, typename IdF>
+__device__ void select_registers(const uint32_t (&ck)[PT], int nk, int k, IdF id, uint32_t *hist,
+                                 uint32_t *red, uint32_t *wsum, int32_t *orow) {
+    const Thr th = block_threshold(ck, nk, k, hist, red);
+    emit_registers(ck, nk, th.tau, th.need_eq, id, wsum, orow);
 }
 
 // (1) per chunk of a long row: the row's sampled bound lo (every chunk CTA
@@ -800,38 +814,178 @@ __global__ void __launch_bounds__(TK_THREADS) topk_final_kernel(TkLong a, int ca
 }
 
 // Few long rows, one launch: a cluster of TC_CL CTAs per row.  CTA r of the
-// cluster holds the keys of the r-th slice of the row in registers (thread t
-// a contiguous run of KPT keys).  Every CTA derives the same sampled bound lo
-// from the same evenly spaced sample (block-wide, bit by bit); each keeps its
-// keys >= lo in index order in its own shared memory.  Rank 0 then reads the
-// cluster's candidates through distributed shared memory, rank by rank (so in
-// index order), into registers and runs the exact selection there.  If the
-// sample misses (fewer than k candidates) or a CTA's candidates overflow,
-// rank 0 runs the exact selection over the whole row from global memory.
+// cluster holds the keys of the r-th slice of the row in registers (the
+// slices cut E, so the loads start before the position is known).  Within a
+// CTA, warp w owns a contiguous part of the slice, and lane l holds, for each
+// step u, the four keys at u * 128 + 4 l .. + 3 of it (each warp load reads
+// 512 contiguous bytes).  Every CTA derives the same sampled bound lo from the
+// same evenly spaced sample and writes its keys >= lo, in index order, into
+// its own region of the first CTA's shared memory.  After one cluster barrier
+// the other CTAs leave; the first CTA loads the candidates (regions in rank
+// order, so index order) into registers, thread t holding a contiguous run,
+// and runs the exact selection.  If the sample misses (fewer than k
+// candidates) or a region overflows, it runs the exact selection over the
+// whole row from global memory instead.
 constexpr int TC_CL = 8;              // CTAs per row
-constexpr int TC_CAPL = 2048;         // candidates a CTA keeps
-constexpr int TC_PT = 16;             // candidates per thread in rank 0's selection
+constexpr int TC_CAPR = 1024;         // candidates a CTA may keep
+constexpr int TC_RSTRIDE = TC_CAPR + TC_CAPR / 32;   // a region, one pad word per 32 (no bank conflicts)
+constexpr int TC_PT = 16;             // candidates per thread in the first CTA's selection
+constexpr int TC_SMEM = TC_CL * TC_RSTRIDE * 8;
+constexpr int TC_WARPS = TK_THREADS / 32;
+
+struct TcShared {
+    uint32_t hist[2][2048];           // radix histograms, one being counted while the other is cleared
+    uint32_t wtot[TC_WARPS];
+    uint32_t wand[TC_WARPS], wor[TC_WARPS];
+    uint32_t wsum[32];
+    uint32_t res[3];                  // bin, count above it, its count
+    uint32_t rcount[TC_CL];           // first CTA: each region's count, ~0u on overflow
+};
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// The bin of hist (2048 bins, larger keys in higher bins) that holds the
+// remaining-th largest key, the count above it and its own count, into
+// sh.res.  Warp w scans bins 128 w .. 128 w + 127, four per lane; a suffix sum
+// over the lanes and one over the warp totals place every lane.  Two
+// barriers; also clears the histogram `other` for the next pass.
+__device__ __forceinline__ void lean_find(const uint32_t *hist, uint32_t *other, uint32_t remaining,
+                                          TcShared &sh) {
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int b0 = w * 128 + lane * 4;
+    const uint4 hv = *reinterpret_cast<const uint4 *>(hist + b0);
+    const uint32_t h[4] = {hv.x, hv.y, hv.z, hv.w};
+    const uint32_t c = h[0] + h[1] + h[2] + h[3];
+    uint32_t sfx = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_down_sync(0xffffffffu, sfx, o);
+        if (lane + o < 32) sfx += t;
+    }
+    if (lane == 0) sh.wtot[w] = sfx;
+    *reinterpret_cast<uint4 *>(other + b0) = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    uint32_t above = sfx - c;
+#pragma unroll
+    for (int v = 0; v < TC_WARPS; v++) above += v > w ? sh.wtot[v] : 0u;
+#pragma unroll
+    for (int i = 3; i >= 0; i--) {
+        if (above < remaining && above + h[i] >= remaining) {
+            sh.res[0] = (uint32_t)(b0 + i);
+            sh.res[1] = above;
+            sh.res[2] = h[i];
+        }
+        above += h[i];
+    }
+    __syncthreads();
+}
+
+// The rank-th largest (1-based) of the valid keys in registers, bits stop and
+// up (the lower bits of the result are those all keys share, else zero):
+// radix select with 11-bit digits starting at the highest bit in which the
+// keys differ, so that keys crowded into a narrow range spread over the bins;
+// plain shared-memory atomics.  need gets how many keys equal to the result
+// are taken (meaningful when stop = 0).  sh.hist[0] must be clear on entry,
+// and is again on return.
+template <int NK, typename OkF>
+__device__ void radix_kth(const uint32_t (&kr)[NK], OkF ok, uint32_t rank, int stop, TcShared &sh,
+                          uint32_t &tau, uint32_t &need) {
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    uint32_t a1 = 0xffffffffu, o1 = 0u;
+#pragma unroll
+    for (int u = 0; u < NK; u++)
+        if (ok(u)) {
+            a1 &= kr[u];
+            o1 |= kr[u];
+        }
+    a1 = __reduce_and_sync(0xffffffffu, a1);
+    o1 = __reduce_or_sync(0xffffffffu, o1);
+    if (lane == 0) {
+        sh.wand[w] = a1;
+        sh.wor[w] = o1;
+    }
+    __syncthreads();
+    a1 = 0xffffffffu;
+    o1 = 0u;
+#pragma unroll
+    for (int v = 0; v < TC_WARPS; v++) {
+        a1 &= sh.wand[v];
+        o1 |= sh.wor[v];
+    }
+    const uint32_t vary = a1 ^ o1;
+    uint32_t prefix = a1 & ~vary, pmask = ~vary, remaining = rank;
+    int hi = vary ? 31 - __clz(vary) : -1;
+    int buf = 0;
+#pragma unroll 1
+    while (hi >= stop) {
+        const int lo_bit = hi - 10 > stop ? hi - 10 : stop;
+        const uint32_t dmask = (2u << (hi - lo_bit)) - 1u;
+        uint32_t *hcur = sh.hist[buf];
+#pragma unroll
+        for (int u = 0; u < NK; u++)
+            if (ok(u) && (kr[u] & pmask) == prefix) atomicAdd(&hcur[(kr[u] >> lo_bit) & dmask], 1u);
+        __syncthreads();
+        lean_find(hcur, sh.hist[buf ^ 1], remaining, sh);
+        prefix |= sh.res[0] << lo_bit;
+        remaining -= sh.res[1];
+        pmask |= dmask << lo_bit;
+        hi = lo_bit - 1;
+        buf ^= 1;
+    }
+    if (buf) {                        // hist[1] was cleared last: clear hist[0] too
+        for (int i = tid; i < 2048; i += TK_THREADS) sh.hist[0][i] = 0u;
+        __syncthreads();
+    }
+    tau = prefix & ~((1u << stop) - 1u & vary);
+    need = remaining;
+}
 
 template <int KPT>
-__global__ void __cluster_dims__(TC_CL, 1, 1) __launch_bounds__(TK_THREADS, 1)
+__global__ void __cluster_dims__(TC_CL, 1, 1) __launch_bounds__(TK_THREADS, KPT <= 8 ? 2 : 1)
 topk_cluster_kernel(const float *__restrict__ scores, const int64_t *__restrict__ q_pos,
                     int32_t *__restrict__ idx, int32_t *__restrict__ cnt, int64_t E, int k, int m) {
-    __shared__ union {
-        struct {
-            uint32_t key[TC_CAPL];
-            int32_t id[TC_CAPL];
-        } c;
-        TkShared tk;                  // rank 0's whole-row fallback, after the candidates are dead
-    } u;
-    __shared__ uint32_t s_count;      // candidates kept here; ~0u: overflow
-    __shared__ uint32_t wsum[32];
-    __shared__ uint32_t hist[256];
-    __shared__ uint32_t red[40];
+    static_assert(KPT % 4 == 0, "keys come in groups of four");
+    constexpr int U = KPT / 4;        // steps per warp
+    extern __shared__ __align__(16) uint8_t tc_raw[];
+    uint32_t *rkey = reinterpret_cast<uint32_t *>(tc_raw);                  // first CTA: [TC_CL][TC_RSTRIDE]
+    int32_t *rid = reinterpret_cast<int32_t *>(tc_raw + TC_CL * TC_RSTRIDE * 4);
+    __shared__ __align__(16) TcShared sh;
+    __shared__ TkShared tk;           // the whole-row fallback
     namespace cg = cooperative_groups;
     cg::cluster_group cl = cg::this_cluster();
     const unsigned rank = cl.block_rank();
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int64_t row = blockIdx.x / TC_CL;
+    // the peers' shared memory is written only after every CTA of the cluster
+    // has started: arrive now, wait just before the first remote write
+    cluster_arrive_relaxed();
+    const float *s = scores + row * E;
+    const int64_t per = (((E + TC_CL - 1) / TC_CL) + 3) & ~(int64_t)3;
+    const int64_t c0 = (int64_t)rank * per;
+    const int64_t c1 = c0 + per < E ? c0 + per : E;
+    const int64_t wb = c0 + (int64_t)w * (32 * KPT) + 4 * lane;   // this lane's first key
+    uint32_t key[KPT];
+    const bool vec = (((uintptr_t)s) & 15) == 0;
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+        const int64_t j = wb + (int64_t)u * 128;
+        if (vec && j + 4 <= c1) {
+            const float4 v = __ldcs(reinterpret_cast<const float4 *>(s + j));
+            key[4 * u] = score_key(v.x);
+            key[4 * u + 1] = score_key(v.y);
+            key[4 * u + 2] = score_key(v.z);
+            key[4 * u + 3] = score_key(v.w);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; e++) key[4 * u + e] = j + e < c1 ? score_key(__ldcs(s + j + e)) : 0u;
+        }
+    }
+    for (int i = tid; i < 2048; i += TK_THREADS) sh.hist[0][i] = 0u;
     const int64_t nv = visible_count(q_pos[row], m, E);
     int32_t *orow = idx + row * (int64_t)k;
     if (nv <= k) {                    // the same in every CTA of the cluster
@@ -839,80 +993,88 @@ topk_cluster_kernel(const float *__restrict__ scores, const int64_t *__restrict_
             for (int i = tid; i < k; i += TK_THREADS) orow[i] = i < nv ? i : -1;
             if (tid == 0) cnt[row] = (int32_t)nv;
         }
+        cluster_wait();
         return;
     }
-    const float *s = scores + row * E;
-    // this CTA's slice (a multiple of 4 keys long) and this thread's run
-    const int64_t per = (((nv + TC_CL - 1) / TC_CL) + 3) & ~(int64_t)3;
-    const int64_t c0 = (int64_t)rank * per;
-    const int64_t c1 = c0 + per < nv ? c0 + per : nv;
-    const int64_t j0 = c0 + (int64_t)tid * KPT;
-    const int64_t left = c1 - j0;
-    const int nk = (int)(left < 0 ? 0 : (left > KPT ? KPT : left));
-    uint32_t key[KPT];
-    const bool vec = (((uintptr_t)s) & 15) == 0;
-#pragma unroll
-    for (int q = 0; q < KPT / 4; q++) {
-        if (vec && 4 * q + 4 <= nk) {
-            const float4 v = __ldcs(reinterpret_cast<const float4 *>(s + j0 + 4 * q));
-            key[4 * q] = score_key(v.x);
-            key[4 * q + 1] = score_key(v.y);
-            key[4 * q + 2] = score_key(v.z);
-            key[4 * q + 3] = score_key(v.w);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 4; e++) key[4 * q + e] = 4 * q + e < nk ? score_key(__ldcs(s + j0 + 4 * q + e)) : 0u;
-        }
-    }
+    const int64_t cv = c1 < nv ? c1 : nv;                    // visible keys end here
+    // this lane's keys are visible while their offset from wb is below lim
+    const int64_t lim64 = cv - wb;
+    const int lim = (int)(lim64 < 0 ? 0 : (lim64 > 0x7fffffff ? 0x7fffffff : lim64));
     // the bound: the top 24 bits of the r-th largest of TK_LSAMPLE evenly
-    // spaced keys (two per thread), the largest 24-bit prefix that at least r
-    // sample keys reach
+    // spaced keys (two per thread)
     const int S = (int)(nv < TK_LSAMPLE ? nv : TK_LSAMPLE);
     uint32_t sk[2];
+    bool sv[2];
 #pragma unroll
     for (int h = 0; h < 2; h++) {
         const int i = tid + h * TK_THREADS;
         const int64_t pos = S == TK_LSAMPLE ? (((int64_t)i * nv) >> 10) : i;   // TK_LSAMPLE = 2^10
-        sk[h] = i < S ? score_key(s[pos]) : 0u;
+        sv[h] = i < S;
+        sk[h] = sv[h] ? score_key(s[pos]) : 0u;
     }
+    __syncthreads();                  // hist[0] is clear
     const int r = S < TK_LSAMPLE ? k : sample_rank(nv, k, S);
-    uint32_t lo = 0;
-    if (r < S) {
-#pragma unroll 1
-        for (int b = 31; b >= 8; b--) {
-            const uint32_t c = lo | (1u << b);
-            const int n0 = __syncthreads_count(sk[0] >= c);
-            const int n1 = __syncthreads_count(sk[1] >= c);
-            if (n0 + n1 >= r) lo = c;
+    uint32_t lo = 0, unused;
+    if (r < S) radix_kth(sk, [&](int h) { return sv[h]; }, (uint32_t)r, 8, sh, lo, unused);
+    // this CTA's keys >= lo, in index order: per warp, steps in order, lanes
+    // in order within a step, a lane's four keys in order
+    uint32_t wcount = 0;
+#pragma unroll
+    for (int u = 0; u < U; u++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) wcount += u * 128 + e < lim && key[4 * u + e] >= lo ? 1u : 0u;
+    wcount = __reduce_add_sync(0xffffffffu, wcount);
+    if (lane == 0) sh.wtot[w] = wcount;
+    __syncthreads();
+    uint32_t base = 0, tot = 0;
+#pragma unroll
+    for (int v = 0; v < TC_WARPS; v++) {
+        const uint32_t x = sh.wtot[v];
+        base += v < w ? x : 0u;
+        tot += x;
+    }
+    cluster_wait();
+    if (tot <= (uint32_t)TC_CAPR) {
+        uint32_t *dk = cl.map_shared_rank(rkey, 0) + rank * TC_RSTRIDE;
+        int32_t *di = cl.map_shared_rank(rid, 0) + rank * TC_RSTRIDE;
+        const unsigned lt = (1u << lane) - 1u;
+        uint32_t run = base;
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            bool in[4];
+            uint32_t c = 0;
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                in[e] = u * 128 + e < lim && key[4 * u + e] >= lo;
+                c += in[e] ? 1u : 0u;
+            }
+            // the lanes' counts (0..4) bit by bit: their prefix over the lanes
+            // from three ballots
+            const unsigned b0 = __ballot_sync(0xffffffffu, c & 1u), b1 = __ballot_sync(0xffffffffu, c & 2u),
+                           b2 = __ballot_sync(0xffffffffu, c & 4u);
+            if ((b0 | b1 | b2) == 0u) continue;
+            uint32_t p = run + (uint32_t)__popc(b0 & lt) + 2u * (uint32_t)__popc(b1 & lt) +
+                         4u * (uint32_t)__popc(b2 & lt);
+            const int64_t j = wb + (int64_t)u * 128;
+#pragma unroll
+            for (int e = 0; e < 4; e++)
+                if (in[e]) {
+                    dk[p + (p >> 5)] = key[4 * u + e];
+                    di[p + (p >> 5)] = (int32_t)(j + e);
+                    p++;
+                }
+            run += (uint32_t)__popc(b0) + 2u * (uint32_t)__popc(b1) + 4u * (uint32_t)__popc(b2);
         }
     }
-    // this CTA's keys >= lo, in index order
-    uint32_t mine = 0;
-#pragma unroll
-    for (int q = 0; q < KPT; q++) mine += q < nk && key[q] >= lo ? 1u : 0u;
-    uint32_t tot;
-    uint32_t p = block_excl_scan(mine, wsum, &tot);
-    if (tot <= (uint32_t)TC_CAPL) {
-#pragma unroll
-        for (int q = 0; q < KPT; q++)
-            if (q < nk && key[q] >= lo) {
-                u.c.key[p] = key[q];
-                u.c.id[p] = (int32_t)(j0 + q);
-                p++;
-            }
-    }
-    if (tid == 0) s_count = tot <= (uint32_t)TC_CAPL ? tot : 0xffffffffu;
-    cl.sync();                        // every CTA's candidates are in place
-    if (rank != 0) {
-        cl.sync();                    // rank 0 has read them
-        return;
-    }
+    if (tid == 0) cl.map_shared_rank(sh.rcount, 0)[rank] = tot <= (uint32_t)TC_CAPR ? tot : 0xffffffffu;
+    cl.sync();                        // every region is written
+    if (rank != 0) return;
     uint32_t off[TC_CL + 1];
     bool bad = false;
     off[0] = 0;
 #pragma unroll
     for (int q = 0; q < TC_CL; q++) {
-        const uint32_t cq = *cl.map_shared_rank(&s_count, q);
+        const uint32_t cq = sh.rcount[q];
         bad |= cq == 0xffffffffu;
         off[q + 1] = off[q] + (cq == 0xffffffffu ? 0u : cq);
     }
@@ -923,24 +1085,21 @@ topk_cluster_kernel(const float *__restrict__ scores, const int64_t *__restrict_
 #pragma unroll
         for (int q = 0; q < TC_PT; q++) {
             const uint32_t g = (uint32_t)tid * TC_PT + q;
-            ck[q] = 0u;
-            ci[q] = 0;
-            if (g < n) {
-                int w = 0;
+            int v = 0;
 #pragma unroll
-                for (int v = 1; v < TC_CL; v++) w += g >= off[v] ? 1 : 0;
-                ck[q] = cl.map_shared_rank(u.c.key, w)[g - off[w]];
-                ci[q] = cl.map_shared_rank(u.c.id, w)[g - off[w]];
-            }
+            for (int x = 1; x < TC_CL; x++) v += g >= off[x] ? 1 : 0;
+            const uint32_t pr = g - off[v];
+            const uint32_t at = (uint32_t)v * TC_RSTRIDE + pr + (pr >> 5);
+            ck[q] = g < n ? rkey[at] : 0u;
+            ci[q] = g < n ? rid[at] : 0;
         }
-        cl.sync();                    // the other CTAs may leave
         const int64_t l2 = (int64_t)n - (int64_t)tid * TC_PT;
         const int nk2 = (int)(l2 < 0 ? 0 : (l2 > TC_PT ? TC_PT : l2));
-        select_registers(ck, nk2, k, [&](int q) { return ci[q]; }, hist, red, wsum, orow);
+        uint32_t tau, need_eq;
+        radix_kth(ck, [&](int q) { return q < nk2; }, (uint32_t)k, 0, sh, tau, need_eq);
+        emit_registers(ck, nk2, tau, need_eq, [&](int q) { return ci[q]; }, sh.wsum, orow);
     } else {
-        cl.sync();
-        __syncthreads();              // u.c is dead from here on
-        select_core(u.tk, nv, k, [&](int64_t j) { return score_key(s[j]); },
+        select_core(tk, nv, k, [&](int64_t j) { return score_key(s[j]); },
                     [](int64_t j) { return (int32_t)j; }, orow);
     }
     if (tid == 0) cnt[row] = k;
@@ -987,11 +1146,21 @@ cudaError_t launch_topk_phase(int phase, int64_t B, int64_t Tq, int64_t E, int k
         if (phase != 1) return cudaSuccess;
         if (rows > 65535) return cudaErrorInvalidValue;
         const dim3 g((unsigned)(rows * TC_CL));
-        switch (topk_cluster_kpt(E)) {
-        case 8: topk_cluster_kernel<8><<<g, TK_THREADS, 0, st>>>(scores, q_pos, idx, cnt, E, k, m); break;
-        case 16: topk_cluster_kernel<16><<<g, TK_THREADS, 0, st>>>(scores, q_pos, idx, cnt, E, k, m); break;
-        case 32: topk_cluster_kernel<32><<<g, TK_THREADS, 0, st>>>(scores, q_pos, idx, cnt, E, k, m); break;
-        default: topk_cluster_kernel<64><<<g, TK_THREADS, 0, st>>>(scores, q_pos, idx, cnt, E, k, m); break;
+        const int kpt = topk_cluster_kpt(E);
+        const void *fn = kpt == 8 ? (const void *)topk_cluster_kernel<8>
+                       : kpt == 16 ? (const void *)topk_cluster_kernel<16>
+                       : kpt == 32 ? (const void *)topk_cluster_kernel<32>
+                                   : (const void *)topk_cluster_kernel<64>;
+        static PerDevice cl_smem[4];
+        {
+            cudaError_t e = smem_limit_once(cl_smem[kpt == 8 ? 0 : kpt == 16 ? 1 : kpt == 32 ? 2 : 3], fn, TC_SMEM);
+            if (e != cudaSuccess) return e;
+        }
+        switch (kpt) {
+        case 8: topk_cluster_kernel<8><<<g, TK_THREADS, TC_SMEM, st>>>(scores, q_pos, idx, cnt, E, k, m); break;
+        case 16: topk_cluster_kernel<16><<<g, TK_THREADS, TC_SMEM, st>>>(scores, q_pos, idx, cnt, E, k, m); break;
+        case 32: topk_cluster_kernel<32><<<g, TK_THREADS, TC_SMEM, st>>>(scores, q_pos, idx, cnt, E, k, m); break;
+        default: topk_cluster_kernel<64><<<g, TK_THREADS, TC_SMEM, st>>>(scores, q_pos, idx, cnt, E, k, m); break;
         }
         count_launches(1);
         return cudaGetLastError();
