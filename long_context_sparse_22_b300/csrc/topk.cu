@@ -828,7 +828,7 @@ __global__ void __launch_bounds__(TK_THREADS) topk_final_kernel(TkLong a, int ca
 // whole row from global memory instead.
 constexpr int TC_CL = 8;              // CTAs per row
 constexpr int TC_CAPR = 1024;         // candidates a CTA may keep
-constexpr int TC_RSTRIDE = TC_CAPR + TC_CAPR / 32;   // a region, one pad word per 32 (no bank conflicts)
+constexpr int TC_RSTRIDE = TC_CAPR + TC_CAPR / 8;    // a region: four pad words after every 32
 constexpr int TC_PT = 16;             // candidates per thread in the first CTA's selection
 constexpr int TC_SMEM = TC_CL * TC_RSTRIDE * 8;
 constexpr int TC_WARPS = TK_THREADS / 32;
@@ -837,10 +837,16 @@ struct TcShared {
     uint32_t hist[2][2048];           // radix histograms, one being counted while the other is cleared
     uint32_t wtot[TC_WARPS];
     uint32_t wand[TC_WARPS], wor[TC_WARPS];
-    uint32_t wsum[32];
     uint32_t res[3];                  // bin, count above it, its count
+    uint32_t nsmall, tau, need;       // the last bin's keys, finished by one warp
+    uint32_t small[64];
     uint32_t rcount[TC_CL];           // first CTA: each region's count, ~0u on overflow
 };
+
+// Word offset of candidate p in a region: four pad words after every 32, so
+// that runs of a region read by consecutive threads spread over the banks and
+// groups of four stay 16-byte aligned.
+__device__ __forceinline__ uint32_t padw(uint32_t p) { return p + 4u * (p >> 5); }
 
 __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
@@ -909,6 +915,7 @@ __device__ void radix_kth(const uint32_t (&kr)[NK], OkF ok, uint32_t rank, int s
         sh.wand[w] = a1;
         sh.wor[w] = o1;
     }
+    if (tid == 0) sh.nsmall = 0u;
     __syncthreads();
     a1 = 0xffffffffu;
     o1 = 0u;
@@ -921,6 +928,7 @@ __device__ void radix_kth(const uint32_t (&kr)[NK], OkF ok, uint32_t rank, int s
     uint32_t prefix = a1 & ~vary, pmask = ~vary, remaining = rank;
     int hi = vary ? 31 - __clz(vary) : -1;
     int buf = 0;
+    bool done = false;
 #pragma unroll 1
     while (hi >= stop) {
         const int lo_bit = hi - 10 > stop ? hi - 10 : stop;
@@ -936,13 +944,95 @@ __device__ void radix_kth(const uint32_t (&kr)[NK], OkF ok, uint32_t rank, int s
         pmask |= dmask << lo_bit;
         hi = lo_bit - 1;
         buf ^= 1;
+        if (stop == 0 && hi >= 0 && sh.res[2] <= 64u) {
+            // few keys left in the bin: gather them, and one warp finds the
+            // remaining-th largest by counting, for each key, the keys above it
+            const uint32_t nb = sh.res[2];
+#pragma unroll
+            for (int u = 0; u < NK; u++)
+                if (ok(u) && (kr[u] & pmask) == prefix) sh.small[atomicAdd(&sh.nsmall, 1u)] = kr[u];
+            __syncthreads();
+            if (w == 0) {
+                const uint32_t x0 = (uint32_t)lane < nb ? sh.small[lane] : 0u;
+                const uint32_t x1 = (uint32_t)lane + 32u < nb ? sh.small[lane + 32] : 0u;
+                uint32_t g0 = 0, e0 = 0, g1 = 0, e1 = 0;
+                for (int j = 0; j < 64 && (uint32_t)j < nb; j++) {
+                    const uint32_t y = __shfl_sync(0xffffffffu, j < 32 ? x0 : x1, j & 31);
+                    g0 += y > x0 ? 1u : 0u;
+                    e0 += y == x0 ? 1u : 0u;
+                    g1 += y > x1 ? 1u : 0u;
+                    e1 += y == x1 ? 1u : 0u;
+                }
+                if ((uint32_t)lane < nb && g0 < remaining && g0 + e0 >= remaining) {
+                    sh.tau = x0;
+                    sh.need = remaining - g0;
+                }
+                if ((uint32_t)lane + 32u < nb && g1 < remaining && g1 + e1 >= remaining) {
+                    sh.tau = x1;
+                    sh.need = remaining - g1;
+                }
+            }
+            __syncthreads();
+            prefix = sh.tau;
+            remaining = sh.need;
+            done = true;
+            break;
+        }
     }
-    if (buf) {                        // hist[1] was cleared last: clear hist[0] too
+    if (buf) {                        // hist[0] was counted last: clear it
         for (int i = tid; i < 2048; i += TK_THREADS) sh.hist[0][i] = 0u;
         __syncthreads();
     }
-    tau = prefix & ~((1u << stop) - 1u & vary);
+    tau = done ? prefix : prefix & ~((1u << stop) - 1u & vary);
     need = remaining;
+}
+
+// Writes, in index order, the id of every key above t and of the first
+// need_eq keys equal to t (keys in registers, thread t holding a contiguous
+// run of PT, nk of them valid): lane prefixes of the per-thread counts from
+// ballots of their bits, warp bases from one exchange.
+template <int PT, typename IdF>
+__device__ void emit_ballot(const uint32_t (&ck)[PT], int nk, uint32_t t, uint32_t need_eq, IdF id,
+                            TcShared &sh, int32_t *orow) {
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const unsigned lt = (1u << lane) - 1u;
+    uint32_t n_gt = 0, n_eq = 0;
+#pragma unroll
+    for (int u = 0; u < PT; u++) {
+        n_gt += ck[u] > t && u < nk ? 1u : 0u;
+        n_eq += ck[u] == t && u < nk ? 1u : 0u;
+    }
+    uint32_t pg = 0, pe = 0, tg = 0, te = 0;
+#pragma unroll
+    for (int b = 0; b < 5; b++) {                         // counts are at most 16
+        const unsigned bg = __ballot_sync(0xffffffffu, (n_gt >> b) & 1u);
+        const unsigned be = __ballot_sync(0xffffffffu, (n_eq >> b) & 1u);
+        pg += (uint32_t)__popc(bg & lt) << b;
+        pe += (uint32_t)__popc(be & lt) << b;
+        tg += (uint32_t)__popc(bg) << b;
+        te += (uint32_t)__popc(be) << b;
+    }
+    if (lane == 0) {
+        sh.wtot[w] = tg;
+        sh.wand[w] = te;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int v = 0; v < TC_WARPS; v++) {
+        pg += v < w ? sh.wtot[v] : 0u;
+        pe += v < w ? sh.wand[v] : 0u;
+    }
+    uint32_t eq_before = pe;
+    uint32_t pos = pg + (eq_before < need_eq ? eq_before : need_eq);
+#pragma unroll
+    for (int u = 0; u < PT; u++) {
+        bool sel = false;
+        if (u < nk) {
+            if (ck[u] > t) sel = true;
+            else if (ck[u] == t) sel = eq_before++ < need_eq;
+        }
+        if (sel) orow[pos++] = id(u);
+    }
 }
 
 template <int KPT>
@@ -1000,8 +1090,8 @@ topk_cluster_kernel(const float *__restrict__ scores, const int64_t *__restrict_
     // this lane's keys are visible while their offset from wb is below lim
     const int64_t lim64 = cv - wb;
     const int lim = (int)(lim64 < 0 ? 0 : (lim64 > 0x7fffffff ? 0x7fffffff : lim64));
-    // the bound: the top 24 bits of the r-th largest of TK_LSAMPLE evenly
-    // spaced keys (two per thread)
+    // the bound: the r-th largest of TK_LSAMPLE evenly spaced keys (two per
+    // thread), its bits below 12 cleared
     const int S = (int)(nv < TK_LSAMPLE ? nv : TK_LSAMPLE);
     uint32_t sk[2];
     bool sv[2];
@@ -1015,7 +1105,7 @@ topk_cluster_kernel(const float *__restrict__ scores, const int64_t *__restrict_
     __syncthreads();                  // hist[0] is clear
     const int r = S < TK_LSAMPLE ? k : sample_rank(nv, k, S);
     uint32_t lo = 0, unused;
-    if (r < S) radix_kth(sk, [&](int h) { return sv[h]; }, (uint32_t)r, 8, sh, lo, unused);
+    if (r < S) radix_kth(sk, [&](int h) { return sv[h]; }, (uint32_t)r, 12, sh, lo, unused);
     // this CTA's keys >= lo, in index order: per warp, steps in order, lanes
     // in order within a step, a lane's four keys in order
     uint32_t wcount = 0;
@@ -1033,10 +1123,10 @@ topk_cluster_kernel(const float *__restrict__ scores, const int64_t *__restrict_
         base += v < w ? x : 0u;
         tot += x;
     }
-    cluster_wait();
     if (tot <= (uint32_t)TC_CAPR) {
-        uint32_t *dk = cl.map_shared_rank(rkey, 0) + rank * TC_RSTRIDE;
-        int32_t *di = cl.map_shared_rank(rid, 0) + rank * TC_RSTRIDE;
+        // staged in this CTA's own region (the first CTA's is final)
+        uint32_t *dk = rkey + rank * TC_RSTRIDE;
+        int32_t *di = rid + rank * TC_RSTRIDE;
         const unsigned lt = (1u << lane) - 1u;
         uint32_t run = base;
 #pragma unroll
@@ -1059,11 +1149,25 @@ topk_cluster_kernel(const float *__restrict__ scores, const int64_t *__restrict_
 #pragma unroll
             for (int e = 0; e < 4; e++)
                 if (in[e]) {
-                    dk[p + (p >> 5)] = key[4 * u + e];
-                    di[p + (p >> 5)] = (int32_t)(j + e);
+                    dk[padw(p)] = key[4 * u + e];
+                    di[padw(p)] = (int32_t)(j + e);
                     p++;
                 }
             run += (uint32_t)__popc(b0) + 2u * (uint32_t)__popc(b1) + 4u * (uint32_t)__popc(b2);
+        }
+    }
+    __syncthreads();
+    cluster_wait();
+    if (rank != 0 && tot <= (uint32_t)TC_CAPR && tot > 0) {
+        // the staged region to the first CTA, 16 bytes a store
+        const uint32_t nvec = (padw(tot - 1) + 4u) >> 2;
+        const uint4 *sk4 = reinterpret_cast<const uint4 *>(rkey + rank * TC_RSTRIDE);
+        const uint4 *si4 = reinterpret_cast<const uint4 *>(rid + rank * TC_RSTRIDE);
+        uint4 *dk4 = reinterpret_cast<uint4 *>(cl.map_shared_rank(rkey, 0) + rank * TC_RSTRIDE);
+        uint4 *di4 = reinterpret_cast<uint4 *>(cl.map_shared_rank(rid, 0) + rank * TC_RSTRIDE);
+        for (uint32_t i = (uint32_t)tid; i < nvec; i += TK_THREADS) {
+            dk4[i] = sk4[i];
+            di4[i] = si4[i];
         }
     }
     if (tid == 0) cl.map_shared_rank(sh.rcount, 0)[rank] = tot <= (uint32_t)TC_CAPR ? tot : 0xffffffffu;
@@ -1089,7 +1193,7 @@ topk_cluster_kernel(const float *__restrict__ scores, const int64_t *__restrict_
 #pragma unroll
             for (int x = 1; x < TC_CL; x++) v += g >= off[x] ? 1 : 0;
             const uint32_t pr = g - off[v];
-            const uint32_t at = (uint32_t)v * TC_RSTRIDE + pr + (pr >> 5);
+            const uint32_t at = (uint32_t)v * TC_RSTRIDE + padw(pr);
             ck[q] = g < n ? rkey[at] : 0u;
             ci[q] = g < n ? rid[at] : 0;
         }
@@ -1097,7 +1201,7 @@ topk_cluster_kernel(const float *__restrict__ scores, const int64_t *__restrict_
         const int nk2 = (int)(l2 < 0 ? 0 : (l2 > TC_PT ? TC_PT : l2));
         uint32_t tau, need_eq;
         radix_kth(ck, [&](int q) { return q < nk2; }, (uint32_t)k, 0, sh, tau, need_eq);
-        emit_registers(ck, nk2, tau, need_eq, [&](int q) { return ci[q]; }, sh.wsum, orow);
+        emit_ballot(ck, nk2, tau, need_eq, [&](int q) { return ci[q]; }, sh, orow);
     } else {
         select_core(tk, nv, k, [&](int64_t j) { return score_key(s[j]); },
                     [](int64_t j) { return (int32_t)j; }, orow);
