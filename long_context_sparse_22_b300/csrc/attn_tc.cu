@@ -32,7 +32,8 @@
 //
 // Warp roles (persistent CTAs, items dealt round-robin):
 //   warps 0-3  loaders: q tile (box TMA, then RoPE at t in place while the
-//              item's first tile loads), the entry tiles (two buffers), the
+//              item's first tile loads), the entry tiles (four buffers at
+//              c = 128, two at c = 512; q has two at c = 128), the
 //              presence masks;
 //   warp 4     TMEM allocator and QK issuer (one lane issues);
 //   warps 5-8  softmax (a head's 64 logits spread over four threads), the
@@ -60,11 +61,18 @@ struct AtCfg {
     static constexpr int K_BYTES = NA * ATOM;
     static constexpr int Q_BYTES = NA * HG * 128;
     static constexpr int P_BYTES = HG * 128;      // 64 heads x 64 entries bf16
+    // entry-tile buffers and q buffers: at c = 128 a tile is 16 KB, so four
+    // tiles and two q tiles stay in flight; at c = 512 (64 KB tiles) two and one
+    static constexpr int NKB = C == 128 ? 4 : 2;
+    static constexpr int QB = C == 128 ? 2 : 1;
     static constexpr int OFF_K = 0;
-    static constexpr int OFF_Q = OFF_K + 2 * K_BYTES;
-    static constexpr int OFF_P = OFF_Q + Q_BYTES;
+    static constexpr int OFF_Q = OFF_K + NKB * K_BYTES;
+    static constexpr int OFF_P = OFF_Q + QB * Q_BYTES;
     static constexpr int OFF_MISC = OFF_P + 2 * P_BYTES;
-    static constexpr int MISC_BYTES = 8192;
+    // barriers, masks, scales, angles, row pointers, q gains; at c = 128 also
+    // the packed items' per-row setup (128 threads x 2 items x 80 bytes)
+    static constexpr int MISC_PK = 8192;
+    static constexpr int MISC_BYTES = C == 128 ? MISC_PK + 128 * 2 * 80 : 8192;
     static constexpr int SMEM = OFF_MISC + MISC_BYTES + 1024;   // + alignment slack
     static constexpr int S_COL = 0;               // two S buffers: cols 0, 64
     static constexpr int O_COL = 128;             // O^T chunks: 128 + 64 c
@@ -75,9 +83,9 @@ struct AtCfg {
     static constexpr int SM_WARP0 = 5;            // warps 5-8: softmax and epilogue
     static constexpr int PV_WARP = 9;             // warp 9: PV issue
     static constexpr int THREADS = (PV_WARP + 1) * 32;
-    // c = 128: two CTAs per SM (registers capped at 96, TMEM 2 x 256 columns, shared
-    // memory 2 x 75 KB), so one CTA's hand-off latencies overlap the other's work
-    static constexpr int MIN_BLOCKS = C == 128 ? 2 : 1;
+    // one CTA per SM: at c = 128 two CTAs (registers capped at 96) spilled in the
+    // softmax and measured slower than one
+    static constexpr int MIN_BLOCKS = 1;
 };
 
 struct AttnTcArgs {
@@ -290,33 +298,37 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     uint8_t *sP = smem + Cfg::OFF_P;
     uint8_t *misc = smem + Cfg::OFF_MISC;
     uint64_t *bar = (uint64_t *)misc;                  // 32 barrier slots
-    uint64_t *kfull = bar + 0, *kempty = bar + 2, *sfull = bar + 4, *sempty = bar + 6;
-    uint64_t *pfull = bar + 8, *pempty = bar + 10;
-    uint64_t *qland = bar + 12, *qfull = bar + 13, *qempty = bar + 14;
-    uint64_t *ofull = bar + 15, *oempty = bar + 16, *mdone = bar + 17;
+    uint64_t *kfull = bar + 0, *kempty = bar + 4;      // [NKB]
+    uint64_t *sfull = bar + 8, *sempty = bar + 10, *pfull = bar + 12, *pempty = bar + 14;
+    uint64_t *qland = bar + 16, *qfull = bar + 18, *qempty = bar + 20;   // [QB]
+    uint64_t *ofull = bar + 22, *oempty = bar + 23, *mdone = bar + 24;
     uint32_t *tmem_slot = (uint32_t *)(misc + 256);
     volatile int *abort_flag = (volatile int *)(misc + 260);
-    uint32_t *vmask32 = (uint32_t *)(misc + 272);      // [2 buffers][2 halves] presence bits
+    uint32_t *vmask32 = (uint32_t *)(misc + 272);      // [NKB buffers][2 halves] presence bits
     float *alpha_s = (float *)(misc + 512);            // [2][64]
     float *inv_den_s = (float *)(misc + 1024);         // [64]
     float *cs_s = (float *)(misc + 2048);              // [2][256]: cos, sin of the query angle
-    const __nv_bfloat16 **rowp = (const __nv_bfloat16 **)(misc + 4096);   // [2][64] gathered rows
+    const __nv_bfloat16 **rowp = (const __nv_bfloat16 **)(misc + 4096);   // [NKB][64] gathered rows
     float *gain_s = (float *)(misc + 6144);            // [C] RMSNorm gains of q
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; i++) {
+        for (int i = 0; i < Cfg::NKB; i++) {
             tc::mbar_init(&kfull[i], Cfg::NLOAD);
             tc::mbar_init(&kempty[i], 1);
+        }
+        for (int i = 0; i < 2; i++) {
             tc::mbar_init(&sfull[i], 1);
             tc::mbar_init(&sempty[i], 4);
             tc::mbar_init(&pfull[i], 4);
             tc::mbar_init(&pempty[i], 1);
         }
-        tc::mbar_init(qland, 1);
-        tc::mbar_init(qfull, 1);
-        tc::mbar_init(qempty, 1);
+        for (int i = 0; i < Cfg::QB; i++) {
+            tc::mbar_init(&qland[i], 1);
+            tc::mbar_init(&qfull[i], 1);
+            tc::mbar_init(&qempty[i], 1);
+        }
         tc::mbar_init(ofull, 1);
         tc::mbar_init(oempty, 4);
         tc::mbar_init(mdone, 2);
@@ -339,7 +351,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int tid = threadIdx.x;                     // 0 .. NLOAD-1
         const uint32_t kb0 = tc::smem_u32(sK);
         uint32_t g = 0, ii = 0;
-        uint32_t tma_issued = 0, last_g[2] = {0, 0}, q_pending = 0;
+        uint32_t tma_issued = 0, last_g[Cfg::NKB] = {}, q_pending = 0, q_pend_b = 0, q_pend_par = 0;
         // FP8 records of the next gathered tile, loaded while the current one is
         // converted and multiplied (within an item)
         uint4 pf8[KV8 ? 14 : 1], pf16[KV8 ? 4 : 1], pfs = make_uint4(0, 0, 0, 0);
@@ -379,21 +391,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // this item's q rows (box TMA).  Waits are warp-uniform and the four
             // loader warps agree on a failure through a barrier reduction, so none
             // is left at a named barrier; the barrier also publishes cs_s.
-            if (named_bar_or(2, Cfg::NLOAD, !warp_wait(qempty, (ii & 1) ^ 1, a.status, abort_flag, a.spin))) {
+            const int qb = (int)(ii % Cfg::QB);
+            const uint32_t qpar = (ii / Cfg::QB) & 1;
+            uint8_t *sQb = sQ + qb * Cfg::Q_BYTES;
+            if (named_bar_or(2, Cfg::NLOAD, !warp_wait(&qempty[qb], qpar ^ 1, a.status, abort_flag, a.spin))) {
                 ok = false;
                 break;
             }
             if (tid == 0) {
-                tc::mbar_expect_tx(qland, Cfg::Q_BYTES);
+                tc::mbar_expect_tx(&qland[qb], Cfg::Q_BYTES);
                 for (int at = 0; at < Cfg::NA; at++)
-                    tc::tma_load_2d(sQ + at * (Cfg::HG * 128), &tm_q, at * 64,
-                                    (int)(f.bt * a.H + f.hg * Cfg::HG), qland);
+                    tc::tma_load_2d(sQb + at * (Cfg::HG * 128), &tm_q, at * 64,
+                                    (int)(f.bt * a.H + f.hg * Cfg::HG), &qland[qb]);
                 q_pending = 1;
+                q_pend_b = qb;
+                q_pend_par = qpar;
             }
             // q~ = RoPE(q, t): once q has landed, rotate the rotary pairs in place and
             // hand q to the MMA.  Runs while the item's first tile is in flight.
             auto rope_q = [&]() -> bool {
-                if (named_bar_or(2, Cfg::NLOAD, !warp_wait(qland, ii & 1, a.status, abort_flag, a.spin)))
+                if (named_bar_or(2, Cfg::NLOAD, !warp_wait(&qland[qb], qpar, a.status, abort_flag, a.spin)))
                     return false;
                 if (tid == 0) q_pending = 0;
                 if (a.q_norm) {
@@ -401,7 +418,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     // head (adjacent lanes), each over half of the row's 16-byte chunks
                     const int h = tid >> 1, hf = tid & 1;
                     constexpr int CH = C / 16;           // chunks per half row
-                    uint8_t *hb = sQ + (h >> 3) * 1024;
+                    uint8_t *hb = sQb + (h >> 3) * 1024;
                     float ss = 0.f;
 #pragma unroll 4
                     for (int k = 0; k < CH; k++) {
@@ -436,7 +453,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (np == 32) {
                     // one pair per lane, heads warp, warp + 4, ...: all loads in flight at once
                     const int d = a.rope.first + 2 * lane;
-                    uint8_t *qa = sQ + (d >> 6) * (Cfg::HG * 128);
+                    uint8_t *qa = sQb + (d >> 6) * (Cfg::HG * 128);
                     __nv_bfloat162 x[Cfg::HG / 4];
 #pragma unroll
                     for (int k = 0; k < Cfg::HG / 4; k++) {
@@ -456,7 +473,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     for (int i = tid; i < Cfg::HG * np; i += Cfg::NLOAD) {
                         const int h = i / np, pi = i - h * np;
                         const int d = a.rope.first + 2 * pi;
-                        __nv_bfloat162 *pv = (__nv_bfloat162 *)(sQ + (d >> 6) * (Cfg::HG * 128) +
+                        __nv_bfloat162 *pv = (__nv_bfloat162 *)(sQb + (d >> 6) * (Cfg::HG * 128) +
                                                                 (h >> 3) * 1024 + swz128(h, (d & 63) * 2));
                         const float2 v = __bfloat1622float2(*pv);
                         const int ci = (PACK && a.qpi > 1 ? (h / a.H) * np : 0) + pi;
@@ -466,17 +483,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
                 fence_proxy_async();
                 named_bar(2, Cfg::NLOAD);
-                if (tid == 0) tc::mbar_arrive(qfull);
+                if (tid == 0) tc::mbar_arrive(&qfull[qb]);
                 return true;
             };
             for (int j = f.j0; j < f.j1; j++, g++) {
-                const int buf = g & 1;
+                const int buf = (int)(g % Cfg::NKB);
+                const uint32_t kpar = (g / Cfg::NKB) & 1;
                 // compressed tiles are gathered row by row: selected entries, and with
                 // FP8 entries every compressed tile (its rows are dequantised here)
                 const bool gather = j < f.ntc && (a.idx || KV8);
                 // a gathered tile's row addresses go to shared memory before the wait
                 // for its buffer (the barrier that ends the wait publishes them; the
-                // gather two tiles back, the last reader of this slot, has been issued)
+                // gather NKB tiles back, the last reader of this slot, has been issued)
                 uint32_t bal = pf ? pf_bal : 0u;
                 if (gather && tid < 64 && !pf) {
                     const int64_t pos = (int64_t)j * 64 + tid;
@@ -493,14 +511,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     bal = __ballot_sync(0xffffffffu, v);
                 }
                 if (named_bar_or(2, Cfg::NLOAD,
-                                 !warp_wait(&kempty[buf], ((g >> 1) & 1) ^ 1, a.status, abort_flag, a.spin))) {
+                                 !warp_wait(&kempty[buf], kpar ^ 1, a.status, abort_flag, a.spin))) {
                     ok = false;
                     break;
                 }
                 const uint32_t kb = kb0 + buf * Cfg::K_BYTES;
                 if (gather) {
                     // gather of selected entries: cp.async, 16 bytes per thread and instruction;
-                    // the presence mask is written once the softmax two tiles back is done with it
+                    // the presence mask is written once the softmax NKB tiles back is done with it
                     if (tid < 64 && lane == 0) vmask32[buf * 2 + warp] = bal;
                     // the next tile's selected indices, fetched while this one loads
                     if (a.idx && tid < 64 && j + 1 < f.j1 && j + 1 < f.ntc) {
@@ -553,7 +571,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             // the next gathered tile: its row addresses into the other slot
                             // (its last reader, two tiles back, has finished), its presence
                             // bits kept, its records on their way into registers
-                            const int nb = buf ^ 1;
+                            const int nb = (int)((g + 1) % Cfg::NKB);
                             if (tid < 64) {
                                 const int64_t pos = (int64_t)(j + 1) * 64 + tid;
                                 const bool in = pos < f.ncomp;
@@ -635,13 +653,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         asm volatile("cp.async.wait_group 0;" ::: "memory");
         if (*abort_flag && tid == 0) {
             // let every copy issued by TMA land before the CTA exits
-            for (int s = 0; s < 2; s++)
+            for (int s = 0; s < Cfg::NKB; s++)
                 if (tma_issued & (1u << s))
                     for (long long i = 0; i < tc::DRAIN_LIMIT; i++)
-                        if (tc::mbar_test(&kfull[s], (last_g[s] >> 1) & 1)) break;
+                        if (tc::mbar_test(&kfull[s], (last_g[s] / Cfg::NKB) & 1)) break;
             if (q_pending)
                 for (long long i = 0; i < tc::DRAIN_LIMIT; i++)
-                    if (tc::mbar_test(qland, (ii & 1))) break;
+                    if (tc::mbar_test(&qland[q_pend_b], q_pend_par)) break;
         }
     } else if (warp == Cfg::MMA_WARP || warp == Cfg::PV_WARP) {
         // --------------------------------------------------------------- MMA
@@ -656,11 +674,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             constexpr uint32_t idQK = tc::idesc_bf16_f32(64, 64);
             constexpr uint32_t idPV = tc::idesc_bf16_f32(128, 64) | (1u << 15);   // A MN-major
             // descriptors at the buffer bases; a byte offset o adds o >> 4
-            const uint64_t dq = desc_sw128(tc::smem_u32(sQ), 16, 1024);
-            const uint64_t dk[2] = {desc_sw128(tc::smem_u32(sK), 16, 1024),
-                                    desc_sw128(tc::smem_u32(sK + Cfg::K_BYTES), 16, 1024)};
-            const uint64_t dv[2] = {desc_sw128(tc::smem_u32(sK), Cfg::ATOM, 1024),
-                                    desc_sw128(tc::smem_u32(sK + Cfg::K_BYTES), Cfg::ATOM, 1024)};
+            const uint64_t dq0 = desc_sw128(tc::smem_u32(sQ), 16, 1024);
+            const uint64_t dk0 = desc_sw128(tc::smem_u32(sK), 16, 1024);
+            const uint64_t dv0 = desc_sw128(tc::smem_u32(sK), Cfg::ATOM, 1024);
             const uint64_t dp[2] = {desc_sw128(tc::smem_u32(sP), 16, 1024),
                                     desc_sw128(tc::smem_u32(sP + Cfg::P_BYTES), 16, 1024)};
             uint32_t g = 0, ii = 0;
@@ -671,11 +687,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (f.j0 >= f.j1) continue;
                 const int nt = f.j1 - f.j0;
                 if (is_qk) {
-                    if (!warp_wait(qfull, ii & 1, a.status, abort_flag, a.spin)) break;
+                    const int qb = (int)(ii % Cfg::QB);
+                    if (!warp_wait(&qfull[qb], (ii / Cfg::QB) & 1, a.status, abort_flag, a.spin)) break;
+                    const uint64_t dq = dq0 + (uint64_t)((qb * Cfg::Q_BYTES) >> 4);
                     for (int n = 0; n < nt; n++) {
                         const uint32_t gq = g + n;
-                        const int buf = gq & 1;
-                        if (!warp_wait(&kfull[buf], (gq >> 1) & 1, a.status, abort_flag, a.spin) ||
+                        const int buf = gq & 1;                         // S buffer
+                        const int kbuf = (int)(gq % Cfg::NKB);         // entry tile
+                        if (!warp_wait(&kfull[kbuf], (gq / Cfg::NKB) & 1, a.status, abort_flag, a.spin) ||
                             !warp_wait(&sempty[buf], ((gq >> 1) & 1) ^ 1, a.status, abort_flag, a.spin)) {
                             ok = false;
                             break;
@@ -688,17 +707,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                 for (int kk = 0; kk < 4; kk++)
                                     tc::mma_bf16(tmem + Cfg::S_COL + buf * 64,
                                                  dq + (uint64_t)((at * (Cfg::HG * 128) + kk * 32) >> 4),
-                                                 dk[buf] + (uint64_t)((at * Cfg::ATOM + kk * 32) >> 4), idQK,
+                                                 dk0 + (uint64_t)((kbuf * Cfg::K_BYTES + at * Cfg::ATOM + kk * 32) >> 4), idQK,
                                                  (at | kk) != 0);
                             tc::mma_commit(&sfull[buf]);
-                            if (n == nt - 1) tc::mma_commit(qempty);
+                            if (n == nt - 1) tc::mma_commit(&qempty[qb]);
                         }
                         __syncwarp();
                     }
                 } else {
                     for (int n = 0; n < nt; n++) {
                         const uint32_t gp = g + n;
-                        const int bp = gp & 1;
+                        const int bp = gp & 1;                          // P buffer
+                        const int kbuf = (int)(gp % Cfg::NKB);         // entry tile (V)
                         if (!warp_wait(&pfull[bp], (gp >> 1) & 1, a.status, abort_flag, a.spin) ||
                             (n == 0 && !warp_wait(oempty, (ii & 1) ^ 1, a.status, abort_flag, a.spin))) {
                             ok = false;
@@ -711,11 +731,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                                 for (int ks = 0; ks < 4; ks++)
                                     tc::mma_bf16(tmem + Cfg::O_COL + c * 64,
-                                                 dv[bp] + (uint64_t)(((2 * c) * Cfg::ATOM + ks * 2048) >> 4),
+                                                 dv0 + (uint64_t)((kbuf * Cfg::K_BYTES + (2 * c) * Cfg::ATOM + ks * 2048) >> 4),
                                                  dp[bp] + (uint64_t)((ks * 32) >> 4), idPV,
                                                  (n == 0 && ks == 0) ? 0u : 1u);
                             tc::mma_commit(&pempty[bp]);
-                            tc::mma_commit(&kempty[bp]);
+                            tc::mma_commit(&kempty[kbuf]);
                         }
                         __syncwarp();
                     }
@@ -750,6 +770,43 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         uint32_t g = 0, ii = 0;
         ItemInfo fn;                             // the next item, worked out during the last PV
         bool have_fn = false;
+        // packed items: each row's own list as bounds on the entry offset within
+        // the compressed part (< nv) and on the window offset from p0
+        // (wlo < x <= whi), its sink logit, and the cos / sin of -t_q at this
+        // thread's epilogue dim for each query of the item
+        struct PackRows {
+            bool real[2];
+            int nv[2], wlo[2], whi[2];
+            float zl[2];
+            float dc[4], ds[4];
+        };
+        auto pack_rows = [&](const ItemInfo &ff, PackRows &pr) {
+#pragma unroll
+            for (int u = 0; u < 2; u++) {
+                const int q = hr[u] / a.H;
+                pr.real[u] = q < ff.nq;
+                const int64_t t_r = pr.real[u] ? a.q_pos[ff.bt + q] : ff.t;
+                pr.nv[u] = (int)visible_count(t_r, a.m, a.E);
+                pr.wlo[u] = (int)(t_r - a.n_win - ff.p0);
+                pr.whi[u] = (int)(t_r - ff.p0);
+                pr.zl[u] = a.sink[hr[u] % a.H] * 1.4426950408889634f;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                pr.dc[q] = 1.f;
+                pr.ds[q] = 0.f;
+            }
+            const int de = (Cfg::NC - 1) * 128 + quarter * 32 + lane;
+            if (a.chunk_tiles == 0 && a.derotate && de >= a.rope.first) {
+#pragma unroll
+                for (int q = 0; q < 4; q++)
+                    if (q < ff.nq) rope_cos_sin(a.rope, -a.q_pos[ff.bt + q], (de - a.rope.first) >> 1, pr.dc[q], pr.ds[q]);
+            }
+        };
+        static_assert(sizeof(PackRows) <= 80, "per-thread slot");
+        // this thread's two slots (the item, the next item), c = 128 only
+        PackRows *pslot = reinterpret_cast<PackRows *>(misc + Cfg::MISC_PK + st * 160);
+        bool have_pnext = false;
         int zl_hg = -1;                          // head group whose sink logits zl2 holds
         float zl2[2] = {-INFINITY, -INFINITY};
         for (int64_t it = blockIdx.x; it < a.n_items; it += G) {
@@ -762,19 +819,30 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const bool packed = PACK && a.qpi > 1;   // rows are (query, head) pairs of f.nq queries
             bool real[2];
             float m_run[2], l_run[2];
-            int64_t t_r[2], nv_r[2];             // packed: the row's query position and visible entries
+            // packed: the row's own list, as bounds on the entry offset within the
+            // compressed part (< nv_r) and on the window offset from p0
+            // (wlo_r < x <= whi_r)
+            int nv_r[2], wlo_r[2], whi_r[2];
+            PackRows *pcur = pslot + (ii & 1);
+            if (packed && !have_pnext) {
+                PackRows pn;
+                pack_rows(f, pn);
+                *pcur = pn;
+            }
+            have_pnext = false;
 #pragma unroll
             for (int u = 0; u < 2; u++) {
                 if (packed) {
-                    const int q = hr[u] / a.H;
-                    real[u] = q < f.nq;
-                    t_r[u] = real[u] ? a.q_pos[f.bt + q] : f.t;
-                    nv_r[u] = visible_count(t_r[u], a.m, a.E);
-                    zl2[u] = a.sink[hr[u] % a.H] * 1.4426950408889634f;
+                    real[u] = pcur->real[u];
+                    nv_r[u] = pcur->nv[u];
+                    wlo_r[u] = pcur->wlo[u];
+                    whi_r[u] = pcur->whi[u];
+                    zl2[u] = pcur->zl[u];
                 } else {
                     real[u] = h0 + hr[u] < a.H;
-                    t_r[u] = f.t;
                     nv_r[u] = 0;
+                    wlo_r[u] = 0;
+                    whi_r[u] = 0;
                     if (f.hg != zl_hg) zl2[u] = real[u] ? a.sink[h0 + hr[u]] * 1.4426950408889634f : -INFINITY;
                 }
                 m_run[u] = a.chunk_tiles > 0 ? -INFINITY : zl2[u];
@@ -784,15 +852,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const uint32_t gfirst = g;
             bool fail = false;
             for (int j = f.j0; j < f.j1; j++, g++) {
-                const int buf = g & 1;
+                const int buf = g & 1;                   // S and P buffers
                 const uint32_t par = (g >> 1) & 1;
+                const int kbuf = (int)(g % Cfg::NKB);   // entry tile
+                const uint32_t kpar = (g / Cfg::NKB) & 1;
                 // the loaders' presence mask for this tile (its kfull phase has
                 // completed and cannot advance again before this tile's PV) and the
                 // P buffer (the PV of two tiles back has read it): both are ready
                 // before this tile's logits, so they are checked first
-                bool ok = warp_wait(&kfull[buf], par, a.status, abort_flag, a.spin) &&
+                bool ok = warp_wait(&kfull[kbuf], kpar, a.status, abort_flag, a.spin) &&
                           warp_wait(&pempty[buf], par ^ 1, a.status, abort_flag, a.spin);
-                const uint32_t mlo = ok ? vmask32[buf * 2] : 0u, mhi = ok ? vmask32[buf * 2 + 1] : 0u;
+                const uint32_t mlo = ok ? vmask32[kbuf * 2] : 0u, mhi = ok ? vmask32[kbuf * 2 + 1] : 0u;
                 ok = ok && warp_wait(&sfull[buf], par, a.status, abort_flag, a.spin);
                 uint32_t raw[32];
                 if (ok) {
@@ -811,6 +881,32 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     tc::tmem_ld_wait();
                     tc::tmem_regs_ready<32>(raw);
                 }
+                // each row's visible entries of this tile: the presence mask, and for
+                // packed rows the interval of the tile that is in the row's own list
+                uint32_t rlo[2], rhi[2];
+#pragma unroll
+                for (int u = 0; u < 2; u++) {
+                    rlo[u] = mlo;
+                    rhi[u] = mhi;
+                    if (packed) {
+                        int lo, hi;
+                        if (j < f.ntc) {
+                            lo = 0;
+                            hi = nv_r[u] - j * 64;
+                        } else {
+                            const int base = (j - f.ntc) * 64;
+                            lo = wlo_r[u] - base + 1;
+                            hi = whi_r[u] - base + 1;
+                        }
+                        lo = lo < 0 ? 0 : (lo > 64 ? 64 : lo);
+                        hi = hi < 0 ? 0 : (hi > 64 ? 64 : hi);
+                        const uint64_t below_hi = hi >= 64 ? ~0ull : (1ull << hi) - 1ull;
+                        const uint64_t below_lo = lo >= 64 ? ~0ull : (1ull << lo) - 1ull;
+                        const uint64_t im = hi > lo ? below_hi & ~below_lo : 0ull;
+                        rlo[u] &= (uint32_t)im;
+                        rhi[u] &= (uint32_t)(im >> 32);
+                    }
+                }
                 // v[u][2i + e]: head hr[u], entry 8i + 2 t4 + e  (raw[4i + 2u + e])
                 float v[2][16];
 #pragma unroll
@@ -818,19 +914,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                     for (int e = 0; e < 2; e++) {
                         const int ent = 8 * i + 2 * t4 + e;
-                        const uint32_t bit = ent < 32 ? (mlo >> ent) & 1u : (mhi >> (ent - 32)) & 1u;
 #pragma unroll
                         for (int u = 0; u < 2; u++) {
-                            bool vis = bit != 0;
-                            if (packed) {        // the row's own list: its visible entries, its window
-                                if (j < f.ntc) {
-                                    vis = vis && (int64_t)j * 64 + ent < nv_r[u];
-                                } else {
-                                    const int64_t pw = f.p0 + (int64_t)(j - f.ntc) * 64 + ent;
-                                    vis = vis && pw <= t_r[u] && pw > t_r[u] - a.n_win;
-                                }
-                            }
-                            v[u][2 * i + e] = vis ? __uint_as_float(raw[4 * i + 2 * u + e]) * a.scale_log2 : -INFINITY;
+                            const uint32_t bit = i < 4 ? (rlo[u] >> ent) & 1u : (rhi[u] >> (ent - 32)) & 1u;
+                            v[u][2 * i + e] = bit ? __uint_as_float(raw[4 * i + 2 * u + e]) * a.scale_log2 : -INFINITY;
                         }
                     }
                 bool need[2];
@@ -907,6 +994,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (it + G < a.n_items) {
                 item_info(a, it + G, fn);
                 have_fn = true;
+                if (packed && fn.j0 < fn.j1) {
+                    PackRows pn;
+                    pack_rows(fn, pn);
+                    pslot[(ii + 1) & 1] = pn;
+                    have_pnext = true;
+                }
             }
             float dcr = 1.f, dsr = 0.f;
             {
@@ -982,16 +1075,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         // rows hb .. hb + 31 hold at most two queries (H >= 16): each
                         // row is rotated back by its own query's position
                         const int q0 = hb / a.H, q1 = (hb + 31) / a.H;
-                        float cr0 = 1.f, sr0 = 0.f, cr1 = 1.f, sr1 = 0.f;
-                        if (rot) {
-                            const int pi_ = (d - a.rope.first) >> 1;
-                            rope_cos_sin(a.rope, -(q0 < f.nq ? a.q_pos[f.bt + q0] : f.t), pi_, cr0, sr0);
-                            rope_cos_sin(a.rope, -(q1 < f.nq ? a.q_pos[f.bt + q1] : f.t), pi_, cr1, sr1);
-                        }
+                        const int split = (q0 + 1) * a.H - hb;   // rows h >= split belong to q1
+                        // queries past the item's last are padding rows (never stored)
+                        const float cr0 = pcur->dc[q0 & 3], sr0 = pcur->ds[q0 & 3];
+                        const float cr1 = pcur->dc[q1 & 3], sr1 = pcur->ds[q1 & 3];
 #pragma unroll
                         for (int h = 0; h < 32; h++) {
                             const float op = __shfl_xor_sync(0xffffffffu, o[h], 1);
-                            const bool second = (hb + h) / a.H != q0;
+                            const bool second = h >= split;
                             const float crh = second ? cr1 : cr0, srh = second ? sr1 : sr0;
                             if (rot) o[h] = o[h] * crh + op * ((lane & 1) ? srh : -srh);
                         }
