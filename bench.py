@@ -47,11 +47,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # of the same kernel on a smaller case of the same shape (files in profiles/):
 # attention per query token (attn_tc_sparse_attn_4096q.md,
 # attn_tc_hca_prefill_8192q.md), decode indexer per visible entry
-# (indexer_tc_decode_8x262144.md).  Traffic per launch = this x the launch's units.
+# (indexer_tc_decode_8x262144.md, and indexer_fp4_decode_8x262144.md on the
+# low-precision caches).  Traffic per launch = this x the launch's units.
 TRAFFIC_PER_UNIT = {
-    ("sparse_attn", "prefill"): (301.359616e6 + 236.104192e6) / 4096,
-    ("hca_attn", "prefill"): (545.660928e6 + 491.687424e6) / 8192,
-    ("indexer", "decode"): (537.125120e6 + 9.781760e6) / (8 * 262144),
+    ("sparse_attn", "prefill"): (301.435648e6 + 236.806144e6) / 4096,
+    ("hca_attn", "prefill"): (545.948672e6 + 492.194560e6) / 8192,
+    ("indexer", "decode"): (537.121280e6 + 10.186752e6) / (8 * 262144),
+    # the MXFP4 decode indexer (indexer_fp4_decode_8x262144.md)
+    ("indexer", "decode_lowp"): (142.904576e6 + 6.599680e6) / (8 * 262144),
 }
 
 
@@ -432,7 +435,7 @@ def roofline(wl, stages, steps):
         bound, unit = "hbm", "GB/s"
         achieved = w.get(byte_key, 0) / launches_per_step / (per_launch_ms / 1e3) / 1e9
         peak = pk["hbm_gbs"]
-    phase = "decode" if decode else "prefill"
+    phase = ("decode_lowp" if wl.lowp else "decode") if decode else "prefill"
     # the captures are of the tensor-core kernels (bf16, c = 512)
     tc_path = wl.s["dtype"] == "bf16" and wl.s["c"] == 512
     per_unit = TRAFFIC_PER_UNIT.get((dom, phase)) if tc_path else None
