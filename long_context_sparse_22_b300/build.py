@@ -17,7 +17,7 @@ NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]
-SOURCES = ["api.cu", "compress.cu", "indexer_simt.cu", "indexer_tc.cu", "topk.cu", "attn_simt.cu", "attn_tc.cu", "lowp.cu", "gemm.cu"]
+SOURCES = ["api.cu", "compress.cu", "indexer_simt.cu", "indexer_tc.cu", "topk.cu", "attn_simt.cu", "attn_tc.cu", "attn_pack.cu", "lowp.cu", "gemm.cu"]
 
 
 def _deps():

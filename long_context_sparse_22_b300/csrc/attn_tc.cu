@@ -45,6 +45,7 @@
 // Every wait is taken by a whole warp on an mbarrier (with an iteration cap
 // after which the kernel records a timeout and unwinds), and waits whose
 // phase must already have completed come before the one that can block.
+#include "attn_common.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -172,82 +173,6 @@ __device__ __forceinline__ void item_info(const AttnTcArgs &a, int64_t it, ItemI
         f.j0 = 0;
         f.j1 = f.nt;
     }
-}
-
-__device__ __forceinline__ int swz128(int row, int byte) {   // within a 1024-byte atom group
-    return (row & 7) * 128 + ((((byte >> 4) ^ row) & 7) << 4) + (byte & 15);
-}
-
-__device__ __forceinline__ void fence_proxy_async() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void named_bar(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-// Barrier over n threads that also returns whether any of them passed true.
-__device__ __forceinline__ bool named_bar_or(int id, int n, bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %3, 0;\n\t"
-        "barrier.cta.red.or.pred q, %1, %2, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(id), "r"(n), "r"((uint32_t)v)
-        : "memory");
-    return r != 0;
-}
-
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// 32 lanes x 16 consecutive 32-bit columns, load and store.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_st_wait() {
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = 0;
-    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-
-// Wait by the whole warp, failure agreed by the warp.  Every lane polls the
-// barrier: when lane 0 polled alone while the others waited at a shuffle, the
-// warp's next burst of copies issued several times slower after a wait that
-// had blocked.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, unsigned *status,
-                                          volatile int *abort_flag, long long limit) {
-    const bool ok = tc::mbar_wait(bar, parity, status, abort_flag, limit);
-    return __all_sync(0xffffffffu, ok);
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t bytes) {
@@ -1320,6 +1245,7 @@ static cudaError_t launch_attn_tc_c(int64_t B, const AttnArgs &g, const int32_t 
 cudaError_t launch_attn_tc(int64_t B, const AttnArgs &g, const int32_t *cnt, int n_chunks,
                            void *split_ws, int max_ctas, cudaStream_t st) {
     if (B * g.Tq == 0) return cudaSuccess;
+    if (attn_pack_supported(B, g, n_chunks)) return launch_attn_pack(B, g, max_ctas, st);
     if (g.kv8) {
         if (g.c != 512) return cudaErrorInvalidValue;
         return launch_attn_tc_c<512, true, false>(B, g, cnt, n_chunks, split_ws, max_ctas, st);

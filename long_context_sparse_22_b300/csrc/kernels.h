@@ -143,6 +143,11 @@ int attn_tc_chunks(int64_t rows, int H, int64_t max_list, bool invariant);
 size_t attn_tc_split_bytes(int64_t rows, int H, int c, int n_chunks);
 cudaError_t launch_attn_tc(int64_t B, const AttnArgs &a, const int32_t *cnt, int n_chunks,
                            void *split_ws, int max_ctas, cudaStream_t st);
+// Dense attention with 128 (query, head) rows per item (c = 128, H dividing
+// 128, no split, no log-denominator output, no q norm): attn_pack.cu.
+bool attn_pack_supported(int64_t B, const AttnArgs &g, int n_chunks);
+cudaError_t launch_attn_pack(int64_t B, const AttnArgs &g, int max_ctas, cudaStream_t st);
+
 // SM count of the current device (cached per device).
 int device_sms();
 

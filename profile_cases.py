@@ -6,6 +6,7 @@
 Cases:
   indexer_prefill   indexer_score, 16384 queries x 4096 entries, 64 x 128 (bf16)
   indexer_decode    indexer_score, 8 sequences x 262144 entries, 1 query each (bf16)
+  indexer_decode_flash  indexer_score, 32 sequences x 32768 entries, 1 query each (bf16)
   topk_prefill      topk_select over [16384, 4096] fp32 scores, k = 512
   topk_decode       topk_select over [8, 262144] fp32 scores, k = 1024
   compress          csa_compress, n = 65536, c = 512, m = 4 (bf16, with raw rows)
@@ -248,6 +249,7 @@ def case_csa_prefill():
 CASES = {
     "indexer_prefill": lambda: case_indexer(16384, 4096, 1),
     "indexer_decode": lambda: case_indexer(1, 262144, 8),
+    "indexer_decode_flash": lambda: case_indexer(1, 32768, 32),
     "topk_prefill": lambda: case_topk(16384, 4096, 1, 512),
     "topk_decode": lambda: case_topk(1, 262144, 8, 1024),
     "compress": case_compress,

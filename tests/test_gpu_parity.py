@@ -244,6 +244,11 @@ def test_sparse_attn(csa, orc, dtype, B, T, H, c, E, k, m, n_win, r, derot):
     ("f32", 1, 40, 4, 64, 30, 4, 16, 32, 0),
     ("bf16", 1, 3, 64, 512, 200, 128, 128, 64, (1 << 25) + 77),
     ("f32", 1, 5, 4, 64, 30, 4, 16, 32, (1 << 26) + 3),
+    # c = 128 with 32, 64 and 128 heads: 4, 2 and 1 queries on an item's 128 rows
+    # (37 queries leave a short last item)
+    ("bf16", 2, 37, 32, 128, 40, 128, 128, 64, 0),
+    ("bf16", 1, 9, 64, 128, 30, 4, 16, 32, 0),
+    ("bf16", 1, 3, 128, 128, 20, 128, 128, 64, 0),
 ])
 def test_hca_attn(csa, orc, dtype, B, T, H, c, E, m, n_win, r, t0):
     seed = 500 + E
@@ -263,6 +268,27 @@ def test_hca_attn(csa, orc, dtype, B, T, H, c, E, m, n_win, r, t0):
         ro = orc.attend(q[b], pos[b], kvc[b], m, kv_raw[b], int(raw_pos0[b]), sink, idx=None,
                         n_win=n_win, rope_dims=r)
         check_close(g[b], ro, dtype, "hca_attn out")
+
+
+def test_hca_attn_c128_no_derotate(csa, orc):
+    """Dense attention at c = 128, 16 heads (eight queries per item), output
+    left rotated."""
+    dtype, B, T, H, c, E, m, n_win, r = "bf16", 1, 45, 16, 128, 50, 128, 128, 64
+    seed = 650
+    q = synth.normal(seed, 1, (B, T, H, c), 1.0, dtype)
+    kvc = synth.normal(seed, 2, (B, E, c), 1.0, dtype)
+    t_last = E * m + 3
+    L = n_win + T
+    kv_raw = synth.normal(seed, 3, (B, L, c), 1.0, dtype)
+    sink = synth.normal(seed, 4, (H,), 1.0, "f32")
+    pos = np.tile(t_last - T + 1 + np.arange(T, dtype=np.int64), (B, 1))
+    raw_pos0 = np.full(B, t_last - L + 1, np.int64)
+    p = csa.params(m=m, n_win=n_win, rope_dims=r, derotate=0)
+    out = csa.hca_attn(dev(q), dev(pos), dev(kvc), dev(kv_raw), dev(raw_pos0), dev(sink), p,
+                       ws=_nan_ws(csa))
+    ro = orc.attend(q[0], pos[0], kvc[0], m, kv_raw[0], int(raw_pos0[0]), sink, idx=None, n_win=n_win,
+                    rope_dims=r, derotate=0)
+    check_close(host(out)[0], ro, dtype, "hca_attn c128 no derotate")
 
 
 # ---------------------------------------------------------------- fused
