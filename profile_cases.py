@@ -12,6 +12,7 @@ Cases:
   compress          csa_compress, n = 65536, c = 512, m = 4 (bf16, with raw rows)
   compress_hca      csa_compress, n = 65536, c = 512, m' = 128 (bf16, with raw rows)
   hca_prefill_c128  hca_attn, 8192 queries, 16 heads x 128, m' = 128 + window
+  hca_prefill_c128_qnorm  the same with the q RMSNorm (the 64-row packed kernel)
   sparse_attn       sparse_attn, 4096 queries, 64 heads x 512, k = 512 + window
   hca_decode        hca_attn, 8 sequences x 8192 entries, 128 heads x 512
   hca_prefill       hca_attn, 8192 queries over 64 entries (m' = 128) + window, 64 heads x 512
@@ -218,7 +219,7 @@ def case_hca_decode():
     return lambda: csa.hca_attn(q, pos, kvc, raw, rp0, sink, p, out=out)
 
 
-def case_hca_prefill(H=64, c=512):
+def case_hca_prefill(H=64, c=512, q_norm=False):
     T, m = 8192, 128
     q = _bf16(1, T, H, c)
     E = T // m
@@ -228,7 +229,8 @@ def case_hca_prefill(H=64, c=512):
     rp0 = torch.zeros(1, dtype=torch.int64, device="cuda")
     sink = torch.randn(H, device="cuda")
     out = torch.empty_like(q)
-    p = csa.params(m=m, n_win=128, rope_dims=64)
+    gain = (1 + 0.1 * torch.randn(c, device="cuda")) if q_norm else None
+    p = csa.params(m=m, n_win=128, rope_dims=64, q_norm=gain)
     return lambda: csa.hca_attn(q, pos, kvc, raw, rp0, sink, p, out=out)
 
 
@@ -255,6 +257,7 @@ CASES = {
     "compress": case_compress,
     "compress_hca": lambda: case_compress(128),
     "hca_prefill_c128": lambda: case_hca_prefill(16, 128),
+    "hca_prefill_c128_qnorm": lambda: case_hca_prefill(16, 128, q_norm=True),
     "sparse_attn": case_sparse_attn,
     "hca_decode": case_hca_decode,
     "hca_prefill": case_hca_prefill,
