@@ -1,6 +1,8 @@
 // Dense attention with 128 rows per work item: every visible compressed entry
 // plus the sliding window, for a layer whose head count divides 128, at
-// c = 128 (the heavily compressed layer of the 16-head configuration).
+// c = 128 (the heavily compressed layer of the 16-head configuration), with
+// the optional q RMSNorm ("DeepSeek-V4" book ch.7 "Query and KV normalization") and
+// log-denominator output.
 //
 // ["DeepSeek-V4" book ch.7 "HCA's compressor": HCA attends to every visible
 // compressed entry plus the window; ch.6 "Sliding-window keys and values",
@@ -65,6 +67,9 @@ struct PkArgs {
     const int64_t *raw_pos0;
     const float *sink;
     __nv_bfloat16 *out;
+    float *lse;              // [B*T*H] log-denominators, or nullptr
+    const float *q_norm;     // RMSNorm gains of q (C floats), or nullptr
+    float norm_eps;
     unsigned *status;
     int64_t T, E, L;
     int H, m, n_win, derotate, qpi;
@@ -206,6 +211,39 @@ attn_pack_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (named_bar_or(2, Cfg::NLOAD, !warp_wait(&qland[qb], qpar, a.status, abort_flag, a.spin)))
                     return false;
                 if (tid == 0) q_pending = 0;
+                if (a.q_norm) {
+                    // RMSNorm of each row before its rotation, one row per thread
+                    // (the normalised row is rounded to bf16, then rotated)
+                    const int r = tid;
+                    float ss = 0.f;
+#pragma unroll 4
+                    for (int k = 0; k < 16; k++) {
+                        const int d0 = k * 8;
+                        const uint4 u = *reinterpret_cast<const uint4 *>(sQb + (d0 >> 6) * Cfg::Q_ATOM + (r >> 3) * 1024 +
+                                                                         swz128(r, (d0 & 63) * 2));
+                        float fv[8];
+                        Vec<__nv_bfloat16>::unpack(u, fv);
+#pragma unroll
+                        for (int e = 0; e < 8; e++) ss = fmaf(fv[e], fv[e], ss);
+                    }
+                    const float rs = 1.0f / sqrtf(ss / (float)Cfg::C + a.norm_eps);
+#pragma unroll 4
+                    for (int k = 0; k < 16; k++) {
+                        const int d0 = k * 8;
+                        uint4 *pu = reinterpret_cast<uint4 *>(sQb + (d0 >> 6) * Cfg::Q_ATOM + (r >> 3) * 1024 +
+                                                              swz128(r, (d0 & 63) * 2));
+                        float fv[8];
+                        Vec<__nv_bfloat16>::unpack(*pu, fv);
+                        uint4 o;
+                        __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(&o);
+#pragma unroll
+                        for (int e = 0; e < 4; e++)
+                            o2[e] = __floats2bfloat162_rn(fv[2 * e] * rs * __ldg(a.q_norm + d0 + 2 * e),
+                                                          fv[2 * e + 1] * rs * __ldg(a.q_norm + d0 + 2 * e + 1));
+                        *pu = o;
+                    }
+                    named_bar(2, Cfg::NLOAD);
+                }
                 if (np == 32) {
                     // one pair per lane; warp w rotates rows w, w + 4, ...
                     const int d = a.rope.first + 2 * lane;
@@ -508,6 +546,8 @@ attn_pack_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // with one dim per thread over the 128 rows
             const float den = l_run + (zl != -INFINITY ? ex2(zl - m_run) : 0.f);
             inv_den_s[r] = (real && den > 0.f) ? 1.0f / den : 0.f;
+            if (a.lse && real)
+                a.lse[(f.bt0 + qr) * a.H + hr] = den > 0.f ? (m_run + log2f(den)) * 0.6931471805599453f : -INFINITY;
             const bool ok = warp_wait(ofull, ii & 1, a.status, abort_flag, a.spin);
             if (named_bar_or(1, 128, !ok)) break;
             tc::fence_after_sync();
@@ -568,8 +608,8 @@ attn_pack_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 bool attn_pack_supported(int64_t B, const AttnArgs &g, int n_chunks) {
     // TMA row coordinates are 32-bit
     const int64_t lim = 0x7fff0000LL;
-    return g.c == 128 && !g.kv8 && g.idx == nullptr && n_chunks <= 1 && g.lse == nullptr &&
-           g.q_norm == nullptr && g.H >= 16 && 128 % g.H == 0 && g.rope.pairs <= PkCfg::MAX_PAIRS &&
+    return g.c == 128 && !g.kv8 && g.idx == nullptr && n_chunks <= 1 && g.H >= 16 && 128 % g.H == 0 &&
+           g.rope.pairs <= PkCfg::MAX_PAIRS &&
            g.Tq >= 1 && B * g.Tq * g.H < lim && B * g.E < lim && B * g.L < lim;
 }
 
@@ -582,6 +622,9 @@ cudaError_t launch_attn_pack(int64_t B, const AttnArgs &g, int max_ctas, cudaStr
     a.raw_pos0 = g.raw_pos0;
     a.sink = g.sink;
     a.out = (__nv_bfloat16 *)g.out;
+    a.lse = g.lse;
+    a.q_norm = g.q_norm;
+    a.norm_eps = g.norm_eps;
     a.status = g.status;
     a.T = g.Tq; a.E = g.E; a.L = g.L;
     a.H = g.H; a.m = g.m; a.n_win = g.n_win; a.derotate = g.derotate;

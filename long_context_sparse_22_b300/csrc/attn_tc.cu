@@ -70,10 +70,7 @@ struct AtCfg {
     static constexpr int OFF_Q = OFF_K + NKB * K_BYTES;
     static constexpr int OFF_P = OFF_Q + QB * Q_BYTES;
     static constexpr int OFF_MISC = OFF_P + 2 * P_BYTES;
-    // barriers, masks, scales, angles, row pointers, q gains; at c = 128 also
-    // the packed items' per-row setup (128 threads x 2 items x 80 bytes)
-    static constexpr int MISC_PK = 8192;
-    static constexpr int MISC_BYTES = C == 128 ? MISC_PK + 128 * 2 * 80 : 8192;
+    static constexpr int MISC_BYTES = 8192;       // barriers, masks, scales, angles, row pointers, q gains
     static constexpr int SMEM = OFF_MISC + MISC_BYTES + 1024;   // + alignment slack
     static constexpr int S_COL = 0;               // two S buffers: cols 0, 64
     static constexpr int O_COL = 128;             // O^T chunks: 128 + 64 c
@@ -108,8 +105,6 @@ struct AttnTcArgs {
     int chunk_tiles;         // > 0: split mode with this many tiles per item
     int n_chunks;
     int64_t n_items;
-    int qpi;                 // queries packed into one item's 64 rows (64 / H; 1 = one query)
-    int64_t tq_blocks;       // query blocks per sequence: ceil(T / qpi)
     long long spin;          // polls before a wait between roles gives up
     const float *q_norm;     // RMSNorm gains of q (C floats) or nullptr
     float norm_eps;
@@ -120,7 +115,6 @@ struct AttnTcArgs {
 struct ItemInfo {
     int64_t bt, b, t;        // first query row of the item, its sequence, its largest position
     int64_t tmin;            // smallest query position of the item
-    int nq;                  // queries in the item (> 1 only when queries are packed)
     int hg, chunk;
     int64_t ncomp;           // compressed slots (tiles 0 .. ntc-1)
     int64_t p0, nwin;        // window rows p0 .. p0+nwin-1 (tiles ntc ..)
@@ -136,30 +130,14 @@ __device__ __forceinline__ void item_info(const AttnTcArgs &a, int64_t it, ItemI
         r /= a.n_chunks;
     }
     f.hg = (int)(r % a.n_hg);
-    if (a.qpi == 1) {
-        f.bt = r / a.n_hg;
-        f.b = f.bt / a.T;
-        f.t = a.q_pos[f.bt];
-        f.tmin = f.t;
-        f.nq = 1;
-    } else {
-        // qpi consecutive queries of one sequence share the item (dense lists only)
-        const int64_t qb = r / a.n_hg;
-        f.b = qb / a.tq_blocks;
-        const int64_t i0 = (qb % a.tq_blocks) * a.qpi;
-        f.bt = f.b * a.T + i0;
-        f.nq = (int)(a.T - i0 < a.qpi ? a.T - i0 : a.qpi);
-        f.t = f.tmin = a.q_pos[f.bt];
-        for (int q = 1; q < f.nq; q++) {
-            const int64_t tq = a.q_pos[f.bt + q];
-            f.t = tq > f.t ? tq : f.t;
-            f.tmin = tq < f.tmin ? tq : f.tmin;
-        }
-    }
+    f.bt = r / a.n_hg;
+    f.b = f.bt / a.T;
+    f.t = a.q_pos[f.bt];
+    f.tmin = f.t;
     if (a.idx) f.ncomp = a.cnt ? a.cnt[f.bt] : a.k;
     else f.ncomp = visible_count(f.t, a.m, a.E);
     if (f.ncomp < 0) f.ncomp = 0;
-    int64_t p0 = f.tmin - a.n_win + 1;     // the union of the item's windows
+    int64_t p0 = f.tmin - a.n_win + 1;
     if (p0 < 0) p0 = 0;
     f.p0 = p0;
     f.nwin = a.n_win > 0 && f.t >= 0 ? f.t - p0 + 1 : 0;
@@ -210,7 +188,7 @@ __device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, ui
                  : "memory");
 }
 
-template <int C, bool KV8, bool PACK>
+template <int C, bool KV8>
 __global__ void __launch_bounds__(AtCfg<C>::THREADS, AtCfg<C>::MIN_BLOCKS)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
                const __grid_constant__ CUtensorMap tm_w,
@@ -299,12 +277,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             // the cos / sin of this item's angle and its first selected indices,
             // worked out while the previous item's last QK still reads q
-            // (one set of angles per packed query: query q's pair pi at q * pairs + pi)
-            for (int i = tid; i < a.qpi * a.rope.pairs; i += Cfg::NLOAD) {
-                const int q = i / a.rope.pairs, pi = i - q * a.rope.pairs;
-                const int64_t tq = q == 0 ? (a.qpi == 1 ? f.t : a.q_pos[f.bt]) : (q < f.nq ? a.q_pos[f.bt + q] : f.t);
+            for (int i = tid; i < a.rope.pairs; i += Cfg::NLOAD) {
                 float c_, s_;
-                rope_cos_sin(a.rope, tq, pi, c_, s_);
+                rope_cos_sin(a.rope, f.t, i, c_, s_);
                 cs_s[i] = c_;
                 cs_s[256 + i] = s_;
             }
@@ -388,7 +363,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                     for (int k = 0; k < Cfg::HG / 4; k++) {
                         const int h = warp + 4 * k;
-                        const int ci = PACK && a.qpi > 1 ? (h / a.H) * 32 + lane : lane;
+                        const int ci = lane;
                         const float c_ = cs_s[ci], s_ = cs_s[256 + ci];
                         const float2 v = __bfloat1622float2(x[k]);
                         *(__nv_bfloat162 *)(qa + (h >> 3) * 1024 + swz128(h, (d & 63) * 2)) =
@@ -401,7 +376,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         __nv_bfloat162 *pv = (__nv_bfloat162 *)(sQb + (d >> 6) * (Cfg::HG * 128) +
                                                                 (h >> 3) * 1024 + swz128(h, (d & 63) * 2));
                         const float2 v = __bfloat1622float2(*pv);
-                        const int ci = (PACK && a.qpi > 1 ? (h / a.H) * np : 0) + pi;
+                        const int ci = pi;
                         const float c_ = cs_s[ci], s_ = cs_s[256 + ci];
                         *pv = __floats2bfloat162_rn(v.x * c_ - v.y * s_, v.x * s_ + v.y * c_);
                     }
@@ -695,43 +670,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         uint32_t g = 0, ii = 0;
         ItemInfo fn;                             // the next item, worked out during the last PV
         bool have_fn = false;
-        // packed items: each row's own list as bounds on the entry offset within
-        // the compressed part (< nv) and on the window offset from p0
-        // (wlo < x <= whi), its sink logit, and the cos / sin of -t_q at this
-        // thread's epilogue dim for each query of the item
-        struct PackRows {
-            bool real[2];
-            int nv[2], wlo[2], whi[2];
-            float zl[2];
-            float dc[4], ds[4];
-        };
-        auto pack_rows = [&](const ItemInfo &ff, PackRows &pr) {
-#pragma unroll
-            for (int u = 0; u < 2; u++) {
-                const int q = hr[u] / a.H;
-                pr.real[u] = q < ff.nq;
-                const int64_t t_r = pr.real[u] ? a.q_pos[ff.bt + q] : ff.t;
-                pr.nv[u] = (int)visible_count(t_r, a.m, a.E);
-                pr.wlo[u] = (int)(t_r - a.n_win - ff.p0);
-                pr.whi[u] = (int)(t_r - ff.p0);
-                pr.zl[u] = a.sink[hr[u] % a.H] * 1.4426950408889634f;
-            }
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                pr.dc[q] = 1.f;
-                pr.ds[q] = 0.f;
-            }
-            const int de = (Cfg::NC - 1) * 128 + quarter * 32 + lane;
-            if (a.chunk_tiles == 0 && a.derotate && de >= a.rope.first) {
-#pragma unroll
-                for (int q = 0; q < 4; q++)
-                    if (q < ff.nq) rope_cos_sin(a.rope, -a.q_pos[ff.bt + q], (de - a.rope.first) >> 1, pr.dc[q], pr.ds[q]);
-            }
-        };
-        static_assert(sizeof(PackRows) <= 80, "per-thread slot");
-        // this thread's two slots (the item, the next item), c = 128 only
-        PackRows *pslot = reinterpret_cast<PackRows *>(misc + Cfg::MISC_PK + st * 160);
-        bool have_pnext = false;
         int zl_hg = -1;                          // head group whose sink logits zl2 holds
         float zl2[2] = {-INFINITY, -INFINITY};
         for (int64_t it = blockIdx.x; it < a.n_items; it += G) {
@@ -741,39 +679,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             have_fn = false;
             if (f.j0 >= f.j1) continue;
             const int h0 = f.hg * Cfg::HG;
-            const bool packed = PACK && a.qpi > 1;   // rows are (query, head) pairs of f.nq queries
             bool real[2];
             float m_run[2], l_run[2];
-            // packed: the row's own list, as bounds on the entry offset within the
-            // compressed part (< nv_r) and on the window offset from p0
-            // (wlo_r < x <= whi_r)
-            int nv_r[2], wlo_r[2], whi_r[2];
-            PackRows *pcur = pslot + (ii & 1);
-            if (packed && !have_pnext) {
-                PackRows pn;
-                pack_rows(f, pn);
-                *pcur = pn;
-            }
-            have_pnext = false;
 #pragma unroll
             for (int u = 0; u < 2; u++) {
-                if (packed) {
-                    real[u] = pcur->real[u];
-                    nv_r[u] = pcur->nv[u];
-                    wlo_r[u] = pcur->wlo[u];
-                    whi_r[u] = pcur->whi[u];
-                    zl2[u] = pcur->zl[u];
-                } else {
-                    real[u] = h0 + hr[u] < a.H;
-                    nv_r[u] = 0;
-                    wlo_r[u] = 0;
-                    whi_r[u] = 0;
-                    if (f.hg != zl_hg) zl2[u] = real[u] ? a.sink[h0 + hr[u]] * 1.4426950408889634f : -INFINITY;
-                }
+                real[u] = h0 + hr[u] < a.H;
+                if (f.hg != zl_hg) zl2[u] = real[u] ? a.sink[h0 + hr[u]] * 1.4426950408889634f : -INFINITY;
                 m_run[u] = a.chunk_tiles > 0 ? -INFINITY : zl2[u];
                 l_run[u] = 0.f;
             }
-            zl_hg = packed ? -1 : f.hg;
+            zl_hg = f.hg;
             const uint32_t gfirst = g;
             bool fail = false;
             for (int j = f.j0; j < f.j1; j++, g++) {
@@ -806,32 +721,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     tc::tmem_ld_wait();
                     tc::tmem_regs_ready<32>(raw);
                 }
-                // each row's visible entries of this tile: the presence mask, and for
-                // packed rows the interval of the tile that is in the row's own list
-                uint32_t rlo[2], rhi[2];
-#pragma unroll
-                for (int u = 0; u < 2; u++) {
-                    rlo[u] = mlo;
-                    rhi[u] = mhi;
-                    if (packed) {
-                        int lo, hi;
-                        if (j < f.ntc) {
-                            lo = 0;
-                            hi = nv_r[u] - j * 64;
-                        } else {
-                            const int base = (j - f.ntc) * 64;
-                            lo = wlo_r[u] - base + 1;
-                            hi = whi_r[u] - base + 1;
-                        }
-                        lo = lo < 0 ? 0 : (lo > 64 ? 64 : lo);
-                        hi = hi < 0 ? 0 : (hi > 64 ? 64 : hi);
-                        const uint64_t below_hi = hi >= 64 ? ~0ull : (1ull << hi) - 1ull;
-                        const uint64_t below_lo = lo >= 64 ? ~0ull : (1ull << lo) - 1ull;
-                        const uint64_t im = hi > lo ? below_hi & ~below_lo : 0ull;
-                        rlo[u] &= (uint32_t)im;
-                        rhi[u] &= (uint32_t)(im >> 32);
-                    }
-                }
                 // v[u][2i + e]: head hr[u], entry 8i + 2 t4 + e  (raw[4i + 2u + e])
                 float v[2][16];
 #pragma unroll
@@ -839,11 +728,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                     for (int e = 0; e < 2; e++) {
                         const int ent = 8 * i + 2 * t4 + e;
+                        const uint32_t bit = i < 4 ? (mlo >> ent) & 1u : (mhi >> (ent - 32)) & 1u;
 #pragma unroll
-                        for (int u = 0; u < 2; u++) {
-                            const uint32_t bit = i < 4 ? (rlo[u] >> ent) & 1u : (rhi[u] >> (ent - 32)) & 1u;
+                        for (int u = 0; u < 2; u++)
                             v[u][2 * i + e] = bit ? __uint_as_float(raw[4 * i + 2 * u + e]) * a.scale_log2 : -INFINITY;
-                        }
                     }
                 bool need[2];
                 float alpha[2];
@@ -919,17 +807,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (it + G < a.n_items) {
                 item_info(a, it + G, fn);
                 have_fn = true;
-                if (packed && fn.j0 < fn.j1) {
-                    PackRows pn;
-                    pack_rows(fn, pn);
-                    pslot[(ii + 1) & 1] = pn;
-                    have_pnext = true;
-                }
             }
             float dcr = 1.f, dsr = 0.f;
             {
                 const int dlast = (Cfg::NC - 1) * 128 + quarter * 32 + lane;
-                if (!packed && a.chunk_tiles == 0 && a.derotate && dlast >= a.rope.first)
+                if (a.chunk_tiles == 0 && a.derotate && dlast >= a.rope.first)
                     rope_cos_sin(a.rope, -f.t, (dlast - a.rope.first) >> 1, dcr, dsr);
             }
             // item end: the four threads of a head add their partial sums
@@ -957,7 +839,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const bool ok = warp_wait(ofull, ii & 1, a.status, abort_flag, a.spin);
             if (named_bar_or(1, 128, !ok)) break;
             tc::fence_after_sync();
-            const int nh = packed ? f.nq * a.H : (a.H - h0 < 64 ? a.H - h0 : 64);
+            const int nh = a.H - h0 < 64 ? a.H - h0 : 64;
             const int dl = quarter * 32 + lane;                 // dim within a chunk
             for (int c = 0; c < Cfg::NC; c++) {
                 const int d = c * 128 + dl;
@@ -965,7 +847,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 float cr = 1.f, sr = 0.f;
                 const bool rot_w = a.chunk_tiles == 0 && a.derotate && c * 128 + quarter * 32 + 31 >= a.rope.first;
                 const bool rot = d >= a.rope.first;
-                if (rot_w && rot && !packed) {
+                if (rot_w && rot) {
                     if (c == Cfg::NC - 1) {
                         cr = dcr;
                         sr = dsr;
@@ -996,22 +878,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         o[4 * q4 + 2] *= iv4.z;
                         o[4 * q4 + 3] *= iv4.w;
                     }
-                    if (rot_w && packed) {
-                        // rows hb .. hb + 31 hold at most two queries (H >= 16): each
-                        // row is rotated back by its own query's position
-                        const int q0 = hb / a.H, q1 = (hb + 31) / a.H;
-                        const int split = (q0 + 1) * a.H - hb;   // rows h >= split belong to q1
-                        // queries past the item's last are padding rows (never stored)
-                        const float cr0 = pcur->dc[q0 & 3], sr0 = pcur->ds[q0 & 3];
-                        const float cr1 = pcur->dc[q1 & 3], sr1 = pcur->ds[q1 & 3];
-#pragma unroll
-                        for (int h = 0; h < 32; h++) {
-                            const float op = __shfl_xor_sync(0xffffffffu, o[h], 1);
-                            const bool second = h >= split;
-                            const float crh = second ? cr1 : cr0, srh = second ? sr1 : sr0;
-                            if (rot) o[h] = o[h] * crh + op * ((lane & 1) ? srh : -srh);
-                        }
-                    } else if (rot_w) {
+                    if (rot_w) {
 #pragma unroll
                         for (int h = 0; h < 32; h++) {
                             const float op = __shfl_xor_sync(0xffffffffu, o[h], 1);
@@ -1168,7 +1035,7 @@ int attn_tc_chunks(int64_t rows, int H, int64_t max_list, bool invariant) {
     return (int)((tiles + per - 1) / per);
 }
 
-template <int C, bool KV8, bool PACK>
+template <int C, bool KV8>
 static cudaError_t launch_attn_tc_c(int64_t B, const AttnArgs &g, const int32_t *cnt, int n_chunks,
                                     void *split_ws, int max_ctas, cudaStream_t st) {
     AttnTcArgs a;
@@ -1192,14 +1059,7 @@ static cudaError_t launch_attn_tc_c(int64_t B, const AttnArgs &g, const int32_t 
     a.scale_log2 = g.scale * 1.4426950408889634f;
     a.rope = g.rope;
     const int64_t rows = B * g.Tq;
-    // dense lists with 16 or 32 heads: 64 / H consecutive queries share an item,
-    // their (query, head) pairs on the 64 rows, the union of their lists read once
-    a.qpi = (PACK && !g.idx && (g.H == 16 || g.H == 32) && g.Tq >= 64 / g.H && n_chunks <= 1 &&
-             (64 / g.H) * g.rope.pairs <= 256)
-                ? 64 / g.H
-                : 1;
-    a.tq_blocks = (g.Tq + a.qpi - 1) / a.qpi;
-    const int64_t max_list = (g.idx ? (int64_t)g.k : g.E) + g.n_win + (a.qpi - 1);
+    const int64_t max_list = (g.idx ? (int64_t)g.k : g.E) + g.n_win;
     const int64_t max_tiles = (max_list + 63) / 64 + 1;
     if (n_chunks > 1 && split_ws) {
         a.n_chunks = n_chunks;
@@ -1212,7 +1072,7 @@ static cudaError_t launch_attn_tc_c(int64_t B, const AttnArgs &g, const int32_t 
         a.part_o = nullptr;
         a.part_ml = nullptr;
     }
-    a.n_items = (a.qpi > 1 ? B * a.tq_blocks : rows) * a.n_hg * a.n_chunks;
+    a.n_items = rows * a.n_hg * a.n_chunks;
     using Cfg = AtCfg<C>;
     // tensor maps: q rows [B*T*H, C]; compressed entries [B*E, C] and raw
     // window rows [B*L, C] as 64-row boxes (a map that is never read points
@@ -1228,12 +1088,12 @@ static cudaError_t launch_attn_tc_c(int64_t B, const AttnArgs &g, const int32_t 
         return cudaErrorInvalidValue;
     static PerDevice attr;
     {
-        cudaError_t e = smem_limit_once(attr, (const void *)attn_tc_kernel<C, KV8, PACK>, Cfg::SMEM);
+        cudaError_t e = smem_limit_once(attr, (const void *)attn_tc_kernel<C, KV8>, Cfg::SMEM);
         if (e != cudaSuccess) return e;
     }
     const int sms = (max_ctas > 0 && max_ctas < device_sms() ? max_ctas : device_sms()) * Cfg::MIN_BLOCKS;
     const int grid = (int)(a.n_items < sms ? a.n_items : sms);
-    attn_tc_kernel<C, KV8, PACK><<<grid, Cfg::THREADS, Cfg::SMEM, st>>>(tq, tcmp, tw, a);
+    attn_tc_kernel<C, KV8><<<grid, Cfg::THREADS, Cfg::SMEM, st>>>(tq, tcmp, tw, a);
     count_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.chunk_tiles == 0) return e;
@@ -1248,11 +1108,10 @@ cudaError_t launch_attn_tc(int64_t B, const AttnArgs &g, const int32_t *cnt, int
     if (attn_pack_supported(B, g, n_chunks)) return launch_attn_pack(B, g, max_ctas, st);
     if (g.kv8) {
         if (g.c != 512) return cudaErrorInvalidValue;
-        return launch_attn_tc_c<512, true, false>(B, g, cnt, n_chunks, split_ws, max_ctas, st);
+        return launch_attn_tc_c<512, true>(B, g, cnt, n_chunks, split_ws, max_ctas, st);
     }
-    // queries are packed on the c = 128 kernel (the 16-head dense layer); c = 512 takes one query
-    if (g.c == 128) return launch_attn_tc_c<128, false, true>(B, g, cnt, n_chunks, split_ws, max_ctas, st);
-    if (g.c == 512) return launch_attn_tc_c<512, false, false>(B, g, cnt, n_chunks, split_ws, max_ctas, st);
+    if (g.c == 128) return launch_attn_tc_c<128, false>(B, g, cnt, n_chunks, split_ws, max_ctas, st);
+    if (g.c == 512) return launch_attn_tc_c<512, false>(B, g, cnt, n_chunks, split_ws, max_ctas, st);
     return cudaErrorInvalidValue;
 }
 

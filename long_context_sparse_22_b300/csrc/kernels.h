@@ -144,7 +144,7 @@ size_t attn_tc_split_bytes(int64_t rows, int H, int c, int n_chunks);
 cudaError_t launch_attn_tc(int64_t B, const AttnArgs &a, const int32_t *cnt, int n_chunks,
                            void *split_ws, int max_ctas, cudaStream_t st);
 // Dense attention with 128 (query, head) rows per item (c = 128, H dividing
-// 128, no split, no log-denominator output, no q norm): attn_pack.cu.
+// 128, no split): attn_pack.cu.
 bool attn_pack_supported(int64_t B, const AttnArgs &g, int n_chunks);
 cudaError_t launch_attn_pack(int64_t B, const AttnArgs &g, int max_ctas, cudaStream_t st);
 

@@ -12,7 +12,6 @@ Cases:
   compress          csa_compress, n = 65536, c = 512, m = 4 (bf16, with raw rows)
   compress_hca      csa_compress, n = 65536, c = 512, m' = 128 (bf16, with raw rows)
   hca_prefill_c128  hca_attn, 8192 queries, 16 heads x 128, m' = 128 + window
-  hca_prefill_c128_qnorm  the same with the q RMSNorm (the 64-row packed kernel)
   sparse_attn       sparse_attn, 4096 queries, 64 heads x 512, k = 512 + window
   hca_decode        hca_attn, 8 sequences x 8192 entries, 128 heads x 512
   hca_prefill       hca_attn, 8192 queries over 64 entries (m' = 128) + window, 64 heads x 512
@@ -257,7 +256,6 @@ CASES = {
     "compress": case_compress,
     "compress_hca": lambda: case_compress(128),
     "hca_prefill_c128": lambda: case_hca_prefill(16, 128),
-    "hca_prefill_c128_qnorm": lambda: case_hca_prefill(16, 128, q_norm=True),
     "sparse_attn": case_sparse_attn,
     "hca_decode": case_hca_decode,
     "hca_prefill": case_hca_prefill,

@@ -272,7 +272,7 @@ def test_hca_attn(csa, orc, dtype, B, T, H, c, E, m, n_win, r, t0):
 
 def test_hca_attn_c128_no_derotate(csa, orc):
     """Dense attention at c = 128, 16 heads (eight queries per item), output
-    left rotated."""
+    left rotated, with the log-denominators."""
     dtype, B, T, H, c, E, m, n_win, r = "bf16", 1, 45, 16, 128, 50, 128, 128, 64
     seed = 650
     q = synth.normal(seed, 1, (B, T, H, c), 1.0, dtype)
@@ -284,11 +284,15 @@ def test_hca_attn_c128_no_derotate(csa, orc):
     pos = np.tile(t_last - T + 1 + np.arange(T, dtype=np.int64), (B, 1))
     raw_pos0 = np.full(B, t_last - L + 1, np.int64)
     p = csa.params(m=m, n_win=n_win, rope_dims=r, derotate=0)
-    out = csa.hca_attn(dev(q), dev(pos), dev(kvc), dev(kv_raw), dev(raw_pos0), dev(sink), p,
+    lse = torch.empty((B, T, H), dtype=torch.float32, device="cuda")
+    out = csa.hca_attn(dev(q), dev(pos), dev(kvc), dev(kv_raw), dev(raw_pos0), dev(sink), p, lse=lse,
                        ws=_nan_ws(csa))
-    ro = orc.attend(q[0], pos[0], kvc[0], m, kv_raw[0], int(raw_pos0[0]), sink, idx=None, n_win=n_win,
-                    rope_dims=r, derotate=0)
+    ro, rl = orc.attend(q[0], pos[0], kvc[0], m, kv_raw[0], int(raw_pos0[0]), sink, idx=None, n_win=n_win,
+                        rope_dims=r, derotate=0, want_lse=True)
     check_close(host(out)[0], ro, dtype, "hca_attn c128 no derotate")
+    # log-denominator: the bf16 rounding of the rotated query leaves ~2^-9 relative
+    # error in the logits
+    assert np.abs(host(lse)[0] - rl).max() <= 1e-2
 
 
 # ---------------------------------------------------------------- fused
