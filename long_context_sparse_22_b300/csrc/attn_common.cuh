@@ -40,16 +40,8 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// 32 lanes x 16 consecutive 32-bit columns, load and store.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
+// 32 lanes x 16 consecutive 32-bit columns, load (tc.cuh) and store.
+using tc::tmem_ld16;
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
     asm volatile(
@@ -74,14 +66,6 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr, uint32_t lbo, uint
     return d;
 }
 
-// Wait by the whole warp, failure agreed by the warp.  Every lane polls the
-// barrier: when lane 0 polled alone while the others waited at a shuffle, the
-// warp's next burst of copies issued several times slower after a wait that
-// had blocked.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, unsigned *status,
-                                          volatile int *abort_flag, long long limit) {
-    const bool ok = tc::mbar_wait(bar, parity, status, abort_flag, limit);
-    return __all_sync(0xffffffffu, ok);
-}
+using tc::warp_wait;
 
 }  // namespace csa

@@ -15,7 +15,7 @@
 // Warp roles (one persistent CTA per SM):
 //   warp 0     TMA producer: the query block's qI tile once per work item,
 //              then a ring of kI tiles (STAGES deep);
-//   warp 1     TMEM allocator and MMA issuer (one elected thread);
+//   warp 1     TMEM allocator and MMA issuer (converged warp, one issuing lane);
 //   warps 2..  epilogue: tcgen05.ld of a finished accumulator, ReLU, the
 //              w-weighted head sum, masked fp32 stores; two accumulators
 //              alternate so the epilogue of tile i overlaps the MMA of i+1.
@@ -58,9 +58,9 @@ struct IdxCfg {
     static constexpr int ACC_COLS = N;
     static constexpr int TMEM_COLS = QT == 4 ? 512 : 128;
     static constexpr int EPI_WARPS = QT == 4 ? 8 : 4;
+    static constexpr int TPW = QT * 4 / EPI_WARPS;    // tokens (64 columns each) per epilogue warp
     static constexpr int THREADS = 64 + EPI_WARPS * 32;
-    static constexpr int TOK_PER_WARP = QT * 4 / EPI_WARPS;
-    static constexpr int W_FLOATS = EPI_WARPS * TOK_PER_WARP * HI;
+    static constexpr int W_FLOATS = TPW > 1 ? EPI_WARPS * 64 : 0;   // second token's weights per warp
     static constexpr int SMEM = STAGES * A_BYTES + B_BYTES + W_FLOATS * 4 + 256 + 1024;
 };
 
@@ -119,7 +119,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sA = smem;                                   // [STAGES][KH][128][128 B]
     uint8_t *sB = sA + Cfg::STAGES * Cfg::A_BYTES;        // [KH][N][128 B]
-    float *w_all = (float *)(sB + Cfg::B_BYTES);          // [EPI_WARPS][TOK_PER_WARP * 64]
+    float *w_all = (float *)(sB + Cfg::B_BYTES);          // [EPI_WARPS][64] (prefill)
     uint64_t *bars = (uint64_t *)(w_all + Cfg::W_FLOATS);
     uint64_t *full = bars;                                 // [STAGES]
     uint64_t *empty = full + Cfg::STAGES;                  // [STAGES]
@@ -159,66 +159,74 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0, bphase = 0;
-            uint32_t issued_mask = 0, last_par = 0, b_issued = 0, b_par = 0;
-            Item it;
-            for (int r = 0; idx_item<QT>(a, cta, G, r, it); r++) {
-                if (it.jt0 >= it.jt1) continue;
-                if (!tc::mbar_wait(bempty, bphase ^ 1, a.status, abort_flag, a.spin)) break;
+        // The whole warp runs the loop and waits; one lane issues the copies.
+        const bool leader = lane == 0;
+        int stage = 0;
+        uint32_t phase = 0, bphase = 0;
+        uint32_t issued_mask = 0, last_par = 0, b_issued = 0, b_par = 0;
+        Item it;
+        for (int r = 0; idx_item<QT>(a, cta, G, r, it); r++) {
+            if (it.jt0 >= it.jt1) continue;
+            if (!tc::warp_wait(bempty, bphase ^ 1, a.status, abort_flag, a.spin)) break;
+            if (leader) {
                 tc::mbar_expect_tx(bfull, Cfg::B_BYTES);
                 const int qrow = (int)(((int64_t)it.b * a.T + (int64_t)it.qb * QT) * Cfg::HI);
                 for (int kh = 0; kh < Cfg::KH; kh++)
                     tc::tma_load_2d(sB + kh * Cfg::N * 128, &tm_q, kh * 64, qrow, bfull);
-                b_issued = 1;
-                b_par = bphase;
-                bool ok = true;
-                for (int jt = it.jt0; jt < it.jt1; jt++) {
-                    if (!tc::mbar_wait(&empty[stage], phase ^ 1, a.status, abort_flag, a.spin)) { ok = false; break; }
+            }
+            __syncwarp();
+            b_issued = 1;
+            b_par = bphase;
+            bool ok = true;
+            for (int jt = it.jt0; jt < it.jt1; jt++) {
+                if (!tc::warp_wait(&empty[stage], phase ^ 1, a.status, abort_flag, a.spin)) { ok = false; break; }
+                if (leader) {
                     tc::mbar_expect_tx(&full[stage], Cfg::A_BYTES);
                     const int krow = (int)((int64_t)it.b * a.E + (int64_t)jt * 128);
                     uint8_t *dst = sA + stage * Cfg::A_BYTES;
                     for (int kh = 0; kh < Cfg::KH; kh++)
                         tc::tma_load_2d(dst + kh * 128 * 128, &tm_k, kh * 64, krow, &full[stage]);
-                    issued_mask |= 1u << stage;
-                    last_par = (last_par & ~(1u << stage)) | (phase << stage);
-                    if (++stage == Cfg::STAGES) { stage = 0; phase ^= 1; }
                 }
-                if (!ok) break;
-                bphase ^= 1;
+                __syncwarp();
+                issued_mask |= 1u << stage;
+                last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                if (++stage == Cfg::STAGES) { stage = 0; phase ^= 1; }
             }
-            if (*abort_flag) {
-                // let every copy this thread issued land before the CTA exits
-                for (int s = 0; s < Cfg::STAGES; s++)
-                    if (issued_mask & (1u << s))
-                        for (long long i = 0; i < tc::DRAIN_LIMIT; i++)
-                            if (tc::mbar_test(&full[s], (last_par >> s) & 1u)) break;
-                if (b_issued)
+            if (!ok) break;
+            bphase ^= 1;
+        }
+        if (*abort_flag) {
+            // let every copy this warp issued land before the CTA exits
+            for (int s = 0; s < Cfg::STAGES; s++)
+                if (issued_mask & (1u << s))
                     for (long long i = 0; i < tc::DRAIN_LIMIT; i++)
-                        if (tc::mbar_test(bfull, b_par)) break;
-            }
+                        if (tc::mbar_test(&full[s], (last_par >> s) & 1u)) break;
+            if (b_issued)
+                for (long long i = 0; i < tc::DRAIN_LIMIT; i++)
+                    if (tc::mbar_test(bfull, b_par)) break;
         }
     } else if (warp == 1) {
         // --------------------------------------------------------------- MMA
-        if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_bf16_f32(128, Cfg::N);
-            int stage = 0, acc = 0;
-            uint32_t phase = 0, bphase = 0, accphase = 0;
-            const uint32_t aBase = tc::smem_u32(sA), bBase = tc::smem_u32(sB);
-            Item it;
-            for (int r = 0; idx_item<QT>(a, cta, G, r, it); r++) {
-                if (it.jt0 >= it.jt1) continue;
-                if (!tc::mbar_wait(bfull, bphase, a.status, abort_flag, a.spin)) break;
+        // Converged warp, one issuing lane.
+        const bool leader = lane == 0;
+        constexpr uint32_t idesc = tc::idesc_bf16_f32(128, Cfg::N);
+        int stage = 0, acc = 0;
+        uint32_t phase = 0, bphase = 0, accphase = 0;
+        const uint32_t aBase = tc::smem_u32(sA), bBase = tc::smem_u32(sB);
+        Item it;
+        for (int r = 0; idx_item<QT>(a, cta, G, r, it); r++) {
+            if (it.jt0 >= it.jt1) continue;
+            if (!tc::warp_wait(bfull, bphase, a.status, abort_flag, a.spin)) break;
+            tc::fence_after_sync();
+            bool ok = true;
+            for (int jt = it.jt0; jt < it.jt1; jt++) {
+                if (!tc::warp_wait(&full[stage], phase, a.status, abort_flag, a.spin) ||
+                    !tc::warp_wait(&accempty[acc], accphase ^ 1, a.status, abort_flag, a.spin)) {
+                    ok = false;
+                    break;
+                }
                 tc::fence_after_sync();
-                bool ok = true;
-                for (int jt = it.jt0; jt < it.jt1; jt++) {
-                    if (!tc::mbar_wait(&full[stage], phase, a.status, abort_flag, a.spin) ||
-                        !tc::mbar_wait(&accempty[acc], accphase ^ 1, a.status, abort_flag, a.spin)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::fence_after_sync();
+                if (leader) {
                     const uint32_t d = tmem + acc * Cfg::ACC_COLS;
                     const uint32_t aS = aBase + stage * Cfg::A_BYTES;
 #pragma unroll
@@ -231,25 +239,27 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         }
                     tc::mma_commit(&empty[stage]);
                     tc::mma_commit(&accfull[acc]);
-                    if (++stage == Cfg::STAGES) { stage = 0; phase ^= 1; }
-                    if (++acc == 2) { acc = 0; accphase ^= 1; }
                 }
-                if (!ok) break;
-                tc::mma_commit(bempty);
-                bphase ^= 1;
+                __syncwarp();
+                if (++stage == Cfg::STAGES) { stage = 0; phase ^= 1; }
+                if (++acc == 2) { acc = 0; accphase ^= 1; }
             }
-            // every MMA issued above has completed before TMEM is released
-            tc::mma_commit(mdone);
-            for (long long i = 0; i < tc::DRAIN_LIMIT; i++)
-                if (tc::mbar_test(mdone, 0)) break;
+            if (!ok) break;
+            if (leader) tc::mma_commit(bempty);
+            __syncwarp();
+            bphase ^= 1;
         }
+        // every MMA issued above has completed before TMEM is released
+        if (leader) tc::mma_commit(mdone);
+        __syncwarp();
+        for (long long i = 0; i < tc::DRAIN_LIMIT; i++)
+            if (tc::mbar_test(mdone, 0)) break;
     } else {
         // ---------------------------------------------------------- epilogue
         const int ew = warp - 2;                 // 0 .. EPI_WARPS-1
         const int quarter = warp & 3;            // TMEM lanes this warp may read
-        const int cgroup = ew >> 2;              // column group
-        constexpr int TOK_PER_WARP = Cfg::TOK_PER_WARP;
-        float *w_s = w_all + ew * TOK_PER_WARP * Cfg::HI;   // this warp's tokens only
+        constexpr int TPW = Cfg::TPW;
+        const int tt0 = (ew >> 2) * TPW;         // this warp's first token within the block
         const int row = quarter * 32 + lane;     // entry row within the tile
         int acc = 0;
         uint32_t accphase = 0;
@@ -257,52 +267,84 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         bool ok = true;
         for (int r = 0; ok && idx_item<QT>(a, cta, G, r, it); r++) {
             if (it.jt0 >= it.jt1) continue;
-            // this warp's tokens' head weights -> its own shared slice (no
-            // cross-warp barrier, so a warp that stops early cannot strand others)
-            __syncwarp();
-            for (int i = lane; i < TOK_PER_WARP * Cfg::HI; i += 32) {
-                const int t = it.qb * QT + cgroup * TOK_PER_WARP + i / Cfg::HI;
-                w_s[i] = t < a.T ? a.w[((int64_t)it.b * a.T + t) * Cfg::HI + (i % Cfg::HI)] : 0.f;
-            }
-            __syncwarp();
-            int64_t nvt[TOK_PER_WARP];
+            // The first token's 64 head weights stay in registers for the
+            // whole item; the second token's (prefill) sit in this warp's
+            // slice of shared memory.  The MMA's operand reads keep shared
+            // memory busy, and reloading all the weights from there every
+            // tile left the epilogue, not the tensor core, setting the pace;
+            // registers for both tokens leave only 16 columns per
+            // tensor-memory load, and its round trips then hold the
+            // accumulator longer.
+            float wr[64];
+            float *wsB = w_all + ew * 64;
+            int64_t nv[TPW];
+            float *srow[TPW];
 #pragma unroll
-            for (int u = 0; u < TOK_PER_WARP; u++) {
-                const int t = it.qb * QT + cgroup * TOK_PER_WARP + u;
-                nvt[u] = t < a.T ? visible_count(a.q_pos[(int64_t)it.b * a.T + t], a.m, a.E) : -1;
+            for (int u = 0; u < TPW; u++) {
+                const int t = it.qb * QT + tt0 + u;
+                const bool real = t < a.T;
+                const int64_t brow = (int64_t)it.b * a.T + (real ? t : 0);
+                if (u == 0) {
+                    const float4 *w4 = reinterpret_cast<const float4 *>(a.w + brow * Cfg::HI);
+#pragma unroll
+                    for (int h = 0; h < 16; h++) {
+                        const float4 q = real ? __ldg(w4 + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        wr[4 * h] = q.x; wr[4 * h + 1] = q.y; wr[4 * h + 2] = q.z; wr[4 * h + 3] = q.w;
+                    }
+                } else {
+                    __syncwarp();
+                    wsB[lane] = real ? a.w[brow * Cfg::HI + lane] : 0.f;
+                    wsB[lane + 32] = real ? a.w[brow * Cfg::HI + lane + 32] : 0.f;
+                    __syncwarp();
+                }
+                nv[u] = real ? visible_count(a.q_pos[brow], a.m, a.E) : -1;
+                srow[u] = a.scores + brow * a.E;
             }
+            const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + tt0 * Cfg::HI;
             for (int jt = it.jt0; jt < it.jt1; jt++) {
-                if (!tc::mbar_wait(&accfull[acc], accphase, a.status, abort_flag, a.spin)) { ok = false; break; }
+                if (!tc::warp_wait(&accfull[acc], accphase, a.status, abort_flag, a.spin)) { ok = false; break; }
                 tc::fence_after_sync();
                 const int64_t j = (int64_t)jt * 128 + row;
+                const uint32_t ta = tbase + acc * Cfg::ACC_COLS;
 #pragma unroll
-                for (int u = 0; u < TOK_PER_WARP; u++) {
-                    const int tt = cgroup * TOK_PER_WARP + u;
-                    const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) +
-                                           acc * Cfg::ACC_COLS + tt * Cfg::HI;
-                    float v0[32], v1[32];
-                    tc::tmem_ld32(taddr, v0);
-                    tc::tmem_ld32(taddr + 32, v1);
+                for (int u = 0; u < TPW; u++) {
+                    float v[64];
+                    tc::tmem_ld32(ta + u * 64, v);
+                    tc::tmem_ld32(ta + u * 64 + 32, v + 32);
                     tc::tmem_ld_wait();
-                    tc::tmem_regs_ready<32>(v0);
-                    tc::tmem_regs_ready<32>(v1);
-                    const float *wt = w_s + u * Cfg::HI;
-                    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-                    for (int h = 0; h < 32; h++) {
-                        s0 = fmaf(wt[h], fmaxf(v0[h], 0.f), s0);
-                        s1 = fmaf(wt[32 + h], fmaxf(v1[h], 0.f), s1);
+                    tc::tmem_regs_ready<64>(v);
+                    if (u == TPW - 1) {
+                        tc::fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&accempty[acc]);
                     }
-                    const int t = it.qb * QT + tt;
-                    if (nvt[u] >= 0 && j < a.E) {
-                        float *dst = a.scores + ((int64_t)it.b * a.T + t) * a.E + j;
-                        if (j < nvt[u]) *dst = s0 + s1;
-                        else if (a.write_masked) *dst = -INFINITY;
+                    float s0 = 0.f, s1 = 0.f;
+                    if (u == 0) {
+#pragma unroll
+                        for (int h = 0; h < 32; h++) {
+                            s0 = fmaf(wr[h], fmaxf(v[h], 0.f), s0);
+                            s1 = fmaf(wr[32 + h], fmaxf(v[32 + h], 0.f), s1);
+                        }
+                    } else {
+                        const float4 *wt = reinterpret_cast<const float4 *>(wsB);
+#pragma unroll
+                        for (int h = 0; h < 8; h++) {
+                            const float4 wa = wt[h], wb = wt[8 + h];
+                            s0 = fmaf(wa.x, fmaxf(v[4 * h + 0], 0.f), s0);
+                            s1 = fmaf(wb.x, fmaxf(v[32 + 4 * h + 0], 0.f), s1);
+                            s0 = fmaf(wa.y, fmaxf(v[4 * h + 1], 0.f), s0);
+                            s1 = fmaf(wb.y, fmaxf(v[32 + 4 * h + 1], 0.f), s1);
+                            s0 = fmaf(wa.z, fmaxf(v[4 * h + 2], 0.f), s0);
+                            s1 = fmaf(wb.z, fmaxf(v[32 + 4 * h + 2], 0.f), s1);
+                            s0 = fmaf(wa.w, fmaxf(v[4 * h + 3], 0.f), s0);
+                            s1 = fmaf(wb.w, fmaxf(v[32 + 4 * h + 3], 0.f), s1);
+                        }
+                    }
+                    if (nv[u] >= 0 && j < a.E) {
+                        if (j < nv[u]) srow[u][j] = s0 + s1;
+                        else if (a.write_masked) srow[u][j] = -INFINITY;
                     }
                 }
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&accempty[acc]);
                 if (++acc == 2) { acc = 0; accphase ^= 1; }
             }
         }

@@ -90,6 +90,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
 }
 
 // ----------------------------------------------------------------------- TMA
+// Wait by the whole warp, failure agreed by the warp.  Every lane polls the
+// barrier and the warp stays converged, so a role loop can keep one issuing
+// lane inside a converged warp instead of running on one lane alone.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, unsigned *status,
+                                          volatile int *abort_flag, long long limit) {
+    const bool ok = mbar_wait(bar, parity, status, abort_flag, limit);
+    return __all_sync(0xffffffffu, ok);
+}
+
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
                                             uint64_t *bar) {
     asm volatile(
@@ -160,6 +169,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
         : "r"(taddr));
 #pragma unroll
     for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 lanes x 16 consecutive 32-bit columns -> 16 registers per thread.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {
