@@ -15,8 +15,9 @@
 // Warp roles (one persistent CTA per SM):
 //   warp 0     TMA producer: the query block's qI tile once per work item,
 //              then a ring of kI tiles (STAGES deep);
-//   warp 1     TMEM allocator and MMA issuer (converged warp, one issuing lane);
-//   warps 2..  epilogue: tcgen05.ld of a finished accumulator, ReLU, the
+//   warp 1     TMEM allocator and MMA issuer for the even tiles, warp 2 for the
+//              odd ones (converged warps, one issuing lane each);
+//   warps 3..  epilogue: tcgen05.ld of a finished accumulator, ReLU, the
 //              w-weighted head sum, masked fp32 stores; two accumulators
 //              alternate so the epilogue of tile i overlaps the MMA of i+1.
 // Prefill (QT = 4): a work item is one block of 4 consecutive queries and
@@ -59,7 +60,8 @@ struct IdxCfg {
     static constexpr int TMEM_COLS = QT == 4 ? 512 : 128;
     static constexpr int EPI_WARPS = QT == 4 ? 8 : 4;
     static constexpr int TPW = QT * 4 / EPI_WARPS;    // tokens (64 columns each) per epilogue warp
-    static constexpr int THREADS = 64 + EPI_WARPS * 32;
+    static constexpr int EPI0 = 3;                     // first epilogue warp
+    static constexpr int THREADS = (EPI0 + EPI_WARPS) * 32;
     static constexpr int W_FLOATS = TPW > 1 ? EPI_WARPS * 64 : 0;   // second token's weights per warp
     static constexpr int SMEM = STAGES * A_BYTES + B_BYTES + W_FLOATS * 4 + 256 + 1024;
 };
@@ -127,8 +129,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     uint64_t *bempty = bfull + 1;
     uint64_t *accfull = bempty + 1;                        // [2]
     uint64_t *accempty = accfull + 2;                      // [2]
-    uint64_t *mdone = accempty + 2;                        // every issued MMA has completed
-    uint32_t *tmem_slot = (uint32_t *)(mdone + 1);
+    uint64_t *mdone = accempty + 2;                        // [2] every MMA a warp issued has completed
+    uint32_t *tmem_slot = (uint32_t *)(mdone + 2);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -140,12 +142,13 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tc::mbar_init(&empty[s], 1);
         }
         tc::mbar_init(bfull, 1);
-        tc::mbar_init(bempty, 1);
+        tc::mbar_init(bempty, 2);                          // both MMA warps
         for (int i = 0; i < 2; i++) {
             tc::mbar_init(&accfull[i], 1);
             tc::mbar_init(&accempty[i], Cfg::EPI_WARPS);
         }
-        tc::mbar_init(mdone, 1);
+        tc::mbar_init(&mdone[0], 1);
+        tc::mbar_init(&mdone[1], 1);
         *abort_flag = 0;
         tc::fence_barrier_init();
         tc::prefetch_tmap(&tm_q);
@@ -205,13 +208,16 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 for (long long i = 0; i < tc::DRAIN_LIMIT; i++)
                     if (tc::mbar_test(bfull, b_par)) break;
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 2) {
         // --------------------------------------------------------------- MMA
-        // Converged warp, one issuing lane.
+        // Two issuing warps take alternate tiles (warp 1 the even ones of the
+        // CTA's tile sequence, warp 2 the odd ones), so each always fills
+        // the same accumulator; one warp's barrier waits overlap the other's
+        // issue.  Each warp runs converged with one issuing lane.
+        const int p = warp - 1;
         const bool leader = lane == 0;
         constexpr uint32_t idesc = tc::idesc_bf16_f32(128, Cfg::N);
-        int stage = 0, acc = 0;
-        uint32_t phase = 0, bphase = 0, accphase = 0;
+        uint32_t g = 0, bphase = 0;
         const uint32_t aBase = tc::smem_u32(sA), bBase = tc::smem_u32(sB);
         Item it;
         for (int r = 0; idx_item<QT>(a, cta, G, r, it); r++) {
@@ -219,15 +225,18 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (!tc::warp_wait(bfull, bphase, a.status, abort_flag, a.spin)) break;
             tc::fence_after_sync();
             bool ok = true;
-            for (int jt = it.jt0; jt < it.jt1; jt++) {
+            for (int jt = it.jt0; jt < it.jt1; jt++, g++) {
+                if ((int)(g & 1) != p) continue;
+                const int stage = (int)(g % Cfg::STAGES);
+                const uint32_t phase = (g / Cfg::STAGES) & 1;
                 if (!tc::warp_wait(&full[stage], phase, a.status, abort_flag, a.spin) ||
-                    !tc::warp_wait(&accempty[acc], accphase ^ 1, a.status, abort_flag, a.spin)) {
+                    !tc::warp_wait(&accempty[p], ((g >> 1) & 1) ^ 1, a.status, abort_flag, a.spin)) {
                     ok = false;
                     break;
                 }
                 tc::fence_after_sync();
                 if (leader) {
-                    const uint32_t d = tmem + acc * Cfg::ACC_COLS;
+                    const uint32_t d = tmem + p * Cfg::ACC_COLS;
                     const uint32_t aS = aBase + stage * Cfg::A_BYTES;
 #pragma unroll
                     for (int kh = 0; kh < Cfg::KH; kh++)
@@ -238,25 +247,24 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                             tc::mma_bf16(d, ad, bd, idesc, (kh | kk) != 0);
                         }
                     tc::mma_commit(&empty[stage]);
-                    tc::mma_commit(&accfull[acc]);
+                    tc::mma_commit(&accfull[p]);
                 }
                 __syncwarp();
-                if (++stage == Cfg::STAGES) { stage = 0; phase ^= 1; }
-                if (++acc == 2) { acc = 0; accphase ^= 1; }
             }
             if (!ok) break;
+            // the query tile is free once both warps' products of this item are done
             if (leader) tc::mma_commit(bempty);
             __syncwarp();
             bphase ^= 1;
         }
         // every MMA issued above has completed before TMEM is released
-        if (leader) tc::mma_commit(mdone);
+        if (leader) tc::mma_commit(&mdone[p]);
         __syncwarp();
         for (long long i = 0; i < tc::DRAIN_LIMIT; i++)
-            if (tc::mbar_test(mdone, 0)) break;
+            if (tc::mbar_test(&mdone[p], 0)) break;
     } else {
         // ---------------------------------------------------------- epilogue
-        const int ew = warp - 2;                 // 0 .. EPI_WARPS-1
+        const int ew = warp - Cfg::EPI0;         // 0 .. EPI_WARPS-1
         const int quarter = warp & 3;            // TMEM lanes this warp may read
         constexpr int TPW = Cfg::TPW;
         const int tt0 = (ew >> 2) * TPW;         // this warp's first token within the block
