@@ -266,6 +266,15 @@ csa_status do_attn(csa_dtype dt, int64_t B, int64_t T, int H, int c, int64_t E, 
                 return fail(CSA_ERR_WORKSPACE, "batch_invariant needs the split-KV scratch of attn_ws_size");
             ch = 1;
         }
+        if (ch > 1 && !p->batch_invariant) {
+            // no more chunk items than the launch has CTAs for in one round:
+            // each item ends in a partial-output epilogue, and a last round
+            // that only some CTAs fill costs a whole item's time
+            const int64_t units = B * T * ((H + 63) / 64);
+            const int64_t ctas = max_ctas > 0 && max_ctas < device_sms() ? max_ctas : device_sms();
+            const int64_t fit = ctas / units;
+            if (fit < ch) ch = fit > 1 ? (int)fit : 1;
+        }
         CSA_TRY_CUDA(launch_attn_tc(B, a, cnt, ch, scratch, max_ctas, st),
                      "attention launch (tensor cores)");
         return CSA_OK;
