@@ -52,7 +52,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 TRAFFIC_PER_UNIT = {
     ("sparse_attn", "prefill"): (301.435648e6 + 236.806144e6) / 4096,
     ("hca_attn", "prefill"): (545.948672e6 + 492.194560e6) / 8192,
-    ("indexer", "decode"): (537.121280e6 + 10.186752e6) / (8 * 262144),
+    ("indexer", "decode"): (537.124608e6 + 10.153984e6) / (8 * 262144),
     # the MXFP4 decode indexer (indexer_fp4_decode_8x262144.md)
     ("indexer", "decode_lowp"): (142.904576e6 + 6.599680e6) / (8 * 262144),
 }

@@ -771,11 +771,11 @@ csa_status hybrid_decode(csa_dtype dtype, int64_t B, int32_t H, int32_t c, int32
     // first, on an auxiliary stream, on a third of the SMs; the CSA indexer
     // (which streams kI at the HBM rate and needs few SMs to do so) runs
     // beside it on the rest, then the CSA top-k and sparse attention.  (The
-    // Pro decode step, B = 8 at 1M positions, measured 0.237 / 0.193 / 0.193
-    // / 0.214 ms with 32 / 48 / 64 / 80 SMs for the HCA branch, against 0.246
-    // ms when the HCA attention waited for the CSA top-k's collection; the
-    // outputs are bitwise the same, since no kernel's result depends on its
-    // grid.)
+    // Pro decode step, B = 8 at 1M positions, measured 0.183 / 0.168 / 0.170
+    // ms with 32 / 48 / 64 SMs for the HCA branch: past a third the CSA chain
+    // is the critical path.  It was 0.246 ms when the HCA attention waited
+    // for the CSA top-k's collection.  The outputs are bitwise the same,
+    // since no kernel's result depends on its grid.)
     const bool concurrent = hca && dtype == CSA_BF16 && attn_tc_supported(dtype, c);
     AuxLease ax;
     int rest = 0;
