@@ -249,6 +249,10 @@ def test_sparse_attn(csa, orc, dtype, B, T, H, c, E, k, m, n_win, r, derot):
     ("bf16", 2, 37, 32, 128, 40, 128, 128, 64, 0),
     ("bf16", 1, 9, 64, 128, 30, 4, 16, 32, 0),
     ("bf16", 1, 3, 128, 128, 20, 128, 128, 64, 0),
+    # c = 512 with 64 heads: two sequences, consecutive queries straddling a
+    # block boundary (visible counts E - 1 and E), a window shorter than a tile
+    ("bf16", 2, 37, 64, 512, 300, 128, 128, 64, 300 * 128 + 5),
+    ("bf16", 1, 8, 64, 512, 40, 4, 16, 32, 0),
 ])
 def test_hca_attn(csa, orc, dtype, B, T, H, c, E, m, n_win, r, t0):
     seed = 500 + E
@@ -292,6 +296,29 @@ def test_hca_attn_c128_no_derotate(csa, orc):
     check_close(host(out)[0], ro, dtype, "hca_attn c128 no derotate")
     # log-denominator: the bf16 rounding of the rotated query leaves ~2^-9 relative
     # error in the logits
+    assert np.abs(host(lse)[0] - rl).max() <= 1e-2
+
+
+def test_hca_attn_c512_lse(csa, orc):
+    """Dense attention at c = 512, 64 heads, output left rotated, with the
+    log-denominators."""
+    dtype, B, T, H, c, E, m, n_win, r = "bf16", 1, 6, 64, 512, 150, 128, 128, 64
+    seed = 660
+    q = synth.normal(seed, 1, (B, T, H, c), 1.0, dtype)
+    kvc = synth.normal(seed, 2, (B, E, c), 1.0, dtype)
+    t_last = E * m + 2
+    L = n_win + T
+    kv_raw = synth.normal(seed, 3, (B, L, c), 1.0, dtype)
+    sink = synth.normal(seed, 4, (H,), 1.0, "f32")
+    pos = np.tile(t_last - T + 1 + np.arange(T, dtype=np.int64), (B, 1))
+    raw_pos0 = np.full(B, t_last - L + 1, np.int64)
+    p = csa.params(m=m, n_win=n_win, rope_dims=r, derotate=0)
+    lse = torch.empty((B, T, H), dtype=torch.float32, device="cuda")
+    out = csa.hca_attn(dev(q), dev(pos), dev(kvc), dev(kv_raw), dev(raw_pos0), dev(sink), p, lse=lse,
+                       ws=_nan_ws(csa))
+    ro, rl = orc.attend(q[0], pos[0], kvc[0], m, kv_raw[0], int(raw_pos0[0]), sink, idx=None, n_win=n_win,
+                        rope_dims=r, derotate=0, want_lse=True)
+    check_close(host(out)[0], ro, dtype, "hca_attn c512 no derotate")
     assert np.abs(host(lse)[0] - rl).max() <= 1e-2
 
 
