@@ -50,8 +50,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # (indexer_tc_decode_8x262144.md, and indexer_fp4_decode_8x262144.md on the
 # low-precision caches).  Traffic per launch = this x the launch's units.
 TRAFFIC_PER_UNIT = {
-    ("sparse_attn", "prefill"): (301.435648e6 + 236.806144e6) / 4096,
-    ("hca_attn", "prefill"): (545.948672e6 + 492.194560e6) / 8192,
+    ("sparse_attn", "prefill"): (301.270016e6 + 236.418304e6) / 4096,
+    ("hca_attn", "prefill"): (545.577728e6 + 491.951872e6) / 8192,
     ("indexer", "decode"): (537.124608e6 + 10.153984e6) / (8 * 262144),
     # the MXFP4 decode indexer (indexer_fp4_decode_8x262144.md)
     ("indexer", "decode_lowp"): (142.904576e6 + 6.599680e6) / (8 * 262144),
