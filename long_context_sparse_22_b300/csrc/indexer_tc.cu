@@ -176,6 +176,14 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 const int qrow = (int)(((int64_t)it.b * a.T + (int64_t)it.qb * QT) * Cfg::HI);
                 for (int kh = 0; kh < Cfg::KH; kh++)
                     tc::tma_load_2d(sB + kh * Cfg::N * 128, &tm_q, kh * 64, qrow, bfull);
+                // the next item's queries on their way to L2: its tile loads
+                // only once this item's products are done, and from HBM that
+                // left the tensor pipe idle between items
+                Item nx;
+                if (QT == 4 && idx_item<QT>(a, cta, G, r + 1, nx)) {
+                    const int nrow = (int)(((int64_t)nx.b * a.T + (int64_t)nx.qb * QT) * Cfg::HI);
+                    for (int kh = 0; kh < Cfg::KH; kh++) tc::prefetch_l2_box(&tm_q, kh * 64, nrow);
+                }
             }
             __syncwarp();
             b_issued = 1;
