@@ -225,7 +225,8 @@ struct Fp4Cfg {
     static constexpr int SMEM = OFF_MISC + MISC_BYTES + 1024;
     static constexpr int EPI0 = 2;                        // epilogue warps 2 .. 5
     static constexpr int CONV0 = 6;                       // converter warps 6 .. 13 (two groups of 4)
-    static constexpr int THREADS = 448;
+    static constexpr int MMA2 = 14;                       // second MMA warp (odd tiles)
+    static constexpr int THREADS = 480;
     static constexpr int TMEM_COLS = 128;
 };
 
@@ -311,8 +312,8 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
     uint64_t *afull = sempty + Cfg::SST, *aempty = afull + Cfg::AST;
     uint64_t *bfull = aempty + Cfg::AST, *bempty = bfull + 1;
     uint64_t *wfull = bempty + 1, *wempty = wfull + 2;
-    uint64_t *accfull = wempty + 2, *accempty = accfull + 2, *mdone = accempty + 2;
-    uint64_t *ekfull = mdone + 1, *ekempty = ekfull + Cfg::NEK;
+    uint64_t *accfull = wempty + 2, *accempty = accfull + 2, *mdone = accempty + 2;   // mdone [2]
+    uint64_t *ekfull = mdone + 2, *ekempty = ekfull + Cfg::NEK;
     uint32_t *tmem_slot = (uint32_t *)(misc + 512);
     volatile int *abort_flag = (volatile int *)(misc + 516);
     float *wq = (float *)(misc + 1024);                   // [2][64] w[h] * 2^E_h
@@ -329,14 +330,15 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
             tc::mbar_init(&aempty[s], 1);
         }
         tc::mbar_init(bfull, 4);
-        tc::mbar_init(bempty, 1);
+        tc::mbar_init(bempty, 2);                          // both MMA warps
         for (int i = 0; i < 2; i++) {
             tc::mbar_init(&wfull[i], 4);
             tc::mbar_init(&wempty[i], 4);
             tc::mbar_init(&accfull[i], 1);
             tc::mbar_init(&accempty[i], 4);
         }
-        tc::mbar_init(mdone, 1);
+        tc::mbar_init(&mdone[0], 1);
+        tc::mbar_init(&mdone[1], 1);
         for (int i = 0; i < Cfg::NEK; i++) {
             tc::mbar_init(&ekfull[i], 4);
             tc::mbar_init(&ekempty[i], 4);
@@ -378,27 +380,32 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
                         for (long long i = 0; i < tc::DRAIN_LIMIT; i++)
                             if (tc::mbar_test(&sfull[q], (last_par >> q) & 1u)) break;
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == Cfg::MMA2) {
         // ------------------------------------------------------------ MMA
+        // Two issuing warps take alternate tiles (warp 1 the even ones of the
+        // CTA's tile sequence, warp MMA2 the odd ones), each always with the
+        // same accumulator: one warp's barrier waits overlap the other's issue.
+        const int p = warp == 1 ? 0 : 1;
         if (lane == 0) {
             // kind::f16 with f16 A and B (format fields 0), fp32 accumulation
             constexpr uint32_t idesc = (1u << 4) | ((uint32_t)(64 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-            int st = 0, acc = 0;
-            uint32_t ph = 0, accph = 0, bph = 0;
+            uint32_t g = 0, bph = 0;
             const uint32_t aBase = tc::smem_u32(sA), bBase = tc::smem_u32(sB);
             int b, jt0, jt1;
             bool ok = true;
             for (int r = 0; ok && fp4_item(a, cta, G, r, b, jt0, jt1); r++) {
                 if (jt0 >= jt1) continue;
                 if (!tc::mbar_wait(bfull, bph, a.status, abort_flag, a.spin)) break;
-                for (int jt = jt0; jt < jt1; jt++) {
-                    if (!tc::mbar_wait(&afull[st], ph, a.status, abort_flag, a.spin) ||
-                        !tc::mbar_wait(&accempty[acc], accph ^ 1, a.status, abort_flag, a.spin)) {
+                for (int jt = jt0; jt < jt1; jt++, g++) {
+                    if ((int)(g & 1) != p) continue;
+                    const int st = (int)(g % Cfg::AST);
+                    if (!tc::mbar_wait(&afull[st], (g / Cfg::AST) & 1, a.status, abort_flag, a.spin) ||
+                        !tc::mbar_wait(&accempty[p], ((g >> 1) & 1) ^ 1, a.status, abort_flag, a.spin)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after_sync();
-                    const uint32_t d = tmem + acc * 64;
+                    const uint32_t d = tmem + p * 64;
                     const uint32_t aS = aBase + st * Cfg::A_BYTES;
 #pragma unroll
                     for (int kh = 0; kh < 2; kh++)
@@ -407,17 +414,17 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
                             tc::mma_bf16(d, tc::desc_kmajor_sw128(aS + kh * 16384 + kk * 32),
                                          tc::desc_kmajor_sw128(bBase + kh * 8192 + kk * 32), idesc, (kh | kk) != 0);
                     tc::mma_commit(&aempty[st]);
-                    tc::mma_commit(&accfull[acc]);
-                    if (++st == Cfg::AST) { st = 0; ph ^= 1; }
-                    if (++acc == 2) { acc = 0; accph ^= 1; }
+                    tc::mma_commit(&accfull[p]);
                 }
                 if (!ok) break;
+                // the query tile is free once both warps' products of this item are done
                 tc::mma_commit(bempty);
                 bph ^= 1;
             }
-            tc::mma_commit(mdone);
+            // every MMA issued above has completed before TMEM is released
+            tc::mma_commit(&mdone[p]);
             for (long long i = 0; i < tc::DRAIN_LIMIT; i++)
-                if (tc::mbar_test(mdone, 0)) break;
+                if (tc::mbar_test(&mdone[p], 0)) break;
         }
     } else if (warp < Cfg::CONV0) {
         // -------------------------------------------------------- epilogue
