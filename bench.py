@@ -54,7 +54,7 @@ TRAFFIC_PER_UNIT = {
     ("hca_attn", "prefill"): (545.577728e6 + 491.951872e6) / 8192,
     ("indexer", "decode"): (537.124608e6 + 10.153984e6) / (8 * 262144),
     # the MXFP4 decode indexer (indexer_fp4_decode_8x262144.md)
-    ("indexer", "decode_lowp"): (142.904576e6 + 6.599680e6) / (8 * 262144),
+    ("indexer", "decode_lowp"): (142.905344e6 + 6.296320e6) / (8 * 262144),
 }
 
 
