@@ -202,11 +202,13 @@ cudaError_t launch_quant_mxfp4(csa_dtype dt, int64_t rows, const void *src, void
 // evenly over the CTAs, as in the bf16 decode indexer):
 //   warp 0      TMA producer: per 128-key tile, the 8 KB of codes and the
 //               tile's scale bytes into a staging ring;
-//   warp 1      TMEM allocator and MMA issuer;
+//   warp 1      TMEM allocator and MMA issuer for the even tiles, warp 14
+//               for the odd ones (each with its own accumulator);
 //   warps 2-5   epilogue: head sum, key factor, BF16 rounding, stores;
-//   warps 6-9   converters: the item's query into the f16 B tile (and the
-//               scaled head weights), each staged key tile into an f16 A
-//               tile (128-byte swizzle, K-major).
+//   warps 6-13  converters in two groups of four taking alternate tiles:
+//               each staged key tile into an f16 A tile (128-byte swizzle,
+//               K-major); the first group also converts the item's query
+//               into the f16 B tile (and the scaled head weights).
 struct Fp4Cfg {
     static constexpr int AST = 3;                         // f16 A tiles
     static constexpr int SST = 8;                         // staging slots
