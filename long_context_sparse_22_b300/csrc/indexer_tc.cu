@@ -292,7 +292,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             // tensor-memory load, and its round trips then hold the
             // accumulator longer.
             float wr[64];
-            float *wsB = w_all + ew * 64;
+            float *wsB = TPW > 1 ? w_all + ew * 64 : nullptr;    // prefill only
             int64_t nv[TPW];
             float *srow[TPW];
 #pragma unroll
