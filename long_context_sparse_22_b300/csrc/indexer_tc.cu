@@ -196,7 +196,11 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     const int krow = (int)((int64_t)it.b * a.E + (int64_t)jt * 128);
                     uint8_t *dst = sA + stage * Cfg::A_BYTES;
                     for (int kh = 0; kh < Cfg::KH; kh++)
-                        tc::tma_load_2d(dst + kh * 128 * 128, &tm_k, kh * 64, krow, &full[stage]);
+                        if (QT == 1)   // decode: kI is read once, the scores right after
+                            tc::tma_load_2d_hint(dst + kh * 128 * 128, &tm_k, kh * 64, krow, &full[stage],
+                                                 tc::l2_evict_first());
+                        else
+                            tc::tma_load_2d(dst + kh * 128 * 128, &tm_k, kh * 64, krow, &full[stage]);
                 }
                 __syncwarp();
                 issued_mask |= 1u << stage;
@@ -357,7 +361,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         }
                     }
                     if (nv[u] >= 0 && j < a.E) {
-                        if (j < nv[u]) srow[u][j] = s0 + s1;
+                        if (j < nv[u]) {
+                            // decode: the selection reads the scores next, from L2
+                            // if the key stream has not evicted them
+                            if (QT == 1) tc::st_global_hint(&srow[u][j], s0 + s1, tc::l2_evict_last());
+                            else srow[u][j] = s0 + s1;
+                        }
                         else if (a.write_masked) srow[u][j] = -INFINITY;
                     }
                 }

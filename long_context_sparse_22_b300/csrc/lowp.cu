@@ -369,8 +369,10 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
                     const int64_t key0 = (int64_t)b * a.E + (int64_t)jt * 128;
                     tc::mbar_expect_tx(&sfull[s], Cfg::CODE_BYTES + Cfg::SC_BYTES);
                     uint8_t *dst = sS + s * Cfg::STG_BYTES;
-                    tc::tma_load_2d(dst, &tm_codes, 0, (int)key0, &sfull[s]);
-                    tc::tma_load_2d(dst + Cfg::CODE_BYTES, &tm_sc, 0, (int)(key0 >> 2), &sfull[s]);
+                    // the keys are read once, the scores right after (kept in L2)
+                    const uint64_t pol = tc::l2_evict_first();
+                    tc::tma_load_2d_hint(dst, &tm_codes, 0, (int)key0, &sfull[s], pol);
+                    tc::tma_load_2d_hint(dst + Cfg::CODE_BYTES, &tm_sc, 0, (int)(key0 >> 2), &sfull[s], pol);
                     issued |= 1u << s;
                     last_par = (last_par & ~(1u << s)) | (ph << s);
                     if (++s == Cfg::SST) { s = 0; ph ^= 1; }
@@ -475,7 +477,9 @@ indexer_fp4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_co
                 }
                 const int64_t j = (int64_t)jt * 128 + row;
                 const float sc = (s0 + s1) * pow2f(ek[q * 128 + row]);
-                if (j < nv) a.scores[(int64_t)b * a.E + j] = __bfloat162float(__float2bfloat16_rn(sc));
+                if (j < nv)
+                    tc::st_global_hint(a.scores + (int64_t)b * a.E + j, __bfloat162float(__float2bfloat16_rn(sc)),
+                                       tc::l2_evict_last());
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) {
