@@ -52,9 +52,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 TRAFFIC_PER_UNIT = {
     ("sparse_attn", "prefill"): (301.270016e6 + 236.418304e6) / 4096,
     ("hca_attn", "prefill"): (545.577728e6 + 491.951872e6) / 8192,
-    ("indexer", "decode"): (537.124608e6 + 10.153984e6) / (8 * 262144),
+    ("indexer", "decode"): (537.052928e6 + 3.294976e6) / (8 * 262144),
     # the MXFP4 decode indexer (indexer_fp4_decode_8x262144.md)
-    ("indexer", "decode_lowp"): (142.905344e6 + 6.296320e6) / (8 * 262144),
+    ("indexer", "decode_lowp"): (142.865152e6 + 3.076096e6) / (8 * 262144),
 }
 
 
