@@ -322,6 +322,33 @@ def test_hca_attn_c512_lse(csa, orc):
     assert np.abs(host(lse)[0] - rl).max() <= 1e-2
 
 
+@pytest.mark.parametrize("B", [20, 80])
+def test_hca_attn_decode_chunk_cap(csa, orc, B):
+    """Split-KV decode whose chunk count is capped by the CTAs of one round:
+    128 heads of B one-query sequences are 2 B items before the split, so at
+    B = 20 the length rule's 4 chunks come down to 3, and at B = 80 (160
+    units, more than the SMs) the list is not split at all.  NaN-filled
+    scratch shows any partial the combine reads without an item writing it."""
+    dtype, T, H, c, E, m, n_win, r = "bf16", 1, 128, 512, 700, 128, 128, 64
+    seed = 670 + B
+    q = synth.normal(seed, 1, (B, T, H, c), 1.0, dtype)
+    kvc = synth.normal(seed, 2, (B, E, c), 1.0, dtype)
+    t_last = E * m + 5
+    L = n_win + T
+    kv_raw = synth.normal(seed, 3, (B, L, c), 1.0, dtype)
+    sink = synth.normal(seed, 4, (H,), 1.0, "f32")
+    pos = np.full((B, T), t_last, np.int64)
+    raw_pos0 = np.full(B, t_last - L + 1, np.int64)
+    p = csa.params(m=m, n_win=n_win, rope_dims=r)
+    out = csa.hca_attn(dev(q), dev(pos), dev(kvc), dev(kv_raw), dev(raw_pos0), dev(sink), p,
+                       ws=_nan_ws(csa, 1 << 28))
+    g = host(out)
+    for b in (0, B // 2, B - 1):
+        ro = orc.attend(q[b], pos[b], kvc[b], m, kv_raw[b], int(raw_pos0[b]), sink, idx=None,
+                        n_win=n_win, rope_dims=r)
+        check_close(g[b], ro, dtype, f"hca_attn decode chunk cap b={b}")
+
+
 # ---------------------------------------------------------------- fused
 
 def _prefill_csa_gpu(csa, s, x, idx_out=True):
