@@ -73,6 +73,7 @@ def test_compress(csa, orc, dtype, n, c, m, r, overlap, sc):
 @pytest.mark.parametrize("dtype,B,T,hI,dI,E,m,pos0", [
     ("f32", 1, 2048, 4, 32, 512, 4, 0),
     ("bf16", 2, 40, 64, 128, 2100, 4, 8000),
+    ("bf16", 2, 37, 64, 128, 1500, 4, 3000),      # a last query block with one token
     ("bf16", 3, 1, 64, 128, 5000, 4, 19999),      # decode shape
     ("bf16", 1, 33, 16, 64, 300, 2, 500),
 ])
